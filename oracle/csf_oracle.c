@@ -1,0 +1,249 @@
+/*
+ * CSF scale-codec oracle: plain, slow, single-threaded CPU code.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this library.  It shares no code, header,
+ * table or helper with the CUDA library, and the CUDA library never calls it.
+ *
+ * It restates, loop by loop, what the following web pages say the method
+ * computes (cited by page title and paragraph; the pages have no numbered
+ * sections):
+ *   [FK]   "finegrained-kernels: decode losslessly compressed NVFP4 scales
+ *           (CSF)" -- format paragraph (one base byte per row, most scales as
+ *           4-bit offsets from it, the rest in an exception stream, exact
+ *           reconstruction); helpers paragraph (decode of the whole stack, or
+ *           only of experts with routed tokens, inactive planes untouched).
+ *   [B478] "NVFP4-CSF: expand_scales() for ahead-of-call scale expansion
+ *           (canonical twin of #477)" -- commit message documenting one-bit
+ *           MXFP4 and four-bit NVFP4 offsets from a row base byte.
+ *   [V964] "Load native FP4 experts with optional lossless CSF scales" --
+ *           encoding plus exception index at preparation time.
+ *
+ * The pages print no byte layout.  The layout below is the plainest reading
+ * consistent with them:
+ *   - dense stack: row-major [E][R][C] bytes; a row is one output channel's
+ *     C scale bytes; row index = e*R + r; element index i = row*C + c.
+ *   - NVFP4: window width w = 14; offsets are a flat nibble stream over all
+ *     N = E*R*C elements, element i in byte i>>1, even i in the low nibble;
+ *     nibble 0..14 is an offset, nibble 15 marks an exception.
+ *   - MXFP4: w = 1; two flat LSB-first bit planes: offset bit and escape bit
+ *     (escape bit 1 = exception, its offset bit is written 0).
+ *   - base: smallest byte value present in the row whose window
+ *     [v, v+w] holds the most of the row's bytes.
+ *   - exceptions: bytes outside [base, base+w], appended in row-major order;
+ *     exc_index[row] = number of exceptions in earlier rows (length rows+1,
+ *     last entry = total).
+ *   - decode: dense = base + offset (mod 256), or the exception byte at
+ *     exc_index[row] + (number of earlier escapes in the same row).
+ *   - routed decode: expert e is active iff start[e+1] > start[e]; planes of
+ *     inactive experts are not written.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { CSFO_NVFP4 = 0, CSFO_MXFP4 = 1 };
+enum { CSFO_OK = 0, CSFO_ERR_ARG = 1, CSFO_ERR_CAPACITY = 2, CSFO_ERR_CORRUPT = 3 };
+
+/* Width of the offset window: 4-bit offsets 0..14 (15 is the escape code)
+ * for NVFP4, 1-bit offsets 0..1 for MXFP4 ([B478] offsets commit message). */
+static int window_width(int kind) { return kind == CSFO_NVFP4 ? 14 : 1; }
+
+static unsigned nibble_get(const uint8_t *s, uint64_t i)
+{
+    return (s[i / 2] >> (4 * (i % 2))) & 0xFu;
+}
+
+static void nibble_put(uint8_t *s, uint64_t i, unsigned v)
+{
+    s[i / 2] = (uint8_t)(s[i / 2] | (v << (4 * (i % 2))));
+}
+
+static unsigned bit_get(const uint8_t *s, uint64_t i)
+{
+    return (s[i / 8] >> (i % 8)) & 1u;
+}
+
+static void bit_put(uint8_t *s, uint64_t i, unsigned v)
+{
+    s[i / 8] = (uint8_t)(s[i / 8] | (v << (i % 8)));
+}
+
+/* Byte lengths of the packed streams for one geometry. */
+void csfo_stream_bytes(int kind, int64_t E, int64_t R, int64_t C,
+                       uint64_t *offsets_bytes, uint64_t *escapes_bytes,
+                       uint64_t *base_bytes, uint64_t *index_entries)
+{
+    uint64_t n = (uint64_t)E * (uint64_t)R * (uint64_t)C;
+    uint64_t rows = (uint64_t)E * (uint64_t)R;
+    if (kind == CSFO_NVFP4) {
+        *offsets_bytes = (n + 1) / 2;
+        *escapes_bytes = 0;
+    } else {
+        *offsets_bytes = (n + 7) / 8;
+        *escapes_bytes = (n + 7) / 8;
+    }
+    *base_bytes = rows;
+    *index_entries = rows + 1;
+}
+
+/* Base byte of one row ([FK] format paragraph: one base byte per row, most
+ * scales as offsets from it).  Reading: the smallest value that occurs in the
+ * row among those whose window [v, v+w] covers the most bytes of the row. */
+static unsigned choose_base(const uint8_t *x, int64_t C, int w)
+{
+    uint64_t hist[256];
+    memset(hist, 0, sizeof hist);
+    for (int64_t c = 0; c < C; ++c)
+        hist[x[c]] += 1;
+    unsigned best = 0;
+    int64_t best_count = -1;
+    for (int v = 0; v < 256; ++v) {
+        if (hist[v] == 0)
+            continue;
+        int64_t count = 0;
+        for (int u = v; u <= v + w && u < 256; ++u)
+            count += (int64_t)hist[u];
+        if (count > best_count) {
+            best_count = count;
+            best = (unsigned)v;
+        }
+    }
+    return best;
+}
+
+/*
+ * Encode a dense stack ([FK] format paragraph; [V964] encoding plus index).
+ * Writes base[rows], offsets (and escapes for MXFP4) -- zeroed here first --,
+ * exc_index[rows+1] and up to exc_capacity exception bytes.  *num_exc gets
+ * the total.  Returns CSFO_ERR_CAPACITY if the exceptions did not fit.
+ */
+int csfo_encode(int kind, int64_t E, int64_t R, int64_t C, const uint8_t *dense,
+                uint8_t *base, uint8_t *offsets, uint8_t *escapes,
+                uint32_t *exc_index, uint8_t *exc_bytes, uint64_t exc_capacity,
+                uint64_t *num_exc)
+{
+    if ((kind != CSFO_NVFP4 && kind != CSFO_MXFP4) || E < 0 || R < 0 || C < 1)
+        return CSFO_ERR_ARG;
+    uint64_t ob, eb, bb, ie;
+    csfo_stream_bytes(kind, E, R, C, &ob, &eb, &bb, &ie);
+    memset(offsets, 0, ob);
+    if (kind == CSFO_MXFP4)
+        memset(escapes, 0, eb);
+    int w = window_width(kind);
+    uint64_t rows = (uint64_t)E * (uint64_t)R;
+    uint64_t total = 0;
+    int status = CSFO_OK;
+    for (uint64_t row = 0; row < rows; ++row) {
+        const uint8_t *x = dense + row * (uint64_t)C;
+        unsigned b = choose_base(x, C, w);
+        base[row] = (uint8_t)b;
+        if (total > 0xFFFFFFFFull)
+            return CSFO_ERR_ARG;
+        exc_index[row] = (uint32_t)total;
+        for (int64_t c = 0; c < C; ++c) {
+            uint64_t i = row * (uint64_t)C + (uint64_t)c;
+            int d = (int)x[c] - (int)b;
+            int inside = d >= 0 && d <= w;
+            if (kind == CSFO_NVFP4) {
+                nibble_put(offsets, i, inside ? (unsigned)d : 0xFu);
+            } else {
+                bit_put(offsets, i, inside ? (unsigned)d : 0u);
+                bit_put(escapes, i, inside ? 0u : 1u);
+            }
+            if (!inside) {
+                if (total < exc_capacity)
+                    exc_bytes[total] = x[c];
+                else
+                    status = CSFO_ERR_CAPACITY;
+                total += 1;
+            }
+        }
+    }
+    if (total > 0xFFFFFFFFull)
+        return CSFO_ERR_ARG;
+    exc_index[rows] = (uint32_t)total;
+    *num_exc = total;
+    return status;
+}
+
+/* Escape test of element i ([FK] exception stream; [B478] offsets). */
+static int is_escape(int kind, const uint8_t *offsets, const uint8_t *escapes, uint64_t i)
+{
+    if (kind == CSFO_NVFP4)
+        return nibble_get(offsets, i) == 0xFu;
+    return bit_get(escapes, i) == 1u;
+}
+
+static unsigned offset_of(int kind, const uint8_t *offsets, uint64_t i)
+{
+    if (kind == CSFO_NVFP4)
+        return nibble_get(offsets, i);
+    return bit_get(offsets, i);
+}
+
+/*
+ * Decode ([FK] format and helpers paragraphs).  expert_start is NULL for the
+ * whole stack, else E+1 int64 entries; only experts with start[e+1] > start[e]
+ * are written.  An exception reference past num_exc writes 0 and returns
+ * CSFO_ERR_CORRUPT.
+ */
+int csfo_decode(int kind, int64_t E, int64_t R, int64_t C,
+                const uint8_t *base, const uint8_t *offsets, const uint8_t *escapes,
+                const uint32_t *exc_index, const uint8_t *exc_bytes, uint64_t num_exc,
+                const int64_t *expert_start, uint8_t *out)
+{
+    if ((kind != CSFO_NVFP4 && kind != CSFO_MXFP4) || E < 0 || R < 0 || C < 1)
+        return CSFO_ERR_ARG;
+    int status = CSFO_OK;
+    for (int64_t e = 0; e < E; ++e) {
+        if (expert_start != NULL && !(expert_start[e + 1] > expert_start[e]))
+            continue;
+        for (int64_t r = 0; r < R; ++r) {
+            uint64_t row = (uint64_t)e * (uint64_t)R + (uint64_t)r;
+            uint64_t rank = 0;
+            for (int64_t c = 0; c < C; ++c) {
+                uint64_t i = row * (uint64_t)C + (uint64_t)c;
+                if (is_escape(kind, offsets, escapes, i)) {
+                    uint64_t pos = (uint64_t)exc_index[row] + rank;
+                    rank += 1;
+                    if (pos < num_exc) {
+                        out[i] = exc_bytes[pos];
+                    } else {
+                        out[i] = 0;
+                        status = CSFO_ERR_CORRUPT;
+                    }
+                } else {
+                    out[i] = (uint8_t)((base[row] + offset_of(kind, offsets, i)) & 0xFFu);
+                }
+            }
+        }
+    }
+    return status;
+}
+
+/*
+ * Well-formedness of a stack's index: exc_index[0] == 0, each row's index
+ * step equals the number of escapes in that row, and the last entry equals
+ * num_exc.  Returns CSFO_OK or CSFO_ERR_CORRUPT.
+ */
+int csfo_check(int kind, int64_t E, int64_t R, int64_t C,
+               const uint8_t *offsets, const uint8_t *escapes,
+               const uint32_t *exc_index, uint64_t num_exc)
+{
+    if ((kind != CSFO_NVFP4 && kind != CSFO_MXFP4) || E < 0 || R < 0 || C < 1)
+        return CSFO_ERR_ARG;
+    uint64_t rows = (uint64_t)E * (uint64_t)R;
+    if (exc_index[0] != 0)
+        return CSFO_ERR_CORRUPT;
+    for (uint64_t row = 0; row < rows; ++row) {
+        uint64_t count = 0;
+        for (int64_t c = 0; c < C; ++c)
+            count += (uint64_t)is_escape(kind, offsets, escapes, row * (uint64_t)C + (uint64_t)c);
+        if ((uint64_t)exc_index[row + 1] != (uint64_t)exc_index[row] + count)
+            return CSFO_ERR_CORRUPT;
+    }
+    if ((uint64_t)exc_index[rows] != num_exc)
+        return CSFO_ERR_CORRUPT;
+    return CSFO_OK;
+}
