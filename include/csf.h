@@ -1,0 +1,197 @@
+/*
+ * csf.h -- C ABI of the GB300 (sm_103a) CSF scale codec library (libcsf.so).
+ *
+ * CSF stores the FP8 scale bytes of FP4 MoE expert weights losslessly: one
+ * base byte per row, most scales as small offsets from that base, and the
+ * bytes outside the offset range in an exception stream found through a
+ * per-row prefix index.  Decoding rebuilds the original bytes exactly.
+ *
+ * Sources (web pages, cited by title and paragraph; they have no numbered
+ * sections):
+ *   [FK]   "finegrained-kernels: decode losslessly compressed NVFP4 scales
+ *           (CSF)": format paragraph (base byte per row, 4-bit offsets,
+ *           exception stream, exact bytes); strategy table (decode once, or
+ *           keep compressed and decode into one shared workspace before each
+ *           GEMM); helpers paragraph (a prepare helper that keeps the input
+ *           device, a GPU decoder into caller-owned reusable workspace, the
+ *           grouped-routing expert_start tensor skipping inactive experts in
+ *           both the fixed-stream and exception passes, no CPU sync);
+ *           validation paragraph (reusable odd-offset workspace).
+ *   [B478] "NVFP4-CSF: expand_scales() for ahead-of-call scale expansion
+ *           (canonical twin of #477)": commit messages on one-bit MXFP4 and
+ *           four-bit NVFP4 offsets from a row base byte, on pairing gate/up
+ *           and down scales without extra streams, on both routing integer
+ *           types, and on caller-owned scratch.
+ *   [V964] "Load native FP4 experts with optional lossless CSF scales":
+ *           GPU encoding plus exception index at preparation time.
+ *
+ * Byte layout of a stack of E experts x R rows x C scale bytes
+ * (N = E*R*C elements, rows = E*R; element i = (e*R + r)*C + c):
+ *   base[rows]            one byte per row.
+ *   NVFP4 offsets         flat nibble stream over all N elements: element i
+ *                         in byte i/2, even i in the low nibble.  Nibble
+ *                         0..14 = offset from the row base, 15 = exception.
+ *   MXFP4 offsets/escapes two flat LSB-first bit planes (element i in byte
+ *                         i/8, bit i%8): offset bit, and escape bit (1 =
+ *                         exception; its offset bit is 0).
+ *   exc_index[rows+1]     uint32 exclusive prefix of per-row exception
+ *                         counts; exc_index[rows] = total exceptions.
+ *   exc_bytes[total]      exception bytes, row-major.
+ * Decoded byte: base[row] + offset (mod 256), or, for an exception, the byte
+ * at exc_index[row] + (number of earlier exceptions in the same row).
+ * Encoding is canonical: the base is the smallest byte present in the row
+ * whose window [base, base+w] (w = 14 NVFP4, 1 MXFP4) holds the most of the
+ * row's bytes; pad nibbles/bits past N are 0.
+ *
+ * Conventions shared by every call:
+ *   - All buffer pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates or frees device memory.  Calls are asynchronous on
+ *     `stream` (a cudaStream_t; NULL = the legacy default stream) and never
+ *     synchronise the host.
+ *   - The return value reports argument and launch errors only.  Data errors
+ *     found on the device (a corrupt index, a full exception buffer, a bounded
+ *     wait that gave up) are OR-ed into the optional device word
+ *     `error_word` as CSF_DEV_ERR_* bits; kernels never trap, and their reads
+ *     and writes stay inside the buffers described here.
+ *   - Packed streams are read in 16-byte pieces: `offsets` and `escapes` must
+ *     be 16-byte aligned and allocated to the lengths csf_sizes() reports
+ *     (the packed length rounded up to 16 bytes).
+ */
+#ifndef CSF_H
+#define CSF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CSF_ABI_VERSION 1
+
+typedef enum {
+    CSF_OK = 0,
+    CSF_ERR_ARG = 1,         /* NULL/unaligned pointer, bad kind, host pointer where a device one is needed */
+    CSF_ERR_SIZE = 2,        /* a buffer or scratch smaller than the geometry needs */
+    CSF_ERR_UNSUPPORTED = 3, /* geometry beyond the library's limits (see csf_sizes) */
+    CSF_ERR_CUDA = 4         /* a CUDA runtime call or a launch failed */
+} csf_status;
+
+/* Device error-word bits (OR-ed, never cleared by the library). */
+#define CSF_DEV_ERR_CORRUPT  0x1u /* index disagrees with the escape codes, or points past the stream */
+#define CSF_DEV_ERR_CAPACITY 0x2u /* prepare: more exceptions than exc_capacity (exc_index still complete) */
+#define CSF_DEV_ERR_TIMEOUT  0x4u /* prepare: a bounded inter-block wait gave up */
+
+typedef enum {
+    CSF_NVFP4 = 0, /* UE4M3 scales, one per 16 weights: 4-bit offsets, escape nibble 15 */
+    CSF_MXFP4 = 1  /* UE8M0 scales, one per 32 weights: 1-bit offset plane + 1-bit escape plane */
+} csf_kind;
+
+typedef struct {
+    int32_t kind;        /* csf_kind */
+    int32_t num_experts; /* E >= 1 */
+    int32_t rows;        /* R >= 1 rows (output channels) per expert */
+    int32_t cols;        /* C >= 1 scale bytes per row (K/16 NVFP4, K/32 MXFP4) */
+} csf_geometry;
+
+/* Allocation sizes in bytes for one geometry (csf_sizes). */
+typedef struct {
+    uint64_t dense;           /* E*R*C: the dense stack and a decode workspace */
+    uint64_t base;            /* rows */
+    uint64_t offsets;         /* packed offsets rounded up to 16 */
+    uint64_t escapes;         /* MXFP4 escape plane rounded up to 16; 0 for NVFP4 */
+    uint64_t exc_index;       /* 4*(rows+1) */
+    uint64_t prepare_scratch; /* scratch for csf_prepare */
+} csf_sizes_t;
+
+/*
+ * A compressed stack: device buffers owned by the caller.  csf_prepare fills
+ * them; csf_decode/csf_decode_pair read them.  `num_exc` is the host copy of
+ * exc_index[rows] (the caller reads it once after prepare); `exc_bytes` must
+ * be readable for num_exc bytes rounded up to a multiple of 16.
+ */
+typedef struct {
+    csf_geometry g;
+    uint8_t *base;
+    uint8_t *offsets;
+    uint8_t *escapes;     /* MXFP4 only; NULL for NVFP4 */
+    uint32_t *exc_index;
+    uint8_t *exc_bytes;
+    uint64_t num_exc;
+    uint32_t *error_word; /* optional device word for CSF_DEV_ERR_* bits; may be NULL */
+} csf_stack;
+
+/* Human-readable name of a status code. */
+const char *csf_status_string(csf_status status);
+
+/* CSF_ABI_VERSION of the loaded library. */
+int csf_abi_version(void);
+
+/*
+ * Allocation sizes for a geometry.  Host only, no CUDA calls.  Returns
+ * CSF_ERR_ARG for a bad kind or non-positive sizes, CSF_ERR_UNSUPPORTED when
+ * N >= 2^40 or rows >= 2^31.
+ */
+csf_status csf_sizes(const csf_geometry *g, csf_sizes_t *out);
+
+/*
+ * Encode a dense stack on the GPU: base bytes, offset (and escape) planes,
+ * the exception index and the exception stream, in one pass over the dense
+ * bytes ([FK] format and helpers paragraphs; [V964] encoding plus index).
+ *
+ *   dense          device, E*R*C bytes, row-major [E][R][C], any alignment.
+ *   out            geometry and destination buffers (base, offsets,
+ *                  escapes for MXFP4, exc_index, exc_bytes, error_word).
+ *                  out->num_exc is not written (read exc_index[rows]).
+ *   exc_capacity   bytes available at out->exc_bytes.  Exceptions past it are
+ *                  dropped and CSF_DEV_ERR_CAPACITY is set; exc_index is
+ *                  complete either way, so the caller can re-run with a
+ *                  buffer of exc_index[rows] bytes.  E*R*C always suffices.
+ *   scratch        device, csf_sizes().prepare_scratch bytes, 8-byte
+ *                  aligned; cleared by this call on `stream`.  Calls that
+ *                  share a scratch buffer must not overlap on the GPU.
+ * Blocks of the kernel pass exception-count prefixes to later blocks through
+ * the scratch (a decoupled look-back); every wait is bounded and sets
+ * CSF_DEV_ERR_TIMEOUT rather than hang.
+ * Errors: CSF_ERR_ARG (NULL, misaligned planes, dense not in device memory),
+ * CSF_ERR_SIZE (scratch too small), CSF_ERR_CUDA.
+ */
+csf_status csf_prepare(const uint8_t *dense, csf_stack *out, uint64_t exc_capacity,
+                       void *scratch, size_t scratch_bytes, void *stream);
+
+/*
+ * Decode a stack into a dense workspace ([FK] format, strategy table and
+ * helpers paragraphs).
+ *
+ *   s              the stack (num_exc set).
+ *   ws, ws_bytes   device workspace of at least E*R*C bytes, any byte
+ *                  alignment (odd offsets allowed), row-major [E][R][C].
+ *   expert_start   NULL: decode every expert.  Else a device array of E+1
+ *                  int32 (expert_start_is_int64 == 0) or int64 entries, the
+ *                  grouped-routing prefix: expert e is decoded iff
+ *                  expert_start[e+1] > expert_start[e]; the workspace planes
+ *                  of the other experts are not touched.  The routing is read
+ *                  on the device: no host sync, no selection buffer.
+ * One kernel launch; no host synchronisation.
+ * Errors: CSF_ERR_ARG, CSF_ERR_SIZE (ws_bytes < E*R*C),
+ * CSF_ERR_UNSUPPORTED (routed decode with E > 8192), CSF_ERR_CUDA.
+ */
+csf_status csf_decode(const csf_stack *s, uint8_t *ws, size_t ws_bytes,
+                      const void *expert_start, int expert_start_is_int64, void *stream);
+
+/*
+ * Decode a gate(/up) stack and a down stack in ONE launch with the same
+ * routing ([B478] pairing commit message): same semantics as two csf_decode
+ * calls.  The stacks must have the same number of experts; kinds, rows and
+ * columns may differ.  Errors as csf_decode, plus CSF_ERR_ARG when the
+ * expert counts differ.
+ */
+csf_status csf_decode_pair(const csf_stack *gate, uint8_t *gate_ws, size_t gate_ws_bytes,
+                           const csf_stack *down, uint8_t *down_ws, size_t down_ws_bytes,
+                           const void *expert_start, int expert_start_is_int64, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSF_H */

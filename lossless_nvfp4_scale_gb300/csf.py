@@ -1,0 +1,272 @@
+"""Python binding of libcsf.so (the CSF C ABI in include/csf.h).
+
+Argument marshalling only: every step of prepare and decode runs in the CUDA
+kernels of the library.  PyTorch supplies device memory and streams.  Importing
+this module fails loudly when the compiled library is missing; there is no CPU
+fallback.
+
+Typical use::
+
+    stack = csf.prepare(dense_u8_cuda, csf.NVFP4)        # [E, R, C] uint8
+    ws = torch.empty_like(dense_u8_cuda)
+    csf.decode(stack, ws)                                 # whole stack
+    csf.decode(stack, ws, expert_start=start_i32_cuda)    # routed experts only
+    csf.decode_pair(gate, down, gate_ws, down_ws, expert_start)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+NVFP4 = 0
+MXFP4 = 1
+DEV_ERR_CORRUPT = 0x1
+DEV_ERR_CAPACITY = 0x2
+DEV_ERR_TIMEOUT = 0x4
+
+_c_i32 = ctypes.c_int32
+_c_u64 = ctypes.c_uint64
+_c_vp = ctypes.c_void_p
+
+
+class Geometry(ctypes.Structure):
+    _fields_ = [("kind", _c_i32), ("num_experts", _c_i32), ("rows", _c_i32), ("cols", _c_i32)]
+
+
+class Sizes(ctypes.Structure):
+    _fields_ = [("dense", _c_u64), ("base", _c_u64), ("offsets", _c_u64), ("escapes", _c_u64),
+                ("exc_index", _c_u64), ("prepare_scratch", _c_u64)]
+
+
+class CStack(ctypes.Structure):
+    _fields_ = [("g", Geometry), ("base", _c_vp), ("offsets", _c_vp), ("escapes", _c_vp),
+                ("exc_index", _c_vp), ("exc_bytes", _c_vp), ("num_exc", _c_u64),
+                ("error_word", _c_vp)]
+
+
+class CsfError(RuntimeError):
+    pass
+
+
+def _load():
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise CsfError(f"{path} is missing: build it with `python -m lossless_nvfp4_scale_gb300.build` "
+                       "(there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    lib.csf_status_string.argtypes = [ctypes.c_int]
+    lib.csf_status_string.restype = ctypes.c_char_p
+    lib.csf_abi_version.argtypes = []
+    lib.csf_abi_version.restype = ctypes.c_int
+    lib.csf_sizes.argtypes = [ctypes.POINTER(Geometry), ctypes.POINTER(Sizes)]
+    lib.csf_sizes.restype = ctypes.c_int
+    lib.csf_prepare.argtypes = [_c_vp, ctypes.POINTER(CStack), _c_u64, _c_vp, ctypes.c_size_t, _c_vp]
+    lib.csf_prepare.restype = ctypes.c_int
+    lib.csf_decode.argtypes = [ctypes.POINTER(CStack), _c_vp, ctypes.c_size_t, _c_vp, ctypes.c_int, _c_vp]
+    lib.csf_decode.restype = ctypes.c_int
+    lib.csf_decode_pair.argtypes = [ctypes.POINTER(CStack), _c_vp, ctypes.c_size_t,
+                                    ctypes.POINTER(CStack), _c_vp, ctypes.c_size_t,
+                                    _c_vp, ctypes.c_int, _c_vp]
+    lib.csf_decode_pair.restype = ctypes.c_int
+    return lib
+
+
+lib = _load()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise CsfError(f"{what}: {lib.csf_status_string(status).decode()} (status {status})")
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def sizes(kind: int, E: int, R: int, C: int) -> dict:
+    g = Geometry(kind, E, R, C)
+    out = Sizes()
+    _check(lib.csf_sizes(ctypes.byref(g), ctypes.byref(out)), "csf_sizes")
+    return {f: getattr(out, f) for f, _ in Sizes._fields_}
+
+
+def _pad16(n: int) -> int:
+    return max(16, (n + 15) // 16 * 16)
+
+
+@dataclass
+class Stack:
+    """A compressed stack held in device memory (buffers padded as the ABI asks)."""
+    kind: int
+    E: int
+    R: int
+    C: int
+    base: torch.Tensor
+    offsets: torch.Tensor
+    escapes: torch.Tensor | None
+    exc_index: torch.Tensor     # int32 storage of the uint32 index
+    exc_bytes: torch.Tensor
+    num_exc: int
+    error_word: torch.Tensor    # int32[1]
+
+    @property
+    def shape(self):
+        return (self.E, self.R, self.C)
+
+    @property
+    def dense_bytes(self) -> int:
+        return self.E * self.R * self.C
+
+    def stream_bytes(self) -> dict:
+        """Exact byte lengths of the packed streams (without allocation padding)."""
+        n = self.dense_bytes
+        off = (n + 1) // 2 if self.kind == NVFP4 else (n + 7) // 8
+        return {"base": self.E * self.R, "offsets": off,
+                "escapes": 0 if self.kind == NVFP4 else (n + 7) // 8,
+                "exc_index": 4 * (self.E * self.R + 1), "exc_bytes": self.num_exc}
+
+    def cstruct(self) -> CStack:
+        return CStack(Geometry(self.kind, self.E, self.R, self.C), self.base.data_ptr(),
+                      self.offsets.data_ptr(),
+                      self.escapes.data_ptr() if self.escapes is not None else None,
+                      self.exc_index.data_ptr(), self.exc_bytes.data_ptr(), self.num_exc,
+                      self.error_word.data_ptr())
+
+    def errors(self) -> int:
+        """Device error bits (synchronises on the current stream)."""
+        return int(self.error_word.item())
+
+
+def empty_stack(kind: int, E: int, R: int, C: int, exc_capacity: int = 0, device=None) -> Stack:
+    """Allocate the buffers of a stack for a geometry (contents undefined)."""
+    device = torch.device(device if device is not None else "cuda")
+    sz = sizes(kind, E, R, C)
+    u8 = dict(dtype=torch.uint8, device=device)
+    return Stack(kind, E, R, C,
+                 base=torch.empty(_pad16(sz["base"]), **u8),
+                 offsets=torch.empty(sz["offsets"], **u8),
+                 escapes=torch.empty(sz["escapes"], **u8) if kind == MXFP4 else None,
+                 exc_index=torch.empty(E * R + 1, dtype=torch.int32, device=device),
+                 exc_bytes=torch.empty(_pad16(exc_capacity), **u8),
+                 num_exc=0,
+                 error_word=torch.zeros(1, dtype=torch.int32, device=device))
+
+
+def prepare_scratch(kind: int, E: int, R: int, C: int, device=None) -> torch.Tensor:
+    n = sizes(kind, E, R, C)["prepare_scratch"]
+    return torch.empty(_pad16(n), dtype=torch.uint8, device=device if device is not None else "cuda")
+
+
+def prepare_async(dense: torch.Tensor, out: Stack, scratch: torch.Tensor, exc_capacity: int | None = None,
+                  stream=None) -> None:
+    """Launch csf_prepare into `out` (no host sync).  exc_index[rows] holds the
+    exception total when it completes."""
+    if not dense.is_cuda or dense.dtype != torch.uint8 or not dense.is_contiguous():
+        raise CsfError("prepare: dense must be a contiguous uint8 CUDA tensor")
+    if dense.numel() != out.dense_bytes:
+        raise CsfError("prepare: dense size does not match the stack geometry")
+    cap = out.exc_bytes.numel() if exc_capacity is None else exc_capacity
+    cs = out.cstruct()
+    _check(lib.csf_prepare(dense.data_ptr(), ctypes.byref(cs), cap, scratch.data_ptr(), scratch.numel(),
+                           _stream(stream)), "csf_prepare")
+
+
+def prepare(dense: torch.Tensor, kind: int, stream=None) -> Stack:
+    """Encode a dense [E, R, C] uint8 CUDA stack on the GPU.
+
+    One pass over the dense bytes into an exception staging buffer of E*R*C
+    bytes, then one 4-byte device-to-host read of the exception total, then a
+    copy of the exceptions into an exact-size (16-byte padded) buffer.
+    """
+    if dense.dim() != 3:
+        raise CsfError("prepare: dense must be [E, R, C]")
+    E, R, C = (int(x) for x in dense.shape)
+    dev = dense.device
+    st = empty_stack(kind, E, R, C, exc_capacity=E * R * C, device=dev)
+    scratch = prepare_scratch(kind, E, R, C, device=dev)
+    prepare_async(dense, st, scratch, stream=stream)
+    total = int(st.exc_index[E * R].item()) & 0xFFFFFFFF
+    exc = torch.zeros(_pad16(total), dtype=torch.uint8, device=dev)
+    exc[:total].copy_(st.exc_bytes[:total])
+    st.exc_bytes = exc
+    st.num_exc = total
+    return st
+
+
+def upload(enc: dict, device=None) -> Stack:
+    """Copy a host-side encoded stack (numpy arrays: base, offsets, escapes,
+    exc_index, exc_bytes, num_exc, shape, kind) into padded device buffers."""
+    kind = int(enc["kind"])
+    E, R, C = enc["shape"]
+    st = empty_stack(kind, E, R, C, exc_capacity=int(enc["num_exc"]), device=device)
+    st.base.zero_()
+    st.offsets.zero_()
+    st.exc_bytes.zero_()
+    st.base[:E * R].copy_(torch.from_numpy(enc["base"]))
+    st.offsets[:enc["offsets"].size].copy_(torch.from_numpy(enc["offsets"]))
+    if kind == MXFP4:
+        st.escapes.zero_()
+        st.escapes[:enc["escapes"].size].copy_(torch.from_numpy(enc["escapes"]))
+    st.exc_index.copy_(torch.from_numpy(enc["exc_index"].view("int32")))
+    n = int(enc["num_exc"])
+    if n:
+        st.exc_bytes[:n].copy_(torch.from_numpy(enc["exc_bytes"][:n]))
+    st.num_exc = n
+    return st
+
+
+def _es(expert_start):
+    if expert_start is None:
+        return None, 0
+    if not expert_start.is_cuda or expert_start.dtype not in (torch.int32, torch.int64):
+        raise CsfError("expert_start must be an int32 or int64 CUDA tensor")
+    if not expert_start.is_contiguous():
+        raise CsfError("expert_start must be contiguous")
+    return expert_start.data_ptr(), 1 if expert_start.dtype == torch.int64 else 0
+
+
+def _check_es(stack: Stack, expert_start):
+    if expert_start is not None and expert_start.numel() != stack.E + 1:
+        raise CsfError("expert_start must have E+1 entries")
+
+
+def decode(stack: Stack, ws: torch.Tensor | None = None, expert_start: torch.Tensor | None = None,
+           stream=None) -> torch.Tensor:
+    """Decode into `ws` (uint8 CUDA, >= E*R*C bytes, any byte offset).  With
+    `expert_start` only experts with routed tokens are written."""
+    if ws is None:
+        ws = torch.empty(stack.shape, dtype=torch.uint8, device=stack.base.device)
+    if ws.dtype != torch.uint8 or not ws.is_cuda or not ws.is_contiguous():
+        raise CsfError("decode: ws must be a contiguous uint8 CUDA tensor")
+    _check_es(stack, expert_start)
+    ptr, is64 = _es(expert_start)
+    cs = stack.cstruct()
+    _check(lib.csf_decode(ctypes.byref(cs), ws.data_ptr(), ws.numel(), ptr, is64, _stream(stream)),
+           "csf_decode")
+    return ws
+
+
+def decode_pair(gate: Stack, down: Stack, gate_ws: torch.Tensor | None = None,
+                down_ws: torch.Tensor | None = None, expert_start: torch.Tensor | None = None,
+                stream=None):
+    """Decode a gate(/up) and a down stack in one launch with shared routing."""
+    if gate_ws is None:
+        gate_ws = torch.empty(gate.shape, dtype=torch.uint8, device=gate.base.device)
+    if down_ws is None:
+        down_ws = torch.empty(down.shape, dtype=torch.uint8, device=down.base.device)
+    for ws in (gate_ws, down_ws):
+        if ws.dtype != torch.uint8 or not ws.is_cuda or not ws.is_contiguous():
+            raise CsfError("decode_pair: workspaces must be contiguous uint8 CUDA tensors")
+    _check_es(gate, expert_start)
+    ptr, is64 = _es(expert_start)
+    g, d = gate.cstruct(), down.cstruct()
+    _check(lib.csf_decode_pair(ctypes.byref(g), gate_ws.data_ptr(), gate_ws.numel(),
+                               ctypes.byref(d), down_ws.data_ptr(), down_ws.numel(),
+                               ptr, is64, _stream(stream)), "csf_decode_pair")
+    return gate_ws, down_ws

@@ -1,0 +1,272 @@
+// Host side of the CSF C ABI declared in include/csf.h: argument checks,
+// launch configuration and dispatch.  Every step of the codec runs in the
+// kernels of csf_decode.cu and csf_prepare.cu; nothing here touches the data.
+#include <cstring>
+#include <mutex>
+
+#include "csf_internal.cuh"
+
+using namespace csfk;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool init = false;
+    int sms = 0;
+    int occ_full = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+csf_status device_info(DeviceInfo *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.init) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            decode_occupancy(false, 0, &d.occ_full) != cudaSuccess) {
+            cudaGetLastError();
+            return CSF_ERR_CUDA;
+        }
+        if (d.occ_full < 1) d.occ_full = 1;
+        d.init = true;
+    }
+    *out = d;
+    return CSF_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+csf_status geometry(const csf_geometry *g, uint64_t *n, uint64_t *rows) {
+    if (!g) return CSF_ERR_ARG;
+    if (g->kind != CSF_NVFP4 && g->kind != CSF_MXFP4) return CSF_ERR_ARG;
+    if (g->num_experts < 1 || g->rows < 1 || g->cols < 1) return CSF_ERR_ARG;
+    const uint64_t r = (uint64_t)g->num_experts * (uint64_t)g->rows;
+    const uint64_t e = r * (uint64_t)g->cols;
+    if (r >= (1ull << 31) || e >= (1ull << 40) || g->cols >= (1 << 24)) return CSF_ERR_UNSUPPORTED;
+    *n = e;
+    *rows = r;
+    return CSF_OK;
+}
+
+uint64_t round16(uint64_t v) { return (v + 15) & ~15ull; }
+
+uint64_t prepare_scratch_bytes(const csf_geometry *g, uint64_t rows) {
+    const int32_t tr = prepare_tile_rows(g->kind, g->cols);
+    const uint64_t tiles = (rows + tr - 1) / tr;
+    return 16 + 8 * tiles;
+}
+
+int ws_alignment(const void *p) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    if ((a & 31) == 0) return 32;
+    if ((a & 15) == 0) return 16;
+    if ((a & 3) == 0) return 4;
+    return 1;
+}
+
+csf_status fill_stack(const csf_stack *s, uint8_t *ws, size_t ws_bytes, DecStack *d) {
+    if (!s || !ws) return CSF_ERR_ARG;
+    uint64_t n = 0, rows = 0;
+    csf_status st = geometry(&s->g, &n, &rows);
+    if (st != CSF_OK) return st;
+    if (!s->base || !s->offsets || !s->exc_index || !aligned16(s->offsets)) return CSF_ERR_ARG;
+    if (s->g.kind == CSF_MXFP4 && (!s->escapes || !aligned16(s->escapes))) return CSF_ERR_ARG;
+    if (s->num_exc > 0 && !s->exc_bytes) return CSF_ERR_ARG;
+    if (s->num_exc > 0xFFFFFFFFull) return CSF_ERR_ARG;
+    if (ws_bytes < n) return CSF_ERR_SIZE;
+    const int chunk = s->g.kind == CSF_NVFP4 ? kChunkNv : kChunkMx;
+    std::memset(d, 0, sizeof *d);
+    d->base = s->base;
+    d->offsets = s->offsets;
+    d->escapes = s->escapes;
+    d->exc_index = s->exc_index;
+    d->exc_bytes = s->exc_bytes;
+    d->ws = ws;
+    d->err = s->error_word;
+    d->num_exc = s->num_exc;
+    d->rows = rows;
+    d->n = n;
+    d->R = s->g.rows;
+    d->C = s->g.cols;
+    d->kind = s->g.kind;
+    d->rb = unit_rows(s->g.cols, chunk);
+    const uint32_t step_el = 32u * (uint32_t)chunk;
+    d->step_r = step_el / (uint32_t)s->g.cols;
+    d->step_q = step_el % (uint32_t)s->g.cols;
+    d->ws_align = ws_alignment(ws);
+    return CSF_OK;
+}
+
+uint64_t units_full(const DecStack &d) { return (d.rows + d.rb - 1) / d.rb; }
+
+uint64_t units_all_experts(const DecStack &d, int E) {
+    // Upper bound on the units of all experts: each expert can add one
+    // partial unit at each end.
+    return units_full(d) + (uint64_t)E;
+}
+
+csf_status run_decode(const csf_stack *a, uint8_t *wa, size_t wa_bytes, const csf_stack *b, uint8_t *wb,
+                      size_t wb_bytes, const void *expert_start, int es64, void *stream) {
+    DecParams p;
+    std::memset(&p, 0, sizeof p);
+    csf_status st = fill_stack(a, wa, wa_bytes, &p.st[0]);
+    if (st != CSF_OK) return st;
+    p.nstacks = 1;
+    if (b) {
+        st = fill_stack(b, wb, wb_bytes, &p.st[1]);
+        if (st != CSF_OK) return st;
+        if (b->g.num_experts != a->g.num_experts) return CSF_ERR_ARG;
+        p.nstacks = 2;
+    }
+    p.E = a->g.num_experts;
+    p.expert_start = expert_start;
+    p.es64 = es64 ? 1 : 0;
+    const bool routed = expert_start != nullptr;
+    if (routed && p.E > kMaxRoutedExperts) return CSF_ERR_UNSUPPORTED;
+
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != CSF_OK) return st;
+    size_t smem = 0;
+    int occ = di.occ_full;
+    uint64_t units = 0;
+    if (routed) {
+        smem = 4ull * ((uint64_t)p.E + 2ull * ((uint64_t)p.E + 1));
+        if (decode_occupancy(true, smem, &occ) != cudaSuccess) {
+            cudaGetLastError();
+            return CSF_ERR_CUDA;
+        }
+        if (occ < 1) occ = 1;
+        units = units_all_experts(p.st[0], p.E) + (p.nstacks > 1 ? units_all_experts(p.st[1], p.E) : 0);
+    } else {
+        units = units_full(p.st[0]) + (p.nstacks > 1 ? units_full(p.st[1]) : 0);
+    }
+    uint64_t grid = (uint64_t)di.sms * (uint64_t)occ;
+    const uint64_t need = (units + kWarps - 1) / kWarps;
+    if (need < grid) grid = need;
+    if (grid < 1) grid = 1;
+    if (launch_decode(p, (int)grid, smem, routed, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    return CSF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *csf_status_string(csf_status status) {
+    switch (status) {
+    case CSF_OK: return "ok";
+    case CSF_ERR_ARG: return "invalid argument";
+    case CSF_ERR_SIZE: return "buffer too small";
+    case CSF_ERR_UNSUPPORTED: return "unsupported geometry";
+    case CSF_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+int csf_abi_version(void) { return CSF_ABI_VERSION; }
+
+csf_status csf_sizes(const csf_geometry *g, csf_sizes_t *out) {
+    if (!out) return CSF_ERR_ARG;
+    uint64_t n = 0, rows = 0;
+    csf_status st = geometry(g, &n, &rows);
+    if (st != CSF_OK) return st;
+    out->dense = n;
+    out->base = rows;
+    if (g->kind == CSF_NVFP4) {
+        out->offsets = round16((n + 1) / 2);
+        out->escapes = 0;
+    } else {
+        out->offsets = round16((n + 7) / 8);
+        out->escapes = round16((n + 7) / 8);
+    }
+    out->exc_index = 4 * (rows + 1);
+    out->prepare_scratch = prepare_scratch_bytes(g, rows);
+    return CSF_OK;
+}
+
+csf_status csf_prepare(const uint8_t *dense, csf_stack *out, uint64_t exc_capacity, void *scratch,
+                       size_t scratch_bytes, void *stream) {
+    if (!dense || !out || !scratch) return CSF_ERR_ARG;
+    uint64_t n = 0, rows = 0;
+    csf_status st = geometry(&out->g, &n, &rows);
+    if (st != CSF_OK) return st;
+    const csf_geometry &g = out->g;
+    if (!out->base || !out->offsets || !out->exc_index || !aligned16(out->offsets)) return CSF_ERR_ARG;
+    if (g.kind == CSF_MXFP4 && (!out->escapes || !aligned16(out->escapes))) return CSF_ERR_ARG;
+    if (exc_capacity > 0 && !out->exc_bytes) return CSF_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(scratch) & 7u) != 0) return CSF_ERR_ARG;
+    if (g.cols >= 65536) return CSF_ERR_UNSUPPORTED;
+    const int32_t tr = prepare_tile_rows(g.kind, g.cols);
+    const size_t smem = prepare_smem_bytes(g.kind, g.cols, tr);
+    if (smem > 200 * 1024 || (uint64_t)tr * g.cols >= (1ull << 24)) return CSF_ERR_UNSUPPORTED;
+    const uint64_t need = prepare_scratch_bytes(&g, rows);
+    if (scratch_bytes < need) return CSF_ERR_SIZE;
+
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, dense) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_ARG;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return CSF_ERR_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    PrepParams p;
+    std::memset(&p, 0, sizeof p);
+    p.dense = dense;
+    p.base = out->base;
+    p.offsets = out->offsets;
+    p.escapes = out->escapes;
+    p.exc_index = out->exc_index;
+    p.exc_bytes = out->exc_bytes;
+    p.err = out->error_word;
+    p.ticket = static_cast<unsigned int *>(scratch);
+    p.status = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(scratch) + 16);
+    p.exc_capacity = exc_capacity;
+    p.rows = rows;
+    p.n = n;
+    p.num_tiles = (rows + tr - 1) / tr;
+    p.magic = ((1ull << 40) + (uint64_t)g.cols - 1) / (uint64_t)g.cols;
+    p.C = g.cols;
+    p.kind = g.kind;
+    p.tr = tr;
+    p.dense_aligned = aligned16(dense) ? 1 : 0;
+    const uint64_t te = (uint64_t)tr * g.cols;
+    p.smem_dense = (uint32_t)round16(te);
+    p.smem_planes = (uint32_t)(g.kind == CSF_NVFP4 ? round16((te + 1) / 2) : 2 * round16((te + 7) / 8));
+    if (launch_prepare(p, smem, s) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    return CSF_OK;
+}
+
+csf_status csf_decode(const csf_stack *s, uint8_t *ws, size_t ws_bytes, const void *expert_start,
+                      int expert_start_is_int64, void *stream) {
+    return run_decode(s, ws, ws_bytes, nullptr, nullptr, 0, expert_start, expert_start_is_int64, stream);
+}
+
+csf_status csf_decode_pair(const csf_stack *gate, uint8_t *gate_ws, size_t gate_ws_bytes, const csf_stack *down,
+                           uint8_t *down_ws, size_t down_ws_bytes, const void *expert_start,
+                           int expert_start_is_int64, void *stream) {
+    if (!down) return CSF_ERR_ARG;
+    return run_decode(gate, gate_ws, gate_ws_bytes, down, down_ws, down_ws_bytes, expert_start,
+                      expert_start_is_int64, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,90 @@
+// Internal declarations shared by the CSF library's translation units.
+// Nothing here is part of the C ABI (include/csf.h is).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "csf.h"
+
+namespace csfk {
+
+constexpr int kThreads = 256;               // threads per block, every kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxRoutedExperts = 8192;     // routed decode keeps the active list in smem
+
+// NVFP4 chunk: 16 packed offset bytes = 32 elements.  MXFP4 chunk: 16 bytes of
+// each bit plane = 128 elements.  Decode work starts on chunk boundaries.
+constexpr int kChunkNv = 32;
+constexpr int kChunkMx = 128;
+
+// One stack as the decode kernel sees it.
+struct DecStack {
+    const uint8_t *base;
+    const uint8_t *offsets;
+    const uint8_t *escapes;
+    const uint32_t *exc_index;
+    const uint8_t *exc_bytes;
+    uint8_t *ws;
+    uint32_t *err;        // may be null
+    uint64_t num_exc;
+    uint64_t rows;        // E*R
+    uint64_t n;           // E*R*C
+    int32_t R;
+    int32_t C;
+    int32_t kind;
+    int32_t rb;           // rows per work unit: smallest count whose elements fill whole chunks
+    uint32_t step_r;      // (32 chunks of elements) / C
+    uint32_t step_q;      // (32 chunks of elements) % C
+    int32_t ws_align;     // alignment of ws in bytes (32, 16, 8, 4 or 1)
+    int32_t pad_;
+};
+
+struct DecParams {
+    DecStack st[2];
+    int32_t nstacks;
+    int32_t E;
+    const void *expert_start;   // null: whole stacks
+    int32_t es64;
+    int32_t pad_;
+};
+
+struct PrepParams {
+    const uint8_t *dense;
+    uint8_t *base;
+    uint8_t *offsets;
+    uint8_t *escapes;
+    uint32_t *exc_index;
+    uint8_t *exc_bytes;
+    uint32_t *err;               // may be null
+    unsigned int *ticket;        // scratch: tile ticket counter (zeroed)
+    unsigned long long *status;  // scratch: one look-back word per tile (zeroed)
+    uint64_t exc_capacity;
+    uint64_t rows;
+    uint64_t n;
+    uint64_t num_tiles;
+    uint64_t magic;              // ceil(2^40 / C): tile-local element -> row
+    int32_t C;
+    int32_t kind;
+    int32_t tr;                  // rows per tile
+    int32_t dense_aligned;       // dense pointer is 16-byte aligned
+    uint32_t smem_dense;         // byte sizes of the dynamic smem regions
+    uint32_t smem_planes;
+};
+
+// Rows per unit so that a unit's first element starts a whole chunk.
+inline int32_t unit_rows(int32_t C, int chunk) {
+    int32_t g = C;
+    int32_t a = chunk;
+    while (a) { int32_t t = g % a; g = a; a = t; }   // gcd(C, chunk)
+    return chunk / g;
+}
+
+cudaError_t launch_decode(const DecParams &p, int grid, size_t smem, bool routed, cudaStream_t s);
+cudaError_t decode_occupancy(bool routed, size_t smem, int *blocks_per_sm);
+
+cudaError_t launch_prepare(const PrepParams &p, size_t smem, cudaStream_t s);
+size_t prepare_smem_bytes(int32_t kind, int32_t C, int32_t tr);
+int32_t prepare_tile_rows(int32_t kind, int32_t C);
+
+}  // namespace csfk

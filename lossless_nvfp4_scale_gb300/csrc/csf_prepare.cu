@@ -1,0 +1,379 @@
+// CSF prepare kernel for sm_103a: encodes a dense stack (base byte per row,
+// offset / escape planes, exception index, exception stream) in one pass over
+// the dense bytes.
+//
+// Pages followed (cited by title and paragraph; no numbered sections):
+//   "finegrained-kernels: decode losslessly compressed NVFP4 scales (CSF)":
+//     format paragraph (base byte per row, most scales as 4-bit offsets,
+//     out-of-range values in an exception stream); helpers paragraph
+//     (preparation keeps the input device).
+//   "Load native FP4 experts with optional lossless CSF scales": encoding plus
+//     exception index built on the GPU at preparation time.
+//   "NVFP4-CSF: expand_scales() for ahead-of-call scale expansion (canonical
+//     twin of #477)": commit message on one-bit MXFP4 and four-bit NVFP4
+//     offsets from a row base byte.
+//
+// Base rule (the pages do not give one; plainest reading that minimises the
+// exception stream): the smallest byte value present in the row whose window
+// [v, v+w] (w = 14 NVFP4, 1 MXFP4) holds the most of the row's bytes.
+//
+// Per block = one tile of `tr` rows (a whole number of chunk-aligned row
+// groups, so output planes start on 16-byte boundaries):
+//   1. stage the tile's dense bytes in shared memory (one HBM read);
+//   2. one warp per row: 256-bin histogram in shared memory, window counts
+//      (prefix sums for NVFP4, neighbour sums for MXFP4), warp max-reduce of
+//      (count, -value) picks the base; the row's exception count is C minus
+//      the winning window count;
+//   3. all threads pack offset nibbles / bit planes from the staged bytes;
+//   4. block scan of the per-row counts; the tile total is chained to earlier
+//      tiles by a decoupled look-back (Merrill & Garland, "Single-pass
+//      Parallel Prefix Scan with Decoupled Look-back", 2016) over per-tile
+//      status words in caller scratch; tiles take ids from a ticket counter in
+//      start order, so a block only waits on blocks already running; every
+//      wait is bounded and reports CSF_DEV_ERR_TIMEOUT instead of hanging;
+//   5. write base bytes, planes, exc_index and the exception bytes at their
+//      global positions.
+#include "csf_internal.cuh"
+
+namespace csfk {
+namespace {
+
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+constexpr unsigned long long kFlagAgg = 1ull << 62;
+constexpr unsigned long long kFlagIncl = 2ull << 62;
+constexpr unsigned long long kValMask = (1ull << 62) - 1;
+constexpr int kSpinLimit = 1 << 22;   // polls before a look-back wait gives up
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, int lane, uint32_t &total) {
+    uint32_t x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        uint32_t y = __shfl_up_sync(kFull, x, d);
+        if (lane >= d) x += y;
+    }
+    total = __shfl_sync(kFull, x, 31);
+    return x - v;
+}
+
+__device__ __forceinline__ unsigned long long warp_sum64(unsigned long long v) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void flag(uint32_t *err, uint32_t bits) {
+    if (err) atomicOr(err, bits);
+}
+
+__global__ void __launch_bounds__(kThreads) prepare_kernel(const __grid_constant__ PrepParams P) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ unsigned int s_tile;
+    __shared__ unsigned long long s_excl;
+    __shared__ uint32_t s_wsum[kWarps];
+    __shared__ uint32_t s_total;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int tr = P.tr;
+    const uint32_t C = (uint32_t)P.C;
+    const bool nv = P.kind == CSF_NVFP4;
+    const int wwin = nv ? 14 : 1;
+
+    uint8_t *s_dense = smem;
+    uint8_t *s_planes = smem + P.smem_dense;
+    uint32_t *s_hist = reinterpret_cast<uint32_t *>(s_planes + P.smem_planes);
+    uint32_t *s_cnt = s_hist + kWarps * 256;
+    uint8_t *s_base = reinterpret_cast<uint8_t *>(s_cnt + tr);
+
+    if (tid == 0) s_tile = atomicAdd(P.ticket, 1u);
+    __syncthreads();
+    const uint64_t tile = s_tile;
+    if (tile >= P.num_tiles) return;   // grid == num_tiles, so every ticket is a tile
+    const uint64_t r0 = tile * (uint64_t)tr;
+    const uint64_t r1 = min(r0 + (uint64_t)tr, P.rows);
+    const int nr = (int)(r1 - r0);
+    const uint64_t e0 = r0 * C;
+    const uint32_t ne = (uint32_t)nr * C;
+
+    // 1. Stage the tile's dense bytes.
+    {
+        const uint8_t *src = P.dense + e0;
+        uint32_t done = 0;
+        if (P.dense_aligned) {
+            const uint32_t n16 = ne / 16;
+            for (uint32_t i = tid; i < n16; i += kThreads)
+                reinterpret_cast<uint4 *>(s_dense)[i] = __ldg(reinterpret_cast<const uint4 *>(src) + i);
+            done = n16 * 16;
+        }
+        for (uint32_t i = done + tid; i < ne; i += kThreads) s_dense[i] = __ldg(src + i);
+    }
+    __syncthreads();
+
+    // 2. Base byte and exception count of each row (one warp per row).
+    uint32_t *hist = s_hist + warp * 256;
+    for (int k = warp; k < nr; k += kWarps) {
+        const uint8_t *x = s_dense + (uint32_t)k * C;
+        reinterpret_cast<uint4 *>(hist)[2 * lane] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4 *>(hist)[2 * lane + 1] = make_uint4(0, 0, 0, 0);
+        __syncwarp();
+        for (uint32_t c = lane; c < C; c += 32) atomicAdd(&hist[x[c]], 1u);
+        __syncwarp();
+        uint32_t h[8];
+        {
+            const uint4 a = reinterpret_cast<const uint4 *>(hist)[2 * lane];
+            const uint4 b = reinterpret_cast<const uint4 *>(hist)[2 * lane + 1];
+            h[0] = a.x; h[1] = a.y; h[2] = a.z; h[3] = a.w;
+            h[4] = b.x; h[5] = b.y; h[6] = b.z; h[7] = b.w;
+        }
+        uint32_t key = 0;
+        if (nv) {
+            // Inclusive prefix over the 256 bins; window count of v is
+            // P[min(v+14, 255)] - P[v] + h[v].
+            uint32_t pre[8];
+            uint32_t run = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) { run += h[j]; pre[j] = run; }
+            uint32_t tot;
+            const uint32_t ex = warp_excl_scan(run, lane, tot);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) pre[j] += ex;
+            __syncwarp();
+            reinterpret_cast<uint4 *>(hist)[2 * lane] = make_uint4(pre[0], pre[1], pre[2], pre[3]);
+            reinterpret_cast<uint4 *>(hist)[2 * lane + 1] = make_uint4(pre[4], pre[5], pre[6], pre[7]);
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t v = 8u * lane + j;
+                const uint32_t top = min(v + 14u, 255u);
+                const uint32_t wcount = hist[top] - (pre[j] - h[j]);
+                if (h[j]) key = max(key, (wcount << 8) | (255u - v));
+            }
+        } else {
+            uint32_t nxt = __shfl_down_sync(kFull, h[0], 1);
+            if (lane == 31) nxt = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t v = 8u * lane + j;
+                const uint32_t wcount = h[j] + (j < 7 ? h[j + 1] : nxt);
+                if (h[j]) key = max(key, (wcount << 8) | (255u - v));
+            }
+        }
+        key = __reduce_max_sync(kFull, key);
+        if (lane == 0) {
+            s_base[k] = (uint8_t)(255u - (key & 0xFFu));
+            s_cnt[k] = C - (key >> 8);
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // 3. Pack the planes of the tile (pad bits past the stack end are 0).
+    if (nv) {
+        const uint32_t nbytes = ((ne + 1) / 2 + 15) & ~15u;
+        for (uint32_t wi = tid; wi < nbytes / 4; wi += kThreads) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t el = wi * 8 + j;
+                if (el < ne) {
+                    const uint32_t row = (uint32_t)(((uint64_t)el * P.magic) >> 40);
+                    const uint32_t b = s_base[row];
+                    const uint32_t xv = s_dense[el];
+                    const uint32_t d = xv - b;
+                    const uint32_t nib = (xv >= b && d <= 14u) ? d : 15u;
+                    word |= nib << (4 * j);
+                }
+            }
+            reinterpret_cast<uint32_t *>(s_planes)[wi] = word;
+        }
+    } else {
+        const uint32_t nbytes = ((ne + 7) / 8 + 15) & ~15u;
+        uint32_t *po = reinterpret_cast<uint32_t *>(s_planes);
+        uint32_t *pe = reinterpret_cast<uint32_t *>(s_planes + nbytes);
+        for (uint32_t wi = tid; wi < nbytes / 4; wi += kThreads) {
+            uint32_t ow = 0, xw = 0;
+            const uint32_t el0 = wi * 32;
+            if (el0 < ne) {
+                uint32_t row = (uint32_t)(((uint64_t)el0 * P.magic) >> 40);
+                uint32_t next = (row + 1) * C;
+                uint32_t b = s_base[row];
+#pragma unroll 4
+                for (int j = 0; j < 32; ++j) {
+                    const uint32_t el = el0 + j;
+                    if (el < ne) {
+                        if (el == next) { ++row; next += C; b = s_base[row]; }
+                        const uint32_t xv = s_dense[el];
+                        const uint32_t d = xv - b;
+                        const bool inside = xv >= b && d <= 1u;
+                        ow |= (inside ? d : 0u) << j;
+                        xw |= (inside ? 0u : 1u) << j;
+                    }
+                }
+            }
+            po[wi] = ow;
+            pe[wi] = xw;
+        }
+    }
+
+    // 4a. Block-wide exclusive scan of the per-row counts (in place).
+    const int per = (nr + kThreads - 1) / kThreads;
+    const int k0 = min(tid * per, nr);
+    const int k1 = min(k0 + per, nr);
+    uint32_t local = 0;
+    for (int k = k0; k < k1; ++k) local += s_cnt[k];
+    uint32_t wtot;
+    const uint32_t wex = warp_excl_scan(local, lane, wtot);
+    if (lane == 0) s_wsum[warp] = wtot;
+    __syncthreads();
+    uint32_t boff = 0, btot = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        if (w < warp) boff += s_wsum[w];
+        btot += s_wsum[w];
+    }
+    {
+        uint32_t run = boff + wex;
+        for (int k = k0; k < k1; ++k) {
+            const uint32_t c = s_cnt[k];
+            s_cnt[k] = run;
+            run += c;
+        }
+    }
+    if (tid == 0) s_total = btot;
+
+    // 4b. Decoupled look-back across tiles (warp 0).
+    if (warp == 0) {
+        const unsigned long long total = btot;
+        unsigned long long excl = 0;
+        bool timed_out = false;
+        if (lane == 0) st_release(&P.status[tile], (tile == 0 ? kFlagIncl : kFlagAgg) | total);
+        if (tile > 0) {
+            long long j = (long long)tile - 1;
+            while (true) {
+                const long long idx = j - lane;
+                unsigned long long v = kFlagIncl;   // before tile 0: inclusive zero
+                if (idx >= 0) {
+                    v = ld_acquire(&P.status[idx]);
+                    int spins = 0;
+                    while ((v >> 62) == 0) {
+                        if (++spins > kSpinLimit) { timed_out = true; v = kFlagAgg; break; }
+                        __nanosleep(64);
+                        v = ld_acquire(&P.status[idx]);
+                    }
+                }
+                const uint32_t incl = __ballot_sync(kFull, (v >> 62) == 2);
+                unsigned long long val = v & kValMask;
+                if (incl) {
+                    const int first = __ffs(incl) - 1;
+                    if (lane > first) val = 0;
+                    excl += warp_sum64(val);
+                    break;
+                }
+                excl += warp_sum64(val);
+                j -= 32;
+            }
+            if (lane == 0) st_release(&P.status[tile], kFlagIncl | (excl + total));
+        }
+        if (__any_sync(kFull, timed_out) && lane == 0) flag(P.err, CSF_DEV_ERR_TIMEOUT);
+        if (lane == 0) s_excl = excl;
+    }
+    __syncthreads();
+    const unsigned long long excl = s_excl;
+
+    // 5. Outputs.
+    for (int k = tid; k < nr; k += kThreads) {
+        const unsigned long long v = excl + s_cnt[k];
+        P.exc_index[r0 + k] = (uint32_t)v;
+        P.base[r0 + k] = s_base[k];
+    }
+    if (tile == P.num_tiles - 1 && tid == 0) {
+        const unsigned long long all = excl + s_total;
+        P.exc_index[P.rows] = (uint32_t)all;
+        if (all > 0xFFFFFFFFull) flag(P.err, CSF_DEV_ERR_CAPACITY);
+    }
+    if (nv) {
+        const uint32_t nbytes = ((ne + 1) / 2 + 15) & ~15u;
+        uint4 *dst = reinterpret_cast<uint4 *>(P.offsets + e0 / 2);
+        for (uint32_t i = tid; i < nbytes / 16; i += kThreads) dst[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
+    } else {
+        const uint32_t nbytes = ((ne + 7) / 8 + 15) & ~15u;
+        uint4 *dso = reinterpret_cast<uint4 *>(P.offsets + e0 / 8);
+        uint4 *dse = reinterpret_cast<uint4 *>(P.escapes + e0 / 8);
+        for (uint32_t i = tid; i < nbytes / 16; i += kThreads) {
+            dso[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
+            dse[i] = reinterpret_cast<const uint4 *>(s_planes + nbytes)[i];
+        }
+    }
+    // Exception bytes, row-major, at excl + row prefix + rank in row.
+    bool over = false;
+    for (int k = warp; k < nr; k += kWarps) {
+        const uint8_t *x = s_dense + (uint32_t)k * C;
+        const uint32_t b = s_base[k];
+        unsigned long long run = excl + s_cnt[k];
+        for (uint32_t c0 = 0; c0 < C; c0 += 32) {
+            const uint32_t c = c0 + lane;
+            bool esc = false;
+            uint32_t xv = 0;
+            if (c < C) {
+                xv = x[c];
+                const uint32_t d = xv - b;
+                esc = !(xv >= b && d <= (uint32_t)wwin);
+            }
+            const uint32_t bal = __ballot_sync(kFull, esc);
+            if (esc) {
+                const unsigned long long pos = run + __popc(bal & lanemask_lt());
+                if (pos < P.exc_capacity) P.exc_bytes[pos] = (uint8_t)xv;
+                else over = true;
+            }
+            run += __popc(bal);
+        }
+    }
+    if (__any_sync(kFull, over) && lane == 0) flag(P.err, CSF_DEV_ERR_CAPACITY);
+}
+
+}  // namespace
+
+int32_t prepare_tile_rows(int32_t kind, int32_t C) {
+    const int32_t rbp = unit_rows(C, kind == CSF_NVFP4 ? kChunkNv : kChunkMx);
+    const int64_t per = (int64_t)rbp * C;
+    int64_t k = 16384 / per;
+    if (k < 1) k = 1;
+    return (int32_t)(k * rbp);
+}
+
+static uint32_t round16(uint64_t v) { return (uint32_t)((v + 15) & ~15ull); }
+
+size_t prepare_smem_bytes(int32_t kind, int32_t C, int32_t tr) {
+    const uint64_t te = (uint64_t)tr * C;
+    const uint32_t dense = round16(te);
+    const uint32_t planes = kind == CSF_NVFP4 ? round16((te + 1) / 2) : 2 * round16((te + 7) / 8);
+    return (size_t)dense + planes + kWarps * 256 * 4 + (size_t)tr * 4 + round16(tr);
+}
+
+cudaError_t launch_prepare(const PrepParams &p, size_t smem, cudaStream_t s) {
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    prepare_kernel<<<(unsigned)p.num_tiles, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace csfk

@@ -1,0 +1,84 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every function
+include/csf.h declares, and its host-only paths (sizes, argument checks that
+return before any CUDA call) behave as documented.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from lossless_nvfp4_scale_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def csf():
+    build.ensure_built()
+    from lossless_nvfp4_scale_gb300 import csf as mod
+    return mod
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "csf.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(csf_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(csf):
+    names = declared_functions()
+    assert {"csf_prepare", "csf_decode", "csf_decode_pair", "csf_sizes"} <= set(names)
+    lib = ctypes.CDLL(build.LIB)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/csf.h but not exported"
+
+
+def test_abi_version_and_status_strings(csf):
+    assert csf.lib.csf_abi_version() == 1
+    for code, text in [(0, "ok"), (1, "invalid argument"), (2, "buffer too small"),
+                       (3, "unsupported geometry"), (4, "CUDA error")]:
+        assert csf.lib.csf_status_string(code).decode() == text
+
+
+@pytest.mark.parametrize("kind,E,R,C", [(0, 512, 1024, 100), (0, 512, 2048, 50), (1, 384, 2048, 160),
+                                        (0, 1, 1, 1), (1, 3, 5, 7)])
+def test_sizes(csf, kind, E, R, C):
+    sz = csf.sizes(kind, E, R, C)
+    n = E * R * C
+    assert sz["dense"] == n and sz["base"] == E * R and sz["exc_index"] == 4 * (E * R + 1)
+    packed = (n + 1) // 2 if kind == 0 else (n + 7) // 8
+    assert sz["offsets"] == (packed + 15) // 16 * 16
+    assert sz["escapes"] == (0 if kind == 0 else sz["offsets"])
+    assert sz["prepare_scratch"] >= 16 + 8
+
+
+def test_sizes_rejects_bad_geometry(csf):
+    with pytest.raises(csf.CsfError, match="invalid argument"):
+        csf.sizes(2, 1, 1, 1)
+    with pytest.raises(csf.CsfError, match="invalid argument"):
+        csf.sizes(0, 0, 1, 1)
+    with pytest.raises(csf.CsfError, match="unsupported"):
+        csf.sizes(0, 1 << 16, 1 << 16, 1)
+
+
+def test_null_arguments_rejected_before_cuda(csf):
+    # All of these return before the library touches the CUDA runtime.
+    assert csf.lib.csf_decode(None, None, 0, None, 0, None) == 1
+    assert csf.lib.csf_decode_pair(None, None, 0, None, None, 0, None, 0, None) == 1
+    assert csf.lib.csf_prepare(None, None, 0, None, 0, None) == 1
+    g = csf.Geometry(0, 1, 1, 32)
+    st = csf.CStack(g, 16, 16, None, 16, 16, 0, None)
+    # ws too small for the geometry.
+    assert csf.lib.csf_decode(ctypes.byref(st), 16, 31, None, 0, None) == 2
+    # offsets not 16-byte aligned.
+    st_bad = csf.CStack(g, 16, 17, None, 16, 16, 0, None)
+    assert csf.lib.csf_decode(ctypes.byref(st_bad), 16, 64, None, 0, None) == 1
+    # MXFP4 without an escape plane.
+    st_mx = csf.CStack(csf.Geometry(1, 1, 1, 32), 16, 16, None, 16, 16, 0, None)
+    assert csf.lib.csf_decode(ctypes.byref(st_mx), 16, 64, None, 0, None) == 1
+    # pair with different expert counts.
+    st2 = csf.CStack(csf.Geometry(0, 2, 1, 32), 16, 16, None, 16, 16, 0, None)
+    assert csf.lib.csf_decode_pair(ctypes.byref(st), 16, 64, ctypes.byref(st2), 16, 64, None, 0, None) == 1
+    # routed decode with too many experts for the shared-memory active list.
+    big = csf.CStack(csf.Geometry(0, 8193, 1, 32), 16, 16, None, 16, 16, 0, None)
+    assert csf.lib.csf_decode(ctypes.byref(big), 16, 8193 * 32, 16, 0, None) == 3
