@@ -1,0 +1,419 @@
+"""Benchmark: CSF decode of a 512-expert NVFP4 scale stack on GB300.
+
+One step = one full-stack decode (the whole hot path of a decode call:
+expert gating, fixed-stream expand, exception pass, stores) of the
+512 x 1024 x 100 gate stack (52.43 MB of dense UE4M3 scale bytes), through the
+C ABI.  `value` = dense-scale GB/s, whole job (all ranks).  Also measured in
+the same run (the "rows" object): routed 8-of-512 decode, paired gate+down
+decode (full and routed), GPU prepare of the gate stack, and MXFP4 prepare and
+decode (384 x 2048 x 160).
+
+Timing: every step is bracketed by CUDA events on the launching stream; steps
+are queued behind a device-side sleep so the stream never waits for the host;
+the stack and workspace rotate over 4 copies (328 MB > 129 MB L2), so every
+step reads and writes HBM.  nvidia-smi samples clocks during the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun every rank decodes its own stack (weak scaling, no collective
+on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSF decode µs & dense-scale GB/s per 512-expert stack; % of HBM roofline"
+WORKLOAD = "gate 512x1024x100 NVFP4-CSF full-stack decode"
+FALLBACK_HBM_GBS = 6800.0
+QUEUE = 192          # steps queued behind one device sleep
+ROTATE = 4           # stack/workspace copies (working set > L2)
+
+
+def peak_hbm():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def timed_steps(torch, fn, steps, warmup):
+    """Run `fn(i)` for warmup + steps iterations; returns per-step device ms
+    for the timed steps.  Each block of QUEUE steps is queued behind a device
+    sleep so the events bracket only device work."""
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    durs = []
+    done = 0
+    while done < steps:
+        n = min(QUEUE, steps - done)
+        torch.cuda._sleep(40_000_000)     # ~20 ms: the host queues the block meanwhile
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        ev[0].record()
+        for j in range(n):
+            fn(warmup + done + j)
+            ev[j + 1].record()
+        torch.cuda.synchronize()
+        durs += [ev[j].elapsed_time(ev[j + 1]) for j in range(n)]
+        done += n
+    return durs
+
+
+def stack_traffic(st, rows_active=None):
+    """Algorithmic bytes of one decode: packed streams read + dense written.
+    Routed: only the active experts' share (their index entries are 8 bytes a
+    warp segment and are not counted)."""
+    sb = st.stream_bytes()
+    total_rows = st.E * st.R
+    frac = 1.0 if rows_active is None else rows_active / total_rows
+    read = (sb["offsets"] + sb["escapes"] + sb["base"]) * frac
+    exc = sb["exc_bytes"] * frac
+    return read + exc + st.dense_bytes * frac
+
+
+def run_own(args, rank, world, torch, dist):
+    from lossless_nvfp4_scale_gb300 import build as b, synth
+    b.ensure_built()
+    from lossless_nvfp4_scale_gb300 import csf
+
+    dev = torch.cuda.current_device()
+    hbm, peak_kind = peak_hbm()
+    seed = rank
+
+    # ---- headline: full gate decode -------------------------------------
+    gate_dense = torch.from_numpy(synth.gate_stack(seed=seed)).cuda()
+    gate = csf.prepare(gate_dense, csf.NVFP4)
+    copies = [gate] + [clone_stack(torch, gate) for _ in range(ROTATE - 1)]
+    wss = [torch.empty_like(gate_dense) for _ in range(ROTATE)]
+
+    def step(i):
+        k = i % ROTATE
+        csf.decode(copies[k], wss[k])
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        t0 = time.perf_counter()
+        durs = timed_steps(torch, step, args.steps, args.warmup)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    assert torch.equal(wss[0], gate_dense), "decode output differs from the dense stack"
+    assert gate.errors() == 0
+    total_ms = sum(durs)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    dense_gb = gate.dense_bytes / 1e9
+    value = world * dense_gb * args.steps / (total_ms / 1e3)
+    alg = stack_traffic(gate)
+    mean_ms = statistics.mean(durs)
+    achieved = alg / (mean_ms / 1e3) / 1e9
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded gate-shaped stack; the pages' checkpoint streams are not available)",
+        "config": {"workload": WORKLOAD, "experts": 512, "rows": 1024, "cols": 100,
+                   "dense_bytes": gate.dense_bytes, "exceptions": gate.num_exc,
+                   "l2": f"inputs rotate over {ROTATE} stack+workspace copies "
+                         f"({ROTATE * alg / 1e6:.0f} MB > 129 MB L2)",
+                   "parallelism": f"replicas x{world} (independent stacks, no collective)"},
+        "us_per_stack": round(1e3 * ms_per_step, 3),
+        "us_per_stack_median": round(1e3 * statistics.median(durs), 3),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_source": peak_kind,
+                     "traffic": profiled_traffic(), "algorithmic_bytes": int(alg)},
+        "gpu_launches": args.steps,
+        "wall_s": round(wall, 3),
+    }
+    result["clocks"] = clk.summary()
+    if rank == 0 and not args.skip_rows:
+        result["rows"] = measure_rows(torch, csf, synth, gate, gate_dense, hbm)
+    if rank == 0:
+        result["e2e"] = measure_e2e(torch, csf, gate, gate_dense)
+        if not args.skip_cpu:
+            result["cpu_baseline"] = cpu_baseline(synth)
+    return result
+
+
+def clone_stack(torch, st):
+    import copy
+    c = copy.copy(st)
+    c.base, c.offsets, c.exc_index, c.exc_bytes = (t.clone() for t in (st.base, st.offsets, st.exc_index, st.exc_bytes))
+    if st.escapes is not None:
+        c.escapes = st.escapes.clone()
+    c.error_word = torch.zeros_like(st.error_word)
+    return c
+
+
+def profiled_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source (else null)."""
+    import hashlib
+    try:
+        src = open(os.path.join(ROOT, "lossless_nvfp4_scale_gb300", "csrc", "csf_decode.cu"), "rb").read()
+        digest = hashlib.sha256(src).hexdigest()[:16]
+        info = {}
+        with open(os.path.join(ROOT, "profiles", "decode_gate_512x1024x100.md")) as f:
+            for ln in f:
+                if ":" in ln and ln.startswith("- "):
+                    k, v = ln[2:].split(":", 1)
+                    info[k.strip()] = v.strip().strip("`")
+        if info.get("csf_decode.cu sha256[:16]") == digest:
+            return float(info["dram bytes per launch"])
+    except Exception:
+        pass
+    return None
+
+
+def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
+    rows = {}
+    E = 512
+    start = torch.from_numpy(synth.routing(E=E, active=8, tokens=64, seed=0)).cuda()
+    active = int((start[1:] > start[:-1]).sum().item())
+    ws = torch.full_like(gate_dense, 0xFF)
+
+    def rec(name, durs, alg, extra=None):
+        m = statistics.mean(durs)
+        d = {"us": round(1e3 * m, 3), "us_median": round(1e3 * statistics.median(durs), 3),
+             "algorithmic_MB": round(alg / 1e6, 3), "GB_s": round(alg / (m / 1e3) / 1e9, 1),
+             "hbm_frac": round(alg / (m / 1e3) / 1e9 / hbm, 4)}
+        if extra:
+            d.update(extra)
+        rows[name] = d
+
+    # routed 8 of 512 (latency-bound: report next to an empty-launch floor)
+    durs = timed_steps(torch, lambda i: csf.decode(gate, ws, expert_start=start), 400, 20)
+    rec("routed_8of512", durs, stack_traffic(gate, rows_active=active * 1024))
+    z = torch.zeros(1, device="cuda")
+    floor = timed_steps(torch, lambda i: z.add_(1), 400, 20)
+    rows["routed_8of512"]["empty_launch_floor_us"] = round(1e3 * statistics.mean(floor), 3)
+
+    # paired gate + down
+    down_dense = torch.from_numpy(synth.down_stack(seed=0)).cuda()
+    down = csf.prepare(down_dense, csf.NVFP4)
+    gws, dws = torch.empty_like(gate_dense), torch.empty_like(down_dense)
+    g2, d2 = clone_stack(torch, gate), clone_stack(torch, down)
+    gws2, dws2 = torch.empty_like(gate_dense), torch.empty_like(down_dense)
+    pairs = [(gate, down, gws, dws), (g2, d2, gws2, dws2)]
+    durs = timed_steps(torch, lambda i: csf.decode_pair(*pairs[i % 2]), 200, 10)
+    assert torch.equal(gws, gate_dense) and torch.equal(dws, down_dense)
+    rec("pair_full", durs, stack_traffic(gate) + stack_traffic(down))
+    durs = timed_steps(torch, lambda i: csf.decode_pair(gate, down, gws, dws, expert_start=start), 400, 20)
+    rec("pair_routed_8of512", durs,
+        stack_traffic(gate, rows_active=active * 1024) + stack_traffic(down, rows_active=active * 2048))
+    del g2, d2, gws2, dws2, pairs
+
+    # GPU prepare of the gate stack (reads dense once, writes the streams)
+    E_, R_, C_ = gate.shape
+    pst = csf.empty_stack(csf.NVFP4, E_, R_, C_, exc_capacity=gate.dense_bytes)
+    scr = csf.prepare_scratch(csf.NVFP4, E_, R_, C_)
+    durs = timed_steps(torch, lambda i: csf.prepare_async(gate_dense, pst, scr), 100, 5)
+    sb = gate.stream_bytes()
+    rec("prepare_gate", durs, gate.dense_bytes + sb["offsets"] + sb["base"] + sb["exc_index"] + sb["exc_bytes"])
+    del pst, scr
+
+    # MXFP4: prepare + decode
+    mx_dense = torch.from_numpy(synth.mxfp4_stack(seed=0)).cuda()
+    mx = csf.prepare(mx_dense, csf.MXFP4)
+    E_, R_, C_ = mx.shape
+    pst = csf.empty_stack(csf.MXFP4, E_, R_, C_, exc_capacity=mx.dense_bytes)
+    scr = csf.prepare_scratch(csf.MXFP4, E_, R_, C_)
+    durs = timed_steps(torch, lambda i: csf.prepare_async(mx_dense, pst, scr), 50, 5)
+    sb = mx.stream_bytes()
+    rec("prepare_mxfp4", durs, mx.dense_bytes + sb["offsets"] + sb["escapes"] + sb["base"] + sb["exc_index"]
+        + sb["exc_bytes"], {"exception_rate": round(mx.num_exc / mx.dense_bytes, 4)})
+    del pst, scr
+    mx2 = clone_stack(torch, mx)
+    mws = [torch.empty_like(mx_dense), torch.empty_like(mx_dense)]
+    mcs = [mx, mx2]
+    durs = timed_steps(torch, lambda i: csf.decode(mcs[i % 2], mws[i % 2]), 100, 5)
+    assert torch.equal(mws[0], mx_dense)
+    rec("decode_mxfp4", durs, stack_traffic(mx))
+    return rows
+
+
+def measure_e2e(torch, csf, gate, gate_dense, steps=10):
+    """Same metric end to end through the public API with HOST buffers:
+    pinned host compressed stack -> device, decode, dense -> pinned host."""
+    import copy
+    host = {}
+    for name in ("base", "offsets", "exc_index", "exc_bytes"):
+        t = getattr(gate, name)
+        host[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        host[name].copy_(t)
+    dev = copy.copy(gate)
+    for name in host:
+        setattr(dev, name, torch.empty_like(getattr(gate, name)))
+    out_host = torch.empty(gate_dense.shape, dtype=torch.uint8, pin_memory=True)
+    ws = torch.empty_like(gate_dense)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    times = []
+    for i in range(steps + 2):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for name, t in host.items():
+            getattr(dev, name).copy_(t, non_blocking=True)
+        csf.decode(dev, ws)
+        out_host.copy_(ws, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= 2:
+            times.append(time.perf_counter() - t0)
+    assert torch.equal(out_host, gate_dense.cpu())
+    t = statistics.median(times)
+    return {"value": round(gate.dense_bytes / t / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(gate.dense_bytes),
+            "us_per_step": round(1e6 * t, 1)}
+
+
+def cpu_baseline(synth, budget_s=8.0):
+    """The CPU oracle's decode, as it stands, on a bounded sample (experts of
+    the same gate stack), one thread."""
+    import oracle
+    E = 64
+    dense = synth.gate_stack(seed=0, E=E)
+    enc = oracle.encode(oracle.NVFP4, dense)
+    reps, t = 0, 0.0
+    while t < budget_s:
+        t0 = time.perf_counter()
+        out, st = oracle.decode(enc)
+        t += time.perf_counter() - t0
+        reps += 1
+    assert st == oracle.OK and np.array_equal(out, dense)
+    gbs = reps * dense.size / t / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{E} of the 512 experts ({dense.size / 1e6:.1f} MB dense), {reps} decodes, "
+                      f"{t:.1f} s, 1 thread; us per 512-expert stack = {1e6 * 512 / E * t / reps:.0f}"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: same metric and workload, each
+    step decodes a bounded sample (16 experts) of the gate stack."""
+    import oracle
+    from lossless_nvfp4_scale_gb300 import synth
+    E = 16
+    dense = synth.gate_stack(seed=0, E=E)
+    enc = oracle.encode(oracle.NVFP4, dense)
+    for _ in range(args.warmup):
+        oracle.decode(enc)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        out, st = oracle.decode(enc)
+    t = time.perf_counter() - t0
+    assert st == oracle.OK and np.array_equal(out, dense)
+    value = args.steps * dense.size / t / 1e9
+    sample = f"{E} of the 512 experts per step ({dense.size / 1e6:.2f} MB dense), 1 thread"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="own", choices=["own", "reference"])
+    ap.add_argument("--skip-rows", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    res = run_own(args, rank, world, torch, dist)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,302 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Integer byte work, so the bar is bit-exact everywhere.  Inputs are the seeded
+synthetic stacks of lossless_nvfp4_scale_gb300.synth; expected values come
+from the oracle only.  Covers small ragged geometries (several work units,
+ragged tails, odd C, C < chunk), the full-size stacks of the pages' workloads
+(512 x 1024 x 100 gate, 512 x 2048 x 50 down, 384 x 2048 x 160 MXFP4) in the
+launch configuration the benchmark times, routed decode into a poisoned
+workspace, paired decode, odd-offset workspaces with guard bytes, CUDA-graph
+replay, both routing integer types, and corrupt or over-capacity inputs
+(planted on the CPU) reported through the device error word.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from lossless_nvfp4_scale_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def csf():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from lossless_nvfp4_scale_gb300 import build
+    build.ensure_built()
+    from lossless_nvfp4_scale_gb300 import csf as mod
+    return mod
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def assert_stack_matches(st, enc):
+    E, R, C = enc["shape"]
+    sb = st.stream_bytes()
+    assert st.num_exc == enc["num_exc"]
+    assert np.array_equal(_np(st.base[:E * R]), enc["base"])
+    assert np.array_equal(_np(st.offsets[:sb["offsets"]]), enc["offsets"])
+    if enc["kind"] == oracle.MXFP4:
+        assert np.array_equal(_np(st.escapes[:sb["escapes"]]), enc["escapes"])
+    assert np.array_equal(_np(st.exc_index).view(np.uint32), enc["exc_index"])
+    assert np.array_equal(_np(st.exc_bytes[:st.num_exc]), enc["exc_bytes"])
+    # Allocation padding past the stream is written as zeros.
+    assert not _np(st.offsets[sb["offsets"]:]).any()
+
+
+def _dense_cuda(dense):
+    return torch.from_numpy(dense).cuda()
+
+
+SMALL = [
+    (0, 1, 1, 1), (0, 1, 1, 31), (0, 3, 5, 7), (0, 2, 33, 17), (0, 5, 37, 100), (0, 7, 13, 3),
+    (0, 4, 64, 8), (0, 3, 40, 64), (0, 2, 3, 1000),
+    (1, 1, 1, 1), (1, 3, 5, 7), (1, 2, 37, 160), (1, 4, 9, 33), (1, 3, 11, 128), (1, 2, 5, 500),
+]
+
+
+def _small_dense(kind, E, R, C, seed):
+    w = 14 if kind == 0 else 1
+    return synth.random_rows(seed, E * R, C, spread=3 * w + 3, replace_p=0.08).reshape(E, R, C)
+
+
+@pytest.mark.parametrize("kind,E,R,C", SMALL)
+def test_prepare_and_decode_small(csf, kind, E, R, C):
+    dense = _small_dense(kind, E, R, C, seed=E * 1000 + R * 10 + C)
+    enc = oracle.encode(kind, dense)
+    st = csf.prepare(_dense_cuda(dense), kind)
+    torch.cuda.synchronize()
+    assert st.errors() == 0
+    assert_stack_matches(st, enc)
+    # Decode the oracle's stream (independent of the GPU prepare).
+    up = csf.upload(enc)
+    ws = torch.full(dense.shape, 0x5A, dtype=torch.uint8, device="cuda")
+    csf.decode(up, ws)
+    assert np.array_equal(_np(ws), dense)
+    assert up.errors() == 0
+
+
+@pytest.mark.parametrize("kind,E,R,C", [(0, 6, 5, 7), (0, 5, 37, 100), (1, 6, 9, 33), (1, 4, 37, 160),
+                                        (0, 9, 13, 3)])
+@pytest.mark.parametrize("is64", [False, True])
+def test_routed_small_poisoned(csf, kind, E, R, C, is64):
+    dense = _small_dense(kind, E, R, C, seed=7 + C)
+    enc = oracle.encode(kind, dense)
+    up = csf.upload(enc)
+    counts = np.zeros(E, np.int64)
+    counts[[0, E // 2, E - 1]] = [2, 1, 3]          # first, middle and last experts
+    start = np.concatenate([[0], np.cumsum(counts)])
+    es = torch.from_numpy(start.astype(np.int64 if is64 else np.int32)).cuda()
+    ws = torch.full(dense.shape, 0xFF, dtype=torch.uint8, device="cuda")
+    csf.decode(up, ws, expert_start=es)
+    want, st = oracle.decode(enc, start, np.full(dense.shape, 0xFF, np.uint8))
+    assert st == oracle.OK
+    assert np.array_equal(_np(ws), want)
+    assert up.errors() == 0
+
+
+def test_routed_edge_cases(csf):
+    dense = _small_dense(0, 8, 16, 100, seed=3)
+    enc = oracle.encode(0, dense)
+    up = csf.upload(enc)
+    E = 8
+    cases = {
+        "none": np.zeros(E + 1, np.int64),
+        "all": np.arange(E + 1, dtype=np.int64),
+        "last": np.concatenate([np.zeros(E, np.int64), [5]]),
+        "zero-length groups": np.array([0, 0, 4, 4, 4, 9, 9, 9, 9], np.int64),
+        "decreasing": np.array([5, 3, 4, 4, -1, 0, 0, 2, 2], np.int64),
+    }
+    for name, start in cases.items():
+        ws = torch.full(dense.shape, 0xFF, dtype=torch.uint8, device="cuda")
+        csf.decode(up, ws, expert_start=torch.from_numpy(start.astype(np.int32)).cuda())
+        want, _ = oracle.decode(enc, start, np.full(dense.shape, 0xFF, np.uint8))
+        assert np.array_equal(_np(ws), want), name
+
+
+@pytest.mark.parametrize("offset", [0, 1, 3, 8, 15, 16, 17])
+def test_odd_offset_workspace_with_guards(csf, offset):
+    for kind, shape in ((0, (3, 40, 100)), (1, (2, 37, 160))):
+        dense = _small_dense(kind, *shape, seed=offset)
+        up = csf.upload(oracle.encode(kind, dense))
+        n = dense.size
+        buf = torch.full((n + 64,), 0xAB, dtype=torch.uint8, device="cuda")
+        ws = buf[offset:offset + n]
+        csf.decode(up, ws)
+        host = _np(buf)
+        assert np.array_equal(host[offset:offset + n], dense.ravel())
+        assert (host[:offset] == 0xAB).all() and (host[offset + n:] == 0xAB).all()
+        # routed into an odd-offset workspace: inactive planes keep the guard value
+        start = np.array([0, 1] + [1] * (shape[0] - 1), np.int32)
+        buf.fill_(0xAB)
+        csf.decode(up, buf[offset:offset + n], expert_start=torch.from_numpy(start).cuda())
+        host = _np(buf)
+        plane = shape[1] * shape[2]
+        assert np.array_equal(host[offset:offset + plane], dense[0].ravel())
+        assert (host[offset + plane:] == 0xAB).all() and (host[:offset] == 0xAB).all()
+
+
+def test_special_streams(csf):
+    # All-escape rows (decoder only) and a zero-exception stack.
+    exc = np.arange(100, 100 + 3 * 40, dtype=np.uint8)
+    enc = {"kind": 0, "shape": (1, 3, 40), "base": np.array([1, 2, 3], np.uint8),
+           "offsets": np.full(60, 0xFF, np.uint8), "escapes": np.zeros(0, np.uint8),
+           "exc_index": np.array([0, 40, 80, 120], np.uint32), "exc_bytes": exc, "num_exc": 120}
+    ws = csf.decode(csf.upload(enc))
+    assert np.array_equal(_np(ws).ravel(), exc)
+    dense = np.full((2, 16, 100), 0x40, np.uint8)
+    dense[:, :, 1::2] = 0x4E
+    enc = oracle.encode(0, dense)
+    assert enc["num_exc"] == 0
+    st = csf.prepare(_dense_cuda(dense), 0)
+    assert_stack_matches(st, enc)
+    assert np.array_equal(_np(csf.decode(st)), dense)
+
+
+def test_corrupt_index_sets_error_word(csf):
+    dense = synth.stack("tiny")
+    enc = oracle.encode(0, dense)
+    bad = dict(enc)
+    bad["exc_index"] = enc["exc_index"].copy()
+    bad["exc_index"][100:] += 1          # planted on the CPU: row 99's step is off by one
+    assert oracle.check(bad) == oracle.ERR_CORRUPT
+    up = csf.upload(bad)
+    csf.decode(up)
+    assert up.errors() & csf.DEV_ERR_CORRUPT
+    bad = dict(enc)
+    bad["num_exc"] = enc["num_exc"] - 3  # stream shorter than the index says
+    bad["exc_bytes"] = enc["exc_bytes"][:-3]
+    up = csf.upload(bad)
+    csf.decode(up)
+    assert up.errors() & csf.DEV_ERR_CORRUPT
+    good = csf.upload(enc)
+    csf.decode(good)
+    assert good.errors() == 0
+
+
+def test_prepare_capacity_overflow_reports_and_keeps_index(csf):
+    dense = synth.stack("tiny")
+    enc = oracle.encode(0, dense)
+    E, R, C = dense.shape
+    st = csf.empty_stack(0, E, R, C, exc_capacity=16)
+    scratch = csf.prepare_scratch(0, E, R, C)
+    csf.prepare_async(_dense_cuda(dense), st, scratch, exc_capacity=5)
+    torch.cuda.synchronize()
+    assert st.errors() & csf.DEV_ERR_CAPACITY
+    assert np.array_equal(_np(st.exc_index).view(np.uint32), enc["exc_index"])
+    assert np.array_equal(_np(st.exc_bytes[:5]), enc["exc_bytes"][:5])
+
+
+def test_cuda_graph_replay_with_repoisoning(csf):
+    dense = synth.gate_stack(E=16, R=64)
+    enc = oracle.encode(0, dense)
+    up = csf.upload(enc)
+    start = synth.routing(E=16, active=4, tokens=16, seed=1)
+    es = torch.from_numpy(start).cuda()
+    ws = torch.full(dense.shape, 0xFF, dtype=torch.uint8, device="cuda")
+    want, _ = oracle.decode(enc, start, np.full(dense.shape, 0xFF, np.uint8))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        csf.decode(up, ws, expert_start=es)   # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        csf.decode(up, ws, expert_start=es)
+    for _ in range(8):
+        ws.fill_(0xFF)
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(_np(ws), want)
+
+
+# ---------------------------------------------------------------- full sizes
+
+@pytest.fixture(scope="module")
+def gate(csf):
+    dense = synth.stack("gate")
+    enc = oracle.encode(0, dense)
+    return dense, enc
+
+
+@pytest.fixture(scope="module")
+def down(csf):
+    dense = synth.stack("down")
+    enc = oracle.encode(0, dense)
+    return dense, enc
+
+
+def test_full_gate_prepare_and_decode(csf, gate):
+    dense, enc = gate
+    d = _dense_cuda(dense)
+    st = csf.prepare(d, 0)
+    assert st.errors() == 0
+    assert_stack_matches(st, enc)
+    ws = torch.empty_like(d)
+    csf.decode(st, ws)
+    assert torch.equal(ws, d)
+    up = csf.upload(enc)
+    ws.fill_(0)
+    csf.decode(up, ws)
+    assert torch.equal(ws, d) and up.errors() == 0
+
+
+@pytest.mark.parametrize("is64", [False, True])
+def test_full_gate_routed_8_of_512_poisoned(csf, gate, is64):
+    dense, enc = gate
+    d = _dense_cuda(dense)
+    up = csf.upload(enc)
+    start = synth.routing(E=512, active=8, tokens=64, seed=0, dtype=np.int64 if is64 else np.int32)
+    active = np.flatnonzero(np.diff(start.astype(np.int64)) > 0)
+    assert active.size == 8
+    ws = torch.full_like(d, 0xFF)
+    csf.decode(up, ws, expert_start=torch.from_numpy(start).cuda())
+    mask = torch.zeros(512, dtype=torch.bool, device="cuda")
+    mask[torch.from_numpy(active).cuda()] = True
+    assert torch.equal(ws[mask], d[mask])
+    assert bool((ws[~mask] == 0xFF).all())
+
+
+def test_full_pair_decode(csf, gate, down):
+    (gd, genc), (dd, denc) = gate, down
+    g_up, d_up = csf.upload(genc), csf.upload(denc)
+    gdc, ddc = _dense_cuda(gd), _dense_cuda(dd)
+    gws, dws = torch.full_like(gdc, 0xFF), torch.full_like(ddc, 0xFF)
+    csf.decode_pair(g_up, d_up, gws, dws)
+    assert torch.equal(gws, gdc) and torch.equal(dws, ddc)
+    start = synth.routing(E=512, active=8, tokens=64, seed=0)
+    active = torch.from_numpy(np.flatnonzero(np.diff(start.astype(np.int64)) > 0)).cuda()
+    gws.fill_(0xFF)
+    dws.fill_(0xFF)
+    csf.decode_pair(g_up, d_up, gws, dws, expert_start=torch.from_numpy(start).cuda())
+    mask = torch.zeros(512, dtype=torch.bool, device="cuda")
+    mask[active] = True
+    assert torch.equal(gws[mask], gdc[mask]) and torch.equal(dws[mask], ddc[mask])
+    assert bool((gws[~mask] == 0xFF).all()) and bool((dws[~mask] == 0xFF).all())
+    assert g_up.errors() == 0 and d_up.errors() == 0
+    # GPU prepare of the heavy-tailed down stack matches the oracle.
+    st = csf.prepare(ddc, 0)
+    assert_stack_matches(st, denc)
+
+
+def test_full_mxfp4_prepare_and_decode(csf):
+    dense = synth.stack("mxfp4")
+    enc = oracle.encode(1, dense)
+    d = _dense_cuda(dense)
+    st = csf.prepare(d, 1)
+    assert st.errors() == 0
+    assert_stack_matches(st, enc)
+    ws = torch.empty_like(d)
+    csf.decode(st, ws)
+    assert torch.equal(ws, d)
+    start = synth.routing(E=384, active=8, tokens=64, seed=0)
+    active = torch.from_numpy(np.flatnonzero(np.diff(start.astype(np.int64)) > 0)).cuda()
+    ws.fill_(0xFF)
+    csf.decode(st, ws, expert_start=torch.from_numpy(start).cuda())
+    mask = torch.zeros(384, dtype=torch.bool, device="cuda")
+    mask[active] = True
+    assert torch.equal(ws[mask], d[mask]) and bool((ws[~mask] == 0xFF).all())
