@@ -159,6 +159,32 @@ csf_status csf_sizes(const csf_geometry *g, csf_sizes_t *out);
 csf_status csf_prepare(const uint8_t *dense, csf_stack *out, uint64_t exc_capacity,
                        void *scratch, size_t scratch_bytes, void *stream);
 
+/* Size of the device scratch array built into the library for
+ * csf_prepare_static (held on every GPU that loads the library). */
+#define CSF_STATIC_SCRATCH_BYTES (256u * 1024u)
+
+/*
+ * csf_prepare without a scratch argument, for callers that cannot allocate
+ * device memory.  The pages have no counterpart; this is a convenience of this
+ * library.  Some callers cannot call cudaMalloc: a plugin inside a host
+ * process whose caching allocator owns all device memory, code that runs
+ * where an allocation would implicitly synchronise the device or disturb a
+ * stream capture, code with a fixed memory budget.  This entry point
+ * allocates nothing: its scratch (a ticket counter and one look-back word per
+ * tile of rows) is a CSF_STATIC_SCRATCH_BYTES device array inside the library.
+ * The caller still passes `dense` and every output buffer, as for csf_prepare,
+ * and the results are the same bytes.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture.  Every call shares the one array and clears the part it uses on
+ * `stream` first: calls that overlap on the GPU race, so order them.
+ * Errors: as csf_prepare, plus CSF_ERR_SIZE when the geometry needs more than
+ * CSF_STATIC_SCRATCH_BYTES of scratch (16 + 8 bytes per tile of rows; about
+ * 5 million rows for NVFP4 with C = 100, 3 million for MXFP4 with C = 160).
+ */
+csf_status csf_prepare_static(const uint8_t *dense, csf_stack *out, uint64_t exc_capacity, void *stream);
+
 /*
  * Decode a stack into a dense workspace ([FK] format, strategy table and
  * helpers paragraphs).

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libcsf.so")
-SOURCES = ["csf_api.cu", "csf_decode.cu", "csf_prepare.cu"]
+SOURCES = ["csf_api.cu", "csf_decode.cu", "csf_prepare.cu", "csf_prepare_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
