@@ -44,6 +44,8 @@ csf_status device_info(DeviceInfo *out) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+uint64_t round16(uint64_t v) { return (v + 15) & ~15ull; }
+
 csf_status geometry(const csf_geometry *g, uint64_t *n, uint64_t *rows) {
     if (!g) return CSF_ERR_ARG;
     if (g->kind != CSF_NVFP4 && g->kind != CSF_MXFP4) return CSF_ERR_ARG;
@@ -55,8 +57,6 @@ csf_status geometry(const csf_geometry *g, uint64_t *n, uint64_t *rows) {
     *rows = r;
     return CSF_OK;
 }
-
-uint64_t round16(uint64_t v) { return (v + 15) & ~15ull; }
 
 uint64_t prepare_scratch_bytes(const csf_geometry *g, uint64_t rows) {
     const int32_t tr = prepare_tile_rows(g->kind, g->cols);
@@ -82,7 +82,7 @@ csf_status fill_stack(const csf_stack *s, uint8_t *ws, size_t ws_bytes, DecStack
     if (s->num_exc > 0 && !s->exc_bytes) return CSF_ERR_ARG;
     if (s->num_exc > 0xFFFFFFFFull) return CSF_ERR_ARG;
     if (ws_bytes < n) return CSF_ERR_SIZE;
-    const int chunk = s->g.kind == CSF_NVFP4 ? kChunkNv : kChunkMx;
+    const int chunk = s->g.kind == CSF_NVFP4 ? kLaneNv : kLaneMx;
     std::memset(d, 0, sizeof *d);
     d->base = s->base;
     d->offsets = s->offsets;
@@ -102,6 +102,10 @@ csf_status fill_stack(const csf_stack *s, uint8_t *ws, size_t ws_bytes, DecStack
     d->step_r = step_el / (uint32_t)s->g.cols;
     d->step_q = step_el % (uint32_t)s->g.cols;
     d->ws_align = ws_alignment(ws);
+    d->off_align32 = (reinterpret_cast<uintptr_t>(s->offsets) & 31u) == 0 ? 1 : 0;
+    d->off_bytes = s->g.kind == CSF_NVFP4 ? round16((n + 1) / 2) : round16((n + 7) / 8);
+    d->max_units = (1ull << 30) / ((uint64_t)d->rb * (uint64_t)d->C);
+    if (d->max_units < 1) d->max_units = 1;
     return CSF_OK;
 }
 

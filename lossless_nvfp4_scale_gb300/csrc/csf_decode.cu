@@ -17,30 +17,33 @@
 //     reconstruction and exception lookup.
 //
 // Design (GB300 first; HBM-bound byte work, no tensor cores):
-//   * Work unit = a run of `rb` rows whose elements fill whole chunks
-//     (32 elements = 16 offset bytes for NVFP4, 128 elements = 16 bytes of
+//   * Work unit = a run of `rb` rows whose elements fill whole lane chunks
+//     (64 elements = 32 offset bytes for NVFP4; 128 elements = 16 bytes of
 //     each bit plane for MXFP4).  Every warp of a persistent grid takes one
-//     contiguous range of units (balanced to one unit), so it reads a single
-//     exc_index entry at the start of each contiguous segment and then walks
-//     the exception stream in order: exceptions of consecutive rows are
-//     consecutive, so the running position is the segment's first index plus
-//     the escapes met so far (warp ballot-free scan of per-lane popcounts).
-//     The per-row index is checked against that position at the segment end.
-//   * Lanes read 16-byte pieces of the offset stream (coalesced), expand them
-//     with byte permutes and carry-free byte adds, patch escapes in registers
-//     from the exception stream, and write each 32-byte piece with one
-//     256-bit store (full sectors, no read-for-ownership).
+//     contiguous range of units (balanced to one unit), reads one exc_index
+//     entry where each contiguous segment starts, and walks the exception
+//     stream in order: exceptions of consecutive rows are consecutive, so an
+//     escape's position is the segment's first index plus the escapes before
+//     it (a warp scan of per-lane popcounts).  The index entry at the segment
+//     end is checked against the running position.
+//   * Lanes read 256-bit pieces of the offset stream (coalesced across the
+//     warp), prefetching the next piece while the current one is expanded
+//     with byte permutes (NVFP4) or a bit-to-byte spreading multiply (MXFP4)
+//     and carry-free byte adds of the row bases.
+//   * Escapes are patched in a lane-private, bank-swizzled shared-memory slot
+//     (one byte store each); each 32 dense bytes leave with one 256-bit store.
 //   * Routed mode: every block compacts the active experts of `expert_start`
 //     into shared memory with ballots and prefix sums; the units of inactive
 //     experts never exist, so their workspace planes are never written.
 //   * A unit whose rows straddle an expert boundary (R*C not a multiple of the
-//     chunk) is decoded whole but stored only inside its expert's rows.
+//     lane chunk) is decoded whole but stored only inside its expert's rows.
 #include "csf_internal.cuh"
 
 namespace csfk {
 namespace {
 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
+constexpr int kStageBytes = 4096;   // per warp: 32 lanes x 128 bytes
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
@@ -52,28 +55,30 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, int lane, uint32_
     uint32_t x = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        uint32_t y = __shfl_up_sync(kFull, x, d);
+        const uint32_t y = __shfl_up_sync(kFull, x, d);
         if (lane >= d) x += y;
     }
     total = __shfl_sync(kFull, x, 31);
     return x - v;
 }
 
-__device__ __forceinline__ uint4 ldg16(const uint8_t *p) {
-    return __ldg(reinterpret_cast<const uint4 *>(p));
+__device__ __forceinline__ void ld_v8(const uint8_t *p, uint32_t (&w)[8]) {
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+                   "=r"(w[7])
+                 : "l"(p));
 }
 
-__device__ __forceinline__ void st_v8(uint8_t *p, const uint32_t (&w)[8]) {
+__device__ __forceinline__ void st_v8(uint8_t *p, const uint32_t *w) {
     asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
                  "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                  : "memory");
 }
 
-// Store 32 decoded bytes for elements [p, p+32) to ws + p, keeping only the
-// bytes inside [lo, hi).  `align` is the byte alignment of ws (p is a
-// multiple of 32).
-__device__ __forceinline__ void store32(uint8_t *ws, int align, uint64_t p, const uint32_t (&w)[8],
-                                        uint64_t lo, uint64_t hi) {
+// Store 32 decoded bytes of local elements [p, p+32) at ws + p, keeping only
+// the bytes inside [lo, hi).  `align` = byte alignment of ws (p % 32 == 0).
+__device__ __forceinline__ void store32(uint8_t *ws, int align, uint32_t p, const uint32_t *w, uint32_t lo,
+                                        uint32_t hi) {
     uint8_t *d = ws + p;
     if (p >= lo && p + 32 <= hi) {
         if (align >= 32) {
@@ -91,241 +96,341 @@ __device__ __forceinline__ void store32(uint8_t *ws, int align, uint64_t p, cons
     } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-            uint64_t q = p + j;
+            const uint32_t q = p + j;
             if (q >= lo && q < hi) d[j] = (uint8_t)(w[j >> 2] >> (8 * (j & 3)));
         }
     }
 }
 
-// Bytes [j] of bw = base byte of the row of element (start + j), for NW words
-// (4*NW elements).  `b` = elements from `start` to the next row start;
-// `second` = base of that next row; rows after it are loaded here.
-template <int NW>
-__device__ __forceinline__ void base_words(uint32_t (&bw)[NW], uint32_t first, uint32_t second, int b,
-                                           const uint8_t *__restrict__ base, uint64_t row_after_next,
-                                           uint64_t rows, uint32_t C) {
-    const uint32_t a = first * 0x01010101u;
-#pragma unroll
-    for (int k = 0; k < NW; ++k) bw[k] = a;
-    if (b < 4 * NW) {
-        uint32_t nb = second * 0x01010101u;
-        uint64_t rn = row_after_next;
-        while (true) {
-#pragma unroll
-            for (int k = 0; k < NW; ++k) {
-                int d8 = 8 * (b - 4 * k);
-                uint32_t s = (uint32_t)min(max(d8, 0), 32);
-                uint32_t m = __funnelshift_lc(0u, 0xFFFFFFFFu, s);  // bytes at or after the boundary
-                bw[k] = (bw[k] & ~m) | (nb & m);
-            }
-            b += (int)C;
-            if (b >= 4 * NW) break;
-            nb = (rn < rows ? (uint32_t)__ldg(base + rn) : 0u) * 0x01010101u;
-            ++rn;
-        }
-    }
-}
-
-// base + offset, byte-wise mod 256, for offsets below 0x80 (no carry between
-// bytes: the low 7 bits are added, bit 7 is folded back with XOR).
+// base + offset, byte-wise mod 256, for offsets below 0x80 (the low 7 bits
+// are added, bit 7 is folded back with XOR, so no carry crosses a byte).
 __device__ __forceinline__ uint32_t add_base(uint32_t bw, uint32_t off) {
     return ((bw & 0x7F7F7F7Fu) + off) ^ (bw & 0x80808080u);
 }
 
-__device__ __forceinline__ uint32_t exc_at(const DecStack &S, uint64_t x, bool &bad) {
-    if (x < S.num_exc) return (uint32_t)__ldg(S.exc_bytes + x);
-    bad = true;
-    return 0u;
+// Mask of the bytes of word k (elements 4k..4k+3 of a run) that lie at or
+// after element b of the run.
+__device__ __forceinline__ uint32_t bytes_from(int b, int k) {
+    const uint32_t s = (uint32_t)max(8 * (b - 4 * k), 0);
+    return __funnelshift_lc(0u, 0xFFFFFFFFu, s);   // shift >= 32 gives 0
 }
 
 __device__ __forceinline__ void flag(uint32_t *err, uint32_t bits) {
     if (err) atomicOr(err, bits);
 }
 
-// Insert exception bytes into one output word for the set escape bits of
-// `m` (bit 4j <-> byte j for NVFP4, bit j <-> byte j for MXFP4).
-template <int STRIDE>
-__device__ __forceinline__ void patch_word(uint32_t &w, uint32_t m, const DecStack &S, uint64_t &x, bool &bad) {
-    while (m) {
-        const uint32_t b = (uint32_t)(__ffs(m) - 1);
-        m &= m - 1;
-        const uint32_t sh = 8u * (b / STRIDE);
-        const uint32_t e = exc_at(S, x, bad);
-        ++x;
-        w = (w & ~(0xFFu << sh)) | (e << sh);
+// Replicated row bases for NW words (4*NW elements) starting at a run whose
+// first row has base `first`; `b` = elements to the next row start; rows after
+// the first are read from base[rn], base[rn+1], ... (rn = that next row).
+template <int NW>
+__device__ __forceinline__ void base_words_general(uint32_t (&bw)[NW], uint32_t first, int b,
+                                                   const uint8_t *__restrict__ base, uint64_t rn, uint64_t rows,
+                                                   uint32_t C) {
+    const uint32_t a = first * 0x01010101u;
+#pragma unroll
+    for (int k = 0; k < NW; ++k) bw[k] = a;
+    while (b < 4 * NW) {
+        const uint32_t nb = (rn < rows ? (uint32_t)__ldg(base + rn) : 0u) * 0x01010101u;
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+            const uint32_t m = bytes_from(b, k);
+            bw[k] = (bw[k] & ~m) | (nb & m);
+        }
+        b += (int)C;
+        ++rn;
     }
 }
 
-// Decode rows [row_a, row_b) of an NVFP4 stack (row_a*C a multiple of 32),
-// storing only elements in [lo, hi).  Whole warp; U chunks per lane per step.
-template <int U>
+// ------------------------------------------------------------------ NVFP4
+
+// Decode rows [row_a, row_b) of an NVFP4 stack (row_a*C a multiple of 64),
+// storing only global elements in [lo, hi).  Whole warp.
 __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b, uint64_t lo, uint64_t hi,
-                              int lane) {
+                              int lane, uint8_t *stage) {
     const uint32_t C = (uint32_t)S.C;
     const uint64_t sa = row_a * C;
-    const uint64_t sb = row_b * C;
-    const uint64_t c_begin = sa / kChunkNv;
-    const uint64_t c_end = (sb + kChunkNv - 1) / kChunkNv;
-    uint64_t X = 0;
+    const uint32_t nel = (uint32_t)(row_b * C - sa);
+    const uint32_t nch = (nel + kLaneNv - 1) / kLaneNv;
+    const uint8_t *offs = S.offsets + sa / 2;
+    const uint64_t avail64 = S.off_bytes - sa / 2;
+    const uint32_t avail = avail64 > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)avail64;
+    const uint8_t *bases = S.base + row_a;
+    const uint64_t rows_left = S.rows - row_a;
+    uint8_t *ws = S.ws + sa;
+    const uint32_t lo_l = (uint32_t)(lo - sa);
+    const uint32_t hi_l = (uint32_t)(hi - sa);
+    const bool fast = lo_l == 0 && hi_l == nel && S.ws_align >= 32;
+    const bool v8ok = S.off_align32 != 0;
+    const uint32_t nexc = (uint32_t)S.num_exc;
+    uint32_t X = 0;
     if (lane == 0) X = __ldg(S.exc_index + row_a);
     X = __shfl_sync(kFull, X, 0);
     bool bad = false;
-    const uint32_t lane_el = (uint32_t)lane * kChunkNv;
-    uint64_t r = row_a + lane_el / C;
-    uint32_t q = lane_el % C;
-    for (uint64_t cb = c_begin; cb < c_end; cb += 32 * U) {
-        uint4 off[U];
-        uint32_t bA[U], bB[U], qu[U];
-        uint64_t ru[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint64_t c = cb + 32 * u + lane;
-            ru[u] = r;
-            qu[u] = q;
-            if (c < c_end) {
-                off[u] = ldg16(S.offsets + c * 16);
-                bA[u] = __ldg(S.base + r);
-                bB[u] = (r + 1 < S.rows) ? (uint32_t)__ldg(S.base + r + 1) : 0u;
+    const uint32_t g = ((uint32_t)lane >> 1) & 3u;          // smem slot swizzle
+    uint8_t *my = stage + lane * 64;
+
+    uint32_t rr = ((uint32_t)lane * kLaneNv) / C;
+    uint32_t q = ((uint32_t)lane * kLaneNv) % C;
+    uint32_t w[8], bA = 0, bB = 0;
+
+    auto load = [&](uint32_t c, uint32_t r) {
+        if (c < nch) {
+            const uint8_t *p = offs + (size_t)c * 32;
+            if (v8ok && c * 32 + 32 <= avail) {
+                ld_v8(p, w);
             } else {
-                off[u] = make_uint4(0, 0, 0, 0);
-                bA[u] = bB[u] = 0;
+                const uint4 a = __ldg(reinterpret_cast<const uint4 *>(p));
+                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+                if (c * 32 + 32 <= avail) {
+                    const uint4 b2 = __ldg(reinterpret_cast<const uint4 *>(p + 16));
+                    w[4] = b2.x; w[5] = b2.y; w[6] = b2.z; w[7] = b2.w;
+                } else {
+                    w[4] = w[5] = w[6] = w[7] = 0;
+                }
             }
-            q += S.step_q;
-            r += S.step_r;
-            if (q >= C) { q -= C; ++r; }
+            bA = __ldg(bases + r);
+            bB = (r + 1 < rows_left) ? (uint32_t)__ldg(bases + r + 1) : 0u;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = 0;
+            bA = bB = 0;
         }
+    };
+    load((uint32_t)lane, rr);
+
+    for (uint32_t cb = 0; cb < nch; cb += 32) {
+        const uint32_t cc = cb + lane;
+        uint32_t cw[8];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint64_t c = cb + 32 * u + lane;
-            const uint64_t p = c * kChunkNv;
-            const int nv = c < c_end ? (int)min(sb - p, (uint64_t)kChunkNv) : 0;
-            uint32_t bw[8];
-            base_words<8>(bw, bA[u], bB[u], (int)(C - qu[u]), S.base, ru[u] + 2, S.rows, C);
-            const uint32_t wv[4] = {off[u].x, off[u].y, off[u].z, off[u].w};
-            uint32_t out[8], t[4];
+        for (int i = 0; i < 8; ++i) cw[i] = w[i];
+        const uint32_t cA = bA, cB = bB, cq = q, crr = rr;
+        q += S.step_q;
+        rr += S.step_r;
+        if (q >= C) { q -= C; ++rr; }
+        if (cb + 32 < nch) load(cc + 32, rr);                // prefetch the next piece
+
+        const uint32_t p = cc * kLaneNv;
+        const int nv = cc < nch ? (int)min(nel - p, (uint32_t)kLaneNv) : 0;
+        const int b = (int)(C - cq);                           // elements to the next row start
+        uint32_t out[16], t[8];
+        if (C >= kLaneNv) {
+            // At most one row boundary in the 64 elements.
+            const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t w = wv[i];
-                const uint32_t lo4 = w & 0x0F0F0F0Fu;
-                const uint32_t hi4 = (w >> 4) & 0x0F0F0F0Fu;
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t x = cw[i];
+                const uint32_t lo4 = x & 0x0F0F0F0Fu;
+                const uint32_t hi4 = (x >> 4) & 0x0F0F0F0Fu;
+                const uint32_t tt = x & (x >> 1);
+                t[i] = tt & (tt >> 2) & 0x11111111u;            // nibble == 15
+                const uint32_t m0 = bytes_from(b, 2 * i), m1 = bytes_from(b, 2 * i + 1);
+                out[2 * i] = add_base((A & ~m0) | (B & m0), __byte_perm(lo4, hi4, 0x5140));
+                out[2 * i + 1] = add_base((A & ~m1) | (B & m1), __byte_perm(lo4, hi4, 0x7362));
+            }
+        } else {
+            uint32_t bw[16];
+            base_words_general<16>(bw, cA, b, S.base, row_a + crr + 1, S.rows, C);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t x = cw[i];
+                const uint32_t lo4 = x & 0x0F0F0F0Fu;
+                const uint32_t hi4 = (x >> 4) & 0x0F0F0F0Fu;
+                const uint32_t tt = x & (x >> 1);
+                t[i] = tt & (tt >> 2) & 0x11111111u;
                 out[2 * i] = add_base(bw[2 * i], __byte_perm(lo4, hi4, 0x5140));
                 out[2 * i + 1] = add_base(bw[2 * i + 1], __byte_perm(lo4, hi4, 0x7362));
-                uint32_t esc = w & (w >> 1) & (w >> 2) & (w >> 3) & 0x11111111u;  // nibble == 15
-                const int nvi = min(max(nv - 8 * i, 0), 8);
-                if (nvi < 8) esc &= (1u << (4 * nvi)) - 1u;
-                t[i] = esc;
             }
-            const uint32_t cnt = __popc(t[0]) + __popc(t[1]) + __popc(t[2]) + __popc(t[3]);
-            uint32_t tot;
-            const uint32_t ex = warp_excl_scan(cnt, lane, tot);
-            uint64_t xl = X + ex;
-            X += tot;
-            if (cnt) {
+        }
+        if (nv < kLaneNv) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    patch_word<4>(out[k], (t[k >> 1] >> (16 * (k & 1))) & 0x1111u, S, xl, bad);
+            for (int i = 0; i < 8; ++i) {
+                const int nvi = min(max(nv - 8 * i, 0), 8);
+                if (nvi < 8) t[i] &= (1u << (4 * nvi)) - 1u;
             }
-            if (nv > 0) store32(S.ws, S.ws_align, p, out, lo, hi);
+        }
+        const uint32_t cnt = __popc(t[0]) + __popc(t[1]) + __popc(t[2]) + __popc(t[3]) + __popc(t[4]) +
+                             __popc(t[5]) + __popc(t[6]) + __popc(t[7]);
+        uint32_t tot;
+        uint32_t xl = X + warp_excl_scan(cnt, lane, tot);
+        X += tot;
+        if (__any_sync(kFull, cnt != 0)) {
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                *reinterpret_cast<uint4 *>(my + 16 * (s ^ g)) =
+                    make_uint4(out[4 * s], out[4 * s + 1], out[4 * s + 2], out[4 * s + 3]);
+            if (cnt) {
+                const bool ok = xl <= nexc && cnt <= nexc - xl;
+                if (!ok) bad = true;
+                // Words 2a and 2a+1 as one 64-bit mask: bit 4n <-> element
+                // 16a + n, so ascending bits visit escapes in element order,
+                // the order of the exception stream.
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    uint64_t f = (uint64_t)t[2 * a] | ((uint64_t)t[2 * a + 1] << 32);
+                    while (f) {
+                        const uint32_t bp = (uint32_t)(__ffsll((long long)f) - 1);
+                        f &= f - 1;
+                        const uint32_t j = 16u * a + (bp >> 2);
+                        const uint8_t e = ok ? __ldg(S.exc_bytes + xl) : (uint8_t)0;
+                        ++xl;
+                        my[16 * ((j >> 4) ^ g) + (j & 15)] = e;
+                    }
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(my + 16 * (s ^ g));
+                out[4 * s] = v.x; out[4 * s + 1] = v.y; out[4 * s + 2] = v.z; out[4 * s + 3] = v.w;
+            }
+        }
+        if (nv == kLaneNv && fast) {
+            st_v8(ws + p, out);
+            st_v8(ws + p + 32, out + 8);
+        } else if (nv > 0) {
+            store32(ws, S.ws_align, p, out, lo_l, hi_l);
+            if (nv > 32) store32(ws, S.ws_align, p + 32, out + 8, lo_l, hi_l);
         }
     }
-    if (lane == 0) {
-        const uint64_t expect = __ldg(S.exc_index + row_b);
-        if (expect != X) bad = true;
-    }
+    if (lane == 0 && __ldg(S.exc_index + row_b) != X) bad = true;
     if (__any_sync(kFull, bad) && lane == 0) flag(S.err, CSF_DEV_ERR_CORRUPT);
 }
 
+// ------------------------------------------------------------------ MXFP4
+
 // Decode rows [row_a, row_b) of an MXFP4 stack (row_a*C a multiple of 128).
-template <int U>
 __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b, uint64_t lo, uint64_t hi,
-                              int lane) {
+                              int lane, uint8_t *stage) {
     const uint32_t C = (uint32_t)S.C;
     const uint64_t sa = row_a * C;
-    const uint64_t sb = row_b * C;
-    const uint64_t c_begin = sa / kChunkMx;
-    const uint64_t c_end = (sb + kChunkMx - 1) / kChunkMx;
-    uint64_t X = 0;
+    const uint32_t nel = (uint32_t)(row_b * C - sa);
+    const uint32_t nch = (nel + kLaneMx - 1) / kLaneMx;
+    const uint8_t *offs = S.offsets + sa / 8;
+    const uint8_t *escs = S.escapes + sa / 8;
+    const uint8_t *bases = S.base + row_a;
+    const uint64_t rows_left = S.rows - row_a;
+    uint8_t *ws = S.ws + sa;
+    const uint32_t lo_l = (uint32_t)(lo - sa);
+    const uint32_t hi_l = (uint32_t)(hi - sa);
+    const bool fast = lo_l == 0 && hi_l == nel && S.ws_align >= 32;
+    const uint32_t nexc = (uint32_t)S.num_exc;
+    uint32_t X = 0;
     if (lane == 0) X = __ldg(S.exc_index + row_a);
     X = __shfl_sync(kFull, X, 0);
     bool bad = false;
-    const uint32_t lane_el = (uint32_t)lane * kChunkMx;
-    uint64_t r = row_a + lane_el / C;
-    uint32_t q = lane_el % C;
-    for (uint64_t cb = c_begin; cb < c_end; cb += 32 * U) {
-        uint4 ov[U], xv[U];
-        uint32_t bA[U], bB[U], qu[U];
-        uint64_t ru[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint64_t c = cb + 32 * u + lane;
-            ru[u] = r;
-            qu[u] = q;
-            if (c < c_end) {
-                ov[u] = ldg16(S.offsets + c * 16);
-                xv[u] = ldg16(S.escapes + c * 16);
-                bA[u] = __ldg(S.base + r);
-                bB[u] = (r + 1 < S.rows) ? (uint32_t)__ldg(S.base + r + 1) : 0u;
-            } else {
-                ov[u] = xv[u] = make_uint4(0, 0, 0, 0);
-                bA[u] = bB[u] = 0;
-            }
-            q += S.step_q;
-            r += S.step_r;
-            if (q >= C) { q -= C; ++r; }
+    const uint32_t g = (uint32_t)lane & 7u;                  // smem slot swizzle
+    uint8_t *my = stage + lane * 128;
+
+    uint32_t rr = ((uint32_t)lane * kLaneMx) / C;
+    uint32_t q = ((uint32_t)lane * kLaneMx) % C;
+    uint4 ov = make_uint4(0, 0, 0, 0), xv = make_uint4(0, 0, 0, 0);
+    uint32_t bA = 0, bB = 0;
+    auto load = [&](uint32_t c, uint32_t r) {
+        if (c < nch) {
+            ov = __ldg(reinterpret_cast<const uint4 *>(offs + (size_t)c * 16));
+            xv = __ldg(reinterpret_cast<const uint4 *>(escs + (size_t)c * 16));
+            bA = __ldg(bases + r);
+            bB = (r + 1 < rows_left) ? (uint32_t)__ldg(bases + r + 1) : 0u;
+        } else {
+            ov = xv = make_uint4(0, 0, 0, 0);
+            bA = bB = 0;
         }
+    };
+    load((uint32_t)lane, rr);
+
+    for (uint32_t cb = 0; cb < nch; cb += 32) {
+        const uint32_t cc = cb + lane;
+        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+        uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+        const uint32_t cA = bA, cB = bB, cq = q, crr = rr;
+        q += S.step_q;
+        rr += S.step_r;
+        if (q >= C) { q -= C; ++rr; }
+        if (cb + 32 < nch) load(cc + 32, rr);
+
+        const uint32_t p = cc * kLaneMx;
+        const int nv = cc < nch ? (int)min(nel - p, (uint32_t)kLaneMx) : 0;
+        if (nv < kLaneMx) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint64_t c = cb + 32 * u + lane;
-            const uint64_t p = c * kChunkMx;
-            const int nv = c < c_end ? (int)min(sb - p, (uint64_t)kChunkMx) : 0;
-            const uint32_t ow[4] = {ov[u].x, ov[u].y, ov[u].z, ov[u].w};
-            uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const int nvg = min(max(nv - 32 * g, 0), 32);
-                if (nvg < 32) xw[g] &= (nvg == 0) ? 0u : (0xFFFFFFFFu >> (32 - nvg));
+            for (int k = 0; k < 4; ++k) {
+                const int nvg = min(max(nv - 32 * k, 0), 32);
+                if (nvg < 32) xw[k] &= nvg == 0 ? 0u : (0xFFFFFFFFu >> (32 - nvg));
             }
-            const uint32_t cnt = __popc(xw[0]) + __popc(xw[1]) + __popc(xw[2]) + __popc(xw[3]);
-            uint32_t tot;
-            const uint32_t ex = warp_excl_scan(cnt, lane, tot);
-            uint64_t xl = X + ex;
-            X += tot;
-            if (nv == 0) continue;
-            uint64_t rg = ru[u];
-            uint32_t qg = qu[u];
+        }
+        const uint32_t cnt = __popc(xw[0]) + __popc(xw[1]) + __popc(xw[2]) + __popc(xw[3]);
+        uint32_t tot;
+        uint32_t xl = X + warp_excl_scan(cnt, lane, tot);
+        X += tot;
+        if (nv > 0) {
+            uint32_t rg = crr, qg = cq;                        // row / column of the group start
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                if (32 * g < nv) {
-                    const uint32_t first = (rg == ru[u]) ? bA[u] : (rg == ru[u] + 1 ? bB[u] : (uint32_t)__ldg(S.base + rg));
-                    const int bnd = (int)(C - qg);
-                    uint32_t second = 0;
-                    if (bnd < 32) {
-                        const uint64_t rs = rg + 1;
-                        second = (rs == ru[u] + 1) ? bB[u] : (rs < S.rows ? (uint32_t)__ldg(S.base + rs) : 0u);
+            for (int gi = 0; gi < 4; ++gi) {
+                uint32_t out[8];
+                const int bg = (int)(C - qg);                  // elements to the next row start
+                const uint32_t A = rg == crr ? cA
+                                 : (rg == crr + 1 ? cB : (rg < rows_left ? (uint32_t)__ldg(bases + rg) : 0u));
+                if (C >= 32 || bg >= 32) {
+                    // At most one row boundary in the group: bytes at or after
+                    // element bg take row B's base.
+                    uint32_t B = A;
+                    if (bg < 32) {
+                        const uint32_t rn = rg + 1;
+                        B = rn == crr + 1 ? cB : (rn < rows_left ? (uint32_t)__ldg(bases + rn) : 0u);
                     }
-                    uint32_t bw[8];
-                    base_words<8>(bw, first, second, bnd, S.base, rg + 2, S.rows, C);
-                    uint32_t out[8];
+                    const uint32_t A4 = A * 0x01010101u, B4 = B * 0x01010101u;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const uint32_t nib = (ow[g] >> (4 * k)) & 0xFu;
-                        out[k] = add_base(bw[k], (nib * 0x00204081u) & 0x01010101u);  // bit j -> byte j
+                        const uint32_t nib = (ow[gi] >> (4 * k)) & 0xFu;
+                        const uint32_t m = bytes_from(bg, k);
+                        out[k] = add_base((A4 & ~m) | (B4 & m), (nib * 0x00204081u) & 0x01010101u);  // bit j -> byte j
                     }
-                    if (xw[g]) {
+                } else {
+                    uint32_t bw[8];
+                    base_words_general<8>(bw, A, bg, S.base, row_a + rg + 1, S.rows, C);
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) patch_word<1>(out[k], (xw[g] >> (4 * k)) & 0xFu, S, xl, bad);
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t nib = (ow[gi] >> (4 * k)) & 0xFu;
+                        out[k] = add_base(bw[k], (nib * 0x00204081u) & 0x01010101u);
                     }
-                    store32(S.ws, S.ws_align, p + 32 * g, out, lo, hi);
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int s = 2 * gi + h;
+                    *reinterpret_cast<uint4 *>(my + 16 * (s ^ g)) =
+                        make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
                 }
                 qg += 32;
                 while (qg >= C) { qg -= C; ++rg; }
             }
+            if (cnt) {
+                const bool ok = xl <= nexc && cnt <= nexc - xl;
+                if (!ok) bad = true;
+#pragma unroll
+                for (int gi = 0; gi < 4; ++gi) {
+                    uint32_t f = xw[gi];
+                    while (f) {
+                        const uint32_t j = 32u * gi + (uint32_t)(__ffs(f) - 1);
+                        f &= f - 1;
+                        const uint8_t e = ok ? __ldg(S.exc_bytes + xl) : (uint8_t)0;
+                        ++xl;
+                        my[16 * ((j >> 4) ^ g) + (j & 15)] = e;
+                    }
+                }
+            }
+#pragma unroll
+            for (int gi = 0; gi < 4; ++gi) {
+                uint32_t out[8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(my + 16 * ((2 * gi + h) ^ g));
+                    out[4 * h] = v.x; out[4 * h + 1] = v.y; out[4 * h + 2] = v.z; out[4 * h + 3] = v.w;
+                }
+                const uint32_t pg = p + 32u * gi;
+                if (nv == kLaneMx && fast) st_v8(ws + pg, out);
+                else if (32 * gi < nv) store32(ws, S.ws_align, pg, out, lo_l, hi_l);
+            }
         }
     }
-    if (lane == 0) {
-        const uint64_t expect = __ldg(S.exc_index + row_b);
-        if (expect != X) bad = true;
-    }
+    if (lane == 0 && __ldg(S.exc_index + row_b) != X) bad = true;
     if (__any_sync(kFull, bad) && lane == 0) flag(S.err, CSF_DEV_ERR_CORRUPT);
 }
 
@@ -338,6 +443,7 @@ __device__ __forceinline__ uint64_t units_of_expert(const DecStack &S, uint64_t 
 template <bool ROUTED>
 __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_constant__ DecParams P) {
     extern __shared__ __align__(16) uint32_t smem[];
+    __shared__ __align__(16) uint8_t s_stage[kWarps][kStageBytes];
     __shared__ uint32_t s_wsum[3][kWarps];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -398,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
         T0 = (P.st[0].rows + P.st[0].rb - 1) / P.st[0].rb;
         T1 = P.nstacks > 1 ? (P.st[1].rows + P.st[1].rb - 1) / P.st[1].rb : 0;
     }
+    uint8_t *stage = s_stage[warp];
     const uint64_t T = T0 + T1;
     const uint64_t W = (uint64_t)gridDim.x * kWarps;
     const uint64_t w = (uint64_t)blockIdx.x * kWarps + warp;
@@ -413,9 +520,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
         const uint64_t rb = (uint64_t)S.rb;
         const uint64_t C = (uint64_t)S.C;
         if (!ROUTED) {
-            cnt = lend - lu;
+            cnt = min(lend - lu, S.max_units);
             row_a = lu * rb;
-            row_b = min(lend * rb, S.rows);
+            row_b = min((lu + cnt) * rb, S.rows);
             lo = row_a * C;
             hi = row_b * C;
         } else {
@@ -428,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             const uint64_t e = act[jl];
             const uint64_t R = (uint64_t)S.R;
             const uint64_t k = lu - up[jl];
-            cnt = min(lend, (uint64_t)up[jl + 1]) - lu;
+            cnt = min(min(lend, (uint64_t)up[jl + 1]) - lu, S.max_units);
             const uint64_t first_unit = (e * R) / rb;
             row_a = (first_unit + k) * rb;
             row_b = min((first_unit + k + cnt) * rb, S.rows);
@@ -436,9 +543,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             hi = min(row_b, (e + 1) * R) * C;
         }
         if (S.kind == CSF_NVFP4)
-            segment_nvfp4<2>(S, row_a, row_b, lo, hi, lane);
+            segment_nvfp4(S, row_a, row_b, lo, hi, lane, stage);
         else
-            segment_mxfp4<1>(S, row_a, row_b, lo, hi, lane);
+            segment_mxfp4(S, row_a, row_b, lo, hi, lane, stage);
         u += cnt;
     }
 }
@@ -453,7 +560,7 @@ cudaError_t decode_occupancy(bool routed, size_t smem, int *blocks_per_sm) {
 
 cudaError_t launch_decode(const DecParams &p, int grid, size_t smem, bool routed, cudaStream_t s) {
     if (routed) {
-        if (smem > 48 * 1024) {
+        if (smem > 16 * 1024) {
             cudaError_t e = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)smem);
             if (e != cudaSuccess) return e;

@@ -13,10 +13,15 @@ constexpr int kThreads = 256;               // threads per block, every kernel
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxRoutedExperts = 8192;     // routed decode keeps the active list in smem
 
-// NVFP4 chunk: 16 packed offset bytes = 32 elements.  MXFP4 chunk: 16 bytes of
-// each bit plane = 128 elements.  Decode work starts on chunk boundaries.
+// Prepare tiles start where the packed planes start a 16-byte piece:
+// 32 elements (NVFP4 nibbles), 128 elements (MXFP4 bits).
 constexpr int kChunkNv = 32;
 constexpr int kChunkMx = 128;
+// Decode lane chunks: NVFP4 64 elements (32 offset bytes -> 64 dense bytes),
+// MXFP4 128 elements (16 bytes of each plane -> 128 dense bytes).  Decode
+// segments start on lane-chunk boundaries.
+constexpr int kLaneNv = 64;
+constexpr int kLaneMx = 128;
 
 // One stack as the decode kernel sees it.
 struct DecStack {
@@ -34,10 +39,12 @@ struct DecStack {
     int32_t C;
     int32_t kind;
     int32_t rb;           // rows per work unit: smallest count whose elements fill whole chunks
-    uint32_t step_r;      // (32 chunks of elements) / C
-    uint32_t step_q;      // (32 chunks of elements) % C
-    int32_t ws_align;     // alignment of ws in bytes (32, 16, 8, 4 or 1)
-    int32_t pad_;
+    uint32_t step_r;      // (32 lane chunks of elements) / C
+    uint32_t step_q;      // (32 lane chunks of elements) % C
+    int32_t ws_align;     // alignment of ws in bytes (32, 16, 4 or 1)
+    int32_t off_align32;  // offsets pointer is 32-byte aligned (256-bit loads)
+    uint64_t off_bytes;   // readable bytes at offsets (packed length rounded up to 16)
+    uint64_t max_units;   // units per segment so that a segment stays below 2^30 elements
 };
 
 struct DecParams {
