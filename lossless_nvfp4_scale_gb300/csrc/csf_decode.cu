@@ -115,6 +115,16 @@ __device__ __forceinline__ uint32_t bytes_from(int b, int k) {
     return __funnelshift_lc(0u, 0xFFFFFFFFu, s);   // shift >= 32 gives 0
 }
 
+// Escape flags of the 8 elements of one offset word, in element order in
+// bits 0..7 (higher bits are garbage).  lo4 / hi4 hold the even / odd
+// elements' nibbles as bytes; nibble 15 + 1 carries into bit 4 of its byte.
+__device__ __forceinline__ uint32_t escape_flags8(uint32_t lo4, uint32_t hi4) {
+    const uint32_t zl = (lo4 + 0x01010101u) & 0x10101010u;   // element 2m -> bit 8m+4
+    const uint32_t zh = (hi4 + 0x01010101u) & 0x10101010u;   // element 2m+1 -> bit 8m+4
+    // bits 8m+4 / 8m+5 -> bits 2m / 2m+1 of the high product word
+    return __umulhi(zl + 2u * zh, 0x10410400u);
+}
+
 __device__ __forceinline__ void flag(uint32_t *err, uint32_t bits) {
     if (err) atomicOr(err, bits);
 }
@@ -166,7 +176,7 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
     if (lane == 0) X = __ldg(S.exc_index + row_a);
     X = __shfl_sync(kFull, X, 0);
     bool bad = false;
-    const uint32_t g = ((uint32_t)lane >> 1) & 3u;          // smem slot swizzle
+    const uint32_t gs = (((uint32_t)lane >> 1) & 3u) << 4;   // 16-byte slot swizzle (bank spread)
     uint8_t *my = stage + lane * 64;
 
     uint32_t rr = ((uint32_t)lane * kLaneNv) / C;
@@ -212,20 +222,32 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
         const uint32_t p = cc * kLaneNv;
         const int nv = cc < nch ? (int)min(nel - p, (uint32_t)kLaneNv) : 0;
         const int b = (int)(C - cq);                           // elements to the next row start
-        uint32_t out[16], t[8];
+        uint32_t out[16], fl[8];
         if (C >= kLaneNv) {
-            // At most one row boundary in the 64 elements.
+            // At most one row boundary in the 64 elements: bytes at or after
+            // element b take row B's base.
             const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u;
+            if (cA <= 240u && cB <= 240u) {
+                // base + 15 <= 255: a plain add cannot carry between bytes.
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t x = cw[i];
-                const uint32_t lo4 = x & 0x0F0F0F0Fu;
-                const uint32_t hi4 = (x >> 4) & 0x0F0F0F0Fu;
-                const uint32_t tt = x & (x >> 1);
-                t[i] = tt & (tt >> 2) & 0x11111111u;            // nibble == 15
-                const uint32_t m0 = bytes_from(b, 2 * i), m1 = bytes_from(b, 2 * i + 1);
-                out[2 * i] = add_base((A & ~m0) | (B & m0), __byte_perm(lo4, hi4, 0x5140));
-                out[2 * i + 1] = add_base((A & ~m1) | (B & m1), __byte_perm(lo4, hi4, 0x7362));
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t x = cw[i];
+                    const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
+                    fl[i] = escape_flags8(lo4, hi4);
+                    const uint32_t m0 = bytes_from(b, 2 * i), m1 = bytes_from(b, 2 * i + 1);
+                    out[2 * i] = ((A & ~m0) | (B & m0)) + __byte_perm(lo4, hi4, 0x5140);
+                    out[2 * i + 1] = ((A & ~m1) | (B & m1)) + __byte_perm(lo4, hi4, 0x7362);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t x = cw[i];
+                    const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
+                    fl[i] = escape_flags8(lo4, hi4);
+                    const uint32_t m0 = bytes_from(b, 2 * i), m1 = bytes_from(b, 2 * i + 1);
+                    out[2 * i] = add_base((A & ~m0) | (B & m0), __byte_perm(lo4, hi4, 0x5140));
+                    out[2 * i + 1] = add_base((A & ~m1) | (B & m1), __byte_perm(lo4, hi4, 0x7362));
+                }
             }
         } else {
             uint32_t bw[16];
@@ -233,53 +255,46 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const uint32_t x = cw[i];
-                const uint32_t lo4 = x & 0x0F0F0F0Fu;
-                const uint32_t hi4 = (x >> 4) & 0x0F0F0F0Fu;
-                const uint32_t tt = x & (x >> 1);
-                t[i] = tt & (tt >> 2) & 0x11111111u;
+                const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
+                fl[i] = escape_flags8(lo4, hi4);
                 out[2 * i] = add_base(bw[2 * i], __byte_perm(lo4, hi4, 0x5140));
                 out[2 * i + 1] = add_base(bw[2 * i + 1], __byte_perm(lo4, hi4, 0x7362));
             }
         }
+        // Element-ordered escape masks: bit j of f_h <-> element 32h + j.
+        uint32_t f0 = __byte_perm(__byte_perm(fl[0], fl[1], 0x0040), __byte_perm(fl[2], fl[3], 0x0040), 0x5410);
+        uint32_t f1 = __byte_perm(__byte_perm(fl[4], fl[5], 0x0040), __byte_perm(fl[6], fl[7], 0x0040), 0x5410);
         if (nv < kLaneNv) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int nvi = min(max(nv - 8 * i, 0), 8);
-                if (nvi < 8) t[i] &= (1u << (4 * nvi)) - 1u;
-            }
+            f0 &= nv >= 32 ? 0xFFFFFFFFu : (nv == 0 ? 0u : 0xFFFFFFFFu >> (32 - nv));
+            f1 &= nv <= 32 ? 0u : 0xFFFFFFFFu >> (64 - nv);
         }
-        const uint32_t cnt = __popc(t[0]) + __popc(t[1]) + __popc(t[2]) + __popc(t[3]) + __popc(t[4]) +
-                             __popc(t[5]) + __popc(t[6]) + __popc(t[7]);
+        const uint32_t cnt = __popc(f0) + __popc(f1);
         uint32_t tot;
         uint32_t xl = X + warp_excl_scan(cnt, lane, tot);
         X += tot;
         if (__any_sync(kFull, cnt != 0)) {
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                *reinterpret_cast<uint4 *>(my + 16 * (s ^ g)) =
+                *reinterpret_cast<uint4 *>(my + ((16 * s) ^ gs)) =
                     make_uint4(out[4 * s], out[4 * s + 1], out[4 * s + 2], out[4 * s + 3]);
             if (cnt) {
                 const bool ok = xl <= nexc && cnt <= nexc - xl;
                 if (!ok) bad = true;
-                // Words 2a and 2a+1 as one 64-bit mask: bit 4n <-> element
-                // 16a + n, so ascending bits visit escapes in element order,
-                // the order of the exception stream.
 #pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    uint64_t f = (uint64_t)t[2 * a] | ((uint64_t)t[2 * a + 1] << 32);
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t f = h ? f1 : f0;
                     while (f) {
-                        const uint32_t bp = (uint32_t)(__ffsll((long long)f) - 1);
+                        const uint32_t j = 32u * h + (uint32_t)(__ffs(f) - 1);
                         f &= f - 1;
-                        const uint32_t j = 16u * a + (bp >> 2);
                         const uint8_t e = ok ? __ldg(S.exc_bytes + xl) : (uint8_t)0;
                         ++xl;
-                        my[16 * ((j >> 4) ^ g) + (j & 15)] = e;
+                        my[j ^ gs] = e;
                     }
                 }
             }
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(my + 16 * (s ^ g));
+                const uint4 v = *reinterpret_cast<const uint4 *>(my + ((16 * s) ^ gs));
                 out[4 * s] = v.x; out[4 * s + 1] = v.y; out[4 * s + 2] = v.z; out[4 * s + 3] = v.w;
             }
         }
@@ -317,7 +332,7 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
     if (lane == 0) X = __ldg(S.exc_index + row_a);
     X = __shfl_sync(kFull, X, 0);
     bool bad = false;
-    const uint32_t g = (uint32_t)lane & 7u;                  // smem slot swizzle
+    const uint32_t gs = ((uint32_t)lane & 7u) << 4;          // 16-byte slot swizzle (bank spread)
     uint8_t *my = stage + lane * 128;
 
     uint32_t rr = ((uint32_t)lane * kLaneMx) / C;
@@ -377,11 +392,21 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                         B = rn == crr + 1 ? cB : (rn < rows_left ? (uint32_t)__ldg(bases + rn) : 0u);
                     }
                     const uint32_t A4 = A * 0x01010101u, B4 = B * 0x01010101u;
+                    if (A <= 254u && B <= 254u) {
+                        // base + 1 <= 255: a plain add cannot carry between bytes.
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t nib = (ow[gi] >> (4 * k)) & 0xFu;
-                        const uint32_t m = bytes_from(bg, k);
-                        out[k] = add_base((A4 & ~m) | (B4 & m), (nib * 0x00204081u) & 0x01010101u);  // bit j -> byte j
+                        for (int k = 0; k < 8; ++k) {
+                            const uint32_t nib = (ow[gi] >> (4 * k)) & 0xFu;
+                            const uint32_t m = bytes_from(bg, k);
+                            out[k] = ((A4 & ~m) | (B4 & m)) + ((nib * 0x00204081u) & 0x01010101u);  // bit j -> byte j
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const uint32_t nib = (ow[gi] >> (4 * k)) & 0xFu;
+                            const uint32_t m = bytes_from(bg, k);
+                            out[k] = add_base((A4 & ~m) | (B4 & m), (nib * 0x00204081u) & 0x01010101u);
+                        }
                     }
                 } else {
                     uint32_t bw[8];
@@ -395,7 +420,7 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int s = 2 * gi + h;
-                    *reinterpret_cast<uint4 *>(my + 16 * (s ^ g)) =
+                    *reinterpret_cast<uint4 *>(my + ((16 * s) ^ gs)) =
                         make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
                 }
                 qg += 32;
@@ -412,7 +437,7 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                         f &= f - 1;
                         const uint8_t e = ok ? __ldg(S.exc_bytes + xl) : (uint8_t)0;
                         ++xl;
-                        my[16 * ((j >> 4) ^ g) + (j & 15)] = e;
+                        my[j ^ gs] = e;
                     }
                 }
             }
@@ -421,7 +446,7 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                 uint32_t out[8];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(my + 16 * ((2 * gi + h) ^ g));
+                    const uint4 v = *reinterpret_cast<const uint4 *>(my + ((16 * (2 * gi + h)) ^ gs));
                     out[4 * h] = v.x; out[4 * h + 1] = v.y; out[4 * h + 2] = v.z; out[4 * h + 3] = v.w;
                 }
                 const uint32_t pg = p + 32u * gi;
