@@ -8,10 +8,12 @@ the same run (the "rows" object): routed 8-of-512 decode, paired gate+down
 decode (full and routed), GPU prepare of the gate stack, and MXFP4 prepare and
 decode (384 x 2048 x 160).
 
-Timing: every step is bracketed by CUDA events on the launching stream; steps
-are queued behind a device-side sleep so the stream never waits for the host;
-the stack and workspace rotate over 4 copies (328 MB > 129 MB L2), so every
-step reads and writes HBM.  nvidia-smi samples clocks during the timed region.
+Timing: the steps are captured in a CUDA graph (16 launches) and replayed back
+to back; CUDA events on the launching stream bracket the whole timed region,
+so a step's time is the region's time divided by the steps in it (launches
+overlap their ramp-up and drain the way they do in serving).  The stack and
+workspace rotate over 4 copies (321 MB > 129 MB L2), so every step reads and
+writes HBM.  nvidia-smi samples clocks during the timed region.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun every rank decodes its own stack (weak scaling, no collective
@@ -36,7 +38,6 @@ sys.path.insert(0, ROOT)
 METRIC = "CSF decode µs & dense-scale GB/s per 512-expert stack; % of HBM roofline"
 WORKLOAD = "gate 512x1024x100 NVFP4-CSF full-stack decode"
 FALLBACK_HBM_GBS = 6800.0
-QUEUE = 192          # steps queued behind one device sleep
 ROTATE = 4           # stack/workspace copies (working set > L2)
 
 
@@ -49,7 +50,7 @@ def peak_hbm():
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) while the timed region runs."""
+    """nvidia-smi samples (100 ms) while the timed region runs."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -63,7 +64,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -104,27 +105,33 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def timed_steps(torch, fn, steps, warmup):
-    """Run `fn(i)` for warmup + steps iterations; returns per-step device ms
-    for the timed steps.  Each block of QUEUE steps is queued behind a device
-    sleep so the events bracket only device work."""
-    for i in range(warmup):
-        fn(i)
+def timed_steps(torch, fn, steps, warmup, per_graph=16):
+    """Run `fn(i)` `warmup` times eagerly, capture `per_graph` calls into a CUDA
+    graph, then replay it back to back for at least `steps` calls with CUDA
+    events only around the whole timed region (on the launching stream).
+    Returns (total_ms, steps_done)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for i in range(warmup):
+            fn(i)
+    torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    durs = []
-    done = 0
-    while done < steps:
-        n = min(QUEUE, steps - done)
-        torch.cuda._sleep(40_000_000)     # ~20 ms: the host queues the block meanwhile
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
-        ev[0].record()
-        for j in range(n):
-            fn(warmup + done + j)
-            ev[j + 1].record()
-        torch.cuda.synchronize()
-        durs += [ev[j].elapsed_time(ev[j + 1]) for j in range(n)]
-        done += n
-    return durs
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(per_graph):
+            fn(i)
+    reps = max(1, -(-steps // per_graph))
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1), reps * per_graph
 
 
 def stack_traffic(st, rows_active=None):
@@ -163,27 +170,25 @@ def run_own(args, rank, world, torch, dist):
     torch.cuda.synchronize()
     with ClockSampler(dev) as clk:
         t0 = time.perf_counter()
-        durs = timed_steps(torch, step, args.steps, args.warmup)
+        total_ms, steps = timed_steps(torch, step, args.steps, args.warmup)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     if world > 1:
         dist.barrier()
     assert torch.equal(wss[0], gate_dense), "decode output differs from the dense stack"
     assert gate.errors() == 0
-    total_ms = sum(durs)
     if world > 1:
         t = torch.tensor([total_ms], device="cuda", dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
+    ms_per_step = total_ms / steps
     dense_gb = gate.dense_bytes / 1e9
-    value = world * dense_gb * args.steps / (total_ms / 1e3)
+    value = world * dense_gb * steps / (total_ms / 1e3)
     alg = stack_traffic(gate)
-    mean_ms = statistics.mean(durs)
-    achieved = alg / (mean_ms / 1e3) / 1e9
+    achieved = alg / (ms_per_step / 1e3) / 1e9
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded gate-shaped stack; the pages' checkpoint streams are not available)",
         "config": {"workload": WORKLOAD, "experts": 512, "rows": 1024, "cols": 100,
@@ -192,11 +197,10 @@ def run_own(args, rank, world, torch, dist):
                          f"({ROTATE * alg / 1e6:.0f} MB > 129 MB L2)",
                    "parallelism": f"replicas x{world} (independent stacks, no collective)"},
         "us_per_stack": round(1e3 * ms_per_step, 3),
-        "us_per_stack_median": round(1e3 * statistics.median(durs), 3),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "peak_source": peak_kind,
                      "traffic": profiled_traffic(), "algorithmic_bytes": int(alg)},
-        "gpu_launches": args.steps,
+        "gpu_launches": steps,
         "wall_s": round(wall, 3),
     }
     result["clocks"] = clk.summary()
@@ -246,21 +250,21 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
     active = int((start[1:] > start[:-1]).sum().item())
     ws = torch.full_like(gate_dense, 0xFF)
 
-    def rec(name, durs, alg, extra=None):
-        m = statistics.mean(durs)
-        d = {"us": round(1e3 * m, 3), "us_median": round(1e3 * statistics.median(durs), 3),
-             "algorithmic_MB": round(alg / 1e6, 3), "GB_s": round(alg / (m / 1e3) / 1e9, 1),
-             "hbm_frac": round(alg / (m / 1e3) / 1e9 / hbm, 4)}
+    def rec(name, timed, alg, extra=None):
+        m = timed[0] / timed[1]
+        d = {"us": round(1e3 * m, 3), "algorithmic_MB": round(alg / 1e6, 3),
+             "GB_s": round(alg / (m / 1e3) / 1e9, 1), "hbm_frac": round(alg / (m / 1e3) / 1e9 / hbm, 4)}
         if extra:
             d.update(extra)
         rows[name] = d
 
-    # routed 8 of 512 (latency-bound: report next to an empty-launch floor)
+    # routed 8 of 512: latency-bound, 1.25 MB, L2-warm like the pages' warm
+    # graph figure; reported next to an empty-launch floor
     durs = timed_steps(torch, lambda i: csf.decode(gate, ws, expert_start=start), 400, 20)
-    rec("routed_8of512", durs, stack_traffic(gate, rows_active=active * 1024))
+    rec("routed_8of512", durs, stack_traffic(gate, rows_active=active * 1024), {"l2": "warm"})
     z = torch.zeros(1, device="cuda")
     floor = timed_steps(torch, lambda i: z.add_(1), 400, 20)
-    rows["routed_8of512"]["empty_launch_floor_us"] = round(1e3 * statistics.mean(floor), 3)
+    rows["routed_8of512"]["empty_launch_floor_us"] = round(1e3 * floor[0] / floor[1], 3)
 
     # paired gate + down
     down_dense = torch.from_numpy(synth.down_stack(seed=0)).cuda()
@@ -274,17 +278,19 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
     rec("pair_full", durs, stack_traffic(gate) + stack_traffic(down))
     durs = timed_steps(torch, lambda i: csf.decode_pair(gate, down, gws, dws, expert_start=start), 400, 20)
     rec("pair_routed_8of512", durs,
-        stack_traffic(gate, rows_active=active * 1024) + stack_traffic(down, rows_active=active * 2048))
+        stack_traffic(gate, rows_active=active * 1024) + stack_traffic(down, rows_active=active * 2048),
+        {"l2": "warm"})
     del g2, d2, gws2, dws2, pairs
 
     # GPU prepare of the gate stack (reads dense once, writes the streams)
     E_, R_, C_ = gate.shape
-    pst = csf.empty_stack(csf.NVFP4, E_, R_, C_, exc_capacity=gate.dense_bytes)
-    scr = csf.prepare_scratch(csf.NVFP4, E_, R_, C_)
-    durs = timed_steps(torch, lambda i: csf.prepare_async(gate_dense, pst, scr), 100, 5)
+    psts = [csf.empty_stack(csf.NVFP4, E_, R_, C_, exc_capacity=gate.dense_bytes) for _ in range(2)]
+    scrs = [csf.prepare_scratch(csf.NVFP4, E_, R_, C_) for _ in range(2)]
+    dens = [gate_dense, gate_dense.clone()]                 # 2 rotating copies: 2 x 82 MB > L2
+    durs = timed_steps(torch, lambda i: csf.prepare_async(dens[i % 2], psts[i % 2], scrs[i % 2]), 100, 5)
     sb = gate.stream_bytes()
     rec("prepare_gate", durs, gate.dense_bytes + sb["offsets"] + sb["base"] + sb["exc_index"] + sb["exc_bytes"])
-    del pst, scr
+    del psts, scrs, dens
 
     # MXFP4: prepare + decode
     mx_dense = torch.from_numpy(synth.mxfp4_stack(seed=0)).cuda()
@@ -388,7 +394,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=50000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
     ap.add_argument("--skip-rows", action="store_true")

@@ -54,7 +54,7 @@ class CsfError(RuntimeError):
 
 
 def _load():
-    path = _build.LIB
+    path = os.environ.get("CSF_LIBRARY", _build.LIB)
     if not os.path.exists(path):
         raise CsfError(f"{path} is missing: build it with `python -m lossless_nvfp4_scale_gb300.build` "
                        "(there is no CPU fallback)")

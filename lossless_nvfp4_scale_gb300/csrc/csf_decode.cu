@@ -125,6 +125,17 @@ __device__ __forceinline__ uint32_t escape_flags8(uint32_t lo4, uint32_t hi4) {
     return __umulhi(zl + 2u * zh, 0x10410400u);
 }
 
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
+// Lanes 0..n-1 pull the next n 128-byte lines of the exception stream into L1
+// so the next step's exception reads hit.
+__device__ __forceinline__ void prefetch_exceptions(const DecStack &S, uint32_t x, int lane, int n) {
+    const uint64_t at = ((uint64_t)x & ~127ull) + 128ull * (uint64_t)lane;
+    if (lane < n && at < S.num_exc) prefetch_l1(S.exc_bytes + at);
+}
+
 __device__ __forceinline__ void flag(uint32_t *err, uint32_t bits) {
     if (err) atomicOr(err, bits);
 }
@@ -272,6 +283,7 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
         uint32_t tot;
         uint32_t xl = X + warp_excl_scan(cnt, lane, tot);
         X += tot;
+        prefetch_exceptions(S, X, lane, 2 + (int)(tot >> 7));
         if (__any_sync(kFull, cnt != 0)) {
 #pragma unroll
             for (int s = 0; s < 4; ++s)
@@ -375,6 +387,7 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
         uint32_t tot;
         uint32_t xl = X + warp_excl_scan(cnt, lane, tot);
         X += tot;
+        prefetch_exceptions(S, X, lane, min(32, 2 + (int)(tot >> 7)));
         if (nv > 0) {
             uint32_t rg = crr, qg = cq;                        // row / column of the group start
 #pragma unroll
@@ -465,8 +478,12 @@ __device__ __forceinline__ uint64_t units_of_expert(const DecStack &S, uint64_t 
     return ((e + 1) * R + rb - 1) / rb - (e * R) / rb;
 }
 
+#ifndef CSF_DECODE_MIN_BLOCKS
+#define CSF_DECODE_MIN_BLOCKS 3
+#endif
+
 template <bool ROUTED>
-__global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_constant__ DecParams P) {
+__global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel(const __grid_constant__ DecParams P) {
     extern __shared__ __align__(16) uint32_t smem[];
     __shared__ __align__(16) uint8_t s_stage[kWarps][kStageBytes];
     __shared__ uint32_t s_wsum[3][kWarps];
