@@ -290,18 +290,21 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                 *reinterpret_cast<uint4 *>(my + ((16 * s) ^ gs)) =
                     make_uint4(out[4 * s], out[4 * s + 1], out[4 * s + 2], out[4 * s + 3]);
             if (cnt) {
-                const bool ok = xl <= nexc && cnt <= nexc - xl;
-                if (!ok) bad = true;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t f = h ? f1 : f0;
+                if (xl <= nexc && cnt <= nexc - xl) {
+                    // The lane's exceptions are consecutive in the stream.
+                    const uint8_t *ep = S.exc_bytes + xl;
+                    uint32_t f = f0;
                     while (f) {
-                        const uint32_t j = 32u * h + (uint32_t)(__ffs(f) - 1);
+                        my[(uint32_t)(__ffs(f) - 1) ^ gs] = __ldg(ep++);
                         f &= f - 1;
-                        const uint8_t e = ok ? __ldg(S.exc_bytes + xl) : (uint8_t)0;
-                        ++xl;
-                        my[j ^ gs] = e;
                     }
+                    f = f1;
+                    while (f) {
+                        my[(uint32_t)(__ffs(f) + 31) ^ gs] = __ldg(ep++);
+                        f &= f - 1;
+                    }
+                } else {
+                    bad = true;   // index points past the stream: leave the bytes, report
                 }
             }
 #pragma unroll
@@ -440,18 +443,18 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                 while (qg >= C) { qg -= C; ++rg; }
             }
             if (cnt) {
-                const bool ok = xl <= nexc && cnt <= nexc - xl;
-                if (!ok) bad = true;
+                if (xl <= nexc && cnt <= nexc - xl) {
+                    const uint8_t *ep = S.exc_bytes + xl;
 #pragma unroll
-                for (int gi = 0; gi < 4; ++gi) {
-                    uint32_t f = xw[gi];
-                    while (f) {
-                        const uint32_t j = 32u * gi + (uint32_t)(__ffs(f) - 1);
-                        f &= f - 1;
-                        const uint8_t e = ok ? __ldg(S.exc_bytes + xl) : (uint8_t)0;
-                        ++xl;
-                        my[j ^ gs] = e;
+                    for (int gi = 0; gi < 4; ++gi) {
+                        uint32_t f = xw[gi];
+                        while (f) {
+                            my[(32u * gi + (uint32_t)(__ffs(f) - 1)) ^ gs] = __ldg(ep++);
+                            f &= f - 1;
+                        }
                     }
+                } else {
+                    bad = true;
                 }
             }
 #pragma unroll
