@@ -180,8 +180,8 @@ csf_status csf_prepare(const uint8_t *dense, csf_stack *out, uint64_t exc_capaci
  * capture.  Every call shares the one array and clears the part it uses on
  * `stream` first: calls that overlap on the GPU race, so order them.
  * Errors: as csf_prepare, plus CSF_ERR_SIZE when the geometry needs more than
- * CSF_STATIC_SCRATCH_BYTES of scratch (16 + 8 bytes per tile of rows; about
- * 5 million rows for NVFP4 with C = 100, 3 million for MXFP4 with C = 160).
+ * CSF_STATIC_SCRATCH_BYTES of scratch (16 + 8 bytes per tile of rows; tiles
+ * are 128 rows when C <= 255, so about 4 million rows).
  */
 csf_status csf_prepare_static(const uint8_t *dense, csf_stack *out, uint64_t exc_capacity, void *stream);
 

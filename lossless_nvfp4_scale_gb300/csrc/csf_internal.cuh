@@ -77,6 +77,8 @@ struct PrepParams {
     int32_t dense_aligned;       // dense pointer is 16-byte aligned
     uint32_t smem_dense;         // byte sizes of the dynamic smem regions
     uint32_t smem_planes;
+    int32_t stride;              // row stride of the staged tile (row-wise kernel)
+    int32_t pad_;
 };
 
 // Rows per unit so that a unit's first element starts a whole chunk.
@@ -91,6 +93,8 @@ cudaError_t launch_decode(const DecParams &p, int grid, size_t smem, bool routed
 cudaError_t decode_occupancy(bool routed, size_t smem, int *blocks_per_sm);
 
 cudaError_t launch_prepare(const PrepParams &p, size_t smem, cudaStream_t s);
+void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity,
+                      void *scratch, uint64_t rows, uint64_t n);
 size_t prepare_smem_bytes(int32_t kind, int32_t C, int32_t tr);
 int32_t prepare_tile_rows(int32_t kind, int32_t C);
 

@@ -33,6 +33,8 @@
 //      wait is bounded and reports CSF_DEV_ERR_TIMEOUT instead of hanging;
 //   5. write base bytes, planes, exc_index and the exception bytes at their
 //      global positions.
+#include <cstring>
+
 #include "csf_internal.cuh"
 
 namespace csfk {
@@ -79,6 +81,49 @@ __device__ __forceinline__ void st_release(unsigned long long *p, unsigned long 
 
 __device__ __forceinline__ void flag(uint32_t *err, uint32_t bits) {
     if (err) atomicOr(err, bits);
+}
+
+
+// Decoupled look-back (whole warp): publish this tile's exception total, then
+// walk back over earlier tiles' status words until an inclusive prefix is
+// found; publish this tile's inclusive prefix and return its exclusive one.
+// Tiles take ids from a ticket counter in start order, so every tile waited on
+// belongs to a block that is already running; each wait is bounded and sets
+// CSF_DEV_ERR_TIMEOUT instead of hanging.
+__device__ unsigned long long lookback_exclusive(const PrepParams &P, uint64_t tile, unsigned long long total,
+                                                 int lane) {
+    unsigned long long excl = 0;
+    bool timed_out = false;
+    if (lane == 0) st_release(&P.status[tile], (tile == 0 ? kFlagIncl : kFlagAgg) | total);
+    if (tile > 0) {
+        long long j = (long long)tile - 1;
+        while (true) {
+            const long long idx = j - lane;
+            unsigned long long v = kFlagIncl;   // before tile 0: inclusive zero
+            if (idx >= 0) {
+                v = ld_acquire(&P.status[idx]);
+                int spins = 0;
+                while ((v >> 62) == 0) {
+                    if (++spins > kSpinLimit) { timed_out = true; v = kFlagAgg; break; }
+                    __nanosleep(64);
+                    v = ld_acquire(&P.status[idx]);
+                }
+            }
+            const uint32_t incl = __ballot_sync(kFull, (v >> 62) == 2);
+            unsigned long long val = v & kValMask;
+            if (incl) {
+                const int first = __ffs(incl) - 1;
+                if (lane > first) val = 0;
+                excl += warp_sum64(val);
+                break;
+            }
+            excl += warp_sum64(val);
+            j -= 32;
+        }
+        if (lane == 0) st_release(&P.status[tile], kFlagIncl | (excl + total));
+    }
+    if (__any_sync(kFull, timed_out) && lane == 0) flag(P.err, CSF_DEV_ERR_TIMEOUT);
+    return excl;
 }
 
 __global__ void __launch_bounds__(kThreads) prepare_kernel(const __grid_constant__ PrepParams P) {
@@ -260,38 +305,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const __grid_constant
 
     // 4b. Decoupled look-back across tiles (warp 0).
     if (warp == 0) {
-        const unsigned long long total = btot;
-        unsigned long long excl = 0;
-        bool timed_out = false;
-        if (lane == 0) st_release(&P.status[tile], (tile == 0 ? kFlagIncl : kFlagAgg) | total);
-        if (tile > 0) {
-            long long j = (long long)tile - 1;
-            while (true) {
-                const long long idx = j - lane;
-                unsigned long long v = kFlagIncl;   // before tile 0: inclusive zero
-                if (idx >= 0) {
-                    v = ld_acquire(&P.status[idx]);
-                    int spins = 0;
-                    while ((v >> 62) == 0) {
-                        if (++spins > kSpinLimit) { timed_out = true; v = kFlagAgg; break; }
-                        __nanosleep(64);
-                        v = ld_acquire(&P.status[idx]);
-                    }
-                }
-                const uint32_t incl = __ballot_sync(kFull, (v >> 62) == 2);
-                unsigned long long val = v & kValMask;
-                if (incl) {
-                    const int first = __ffs(incl) - 1;
-                    if (lane > first) val = 0;
-                    excl += warp_sum64(val);
-                    break;
-                }
-                excl += warp_sum64(val);
-                j -= 32;
-            }
-            if (lane == 0) st_release(&P.status[tile], kFlagIncl | (excl + total));
-        }
-        if (__any_sync(kFull, timed_out) && lane == 0) flag(P.err, CSF_DEV_ERR_TIMEOUT);
+        const unsigned long long excl = lookback_exclusive(P, tile, btot, lane);
         if (lane == 0) s_excl = excl;
     }
     __syncthreads();
@@ -348,9 +362,290 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const __grid_constant
     if (__any_sync(kFull, over) && lane == 0) flag(P.err, CSF_DEV_ERR_CAPACITY);
 }
 
+
+// ---------------------------------------------------------------- row-wise
+
+// Rows (and threads) per block in the row-wise kernel; a multiple of every
+// chunk-alignment row count (it divides into 32 and 128-element pieces).
+constexpr int kRowTile = 128;
+
+// Row-wise prepare for C <= 255 (byte counters cannot overflow).  One thread
+// per row: a thread-private 256-bin histogram of byte counters (word k of
+// thread t at hist[k * kRowTile + t], so a warp's accesses hit 32 banks), an
+// occupancy mask of 8-bin groups, window counts for the occupied words only
+// (byte prefix sums for NVFP4, neighbour sums for MXFP4), and the packed
+// 16-bit key (count << 8 | 255 - value) whose maximum is the most bytes with
+// the smallest value.  The histogram area is reused to stage the tile's
+// exception bytes in row-major order for one coalesced copy-out.
+__global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_constant__ PrepParams P) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ unsigned int s_tile;
+    __shared__ unsigned long long s_excl;
+    __shared__ uint32_t s_wsum[kRowTile / 32];
+    __shared__ uint32_t s_total;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const uint32_t C = (uint32_t)P.C;
+    const bool nv = P.kind == CSF_NVFP4;
+    const uint32_t stride = (uint32_t)P.stride;
+
+    uint32_t *s_hist = reinterpret_cast<uint32_t *>(smem);            // 64 x kRowTile words
+    uint8_t *s_exc = smem;                                             // after the base pass
+    uint8_t *s_dense = smem + 256 * kRowTile;
+    uint8_t *s_planes = s_dense + P.smem_dense;
+    uint8_t *s_base = s_planes + P.smem_planes;
+    uint32_t *s_pre = reinterpret_cast<uint32_t *>(s_base + kRowTile);
+
+    if (tid == 0) s_tile = atomicAdd(P.ticket, 1u);
+    __syncthreads();
+    const uint64_t tile = s_tile;
+    if (tile >= P.num_tiles) return;
+    const uint64_t r0 = tile * (uint64_t)kRowTile;
+    const uint64_t r1 = min(r0 + (uint64_t)kRowTile, P.rows);
+    const int nr = (int)(r1 - r0);
+    const uint64_t e0 = r0 * C;
+    const uint32_t ne = (uint32_t)nr * C;
+
+    // 1. Zero the histograms and planes; stage the rows at `stride`.
+    for (int i = tid; i < 64 * kRowTile / 4; i += kRowTile)
+        reinterpret_cast<uint4 *>(s_hist)[i] = make_uint4(0, 0, 0, 0);
+    for (uint32_t i = tid; i < P.smem_planes / 16; i += kRowTile)
+        reinterpret_cast<uint4 *>(s_planes)[i] = make_uint4(0, 0, 0, 0);
+    {
+        const uint8_t *src = P.dense + e0;
+        if (stride == C) {
+            uint32_t done = 0;
+            if (P.dense_aligned) {
+                const uint32_t n16 = ne / 16;
+                for (uint32_t i = tid; i < n16; i += kRowTile)
+                    reinterpret_cast<uint4 *>(s_dense)[i] = __ldg(reinterpret_cast<const uint4 *>(src) + i);
+                done = n16 * 16;
+            }
+            for (uint32_t i = done + tid; i < ne; i += kRowTile) s_dense[i] = __ldg(src + i);
+        } else {
+            // C % 4 == 0 here: 4-byte words never straddle rows.
+            auto put = [&](uint32_t e, uint32_t w) {
+                const uint32_t row = (uint32_t)(((uint64_t)e * P.magic) >> 40);
+                *reinterpret_cast<uint32_t *>(s_dense + row * stride + (e - row * C)) = w;
+            };
+            uint32_t done = 0;
+            if (P.dense_aligned) {
+                const uint32_t n16 = ne / 16;
+                for (uint32_t i = tid; i < n16; i += kRowTile) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src) + i);
+                    put(16 * i, v.x); put(16 * i + 4, v.y); put(16 * i + 8, v.z); put(16 * i + 12, v.w);
+                }
+                done = n16 * 16;
+            }
+            for (uint32_t e = done + 4 * tid; e < ne; e += 4 * kRowTile) {
+                const uint32_t w = (uint32_t)__ldg(src + e) | ((uint32_t)__ldg(src + e + 1) << 8) |
+                                   ((uint32_t)__ldg(src + e + 2) << 16) | ((uint32_t)__ldg(src + e + 3) << 24);
+                put(e, w);
+            }
+        }
+    }
+    __syncthreads();
+
+    // 2. Base byte and exception count of this thread's row.
+    uint32_t base = 0, count = 0;
+    if (tid < nr) {
+        const uint8_t *row = s_dense + tid * stride;
+        uint32_t *h = s_hist + tid;
+        uint32_t occ = 0;
+        // Shared-memory reductions (no returned value): increments of the same
+        // word need no read-after-write chain through this thread.
+        auto add = [&](uint32_t v) {
+            atomicAdd(h + (v >> 2) * kRowTile, 1u << ((v & 3u) << 3));
+            occ |= 1u << (v >> 3);
+        };
+        if ((stride & 3u) == 0) {
+            const uint32_t *rw = reinterpret_cast<const uint32_t *>(row);
+            for (uint32_t k = 0; k < C / 4; ++k) {
+                const uint32_t x = rw[k];
+                add(x & 0xFFu); add((x >> 8) & 0xFFu); add((x >> 16) & 0xFFu); add(x >> 24);
+            }
+            for (uint32_t c = C & ~3u; c < C; ++c) add(row[c]);
+        } else {
+            for (uint32_t c = 0; c < C; ++c) add(row[c]);
+        }
+        uint32_t best = 0;
+        while (occ) {
+            const uint32_t g = (uint32_t)(__ffs(occ) - 1);
+            occ &= occ - 1;
+#pragma unroll
+            for (uint32_t m = 2 * g; m < 2 * g + 2; ++m) {
+                const uint32_t hm = h[m * kRowTile];
+                if (hm == 0) continue;
+                uint32_t W;
+                if (nv) {
+                    // window [v, v+14]: byte prefix sums over words m..m+4
+                    const uint32_t q0 = hm * 0x01010101u;
+                    uint32_t c = q0 >> 24;
+                    uint32_t q[4];
+#pragma unroll
+                    for (int i = 1; i <= 4; ++i) {
+                        const uint32_t hw = (m + i < 64) ? h[(m + i) * kRowTile] : 0u;
+                        q[i - 1] = hw * 0x01010101u + c * 0x01010101u;
+                        c = q[i - 1] >> 24;
+                    }
+                    W = __byte_perm(q[2], q[3], 0x5432) - (q0 << 8);
+                } else {
+                    // window [v, v+1]
+                    const uint32_t hn = (m + 1 < 64) ? h[(m + 1) * kRowTile] : 0u;
+                    W = hm + __byte_perm(hm, hn, 0x4321);
+                }
+                const uint32_t f = (((hm & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | hm) & 0x80808080u;
+                const uint32_t Wm = W & (f | (f - (f >> 7)));               // present values only
+                const uint32_t cm = 4u * m;
+                const uint32_t kE = (Wm & 0x00FF00FFu) * 256u + (0x00FD00FFu - cm * 0x00010001u);
+                const uint32_t kO = ((Wm >> 8) & 0x00FF00FFu) * 256u + (0x00FC00FEu - cm * 0x00010001u);
+                best = __vmaxu2(best, __vmaxu2(kE, kO));
+            }
+        }
+        const uint32_t key = max(best & 0xFFFFu, best >> 16);
+        base = 255u - (key & 0xFFu);
+        count = C - (key >> 8);
+        s_base[tid] = (uint8_t)base;
+    }
+
+    // 3. Block scan of the per-row counts.
+    uint32_t wtot;
+    const uint32_t wex = warp_excl_scan(count, lane, wtot);
+    if (lane == 0) s_wsum[warp] = wtot;
+    __syncthreads();   // also ends every histogram read: s_exc may overwrite it
+    uint32_t boff = 0, btot = 0;
+#pragma unroll
+    for (int w = 0; w < kRowTile / 32; ++w) {
+        if (w < warp) boff += s_wsum[w];
+        btot += s_wsum[w];
+    }
+    const uint32_t pre = boff + wex;
+    if (tid < nr) s_pre[tid] = pre;
+    if (tid == 0) s_total = btot;
+
+    // 4. Look-back across tiles (warp 0), overlapping the packing below.
+    if (warp == 0) {
+        const unsigned long long excl = lookback_exclusive(P, tile, btot, lane);
+        if (lane == 0) s_excl = excl;
+    }
+
+    // 5. Pack this row's planes; stage its exceptions at their tile position.
+    if (tid < nr) {
+        const uint8_t *row = s_dense + tid * stride;
+        uint32_t pos = pre;
+        uint32_t el = (uint32_t)tid * C;   // tile-local element index
+        const uint32_t w = nv ? 14u : 1u;
+        uint32_t *po = reinterpret_cast<uint32_t *>(s_planes);
+        uint32_t *px = reinterpret_cast<uint32_t *>(s_planes + P.smem_planes / 2);
+        // Codes of 4 elements: NVFP4 nibbles in bits 0..15, MXFP4 offset bits in
+        // bits 0..3 and escape bits in 4..7.
+        auto code4 = [&](uint32_t x, uint32_t nb) {
+            uint32_t cd = 0;
+#pragma unroll
+            for (uint32_t j = 0; j < 4; ++j) {
+                if (j < nb) {
+                    const uint32_t v = (x >> (8 * j)) & 0xFFu;
+                    const uint32_t d = v - base;
+                    const bool inside = v >= base && d <= w;
+                    if (!inside) s_exc[pos++] = (uint8_t)v;
+                    if (nv) cd |= (inside ? d : 15u) << (4 * j);
+                    else cd |= (inside ? (d << j) : (0x10u << j));
+                }
+            }
+            return cd;
+        };
+        uint32_t acc = 0, ax = 0;
+        auto flush = [&](bool force) {
+            if (nv) {
+                if ((el & 7u) == 0 || force) {
+                    if (acc) atomicOr(po + ((el - 1) >> 3), acc);
+                    acc = 0;
+                }
+            } else if ((el & 31u) == 0 || force) {
+                if (acc) atomicOr(po + ((el - 1) >> 5), acc);
+                if (ax) atomicOr(px + ((el - 1) >> 5), ax);
+                acc = ax = 0;
+            }
+        };
+        if ((stride & 3u) == 0 && (el & 3u) == 0) {
+            // Whole words; groups of 4 never straddle an output word.
+            const uint32_t *rw = reinterpret_cast<const uint32_t *>(row);
+            for (uint32_t k = 0; k < C / 4; ++k) {
+                const uint32_t cd = code4(rw[k], 4);
+                if (nv) acc |= cd << (4 * (el & 7u));
+                else { acc |= (cd & 0xFu) << (el & 31u); ax |= (cd >> 4) << (el & 31u); }
+                el += 4;
+                flush(k == C / 4 - 1 && (C & 3u) == 0);
+            }
+            for (uint32_t c = C & ~3u; c < C; ++c) {
+                const uint32_t cd = code4(row[c], 1);
+                if (nv) acc |= cd << (4 * (el & 7u));
+                else { acc |= (cd & 1u) << (el & 31u); ax |= ((cd >> 4) & 1u) << (el & 31u); }
+                ++el;
+                flush(c == C - 1);
+            }
+        } else {
+            for (uint32_t c = 0; c < C; ++c) {
+                const uint32_t cd = code4(row[c], 1);
+                if (nv) acc |= cd << (4 * (el & 7u));
+                else { acc |= (cd & 1u) << (el & 31u); ax |= ((cd >> 4) & 1u) << (el & 31u); }
+                ++el;
+                flush(c == C - 1);
+            }
+        }
+    }
+    __syncthreads();
+    const unsigned long long excl = s_excl;
+    const uint32_t total = s_total;
+
+    // 6. Outputs.
+    for (int k = tid; k < nr; k += kRowTile) {
+        P.exc_index[r0 + k] = (uint32_t)(excl + s_pre[k]);
+        P.base[r0 + k] = s_base[k];
+    }
+    if (tile == P.num_tiles - 1 && tid == 0) {
+        const unsigned long long all = excl + total;
+        P.exc_index[P.rows] = (uint32_t)all;
+        if (all > 0xFFFFFFFFull) flag(P.err, CSF_DEV_ERR_CAPACITY);
+    }
+    if (nv) {
+        const uint32_t nbytes = ((ne + 1) / 2 + 15) & ~15u;
+        uint4 *dst = reinterpret_cast<uint4 *>(P.offsets + e0 / 2);
+        for (uint32_t i = tid; i < nbytes / 16; i += kRowTile) dst[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
+    } else {
+        const uint32_t nbytes = ((ne + 7) / 8 + 15) & ~15u;
+        const uint32_t pbytes = P.smem_planes / 2;
+        uint4 *dso = reinterpret_cast<uint4 *>(P.offsets + e0 / 8);
+        uint4 *dse = reinterpret_cast<uint4 *>(P.escapes + e0 / 8);
+        for (uint32_t i = tid; i < nbytes / 16; i += kRowTile) {
+            dso[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
+            dse[i] = reinterpret_cast<const uint4 *>(s_planes + pbytes)[i];
+        }
+    }
+    bool over = false;
+    for (uint32_t i = tid; i < total; i += kRowTile) {
+        const unsigned long long pos = excl + i;
+        if (pos < P.exc_capacity) P.exc_bytes[pos] = s_exc[i];
+        else over = true;
+    }
+    if (over) flag(P.err, CSF_DEV_ERR_CAPACITY);
+}
+
 }  // namespace
 
+static bool rows_path(int32_t C) { return C <= 255; }
+
+// Smem row stride of the staged tile in the row-wise kernel: rows of C % 4 == 0
+// bytes are read as words, so their word stride is made odd (conflict-free).
+static int32_t rows_stride(int32_t C) {
+    if (C % 4 != 0) return C;
+    return ((C / 4) % 2 == 1) ? C : C + 4;
+}
+
 int32_t prepare_tile_rows(int32_t kind, int32_t C) {
+    if (rows_path(C)) return kRowTile;
     const int32_t rbp = unit_rows(C, kind == CSF_NVFP4 ? kChunkNv : kChunkMx);
     const int64_t per = (int64_t)rbp * C;
     int64_t k = 16384 / per;
@@ -360,14 +655,55 @@ int32_t prepare_tile_rows(int32_t kind, int32_t C) {
 
 static uint32_t round16(uint64_t v) { return (uint32_t)((v + 15) & ~15ull); }
 
+static uint32_t planes_bytes(int32_t kind, uint64_t te) {
+    return kind == CSF_NVFP4 ? round16((te + 1) / 2) : 2 * round16((te + 7) / 8);
+}
+
 size_t prepare_smem_bytes(int32_t kind, int32_t C, int32_t tr) {
     const uint64_t te = (uint64_t)tr * C;
-    const uint32_t dense = round16(te);
-    const uint32_t planes = kind == CSF_NVFP4 ? round16((te + 1) / 2) : 2 * round16((te + 7) / 8);
-    return (size_t)dense + planes + kWarps * 256 * 4 + (size_t)tr * 4 + round16(tr);
+    if (rows_path(C))
+        return 256u * kRowTile + round16((uint64_t)kRowTile * rows_stride(C)) + planes_bytes(kind, te) + kRowTile +
+               4u * kRowTile;
+    return (size_t)round16(te) + planes_bytes(kind, te) + kWarps * 256 * 4 + (size_t)tr * 4 + round16(tr);
+}
+
+void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity,
+                      void *scratch, uint64_t rows, uint64_t n) {
+    const csf_geometry &g = out.g;
+    const int32_t tr = prepare_tile_rows(g.kind, g.cols);
+    std::memset(&p, 0, sizeof p);
+    p.dense = dense;
+    p.base = out.base;
+    p.offsets = out.offsets;
+    p.escapes = out.escapes;
+    p.exc_index = out.exc_index;
+    p.exc_bytes = out.exc_bytes;
+    p.err = out.error_word;
+    p.ticket = static_cast<unsigned int *>(scratch);
+    p.status = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(scratch) + 16);
+    p.exc_capacity = exc_capacity;
+    p.rows = rows;
+    p.n = n;
+    p.num_tiles = (rows + tr - 1) / tr;
+    p.magic = ((1ull << 40) + (uint64_t)g.cols - 1) / (uint64_t)g.cols;
+    p.C = g.cols;
+    p.kind = g.kind;
+    p.tr = tr;
+    p.dense_aligned = (reinterpret_cast<uintptr_t>(dense) & 15u) == 0 ? 1 : 0;
+    const uint64_t te = (uint64_t)tr * g.cols;
+    p.stride = rows_path(g.cols) ? rows_stride(g.cols) : g.cols;
+    p.smem_dense = rows_path(g.cols) ? round16((uint64_t)kRowTile * p.stride) : round16(te);
+    p.smem_planes = planes_bytes(g.kind, te);
 }
 
 cudaError_t launch_prepare(const PrepParams &p, size_t smem, cudaStream_t s) {
+    if (rows_path(p.C)) {
+        cudaError_t e = cudaFuncSetAttribute(prepare_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        prepare_rows_kernel<<<(unsigned)p.num_tiles, kRowTile, smem, s>>>(p);
+        return cudaGetLastError();
+    }
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;

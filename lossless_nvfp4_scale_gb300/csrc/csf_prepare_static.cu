@@ -58,8 +58,6 @@ csf_status static_scratch(void **out) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-uint64_t round16(uint64_t v) { return (v + 15) & ~15ull; }
-
 }  // namespace
 
 extern "C" csf_status csf_prepare_static(const uint8_t *dense, csf_stack *out, uint64_t exc_capacity, void *stream) {
@@ -96,28 +94,7 @@ extern "C" csf_status csf_prepare_static(const uint8_t *dense, csf_stack *out, u
         return CSF_ERR_CUDA;
     }
     PrepParams p;
-    std::memset(&p, 0, sizeof p);
-    p.dense = dense;
-    p.base = out->base;
-    p.offsets = out->offsets;
-    p.escapes = out->escapes;
-    p.exc_index = out->exc_index;
-    p.exc_bytes = out->exc_bytes;
-    p.err = out->error_word;
-    p.ticket = static_cast<unsigned int *>(scratch);
-    p.status = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(scratch) + 16);
-    p.exc_capacity = exc_capacity;
-    p.rows = rows;
-    p.n = n;
-    p.num_tiles = tiles;
-    p.magic = ((1ull << 40) + (uint64_t)g.cols - 1) / (uint64_t)g.cols;
-    p.C = g.cols;
-    p.kind = g.kind;
-    p.tr = tr;
-    p.dense_aligned = aligned16(dense) ? 1 : 0;
-    const uint64_t te = (uint64_t)tr * g.cols;
-    p.smem_dense = (uint32_t)round16(te);
-    p.smem_planes = (uint32_t)(g.kind == CSF_NVFP4 ? round16((te + 1) / 2) : 2 * round16((te + 7) / 8));
+    make_prep_params(p, dense, *out, exc_capacity, scratch, rows, n);
     if (launch_prepare(p, smem, s) != cudaSuccess) {
         cudaGetLastError();
         return CSF_ERR_CUDA;
