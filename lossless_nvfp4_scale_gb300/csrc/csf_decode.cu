@@ -192,7 +192,7 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
 
     uint32_t rr = ((uint32_t)lane * kLaneNv) / C;
     uint32_t q = ((uint32_t)lane * kLaneNv) % C;
-    uint32_t w[8], bA = 0, bB = 0;
+    uint32_t w[8], bA = 0, bB = 0, bD = 0;
 
     auto load = [&](uint32_t c, uint32_t r) {
         if (c < nch) {
@@ -211,10 +211,11 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
             }
             bA = __ldg(bases + r);
             bB = (r + 1 < rows_left) ? (uint32_t)__ldg(bases + r + 1) : 0u;
+            if (C < kLaneNv) bD = (r + 2 < rows_left) ? (uint32_t)__ldg(bases + r + 2) : 0u;
         } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i) w[i] = 0;
-            bA = bB = 0;
+            bA = bB = bD = 0;
         }
     };
     load((uint32_t)lane, rr);
@@ -224,7 +225,7 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
         uint32_t cw[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) cw[i] = w[i];
-        const uint32_t cA = bA, cB = bB, cq = q, crr = rr;
+        const uint32_t cA = bA, cB = bB, cD = bD, cq = q, crr = rr;
         q += S.step_q;
         rr += S.step_r;
         if (q >= C) { q -= C; ++rr; }
@@ -258,6 +259,24 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                     const uint32_t m0 = bytes_from(b, 2 * i), m1 = bytes_from(b, 2 * i + 1);
                     out[2 * i] = add_base((A & ~m0) | (B & m0), __byte_perm(lo4, hi4, 0x5140));
                     out[2 * i + 1] = add_base((A & ~m1) | (B & m1), __byte_perm(lo4, hi4, 0x7362));
+                }
+            }
+        } else if (C >= 32) {
+            // At most two row boundaries in the 64 elements (at b and b + C).
+            const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u, D = cD * 0x01010101u;
+            const int b2 = b + (int)C;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t x = cw[i];
+                const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
+                fl[i] = escape_flags8(lo4, hi4);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int k = 2 * i + h;
+                    const uint32_t m1 = bytes_from(b, k), m2 = bytes_from(b2, k);
+                    const uint32_t bw = (((A & ~m1) | (B & m1)) & ~m2) | (D & m2);
+                    const uint32_t o = __byte_perm(lo4, hi4, h ? 0x7362 : 0x5140);
+                    out[k] = (cA <= 240u && cB <= 240u && cD <= 240u) ? bw + o : add_base(bw, o);
                 }
             }
         } else {

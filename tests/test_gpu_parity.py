@@ -54,7 +54,7 @@ def _dense_cuda(dense):
 
 SMALL = [
     (0, 1, 1, 1), (0, 1, 1, 31), (0, 3, 5, 7), (0, 2, 33, 17), (0, 5, 37, 100), (0, 7, 13, 3),
-    (0, 4, 64, 8), (0, 3, 40, 64), (0, 2, 3, 1000),
+    (0, 4, 64, 8), (0, 3, 40, 64), (0, 2, 3, 1000), (0, 5, 37, 50), (0, 3, 41, 33), (0, 2, 9, 63),
     (1, 1, 1, 1), (1, 3, 5, 7), (1, 2, 37, 160), (1, 4, 9, 33), (1, 3, 11, 128), (1, 2, 5, 500),
 ]
 
