@@ -134,6 +134,14 @@ def timed_steps(torch, fn, steps, warmup, per_graph=16):
     return e0.elapsed_time(e1), reps * per_graph
 
 
+def reduce_max(torch, dist, value, device):
+    """Maximum of a per-rank float over all ranks (the job's time is its slowest
+    rank's); no data-path collective exists, this is timing only."""
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def stack_traffic(st, rows_active=None):
     """Algorithmic bytes of one decode: packed streams read + dense written.
     Routed: only the active experts' share (their index entries are 8 bytes a
@@ -178,9 +186,7 @@ def run_own(args, rank, world, torch, dist):
     assert torch.equal(wss[0], gate_dense), "decode output differs from the dense stack"
     assert gate.errors() == 0
     if world > 1:
-        t = torch.tensor([total_ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = reduce_max(torch, dist, total_ms, "cuda")
     ms_per_step = total_ms / steps
     dense_gb = gate.dense_bytes / 1e9
     value = world * dense_gb * steps / (total_ms / 1e3)
