@@ -125,17 +125,6 @@ __device__ __forceinline__ uint32_t escape_flags8(uint32_t lo4, uint32_t hi4) {
     return __umulhi(zl + 2u * zh, 0x10410400u);
 }
 
-__device__ __forceinline__ void prefetch_l1(const void *p) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-}
-
-// Lanes 0..n-1 pull the next n 128-byte lines of the exception stream into L1
-// so the next step's exception reads hit.
-__device__ __forceinline__ void prefetch_exceptions(const DecStack &S, uint32_t x, int lane, int n) {
-    const uint64_t at = ((uint64_t)x & ~127ull) + 128ull * (uint64_t)lane;
-    if (lane < n && at < S.num_exc) prefetch_l1(S.exc_bytes + at);
-}
-
 __device__ __forceinline__ void flag(uint32_t *err, uint32_t bits) {
     if (err) atomicOr(err, bits);
 }
@@ -239,7 +228,19 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
             // At most one row boundary in the 64 elements: bytes at or after
             // element b take row B's base.
             const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u;
-            if (cA <= 240u && cB <= 240u) {
+            if (cA <= 240u && cB <= 240u && (C & 3u) == 0) {
+                // Row boundaries fall on whole words (C % 4 == 0) and base + 15
+                // <= 255 (a plain add cannot carry between bytes).
+                const int kb = b >> 2;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t x = cw[i];
+                    const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
+                    fl[i] = escape_flags8(lo4, hi4);
+                    out[2 * i] = (2 * i >= kb ? B : A) + __byte_perm(lo4, hi4, 0x5140);
+                    out[2 * i + 1] = (2 * i + 1 >= kb ? B : A) + __byte_perm(lo4, hi4, 0x7362);
+                }
+            } else if (cA <= 240u && cB <= 240u) {
                 // base + 15 <= 255: a plain add cannot carry between bytes.
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -302,7 +303,6 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
         uint32_t tot;
         uint32_t xl = X + warp_excl_scan(cnt, lane, tot);
         X += tot;
-        prefetch_exceptions(S, X, lane, 2 + (int)(tot >> 7));
         if (__any_sync(kFull, cnt != 0)) {
 #pragma unroll
             for (int s = 0; s < 4; ++s)
@@ -409,7 +409,6 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
         uint32_t tot;
         uint32_t xl = X + warp_excl_scan(cnt, lane, tot);
         X += tot;
-        prefetch_exceptions(S, X, lane, min(32, 2 + (int)(tot >> 7)));
         if (nv > 0) {
             uint32_t rg = crr, qg = cq;                        // row / column of the group start
 #pragma unroll
