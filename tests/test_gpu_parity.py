@@ -52,6 +52,18 @@ def _dense_cuda(dense):
     return torch.from_numpy(dense).cuda()
 
 
+def test_tiny_workload_seed0_round_trip(csf):
+    # The 4 x 64 x 8 NVFP4 workload (base U[0x20,0x60], offsets U{0..14}, 3%
+    # random bytes, seed 0): GPU encode and decode against the oracle.
+    dense = synth.stack("tiny")
+    enc = oracle.encode(0, dense)
+    st = csf.prepare(_dense_cuda(dense), 0)
+    assert st.errors() == 0
+    assert_stack_matches(st, enc)
+    assert np.array_equal(_np(csf.decode(st)), dense)
+    assert np.array_equal(_np(csf.decode(csf.upload(enc))), dense)
+
+
 SMALL = [
     (0, 1, 1, 1), (0, 1, 1, 31), (0, 3, 5, 7), (0, 2, 33, 17), (0, 5, 37, 100), (0, 7, 13, 3),
     (0, 4, 64, 8), (0, 3, 40, 64), (0, 2, 3, 1000), (0, 5, 37, 50), (0, 3, 41, 33), (0, 2, 9, 63),
