@@ -1,7 +1,7 @@
 """CPU oracle for the CSF scale codec -- TEST INFRASTRUCTURE ONLY.
 
 Plain, slow, single-threaded reference of what the CSF method computes
-(encode, decode, routed decode, index check), written in plain C
+(encode, decode, routed and row-range decode, index check), written in plain C
 (``csf_oracle.c``) and reached through ``ctypes``.  Only the test suite, the
 smoke check and the benchmark's CPU-baseline leg may import this package.  It
 shares no code with the CUDA library, and the product path never routes
@@ -66,7 +66,7 @@ def _load():
         lib.csfo_encode.restype = ctypes.c_int
         lib.csfo_decode.argtypes = [ctypes.c_int, _i64, _i64, _i64, _u8p, _u8p,
                                     _u8p, _u32p, _u8p, ctypes.c_uint64, _i64p,
-                                    _u8p]
+                                    _i64, _i64, _u8p]
         lib.csfo_decode.restype = ctypes.c_int
         lib.csfo_check.argtypes = [ctypes.c_int, _i64, _i64, _i64, _u8p, _u8p,
                                    _u32p, ctypes.c_uint64]
@@ -113,13 +113,15 @@ def encode(kind: int, dense: np.ndarray) -> dict:
             "exc_bytes": exc[:num.value].copy(), "num_exc": num.value}
 
 
-def decode(enc: dict, expert_start=None, out: np.ndarray | None = None):
+def decode(enc: dict, expert_start=None, out: np.ndarray | None = None, rows=None):
     """Decode a stack; returns (dense [E, R, C] uint8, status).
 
     ``expert_start`` (E+1 integers) selects the active experts; planes of
-    inactive experts in ``out`` are left as they were.
+    inactive experts in ``out`` are left as they were.  ``rows`` = (lo, hi)
+    writes only rows lo <= r < hi of each selected expert (default: all).
     """
     E, R, C = enc["shape"]
+    lo, hi = (0, R) if rows is None else rows
     if out is None:
         out = np.zeros((E, R, C), np.uint8)
     assert out.dtype == np.uint8 and out.shape == (E, R, C)
@@ -132,7 +134,7 @@ def decode(enc: dict, expert_start=None, out: np.ndarray | None = None):
                              _ptr(enc["offsets"], _u8p),
                              _ptr(enc["escapes"] if enc["escapes"].size else None, _u8p),
                              _ptr(enc["exc_index"], _u32p), _ptr(exc, _u8p),
-                             enc["num_exc"], _ptr(es, _i64p), _ptr(out, _u8p))
+                             enc["num_exc"], _ptr(es, _i64p), lo, hi, _ptr(out, _u8p))
     return out, st
 
 

@@ -37,6 +37,8 @@
  *     exc_index[row] + (number of earlier escapes in the same row).
  *   - routed decode: expert e is active iff start[e+1] > start[e]; planes of
  *     inactive experts are not written.
+ *   - row-range decode: only rows [row_lo, row_hi) of each written expert are
+ *     written (the gate half of a fused gate/up expert is rows [0, R/2)).
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -185,21 +187,25 @@ static unsigned offset_of(int kind, const uint8_t *offsets, uint64_t i)
 /*
  * Decode ([FK] format and helpers paragraphs).  expert_start is NULL for the
  * whole stack, else E+1 int64 entries; only experts with start[e+1] > start[e]
- * are written.  An exception reference past num_exc writes 0 and returns
- * CSFO_ERR_CORRUPT.
+ * are written.  Within each written expert only rows row_lo <= r < row_hi are
+ * written ([B478] pairing commit message: decode only the gate half that a
+ * fused gate/up consumer reads; 0 and R give every row).  An exception
+ * reference past num_exc writes 0 and returns CSFO_ERR_CORRUPT.
  */
 int csfo_decode(int kind, int64_t E, int64_t R, int64_t C,
                 const uint8_t *base, const uint8_t *offsets, const uint8_t *escapes,
                 const uint32_t *exc_index, const uint8_t *exc_bytes, uint64_t num_exc,
-                const int64_t *expert_start, uint8_t *out)
+                const int64_t *expert_start, int64_t row_lo, int64_t row_hi, uint8_t *out)
 {
     if ((kind != CSFO_NVFP4 && kind != CSFO_MXFP4) || E < 0 || R < 0 || C < 1)
+        return CSFO_ERR_ARG;
+    if (row_lo < 0 || row_hi > R || row_lo > row_hi)
         return CSFO_ERR_ARG;
     int status = CSFO_OK;
     for (int64_t e = 0; e < E; ++e) {
         if (expert_start != NULL && !(expert_start[e + 1] > expert_start[e]))
             continue;
-        for (int64_t r = 0; r < R; ++r) {
+        for (int64_t r = row_lo; r < row_hi; ++r) {
             uint64_t row = (uint64_t)e * (uint64_t)R + (uint64_t)r;
             uint64_t rank = 0;
             for (int64_t c = 0; c < C; ++c) {

@@ -221,6 +221,34 @@ def test_routed_decode_equals_masked_full_decode():
     assert np.array_equal(out2[1], dense[1]) and (out2[[0, 2, 3]] == 0xAA).all()
 
 
+@pytest.mark.parametrize("kind", [oracle.NVFP4, oracle.MXFP4])
+def test_row_range_decode_is_the_input_rows(kind):
+    """Row-range decode ("decode only consumed gate halves", [B478] pairing
+    commit message): rows [lo, hi) of each written expert are the original
+    input rows and every other byte keeps its old value.  Rows that start
+    mid-expert take their exceptions from their own index entry, which a
+    rank counted from the expert's first row would get wrong."""
+    E, R, C = 3, 10, 9
+    dense = synth.random_rows(7, E * R, C, spread=24, replace_p=0.3).reshape(E, R, C)
+    enc = oracle.encode(kind, dense)
+    assert enc["num_exc"] > 20
+    for lo, hi in [(0, R), (0, R // 2), (R // 2, R), (3, 4), (7, 10)]:
+        out, st = oracle.decode(enc, None, np.full(dense.shape, 0x5A, np.uint8), rows=(lo, hi))
+        assert st == oracle.OK
+        assert np.array_equal(out[:, lo:hi], dense[:, lo:hi])
+        assert (out[:, :lo] == 0x5A).all() and (out[:, hi:] == 0x5A).all()
+    # Routing and row range together; an empty range writes nothing.
+    start = np.array([0, 0, 2, 2], np.int64)               # expert 1 only
+    out, _ = oracle.decode(enc, start, np.full(dense.shape, 0x5A, np.uint8), rows=(2, 6))
+    assert np.array_equal(out[1, 2:6], dense[1, 2:6])
+    out[1, 2:6] = 0x5A
+    assert (out == 0x5A).all()
+    out, st = oracle.decode(enc, None, np.full(dense.shape, 0x5A, np.uint8), rows=(4, 4))
+    assert st == oracle.OK and (out == 0x5A).all()
+    for bad in [(-1, 3), (2, R + 1), (5, 4)]:
+        assert oracle.decode(enc, None, None, rows=bad)[1] == oracle.ERR_ARG
+
+
 # ------------------------------------------------------------------- sizes
 
 @pytest.mark.parametrize("kind,E,R,C", [(0, 3, 5, 7), (0, 2, 4, 100), (1, 3, 5, 7), (1, 2, 4, 160)])
