@@ -272,6 +272,15 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
     floor = timed_steps(torch, lambda i: z.add_(1), 400, 20)
     rows["routed_8of512"]["empty_launch_floor_us"] = round(1e3 * floor[0] / floor[1], 3)
 
+    # gate half of every expert (rows [0, R/2): the stack read as fused
+    # gate/up), rotating over 4 copies (4 x 40 MB of inputs > L2)
+    hc = [gate] + [clone_stack(torch, gate) for _ in range(3)]
+    hw = [torch.empty_like(gate_dense) for _ in range(4)]
+    durs = timed_steps(torch, lambda i: csf.decode(hc[i % 4], hw[i % 4], rows=(0, 512)), 400, 20)
+    assert torch.equal(hw[0][:, :512], gate_dense[:, :512])
+    rec("gate_half_all", durs, stack_traffic(gate, rows_active=512 * 512))
+    del hc, hw
+
     # paired gate + down
     down_dense = torch.from_numpy(synth.down_stack(seed=0)).cuda()
     down = csf.prepare(down_dense, csf.NVFP4)

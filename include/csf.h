@@ -67,7 +67,7 @@
 extern "C" {
 #endif
 
-#define CSF_ABI_VERSION 1
+#define CSF_ABI_VERSION 2
 
 typedef enum {
     CSF_OK = 0,
@@ -106,9 +106,10 @@ typedef struct {
 
 /*
  * A compressed stack: device buffers owned by the caller.  csf_prepare fills
- * them; csf_decode/csf_decode_pair read them.  `num_exc` is the host copy of
- * exc_index[rows] (the caller reads it once after prepare); `exc_bytes` must
- * be readable for num_exc bytes rounded up to a multiple of 16.
+ * them; csf_decode, csf_decode_pair and csf_decode_rows read them.  `num_exc`
+ * is the host copy of exc_index[rows] (the caller reads it once after
+ * prepare); `exc_bytes` must be readable for num_exc bytes rounded up to a
+ * multiple of 16.
  */
 typedef struct {
     csf_geometry g;
@@ -214,6 +215,35 @@ csf_status csf_decode(const csf_stack *s, uint8_t *ws, size_t ws_bytes,
  */
 csf_status csf_decode_pair(const csf_stack *gate, uint8_t *gate_ws, size_t gate_ws_bytes,
                            const csf_stack *down, uint8_t *down_ws, size_t down_ws_bytes,
+                           const void *expert_start, int expert_start_is_int64, void *stream);
+
+/* One stack of a csf_decode_rows call and the rows of each expert it writes. */
+typedef struct {
+    const csf_stack *stack; /* num_exc set */
+    uint8_t *ws;            /* device workspace, >= E*R*C bytes, [E][R][C], any byte alignment */
+    size_t ws_bytes;
+    int32_t row_lo;         /* rows row_lo <= r < row_hi of each selected expert are written; */
+    int32_t row_hi;         /* 0 <= row_lo < row_hi <= R */
+} csf_decode_part;
+
+/*
+ * Decode only a range of rows of each expert ([B478] pairing commit message:
+ * decode only the gate halves that a fused gate/up consumer reads).  For a
+ * fused gate/up stack with R = 2*I rows per expert, the gate half is rows
+ * [0, I).  The workspace keeps the [E][R][C] layout: rows outside the range,
+ * and the planes of experts that expert_start leaves inactive, are not
+ * touched.  One or two parts (for example the gate half of a gate/up stack
+ * and the whole down stack) decode in ONE launch with the same routing.
+ *
+ *   parts, num_parts  1 or 2 parts; every part must have the same number of
+ *                     experts.
+ *   expert_start      as csf_decode (NULL: every expert).
+ * Errors: CSF_ERR_ARG (bad part count, NULL stack, empty or out-of-range
+ * rows, differing expert counts, and the csf_decode cases), CSF_ERR_SIZE,
+ * CSF_ERR_UNSUPPORTED (E > 8192 with routing or a partial row range; the
+ * per-expert work list lives in shared memory), CSF_ERR_CUDA.
+ */
+csf_status csf_decode_rows(const csf_decode_part *parts, int num_parts,
                            const void *expert_start, int expert_start_is_int64, void *stream);
 
 #ifdef __cplusplus

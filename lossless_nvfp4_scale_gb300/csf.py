@@ -12,6 +12,7 @@ Typical use::
     csf.decode(stack, ws)                                 # whole stack
     csf.decode(stack, ws, expert_start=start_i32_cuda)    # routed experts only
     csf.decode_pair(gate, down, gate_ws, down_ws, expert_start)
+    csf.decode(stack, ws, rows=(0, R // 2))               # gate half of fused gate/up
 """
 from __future__ import annotations
 
@@ -49,6 +50,11 @@ class CStack(ctypes.Structure):
                 ("error_word", _c_vp)]
 
 
+class CDecodePart(ctypes.Structure):
+    _fields_ = [("stack", ctypes.POINTER(CStack)), ("ws", _c_vp), ("ws_bytes", ctypes.c_size_t),
+                ("row_lo", _c_i32), ("row_hi", _c_i32)]
+
+
 class CsfError(RuntimeError):
     pass
 
@@ -73,6 +79,8 @@ def _load():
                                     ctypes.POINTER(CStack), _c_vp, ctypes.c_size_t,
                                     _c_vp, ctypes.c_int, _c_vp]
     lib.csf_decode_pair.restype = ctypes.c_int
+    lib.csf_decode_rows.argtypes = [ctypes.POINTER(CDecodePart), ctypes.c_int, _c_vp, ctypes.c_int, _c_vp]
+    lib.csf_decode_rows.restype = ctypes.c_int
     return lib
 
 
@@ -236,15 +244,35 @@ def _check_es(stack: Stack, expert_start):
         raise CsfError("expert_start must have E+1 entries")
 
 
-def decode(stack: Stack, ws: torch.Tensor | None = None, expert_start: torch.Tensor | None = None,
-           stream=None) -> torch.Tensor:
-    """Decode into `ws` (uint8 CUDA, >= E*R*C bytes, any byte offset).  With
-    `expert_start` only experts with routed tokens are written."""
+def _ws_for(stack: Stack, ws, what: str) -> torch.Tensor:
     if ws is None:
         ws = torch.empty(stack.shape, dtype=torch.uint8, device=stack.base.device)
     if ws.dtype != torch.uint8 or not ws.is_cuda or not ws.is_contiguous():
-        raise CsfError("decode: ws must be a contiguous uint8 CUDA tensor")
+        raise CsfError(f"{what}: workspaces must be contiguous uint8 CUDA tensors")
+    return ws
+
+
+def _decode_rows(parts, expert_start, stream):
+    """Marshal (stack, ws, (lo, hi)) triples into one csf_decode_rows call."""
+    cs = [p[0].cstruct() for p in parts]
+    arr = (CDecodePart * len(parts))()
+    for i, ((stack, ws, rows), c) in enumerate(zip(parts, cs)):
+        lo, hi = (0, stack.R) if rows is None else rows
+        arr[i] = CDecodePart(ctypes.pointer(c), ws.data_ptr(), ws.numel(), lo, hi)
+    ptr, is64 = _es(expert_start)
+    _check(lib.csf_decode_rows(arr, len(parts), ptr, is64, _stream(stream)), "csf_decode_rows")
+
+
+def decode(stack: Stack, ws: torch.Tensor | None = None, expert_start: torch.Tensor | None = None,
+           stream=None, rows: tuple[int, int] | None = None) -> torch.Tensor:
+    """Decode into `ws` (uint8 CUDA, >= E*R*C bytes, any byte offset).  With
+    `expert_start` only experts with routed tokens are written; with
+    `rows=(lo, hi)` only rows lo <= r < hi of each of them (csf_decode_rows)."""
+    ws = _ws_for(stack, ws, "decode")
     _check_es(stack, expert_start)
+    if rows is not None:
+        _decode_rows([(stack, ws, rows)], expert_start, stream)
+        return ws
     ptr, is64 = _es(expert_start)
     cs = stack.cstruct()
     _check(lib.csf_decode(ctypes.byref(cs), ws.data_ptr(), ws.numel(), ptr, is64, _stream(stream)),
@@ -254,16 +282,16 @@ def decode(stack: Stack, ws: torch.Tensor | None = None, expert_start: torch.Ten
 
 def decode_pair(gate: Stack, down: Stack, gate_ws: torch.Tensor | None = None,
                 down_ws: torch.Tensor | None = None, expert_start: torch.Tensor | None = None,
-                stream=None):
-    """Decode a gate(/up) and a down stack in one launch with shared routing."""
-    if gate_ws is None:
-        gate_ws = torch.empty(gate.shape, dtype=torch.uint8, device=gate.base.device)
-    if down_ws is None:
-        down_ws = torch.empty(down.shape, dtype=torch.uint8, device=down.base.device)
-    for ws in (gate_ws, down_ws):
-        if ws.dtype != torch.uint8 or not ws.is_cuda or not ws.is_contiguous():
-            raise CsfError("decode_pair: workspaces must be contiguous uint8 CUDA tensors")
+                stream=None, gate_rows: tuple[int, int] | None = None,
+                down_rows: tuple[int, int] | None = None):
+    """Decode a gate(/up) and a down stack in one launch with shared routing;
+    `gate_rows`/`down_rows` restrict each to a row range of every expert."""
+    gate_ws = _ws_for(gate, gate_ws, "decode_pair")
+    down_ws = _ws_for(down, down_ws, "decode_pair")
     _check_es(gate, expert_start)
+    if gate_rows is not None or down_rows is not None:
+        _decode_rows([(gate, gate_ws, gate_rows), (down, down_ws, down_rows)], expert_start, stream)
+        return gate_ws, down_ws
     ptr, is64 = _es(expert_start)
     g, d = gate.cstruct(), down.cstruct()
     _check(lib.csf_decode_pair(ctypes.byref(g), gate_ws.data_ptr(), gate_ws.numel(),

@@ -112,56 +112,79 @@ csf_status fill_stack(const csf_stack *s, uint8_t *ws, size_t ws_bytes, DecStack
 uint64_t units_full(const DecStack &d) { return (d.rows + d.rb - 1) / d.rb; }
 
 uint64_t units_all_experts(const DecStack &d, int E) {
-    // Upper bound on the units of all experts: each expert can add one
-    // partial unit at each end.
-    return units_full(d) + (uint64_t)E;
+    // Upper bound on the units of all experts' row ranges: each expert can
+    // add one partial unit at each end.
+    const uint64_t span = (uint64_t)E * (uint64_t)(d.r_hi - d.r_lo);
+    return (span + d.rb - 1) / d.rb + 2ull * (uint64_t)E;
 }
 
-csf_status run_decode(const csf_stack *a, uint8_t *wa, size_t wa_bytes, const csf_stack *b, uint8_t *wb,
-                      size_t wb_bytes, const void *expert_start, int es64, void *stream) {
+csf_status run_decode(const csf_decode_part *parts, int nparts, const void *expert_start, int es64,
+                      void *stream) {
+    if (!parts || nparts < 1 || nparts > 2) return CSF_ERR_ARG;
     DecParams p;
     std::memset(&p, 0, sizeof p);
-    csf_status st = fill_stack(a, wa, wa_bytes, &p.st[0]);
-    if (st != CSF_OK) return st;
-    p.nstacks = 1;
-    if (b) {
-        st = fill_stack(b, wb, wb_bytes, &p.st[1]);
+    bool whole = true;
+    for (int i = 0; i < nparts; ++i) {
+        const csf_decode_part &q = parts[i];
+        csf_status st = fill_stack(q.stack, q.ws, q.ws_bytes, &p.st[i]);
         if (st != CSF_OK) return st;
-        if (b->g.num_experts != a->g.num_experts) return CSF_ERR_ARG;
-        p.nstacks = 2;
+        if (q.row_lo < 0 || q.row_lo >= q.row_hi || q.row_hi > q.stack->g.rows) return CSF_ERR_ARG;
+        p.st[i].r_lo = q.row_lo;
+        p.st[i].r_hi = q.row_hi;
+        const int32_t rb = p.st[i].rb;
+        if (q.stack->g.rows % rb == 0)
+            p.st[i].upe = (uint32_t)((q.row_hi + rb - 1) / rb - q.row_lo / rb);
+        if (q.row_lo != 0 || q.row_hi != q.stack->g.rows) whole = false;
+        if (q.stack->g.num_experts != parts[0].stack->g.num_experts) return CSF_ERR_ARG;
     }
-    p.E = a->g.num_experts;
+    p.nstacks = nparts;
+    p.uniform = 1;
+    for (int i = 0; i < nparts; ++i)
+        if (p.st[i].upe == 0) p.uniform = 0;
+    p.E = parts[0].stack->g.num_experts;
     p.expert_start = expert_start;
     p.es64 = es64 ? 1 : 0;
-    const bool routed = expert_start != nullptr;
-    if (routed && p.E > kMaxRoutedExperts) return CSF_ERR_UNSUPPORTED;
+    const bool per_expert = expert_start != nullptr || !whole;
+    if (per_expert && p.E > kMaxRoutedExperts) return CSF_ERR_UNSUPPORTED;
 
     DeviceInfo di;
-    st = device_info(&di);
+    csf_status st = device_info(&di);
     if (st != CSF_OK) return st;
     size_t smem = 0;
     int occ = di.occ_full;
     uint64_t units = 0;
-    if (routed) {
-        smem = 4ull * ((uint64_t)p.E + 2ull * ((uint64_t)p.E + 1));
+    if (per_expert) {
+        // Active list (E words); prefix arrays (2 x (E+1) words) unless uniform.
+        smem = p.uniform ? (expert_start ? 4ull * (uint64_t)p.E : 0)
+                         : 4ull * ((uint64_t)p.E + 2ull * ((uint64_t)p.E + 1));
         if (decode_occupancy(true, smem, &occ) != cudaSuccess) {
             cudaGetLastError();
             return CSF_ERR_CUDA;
         }
         if (occ < 1) occ = 1;
-        units = units_all_experts(p.st[0], p.E) + (p.nstacks > 1 ? units_all_experts(p.st[1], p.E) : 0);
+        for (int i = 0; i < nparts; ++i) units += units_all_experts(p.st[i], p.E);
     } else {
-        units = units_full(p.st[0]) + (p.nstacks > 1 ? units_full(p.st[1]) : 0);
+        for (int i = 0; i < nparts; ++i) units += units_full(p.st[i]);
     }
     uint64_t grid = (uint64_t)di.sms * (uint64_t)occ;
     const uint64_t need = (units + kWarps - 1) / kWarps;
     if (need < grid) grid = need;
     if (grid < 1) grid = 1;
-    if (launch_decode(p, (int)grid, smem, routed, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    if (launch_decode(p, (int)grid, smem, per_expert, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return CSF_ERR_CUDA;
     }
     return CSF_OK;
+}
+
+csf_decode_part whole_part(const csf_stack *s, uint8_t *ws, size_t ws_bytes) {
+    csf_decode_part q;
+    q.stack = s;
+    q.ws = ws;
+    q.ws_bytes = ws_bytes;
+    q.row_lo = 0;
+    q.row_hi = s ? s->g.rows : 0;
+    return q;
 }
 
 }  // namespace
@@ -241,15 +264,25 @@ csf_status csf_prepare(const uint8_t *dense, csf_stack *out, uint64_t exc_capaci
 
 csf_status csf_decode(const csf_stack *s, uint8_t *ws, size_t ws_bytes, const void *expert_start,
                       int expert_start_is_int64, void *stream) {
-    return run_decode(s, ws, ws_bytes, nullptr, nullptr, 0, expert_start, expert_start_is_int64, stream);
+    if (!s) return CSF_ERR_ARG;
+    const csf_decode_part q = whole_part(s, ws, ws_bytes);
+    return run_decode(&q, 1, expert_start, expert_start_is_int64, stream);
 }
 
 csf_status csf_decode_pair(const csf_stack *gate, uint8_t *gate_ws, size_t gate_ws_bytes, const csf_stack *down,
                            uint8_t *down_ws, size_t down_ws_bytes, const void *expert_start,
                            int expert_start_is_int64, void *stream) {
-    if (!down) return CSF_ERR_ARG;
-    return run_decode(gate, gate_ws, gate_ws_bytes, down, down_ws, down_ws_bytes, expert_start,
-                      expert_start_is_int64, stream);
+    if (!gate || !down) return CSF_ERR_ARG;
+    const csf_decode_part q[2] = {whole_part(gate, gate_ws, gate_ws_bytes), whole_part(down, down_ws, down_ws_bytes)};
+    return run_decode(q, 2, expert_start, expert_start_is_int64, stream);
+}
+
+csf_status csf_decode_rows(const csf_decode_part *parts, int num_parts, const void *expert_start,
+                           int expert_start_is_int64, void *stream) {
+    if (!parts || num_parts < 1 || num_parts > 2) return CSF_ERR_ARG;
+    for (int i = 0; i < num_parts; ++i)
+        if (!parts[i].stack) return CSF_ERR_ARG;
+    return run_decode(parts, num_parts, expert_start, expert_start_is_int64, stream);
 }
 
 }  // extern "C"

@@ -1,6 +1,7 @@
 // CSF decode kernel for sm_103a: rebuilds dense FP8 scale bytes from a
-// compressed stack, for the whole stack or only for routed experts, and for
-// one stack or a gate/down pair in the same launch.
+// compressed stack, for the whole stack or only for routed experts, for every
+// row of an expert or only a row range (the gate half of a fused gate/up
+// expert), and for one stack or a gate/down pair in the same launch.
 //
 // Pages followed (cited by title and paragraph; they have no numbered
 // sections):
@@ -13,8 +14,9 @@
 //   "NVFP4-CSF: expand_scales() for ahead-of-call scale expansion (canonical
 //     twin of #477)": commit messages on one-bit MXFP4 / four-bit NVFP4
 //     offsets, on pairing gate/up and down scales without extra streams,
-//     on both routing integer types, and on vectorised indexed
-//     reconstruction and exception lookup.
+//     on both routing integer types, on decoding only the gate halves a
+//     consumer reads, and on vectorised indexed reconstruction and
+//     exception lookup.
 //
 // Design (GB300 first; HBM-bound byte work, no tensor cores):
 //   * Work unit = a run of `rb` rows whose elements fill whole lane chunks
@@ -32,11 +34,14 @@
 //     and carry-free byte adds of the row bases.
 //   * Escapes are patched in a lane-private, bank-swizzled shared-memory slot
 //     (one byte store each); each 32 dense bytes leave with one 256-bit store.
-//   * Routed mode: every block compacts the active experts of `expert_start`
-//     into shared memory with ballots and prefix sums; the units of inactive
-//     experts never exist, so their workspace planes are never written.
-//   * A unit whose rows straddle an expert boundary (R*C not a multiple of the
-//     lane chunk) is decoded whole but stored only inside its expert's rows.
+//   * Per-expert mode (routing and/or row ranges): every block compacts the
+//     active experts of `expert_start` (all experts without it) into shared
+//     memory with ballots and prefix sums, each with the units that hold its
+//     rows [r_lo, r_hi); units of inactive experts and of rows outside the
+//     range never exist, so those workspace bytes are never written.
+//   * A unit whose rows straddle an expert or range boundary (R*C not a
+//     multiple of the lane chunk) is decoded whole but stored only inside the
+//     selected rows.
 #include "csf_internal.cuh"
 
 namespace csfk {
@@ -172,9 +177,6 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
     const bool fast = lo_l == 0 && hi_l == nel && S.ws_align >= 32;
     const bool v8ok = S.off_align32 != 0;
     const uint32_t nexc = (uint32_t)S.num_exc;
-    uint32_t X = 0;
-    if (lane == 0) X = __ldg(S.exc_index + row_a);
-    X = __shfl_sync(kFull, X, 0);
     bool bad = false;
     const uint32_t gs = (((uint32_t)lane >> 1) & 3u) << 4;   // 16-byte slot swizzle (bank spread)
     uint8_t *my = stage + lane * 64;
@@ -208,6 +210,13 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
         }
     };
     load((uint32_t)lane, rr);
+    // The index entries at both ends of the segment travel with the first
+    // piece: one memory round trip before the first expand.  Lane 1 keeps the
+    // end entry for the final check.
+    uint32_t X = 0, Xend = 0;
+    if (lane == 0) X = __ldg(S.exc_index + row_a);
+    if (lane == 1) Xend = __ldg(S.exc_index + row_b);
+    X = __shfl_sync(kFull, X, 0);
 
     for (uint32_t cb = 0; cb < nch; cb += 32) {
         const uint32_t cc = cb + lane;
@@ -340,7 +349,7 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
             if (nv > 32) store32(ws, S.ws_align, p + 32, out + 8, lo_l, hi_l);
         }
     }
-    if (lane == 0 && __ldg(S.exc_index + row_b) != X) bad = true;
+    if (lane == 1 && Xend != X) bad = true;
     if (__any_sync(kFull, bad) && lane == 0) flag(S.err, CSF_DEV_ERR_CORRUPT);
 }
 
@@ -362,9 +371,6 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
     const uint32_t hi_l = (uint32_t)(hi - sa);
     const bool fast = lo_l == 0 && hi_l == nel && S.ws_align >= 32;
     const uint32_t nexc = (uint32_t)S.num_exc;
-    uint32_t X = 0;
-    if (lane == 0) X = __ldg(S.exc_index + row_a);
-    X = __shfl_sync(kFull, X, 0);
     bool bad = false;
     const uint32_t gs = ((uint32_t)lane & 7u) << 4;          // 16-byte slot swizzle (bank spread)
     uint8_t *my = stage + lane * 128;
@@ -385,6 +391,10 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
         }
     };
     load((uint32_t)lane, rr);
+    uint32_t X = 0, Xend = 0;                                  // as in segment_nvfp4
+    if (lane == 0) X = __ldg(S.exc_index + row_a);
+    if (lane == 1) Xend = __ldg(S.exc_index + row_b);
+    X = __shfl_sync(kFull, X, 0);
 
     for (uint32_t cb = 0; cb < nch; cb += 32) {
         const uint32_t cc = cb + lane;
@@ -489,21 +499,26 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
             }
         }
     }
-    if (lane == 0 && __ldg(S.exc_index + row_b) != X) bad = true;
+    if (lane == 1 && Xend != X) bad = true;
     if (__any_sync(kFull, bad) && lane == 0) flag(S.err, CSF_DEV_ERR_CORRUPT);
 }
 
-__device__ __forceinline__ uint64_t units_of_expert(const DecStack &S, uint64_t e) {
-    const uint64_t R = (uint64_t)S.R;
-    const uint64_t rb = (uint64_t)S.rb;
-    return ((e + 1) * R + rb - 1) / rb - (e * R) / rb;
+// Units that hold rows [r_lo, r_hi) of expert e.
+// Rows stay below 2^31, so 32-bit arithmetic holds.
+__device__ __forceinline__ uint32_t units_of_expert(const DecStack &S, uint32_t e) {
+    const uint32_t r0 = e * (uint32_t)S.R + (uint32_t)S.r_lo;
+    const uint32_t r1 = e * (uint32_t)S.R + (uint32_t)S.r_hi;
+    const uint32_t rb = (uint32_t)S.rb;
+    return (r1 + rb - 1) / rb - r0 / rb;
 }
 
 #ifndef CSF_DECODE_MIN_BLOCKS
 #define CSF_DECODE_MIN_BLOCKS 3
 #endif
 
-template <bool ROUTED>
+// PER_EXPERT: the work list is built per selected expert (routing, row
+// ranges); otherwise it covers the whole stacks.
+template <bool PER_EXPERT>
 __global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel(const __grid_constant__ DecParams P) {
     extern __shared__ __align__(16) uint32_t smem[];
     __shared__ __align__(16) uint8_t s_stage[kWarps][kStageBytes];
@@ -515,14 +530,52 @@ __global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel
     uint32_t *act = smem;
     uint32_t *up0 = smem + P.E;
     uint32_t *up1 = up0 + P.E + 1;
-    if (ROUTED) {
-        // Active-expert compaction: expert e is active iff start[e+1] > start[e].
+    if (PER_EXPERT && P.uniform) {
+        // Every expert has upe units: only the active ids are needed (none
+        // without routing: expert j is entry j).
+        uint32_t run_n = (uint32_t)P.E;
+        if (P.expert_start != nullptr) {
+            run_n = 0;
+            for (int e0 = 0; e0 < P.E; e0 += kThreads) {
+                const int e = e0 + threadIdx.x;
+                bool a = false;
+                if (e < P.E) {
+                    if (P.es64) {
+                        const long long *st = static_cast<const long long *>(P.expert_start);
+                        a = __ldg(st + e + 1) > __ldg(st + e);
+                    } else {
+                        const int *st = static_cast<const int *>(P.expert_start);
+                        a = __ldg(st + e + 1) > __ldg(st + e);
+                    }
+                }
+                const uint32_t bal = __ballot_sync(kFull, a);
+                if (lane == 0) s_wsum[0][warp] = __popc(bal);
+                __syncthreads();
+                uint32_t bn = run_n, tn = 0;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    if (w < warp) bn += s_wsum[0][w];
+                    tn += s_wsum[0][w];
+                }
+                if (a) act[bn + __popc(bal & lanemask_lt())] = (uint32_t)e;
+                run_n += tn;
+                __syncthreads();
+            }
+        }
+        n_act = run_n;
+        T0 = (uint64_t)n_act * P.st[0].upe;
+        T1 = P.nstacks > 1 ? (uint64_t)n_act * P.st[1].upe : 0;
+    } else if (PER_EXPERT) {
+        // Active-expert compaction: expert e is active iff start[e+1] > start[e]
+        // (every expert without routing), with each stack's unit prefix.
         uint32_t run_n = 0, run0 = 0, run1 = 0;
         for (int e0 = 0; e0 < P.E; e0 += kThreads) {
             const int e = e0 + threadIdx.x;
             bool a = false;
             if (e < P.E) {
-                if (P.es64) {
+                if (P.expert_start == nullptr) {
+                    a = true;
+                } else if (P.es64) {
                     const long long *s = static_cast<const long long *>(P.expert_start);
                     a = __ldg(s + e + 1) > __ldg(s + e);
                 } else {
@@ -530,8 +583,8 @@ __global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel
                     a = __ldg(s + e + 1) > __ldg(s + e);
                 }
             }
-            const uint32_t u0 = a ? (uint32_t)units_of_expert(P.st[0], (uint64_t)e) : 0u;
-            const uint32_t u1 = (a && P.nstacks > 1) ? (uint32_t)units_of_expert(P.st[1], (uint64_t)e) : 0u;
+            const uint32_t u0 = a ? units_of_expert(P.st[0], (uint32_t)e) : 0u;
+            const uint32_t u1 = (a && P.nstacks > 1) ? units_of_expert(P.st[1], (uint32_t)e) : 0u;
             const uint32_t bal = __ballot_sync(kFull, a);
             uint32_t t0, t1;
             const uint32_t x0 = warp_excl_scan(u0, lane, t0);
@@ -582,28 +635,55 @@ __global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel
         uint64_t row_a, row_b, lo, hi, cnt;
         const uint64_t rb = (uint64_t)S.rb;
         const uint64_t C = (uint64_t)S.C;
-        if (!ROUTED) {
+        if (!PER_EXPERT) {
             cnt = min(lend - lu, S.max_units);
             row_a = lu * rb;
             row_b = min((lu + cnt) * rb, S.rows);
             lo = row_a * C;
             hi = row_b * C;
         } else {
-            const uint32_t *up = s ? up1 : up0;
-            uint32_t jl = 0, jh = n_act - 1;   // largest j with up[j] <= lu
-            while (jl < jh) {
-                const uint32_t mid = (jl + jh + 1) >> 1;
-                if ((uint64_t)up[mid] <= lu) jl = mid; else jh = mid - 1;
+            // Entry jl of the active list holds unit lu; the segment ends at
+            // the unit `u_end` where entry je starts.
+            uint32_t jl, je;
+            uint64_t k, u_end;
+            const bool routed = P.expert_start != nullptr;
+            // With whole experts that start on unit boundaries, the units of
+            // consecutive active experts are consecutive in the stack: one
+            // segment runs on through them.
+            const bool run_on = S.r_lo == 0 && S.r_hi == S.R && S.R % S.rb == 0;
+            if (P.uniform) {
+                const uint32_t U = S.upe;
+                jl = (uint32_t)(lu / U);
+                k = lu - (uint64_t)jl * U;
+                je = jl + 1;
+                if (run_on && routed)
+                    while (je < n_act && act[je] == act[je - 1] + 1 && (uint64_t)je * U < lend) ++je;
+                u_end = (uint64_t)je * U;
+            } else {
+                const uint32_t *up = s ? up1 : up0;
+                uint32_t jh = n_act - 1;            // largest jl with up[jl] <= lu
+                jl = 0;
+                while (jl < jh) {
+                    const uint32_t mid = (jl + jh + 1) >> 1;
+                    if ((uint64_t)up[mid] <= lu) jl = mid; else jh = mid - 1;
+                }
+                k = lu - up[jl];
+                je = jl + 1;
+                if (run_on)
+                    while (je < n_act && act[je] == act[je - 1] + 1 && (uint64_t)up[je] < lend) ++je;
+                u_end = up[je];
             }
-            const uint64_t e = act[jl];
+            const uint64_t e = routed || !P.uniform ? act[jl] : jl;
+            const uint64_t e_last = routed || !P.uniform ? act[je - 1] : je - 1;
             const uint64_t R = (uint64_t)S.R;
-            const uint64_t k = lu - up[jl];
-            cnt = min(min(lend, (uint64_t)up[jl + 1]) - lu, S.max_units);
-            const uint64_t first_unit = (e * R) / rb;
+            cnt = min(min(lend, u_end) - lu, S.max_units);
+            const uint64_t r0 = e * R + (uint64_t)S.r_lo;
+            const uint64_t r1 = e_last * R + (uint64_t)S.r_hi;
+            const uint64_t first_unit = r0 / rb;
             row_a = (first_unit + k) * rb;
             row_b = min((first_unit + k + cnt) * rb, S.rows);
-            lo = max(row_a, e * R) * C;
-            hi = min(row_b, (e + 1) * R) * C;
+            lo = max(row_a, r0) * C;
+            hi = min(row_b, r1) * C;
         }
         if (S.kind == CSF_NVFP4)
             segment_nvfp4(S, row_a, row_b, lo, hi, lane, stage);
@@ -615,14 +695,14 @@ __global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel
 
 }  // namespace
 
-cudaError_t decode_occupancy(bool routed, size_t smem, int *blocks_per_sm) {
-    if (routed)
+cudaError_t decode_occupancy(bool per_expert, size_t smem, int *blocks_per_sm) {
+    if (per_expert)
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<true>, kThreads, smem);
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<false>, kThreads, smem);
 }
 
-cudaError_t launch_decode(const DecParams &p, int grid, size_t smem, bool routed, cudaStream_t s) {
-    if (routed) {
+cudaError_t launch_decode(const DecParams &p, int grid, size_t smem, bool per_expert, cudaStream_t s) {
+    if (per_expert) {
         if (smem > 16 * 1024) {
             cudaError_t e = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)smem);

@@ -45,15 +45,19 @@ struct DecStack {
     int32_t off_align32;  // offsets pointer is 32-byte aligned (256-bit loads)
     uint64_t off_bytes;   // readable bytes at offsets (packed length rounded up to 16)
     uint64_t max_units;   // units per segment so that a segment stays below 2^30 elements
+    int32_t r_lo;         // rows [r_lo, r_hi) of each expert are written (0, R: all)
+    int32_t r_hi;
+    uint32_t upe;         // units per expert when R % rb == 0 (every expert alike), else 0
+    uint32_t pad_;
 };
 
 struct DecParams {
     DecStack st[2];
     int32_t nstacks;
     int32_t E;
-    const void *expert_start;   // null: whole stacks
+    const void *expert_start;   // null: every expert
     int32_t es64;
-    int32_t pad_;
+    int32_t uniform;            // every stack has R % rb == 0: unit -> expert is a division
 };
 
 struct PrepParams {

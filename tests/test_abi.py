@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(csf):
 
 
 def test_abi_version_and_status_strings(csf):
-    assert csf.lib.csf_abi_version() == 1
+    assert csf.lib.csf_abi_version() == 2
     for code, text in [(0, "ok"), (1, "invalid argument"), (2, "buffer too small"),
                        (3, "unsupported geometry"), (4, "CUDA error")]:
         assert csf.lib.csf_status_string(code).decode() == text
@@ -82,3 +82,34 @@ def test_null_arguments_rejected_before_cuda(csf):
     # routed decode with too many experts for the shared-memory active list.
     big = csf.CStack(csf.Geometry(0, 8193, 1, 32), 16, 16, None, 16, 16, 0, None)
     assert csf.lib.csf_decode(ctypes.byref(big), 16, 8193 * 32, 16, 0, None) == 3
+
+
+def test_decode_rows_argument_checks_before_cuda(csf):
+    # csf_decode_rows rejects bad part counts and row ranges on the host,
+    # before any CUDA call (the pointers below are never dereferenced).
+    g = csf.Geometry(0, 2, 10, 32)
+    st = csf.CStack(g, 16, 16, None, 16, 16, 0, None)
+
+    def parts(*ranges, stack=st):
+        arr = (csf.CDecodePart * len(ranges))()
+        for i, (lo, hi) in enumerate(ranges):
+            arr[i] = csf.CDecodePart(ctypes.pointer(stack), 16, 1 << 30, lo, hi)
+        return arr
+
+    assert csf.lib.csf_decode_rows(None, 1, None, 0, None) == 1
+    assert csf.lib.csf_decode_rows(parts((0, 5)), 0, None, 0, None) == 1
+    assert csf.lib.csf_decode_rows(parts((0, 5), (0, 5), (0, 5)), 3, None, 0, None) == 1
+    for bad in [(-1, 5), (5, 5), (6, 5), (0, 11)]:
+        assert csf.lib.csf_decode_rows(parts(bad), 1, None, 0, None) == 1, bad
+    nul = (csf.CDecodePart * 1)()
+    nul[0] = csf.CDecodePart(None, 16, 640, 0, 5)
+    assert csf.lib.csf_decode_rows(nul, 1, None, 0, None) == 1
+    # Parts with different expert counts.
+    other = csf.CStack(csf.Geometry(0, 3, 10, 32), 16, 16, None, 16, 16, 0, None)
+    two = (csf.CDecodePart * 2)()
+    two[0] = csf.CDecodePart(ctypes.pointer(st), 16, 640, 0, 5)
+    two[1] = csf.CDecodePart(ctypes.pointer(other), 16, 960, 0, 5)
+    assert csf.lib.csf_decode_rows(two, 2, None, 0, None) == 1
+    # A partial row range keeps the per-expert work list in shared memory.
+    big = csf.CStack(csf.Geometry(0, 8193, 2, 32), 16, 16, None, 16, 16, 0, None)
+    assert csf.lib.csf_decode_rows(parts((0, 1), stack=big), 1, None, 0, None) == 3

@@ -6,7 +6,8 @@ from the oracle only.  Covers small ragged geometries (several work units,
 ragged tails, odd C, C < chunk), the full-size stacks of the pages' workloads
 (512 x 1024 x 100 gate, 512 x 2048 x 50 down, 384 x 2048 x 160 MXFP4) in the
 launch configuration the benchmark times, routed decode into a poisoned
-workspace, paired decode, odd-offset workspaces with guard bytes, CUDA-graph
+workspace, row-range decode (the gate half of a fused gate/up stack), paired
+decode, odd-offset workspaces with guard bytes, CUDA-graph
 replay, both routing integer types, and corrupt or over-capacity inputs
 (planted on the CPU) reported through the device error word.
 """
@@ -111,6 +112,25 @@ def test_routed_small_poisoned(csf, kind, E, R, C, is64):
     assert up.errors() == 0
 
 
+@pytest.mark.parametrize("kind,E,R,C", [(0, 12, 32, 100), (0, 7, 64, 50), (1, 10, 8, 160), (0, 6, 5, 7)])
+def test_routed_runs_of_consecutive_experts(csf, kind, E, R, C):
+    # Runs of consecutive active experts (one segment may run through a run
+    # when experts start on unit boundaries), with gaps, at both ends, and
+    # with a warp range that ends inside a run.
+    dense = _small_dense(kind, E, R, C, seed=E + R + C)
+    enc = oracle.encode(kind, dense)
+    up = csf.upload(enc)
+    patterns = [np.ones(E, np.int64), np.r_[np.ones(3), np.zeros(1), np.ones(E - 4)],
+                np.r_[np.zeros(1), np.ones(E - 2), np.zeros(1)], (np.arange(E) % 3 != 1).astype(np.int64)]
+    for counts in patterns:
+        start = np.concatenate([[0], np.cumsum(counts.astype(np.int64))])
+        ws = torch.full(dense.shape, 0xFF, dtype=torch.uint8, device="cuda")
+        csf.decode(up, ws, expert_start=torch.from_numpy(start).cuda())
+        want, _ = oracle.decode(enc, start, np.full(dense.shape, 0xFF, np.uint8))
+        assert np.array_equal(_np(ws), want), counts
+    assert up.errors() == 0
+
+
 def test_routed_edge_cases(csf):
     dense = _small_dense(0, 8, 16, 100, seed=3)
     enc = oracle.encode(0, dense)
@@ -128,6 +148,65 @@ def test_routed_edge_cases(csf):
         csf.decode(up, ws, expert_start=torch.from_numpy(start.astype(np.int32)).cuda())
         want, _ = oracle.decode(enc, start, np.full(dense.shape, 0xFF, np.uint8))
         assert np.array_equal(_np(ws), want), name
+
+
+# Rows per expert that are (second line) and are not (first line) a multiple
+# of the rows of one work unit: equal or varying unit counts per expert.
+ROW_RANGE_SHAPES = [(0, 5, 10, 7), (0, 4, 38, 100), (0, 3, 12, 50), (0, 6, 9, 3), (1, 4, 10, 33),
+                    (1, 3, 38, 160),
+                    (0, 4, 32, 100), (0, 5, 64, 50), (0, 3, 64, 8), (1, 3, 8, 160), (1, 2, 128, 33)]
+
+
+@pytest.mark.parametrize("kind,E,R,C", ROW_RANGE_SHAPES)
+@pytest.mark.parametrize("routed", [False, True])
+def test_row_range_small_poisoned(csf, kind, E, R, C, routed):
+    # Rows [lo, hi) of each (routed) expert against the oracle, into a
+    # poisoned workspace: halves of a fused gate/up expert, single rows at
+    # either end, a range that starts mid-unit, and the whole expert.
+    dense = _small_dense(kind, E, R, C, seed=11 + C + R)
+    enc = oracle.encode(kind, dense)
+    up = csf.upload(enc)
+    start = None
+    if routed:
+        counts = np.zeros(E, np.int64)
+        counts[[0, E - 1]] = [3, 1]
+        start = np.concatenate([[0], np.cumsum(counts)])
+    es = None if start is None else torch.from_numpy(start.astype(np.int32)).cuda()
+    for lo, hi in [(0, R // 2), (R // 2, R), (0, 1), (R - 1, R), (1, R - 1), (3, 7), (0, R)]:
+        ws = torch.full(dense.shape, 0xFF, dtype=torch.uint8, device="cuda")
+        csf.decode(up, ws, expert_start=es, rows=(lo, hi))
+        want, st = oracle.decode(enc, start, np.full(dense.shape, 0xFF, np.uint8), rows=(lo, hi))
+        assert st == oracle.OK
+        assert np.array_equal(_np(ws), want), (lo, hi)
+    assert up.errors() == 0
+
+
+@pytest.mark.parametrize("offset", [0, 1, 16])
+@pytest.mark.parametrize("routed", [False, True])
+@pytest.mark.parametrize("I,Rd", [(19, 37), (16, 64), (16, 37)])
+def test_row_range_pair_gate_half_and_down(csf, offset, routed, I, Rd):
+    # A fused gate/up stack (R = 2*I rows per expert) decodes only its gate
+    # half [0, I) while the down stack decodes whole, in one launch, into
+    # odd-offset workspaces with guard bytes.
+    E = 6
+    gu = _small_dense(0, E, 2 * I, 100, seed=5)
+    dn = _small_dense(0, E, Rd, 50, seed=6)
+    genc, denc = oracle.encode(0, gu), oracle.encode(0, dn)
+    g_up, d_up = csf.upload(genc), csf.upload(denc)
+    start = np.array([0, 2, 2, 5, 5, 5, 6], np.int64) if routed else None
+    es = None if start is None else torch.from_numpy(start).cuda()
+    gbuf = torch.full((gu.size + 64,), 0xAB, dtype=torch.uint8, device="cuda")
+    dbuf = torch.full((dn.size + 64,), 0xAB, dtype=torch.uint8, device="cuda")
+    gws, dws = gbuf[offset:offset + gu.size], dbuf[offset:offset + dn.size]
+    csf.decode_pair(g_up, d_up, gws, dws, expert_start=es, gate_rows=(0, I))
+    gwant, _ = oracle.decode(genc, start, np.full(gu.shape, 0xAB, np.uint8), rows=(0, I))
+    dwant, _ = oracle.decode(denc, start, np.full(dn.shape, 0xAB, np.uint8))
+    gh, dh = _np(gbuf), _np(dbuf)
+    assert np.array_equal(gh[offset:offset + gu.size], gwant.ravel())
+    assert np.array_equal(dh[offset:offset + dn.size], dwant.ravel())
+    assert (gh[:offset] == 0xAB).all() and (gh[offset + gu.size:] == 0xAB).all()
+    assert (dh[:offset] == 0xAB).all() and (dh[offset + dn.size:] == 0xAB).all()
+    assert g_up.errors() == 0 and d_up.errors() == 0
 
 
 @pytest.mark.parametrize("offset", [0, 1, 3, 8, 15, 16, 17])
@@ -271,6 +350,29 @@ def test_full_gate_routed_8_of_512_poisoned(csf, gate, is64):
     mask[torch.from_numpy(active).cuda()] = True
     assert torch.equal(ws[mask], d[mask])
     assert bool((ws[~mask] == 0xFF).all())
+
+
+@pytest.mark.parametrize("routed", [False, True])
+def test_full_gate_row_range(csf, gate, routed):
+    # The full gate stack read as fused gate/up (rows [0, 512) of each
+    # 1024-row expert are the gate half), in the launch the benchmark times.
+    dense, enc = gate
+    d = _dense_cuda(dense)
+    up = csf.upload(enc)
+    es = None
+    mask = torch.ones(512, dtype=torch.bool, device="cuda")
+    if routed:
+        start = synth.routing(E=512, active=8, tokens=64, seed=0)
+        es = torch.from_numpy(start).cuda()
+        mask[:] = False
+        mask[torch.from_numpy(np.flatnonzero(np.diff(start.astype(np.int64)) > 0)).cuda()] = True
+    for lo, hi in [(0, 512), (512, 1024), (5, 1000)]:
+        ws = torch.full_like(d, 0xFF)
+        csf.decode(up, ws, expert_start=es, rows=(lo, hi))
+        assert torch.equal(ws[mask][:, lo:hi], d[mask][:, lo:hi])
+        assert bool((ws[mask][:, :lo] == 0xFF).all()) and bool((ws[mask][:, hi:] == 0xFF).all())
+        assert bool((ws[~mask] == 0xFF).all())
+    assert up.errors() == 0
 
 
 def test_full_pair_decode(csf, gate, down):
