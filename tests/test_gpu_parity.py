@@ -209,6 +209,29 @@ def test_row_range_pair_gate_half_and_down(csf, offset, routed, I, Rd):
     assert g_up.errors() == 0 and d_up.errors() == 0
 
 
+@pytest.mark.parametrize("shift", [0, 1, 3, 8])
+@pytest.mark.parametrize("kind,E,R,C,replace_p", [(0, 5, 64, 100, 0.02), (0, 3, 40, 100, 0.3),
+                                                  (1, 3, 16, 160, 0.05)])
+def test_exception_stream_at_any_alignment(csf, shift, kind, E, R, C, replace_p):
+    # The exception stream may start at any byte (the decoder stages it in
+    # 16-byte pieces only when it is 16-byte aligned); sparse and dense
+    # exception rates (a warp step's exceptions within or beyond one staged
+    # chunk).
+    w = 14 if kind == 0 else 1
+    dense = synth.random_rows(shift + C, E * R, C, spread=w + 3, replace_p=replace_p).reshape(E, R, C)
+    enc = oracle.encode(kind, dense)
+    up = csf.upload(enc)
+    n = up.num_exc
+    pad = (n + 15) // 16 * 16
+    buf = torch.full((pad + 32,), 0xEE, dtype=torch.uint8, device="cuda")
+    buf[shift:shift + n].copy_(up.exc_bytes[:n])
+    up.exc_bytes = buf[shift:shift + pad + 16]
+    ws = torch.full(dense.shape, 0x5A, dtype=torch.uint8, device="cuda")
+    csf.decode(up, ws)
+    assert np.array_equal(_np(ws), dense)
+    assert up.errors() == 0
+
+
 @pytest.mark.parametrize("offset", [0, 1, 3, 8, 15, 16, 17])
 def test_odd_offset_workspace_with_guards(csf, offset):
     for kind, shape in ((0, (3, 40, 100)), (1, (2, 37, 160))):
