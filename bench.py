@@ -297,6 +297,47 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
         {"l2": "warm"})
     del g2, d2, gws2, dws2, pairs
 
+    # ahead-of-call expansion: the gate + down pair expanded on a side stream
+    # while the launching stream runs other work of the layer, joined before
+    # the step ends.  Two stand-ins for that work: a latency-bound chain of 24
+    # small kernels (the GPU mostly idle), and a bf16 GEMM that fills every SM.
+    ga = torch.randn(4096, 2048, device="cuda", dtype=torch.bfloat16)
+    gb = torch.randn(2048, 4096, device="cuda", dtype=torch.bfloat16)
+    gc = torch.empty(4096, 4096, device="cuda", dtype=torch.bfloat16)
+    small = torch.ones(1 << 16, device="cuda")
+    side = torch.cuda.Stream()
+
+    def chain(i):
+        for _ in range(24):
+            small.mul_(1.0000001)
+
+    def gemm(i):
+        torch.matmul(ga, gb, out=gc)
+
+    def overlapped(work):
+        def f(i):
+            cur = torch.cuda.current_stream()
+            ready = torch.cuda.Event()
+            ready.record(cur)
+            ev = csf.expand_scales([(gate, gws), (down, dws)], side, after=ready)
+            work(i)
+            cur.wait_event(ev)
+        return f
+
+    def us(fn):
+        t = timed_steps(torch, fn, 200, 10)
+        return 1e3 * t[0] / t[1]
+
+    ue = us(lambda i: csf.expand_scales([(gate, gws), (down, dws)]))
+    row = {"expand_us": round(ue, 3)}
+    for name, work in (("latency_bound_chain", chain), ("gemm_bf16_4096x4096x2048", gemm)):
+        uw = us(work)
+        ub = us(overlapped(work))
+        row[name] = {"work_us": round(uw, 3), "both_us": round(ub, 3), "hidden_frac": round((uw + ue - ub) / ue, 3)}
+    assert torch.equal(gws, gate_dense) and torch.equal(dws, down_dense)
+    rows["expand_side_stream"] = row
+    del ga, gb, gc, small
+
     # GPU prepare of the gate stack (reads dense once, writes the streams)
     E_, R_, C_ = gate.shape
     psts = [csf.empty_stack(csf.NVFP4, E_, R_, C_, exc_capacity=gate.dense_bytes) for _ in range(2)]

@@ -22,6 +22,9 @@
  *           four-bit NVFP4 offsets from a row base byte, on pairing gate/up
  *           and down scales without extra streams, on both routing integer
  *           types, and on caller-owned scratch.
+ *   [B477] "NVFP4-CSF: expand_scales() for ahead-of-call scale expansion":
+ *           body (expansion into the shared scratch ahead of the call, on a
+ *           side stream, with the caller ordering the streams).
  *   [V964] "Load native FP4 experts with optional lossless CSF scales":
  *           GPU encoding plus exception index at preparation time.
  *
@@ -245,6 +248,34 @@ typedef struct {
  */
 csf_status csf_decode_rows(const csf_decode_part *parts, int num_parts,
                            const void *expert_start, int expert_start_is_int64, void *stream);
+
+/*
+ * Ahead-of-call expansion ([B477] body and [B478] commit message on
+ * expand_scales): expand every expert of one layer's stacks into their shared
+ * workspaces before the call that reads them, typically on a side stream
+ * while other work (that layer's attention) runs, so the expansion leaves the
+ * critical path.  The caller orders the streams; this call takes the two
+ * events that do it:
+ *
+ *   parts, num_parts  as csf_decode_rows; every expert is written (the
+ *                     routing is not known yet), rows [row_lo, row_hi) of
+ *                     each.
+ *   after          optional cudaEvent_t recorded by the previous user of the
+ *                  workspaces (the call that read them last); `stream` waits
+ *                  for it before the expansion writes.  NULL: no wait.
+ *   done           optional cudaEvent_t recorded on `stream` once the
+ *                  expansion is complete; the consumer's stream waits for it
+ *                  before its first read.  NULL: not recorded.
+ *   stream         the (side) stream that runs the expansion.
+ * Same bytes as csf_decode_rows with expert_start NULL; no host
+ * synchronisation.  Arguments are checked before anything is enqueued.
+ * The expansion uses the full persistent grid: it overlaps well with work
+ * that leaves SMs idle (latency-bound kernels), not with kernels that fill
+ * every SM.
+ * Errors: as csf_decode_rows; CSF_ERR_CUDA when the wait or the record fails
+ * (a wait may already be enqueued when the launch or the record fails).
+ */
+csf_status csf_expand(const csf_decode_part *parts, int num_parts, void *after, void *done, void *stream);
 
 #ifdef __cplusplus
 }

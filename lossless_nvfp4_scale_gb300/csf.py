@@ -13,6 +13,8 @@ Typical use::
     csf.decode(stack, ws, expert_start=start_i32_cuda)    # routed experts only
     csf.decode_pair(gate, down, gate_ws, down_ws, expert_start)
     csf.decode(stack, ws, rows=(0, R // 2))               # gate half of fused gate/up
+    ev = csf.expand_scales([(gate, gate_ws), (down, down_ws)], side_stream, after=last_read)
+    torch.cuda.current_stream().wait_event(ev)            # before the call that reads them
 """
 from __future__ import annotations
 
@@ -81,6 +83,8 @@ def _load():
     lib.csf_decode_pair.restype = ctypes.c_int
     lib.csf_decode_rows.argtypes = [ctypes.POINTER(CDecodePart), ctypes.c_int, _c_vp, ctypes.c_int, _c_vp]
     lib.csf_decode_rows.restype = ctypes.c_int
+    lib.csf_expand.argtypes = [ctypes.POINTER(CDecodePart), ctypes.c_int, _c_vp, _c_vp, _c_vp]
+    lib.csf_expand.restype = ctypes.c_int
     return lib
 
 
@@ -252,15 +256,63 @@ def _ws_for(stack: Stack, ws, what: str) -> torch.Tensor:
     return ws
 
 
-def _decode_rows(parts, expert_start, stream):
-    """Marshal (stack, ws, (lo, hi)) triples into one csf_decode_rows call."""
+def _parts(parts):
+    """Marshal (stack, ws, (lo, hi) or None) triples into csf_decode_part
+    structs; returns the array and the stack structs it points to."""
     cs = [p[0].cstruct() for p in parts]
     arr = (CDecodePart * len(parts))()
     for i, ((stack, ws, rows), c) in enumerate(zip(parts, cs)):
         lo, hi = (0, stack.R) if rows is None else rows
         arr[i] = CDecodePart(ctypes.pointer(c), ws.data_ptr(), ws.numel(), lo, hi)
+    return arr, cs
+
+
+def _decode_rows(parts, expert_start, stream):
+    arr, _keep = _parts(parts)
     ptr, is64 = _es(expert_start)
     _check(lib.csf_decode_rows(arr, len(parts), ptr, is64, _stream(stream)), "csf_decode_rows")
+
+
+def _event_handle(ev, stream) -> int:
+    # torch creates the CUDA event at its first record; record it once on the
+    # stream that will use it so that a handle exists (a later record or wait
+    # through the library supersedes this one).
+    if ev.cuda_event == 0:
+        ev.record(stream)
+    return ev.cuda_event
+
+
+def expand_scales(parts, stream=None, after: torch.cuda.Event | None = None,
+                  done: torch.cuda.Event | None = None) -> torch.cuda.Event | bool:
+    """Ahead-of-call expansion (csf_expand): decode every expert of the given
+    stacks into their workspaces on `stream` (a side stream, typically),
+    after `after` (recorded by the previous reader of the workspaces), and
+    record `done` for the consumer to wait on.
+
+    `parts` is a list of (stack, ws) or (stack, ws, (lo, hi)); entries whose
+    stack is None (scales that are not compressed) are skipped, and False is
+    returned when nothing is left to expand."""
+    todo = [(p[0], _ws_for(p[0], p[1], "expand_scales"), p[2] if len(p) > 2 else None)
+            for p in parts if p[0] is not None]
+    if not todo:
+        return False
+    s = stream if stream is not None else torch.cuda.current_stream()
+    after_h = None
+    if after is not None:
+        if after.cuda_event == 0:
+            raise CsfError("expand_scales: `after` has never been recorded")
+        after_h = after.cuda_event
+        s.wait_event(after)        # before the handle record below (csf_expand waits again)
+    if done is None:
+        done = torch.cuda.Event()
+    done_h = _event_handle(done, s)
+    for i in range(0, len(todo), 2):
+        chunk = todo[i:i + 2]
+        arr, _keep = _parts(chunk)
+        last = i + 2 >= len(todo)
+        _check(lib.csf_expand(arr, len(chunk), after_h if i == 0 else None, done_h if last else None,
+                              s.cuda_stream), "csf_expand")
+    return done
 
 
 def decode(stack: Stack, ws: torch.Tensor | None = None, expert_start: torch.Tensor | None = None,

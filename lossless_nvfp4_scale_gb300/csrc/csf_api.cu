@@ -118,10 +118,20 @@ uint64_t units_all_experts(const DecStack &d, int E) {
     return (span + d.rb - 1) / d.rb + 2ull * (uint64_t)E;
 }
 
-csf_status run_decode(const csf_decode_part *parts, int nparts, const void *expert_start, int es64,
-                      void *stream) {
-    if (!parts || nparts < 1 || nparts > 2) return CSF_ERR_ARG;
+// A checked decode launch: parameters, grid and shared memory.  Building it
+// has no side effect, so callers can enqueue stream waits only once the
+// arguments are known to be good.
+struct DecodeLaunch {
     DecParams p;
+    size_t smem;
+    int grid;
+    bool per_expert;
+};
+
+csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *expert_start, int es64,
+                       DecodeLaunch *L) {
+    if (!parts || nparts < 1 || nparts > 2) return CSF_ERR_ARG;
+    DecParams &p = L->p;
     std::memset(&p, 0, sizeof p);
     bool whole = true;
     for (int i = 0; i < nparts; ++i) {
@@ -170,11 +180,26 @@ csf_status run_decode(const csf_decode_part *parts, int nparts, const void *expe
     const uint64_t need = (units + kWarps - 1) / kWarps;
     if (need < grid) grid = need;
     if (grid < 1) grid = 1;
-    if (launch_decode(p, (int)grid, smem, per_expert, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    L->smem = smem;
+    L->grid = (int)grid;
+    L->per_expert = per_expert;
+    return CSF_OK;
+}
+
+csf_status launch(const DecodeLaunch &L, void *stream) {
+    if (launch_decode(L.p, L.grid, L.smem, L.per_expert, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return CSF_ERR_CUDA;
     }
     return CSF_OK;
+}
+
+csf_status run_decode(const csf_decode_part *parts, int nparts, const void *expert_start, int es64,
+                      void *stream) {
+    DecodeLaunch L;
+    csf_status st = plan_decode(parts, nparts, expert_start, es64, &L);
+    if (st != CSF_OK) return st;
+    return launch(L, stream);
 }
 
 csf_decode_part whole_part(const csf_stack *s, uint8_t *ws, size_t ws_bytes) {
@@ -283,6 +308,27 @@ csf_status csf_decode_rows(const csf_decode_part *parts, int num_parts, const vo
     for (int i = 0; i < num_parts; ++i)
         if (!parts[i].stack) return CSF_ERR_ARG;
     return run_decode(parts, num_parts, expert_start, expert_start_is_int64, stream);
+}
+
+csf_status csf_expand(const csf_decode_part *parts, int num_parts, void *after, void *done, void *stream) {
+    if (!parts || num_parts < 1 || num_parts > 2) return CSF_ERR_ARG;
+    for (int i = 0; i < num_parts; ++i)
+        if (!parts[i].stack) return CSF_ERR_ARG;
+    DecodeLaunch L;
+    csf_status st = plan_decode(parts, num_parts, nullptr, 0, &L);
+    if (st != CSF_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (after && cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(after), 0) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    st = launch(L, stream);
+    if (st != CSF_OK) return st;
+    if (done && cudaEventRecord(static_cast<cudaEvent_t>(done), s) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    return CSF_OK;
 }
 
 }  // extern "C"

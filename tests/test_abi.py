@@ -113,3 +113,21 @@ def test_decode_rows_argument_checks_before_cuda(csf):
     # A partial row range keeps the per-expert work list in shared memory.
     big = csf.CStack(csf.Geometry(0, 8193, 2, 32), 16, 16, None, 16, 16, 0, None)
     assert csf.lib.csf_decode_rows(parts((0, 1), stack=big), 1, None, 0, None) == 3
+
+
+def test_expand_argument_checks_before_cuda(csf):
+    # csf_expand checks its parts before it enqueues a wait, a launch or a
+    # record (nothing below reaches the CUDA runtime).
+    st = csf.CStack(csf.Geometry(0, 2, 10, 32), 16, 16, None, 16, 16, 0, None)
+    assert csf.lib.csf_expand(None, 1, None, None, None) == 1
+    arr = (csf.CDecodePart * 3)()
+    for i in range(3):
+        arr[i] = csf.CDecodePart(ctypes.pointer(st), 16, 1 << 20, 0, 10)
+    assert csf.lib.csf_expand(arr, 0, None, None, None) == 1
+    assert csf.lib.csf_expand(arr, 3, None, None, None) == 1
+    bad = (csf.CDecodePart * 1)()
+    bad[0] = csf.CDecodePart(ctypes.pointer(st), 16, 1 << 20, 4, 4)
+    assert csf.lib.csf_expand(bad, 1, None, None, None) == 1
+    small = (csf.CDecodePart * 1)()
+    small[0] = csf.CDecodePart(ctypes.pointer(st), 16, 639, 0, 10)
+    assert csf.lib.csf_expand(small, 1, None, None, None) == 2
