@@ -1,7 +1,8 @@
 """CPU oracle for the CSF scale codec -- TEST INFRASTRUCTURE ONLY.
 
 Plain, slow, single-threaded reference of what the CSF method computes
-(encode, decode, routed and row-range decode, index check), written in plain C
+(encode, decode, routed and row-range decode, decode into the block-scaled
+GEMM scale layout, index check), written in plain C
 (``csf_oracle.c``) and reached through ``ctypes``.  Only the test suite, the
 smoke check and the benchmark's CPU-baseline leg may import this package.  It
 shares no code with the CUDA library, and the product path never routes
@@ -68,6 +69,10 @@ def _load():
                                     _u8p, _u32p, _u8p, ctypes.c_uint64, _i64p,
                                     _i64, _i64, _u8p]
         lib.csfo_decode.restype = ctypes.c_int
+        lib.csfo_decode_blocked.argtypes = lib.csfo_decode.argtypes
+        lib.csfo_decode_blocked.restype = ctypes.c_int
+        lib.csfo_blocked_bytes.argtypes = [_i64, _i64, _i64]
+        lib.csfo_blocked_bytes.restype = ctypes.c_uint64
         lib.csfo_check.argtypes = [ctypes.c_int, _i64, _i64, _i64, _u8p, _u8p,
                                    _u32p, ctypes.c_uint64]
         lib.csfo_check.restype = ctypes.c_int
@@ -135,6 +140,34 @@ def decode(enc: dict, expert_start=None, out: np.ndarray | None = None, rows=Non
                              _ptr(enc["escapes"] if enc["escapes"].size else None, _u8p),
                              _ptr(enc["exc_index"], _u32p), _ptr(exc, _u8p),
                              enc["num_exc"], _ptr(es, _i64p), lo, hi, _ptr(out, _u8p))
+    return out, st
+
+
+def blocked_bytes(E: int, R: int, C: int) -> int:
+    """Bytes of a stack in the 128 x 4 tiled scale-operand layout."""
+    return int(_load().csfo_blocked_bytes(E, R, C))
+
+
+def decode_blocked(enc: dict, expert_start=None, out: np.ndarray | None = None, rows=None):
+    """Decode into the 128 x 4 tiled scale-operand layout of block-scaled
+    GEMMs (flat uint8 of blocked_bytes(E, R, C)); returns (out, status).
+    ``rows`` = (lo, hi) with lo a multiple of 128 and hi a multiple of 128 or
+    R; tiles outside the selected row blocks and experts keep their bytes."""
+    E, R, C = enc["shape"]
+    lo, hi = (0, R) if rows is None else rows
+    if out is None:
+        out = np.zeros(blocked_bytes(E, R, C), np.uint8)
+    assert out.dtype == np.uint8 and out.size == blocked_bytes(E, R, C)
+    es = None
+    if expert_start is not None:
+        es = np.ascontiguousarray(np.asarray(expert_start, dtype=np.int64))
+        assert es.shape == (E + 1,)
+    exc = enc["exc_bytes"] if enc["exc_bytes"].size else np.zeros(1, np.uint8)
+    st = _load().csfo_decode_blocked(enc["kind"], E, R, C, _ptr(enc["base"], _u8p),
+                                     _ptr(enc["offsets"], _u8p),
+                                     _ptr(enc["escapes"] if enc["escapes"].size else None, _u8p),
+                                     _ptr(enc["exc_index"], _u32p), _ptr(exc, _u8p),
+                                     enc["num_exc"], _ptr(es, _i64p), lo, hi, _ptr(out, _u8p))
     return out, st
 
 

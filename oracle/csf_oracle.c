@@ -39,6 +39,8 @@
  *     inactive experts are not written.
  *   - row-range decode: only rows [row_lo, row_hi) of each written expert are
  *     written (the gate half of a fused gate/up expert is rows [0, R/2)).
+ *   - blocked decode: the same bytes placed in the 128 x 4 tiled scale-operand
+ *     layout of block-scaled GEMMs (see blocked_offset), padding written 0.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -185,6 +187,35 @@ static unsigned offset_of(int kind, const uint8_t *offsets, uint64_t i)
 }
 
 /*
+ * Decode one row (global row index `row`) into out_row[0..C) ([FK] format
+ * paragraph): base + offset mod 256, or the next exception byte of the row.
+ * An exception reference past num_exc writes 0 and returns CSFO_ERR_CORRUPT.
+ */
+static int decode_row(int kind, int64_t C, const uint8_t *base, const uint8_t *offsets,
+                      const uint8_t *escapes, const uint32_t *exc_index, const uint8_t *exc_bytes,
+                      uint64_t num_exc, uint64_t row, uint8_t *out_row)
+{
+    int status = CSFO_OK;
+    uint64_t rank = 0;
+    for (int64_t c = 0; c < C; ++c) {
+        uint64_t i = row * (uint64_t)C + (uint64_t)c;
+        if (is_escape(kind, offsets, escapes, i)) {
+            uint64_t pos = (uint64_t)exc_index[row] + rank;
+            rank += 1;
+            if (pos < num_exc) {
+                out_row[c] = exc_bytes[pos];
+            } else {
+                out_row[c] = 0;
+                status = CSFO_ERR_CORRUPT;
+            }
+        } else {
+            out_row[c] = (uint8_t)((base[row] + offset_of(kind, offsets, i)) & 0xFFu);
+        }
+    }
+    return status;
+}
+
+/*
  * Decode ([FK] format and helpers paragraphs).  expert_start is NULL for the
  * whole stack, else E+1 int64 entries; only experts with start[e+1] > start[e]
  * are written.  Within each written expert only rows row_lo <= r < row_hi are
@@ -207,24 +238,79 @@ int csfo_decode(int kind, int64_t E, int64_t R, int64_t C,
             continue;
         for (int64_t r = row_lo; r < row_hi; ++r) {
             uint64_t row = (uint64_t)e * (uint64_t)R + (uint64_t)r;
-            uint64_t rank = 0;
-            for (int64_t c = 0; c < C; ++c) {
-                uint64_t i = row * (uint64_t)C + (uint64_t)c;
-                if (is_escape(kind, offsets, escapes, i)) {
-                    uint64_t pos = (uint64_t)exc_index[row] + rank;
-                    rank += 1;
-                    if (pos < num_exc) {
-                        out[i] = exc_bytes[pos];
-                    } else {
-                        out[i] = 0;
-                        status = CSFO_ERR_CORRUPT;
-                    }
-                } else {
-                    out[i] = (uint8_t)((base[row] + offset_of(kind, offsets, i)) & 0xFFu);
-                }
-            }
+            if (decode_row(kind, C, base, offsets, escapes, exc_index, exc_bytes, num_exc, row,
+                           out + row * (uint64_t)C) != CSFO_OK)
+                status = CSFO_ERR_CORRUPT;
         }
     }
+    return status;
+}
+
+/*
+ * Byte position of scale (r, c) of expert e in the scale-operand layout of
+ * Blackwell block-scaled GEMMs (the 128 x 4 tiled layout NVIDIA documents for
+ * cuBLASLt block scaling, "32_4_4" swizzle).  Each expert's R x C scale
+ * matrix is padded to RP = R rounded up to 128 rows and CP = C rounded up to
+ * 4 columns and cut into 128 x 4 tiles of 512 bytes, stored row-block by
+ * row-block, column blocks innermost.  Inside a tile, the 16-byte line
+ * r % 32 holds rows r % 32, +32, +64, +96, four columns each:
+ *   offset = (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4.
+ * Experts follow each other, RP * CP bytes apart.
+ */
+static uint64_t blocked_offset(int64_t R, int64_t C, int64_t e, int64_t r, int64_t c)
+{
+    uint64_t RP = (uint64_t)((R + 127) / 128) * 128;
+    uint64_t CP = (uint64_t)((C + 3) / 4) * 4;
+    uint64_t tile = (uint64_t)(r / 128) * (CP / 4) + (uint64_t)(c / 4);
+    return (uint64_t)e * RP * CP + tile * 512 + (uint64_t)(r % 32) * 16 + (uint64_t)((r % 128) / 32) * 4
+           + (uint64_t)(c % 4);
+}
+
+/* Bytes of one stack in the scale-operand layout. */
+uint64_t csfo_blocked_bytes(int64_t E, int64_t R, int64_t C)
+{
+    return (uint64_t)E * (uint64_t)((R + 127) / 128) * 128 * (uint64_t)((C + 3) / 4) * 4;
+}
+
+/*
+ * Decode straight into the scale-operand layout (the decode-into-the-GEMM's
+ * operand idea of the [FK] measurement paragraph, which puts the staging cost
+ * of a separate layout pass before the GEMM).  Writes every tile of the
+ * 128-row blocks that cover rows [row_lo, row_hi) of each selected expert:
+ * row_lo must be a multiple of 128 and row_hi a multiple of 128 or R.  Tile
+ * positions past the expert's rows or columns (the padding) are written 0.
+ * Other tiles, and inactive experts, are left alone.
+ */
+int csfo_decode_blocked(int kind, int64_t E, int64_t R, int64_t C,
+                        const uint8_t *base, const uint8_t *offsets, const uint8_t *escapes,
+                        const uint32_t *exc_index, const uint8_t *exc_bytes, uint64_t num_exc,
+                        const int64_t *expert_start, int64_t row_lo, int64_t row_hi, uint8_t *out)
+{
+    if ((kind != CSFO_NVFP4 && kind != CSFO_MXFP4) || E < 0 || R < 1 || C < 1)
+        return CSFO_ERR_ARG;
+    if (row_lo < 0 || row_hi > R || row_lo >= row_hi || row_lo % 128 != 0 || (row_hi % 128 != 0 && row_hi != R))
+        return CSFO_ERR_ARG;
+    uint8_t *row_bytes = (uint8_t *)malloc((size_t)C);
+    if (!row_bytes)
+        return CSFO_ERR_ARG;
+    int64_t CP = (C + 3) / 4 * 4;
+    int64_t r_end = (row_hi + 127) / 128 * 128;
+    int status = CSFO_OK;
+    for (int64_t e = 0; e < E; ++e) {
+        if (expert_start != NULL && !(expert_start[e + 1] > expert_start[e]))
+            continue;
+        for (int64_t r = row_lo; r < r_end; ++r) {
+            if (r < R) {
+                uint64_t row = (uint64_t)e * (uint64_t)R + (uint64_t)r;
+                if (decode_row(kind, C, base, offsets, escapes, exc_index, exc_bytes, num_exc, row,
+                               row_bytes) != CSFO_OK)
+                    status = CSFO_ERR_CORRUPT;
+            }
+            for (int64_t c = 0; c < CP; ++c)
+                out[blocked_offset(R, C, e, r, c)] = (r < R && c < C) ? row_bytes[c] : 0;
+        }
+    }
+    free(row_bytes);
     return status;
 }
 

@@ -285,3 +285,82 @@ def test_size_against_pages_figures():
     n = dense.size
     assert total == (n + 1) // 2 + n // 100 + enc["num_exc"]
     assert 0.53 <= total / n <= 0.55
+
+
+# ------------------------------------------- scale-operand (blocked) layout
+# The 128 x 4 tiled scale layout that Blackwell block-scaled GEMMs read
+# (cuBLASLt's documented block-scaling-factor layout; PyTorch calls it the
+# 32_4_4 swizzle): per expert, 128-row x 4-column tiles of 512 bytes, row
+# blocks outer and column blocks inner; inside a tile, 16-byte line b holds
+# rows b, b+32, b+64, b+96 with four columns each.
+
+def _reshape_form(dense: np.ndarray) -> np.ndarray:
+    """The layout written as a tensor permutation, independent of the
+    oracle's index arithmetic: pad to (128k, 4m), split into 128 x 4 tiles,
+    order tiles row-block-major, then within a tile view rows as (4, 32) and
+    move the 32 outermost."""
+    E, R, C = dense.shape
+    RP, CP = -(-R // 128) * 128, -(-C // 4) * 4
+    pad = np.zeros((E, RP, CP), np.uint8)
+    pad[:, :R, :C] = dense
+    t = pad.reshape(E, RP // 128, 128, CP // 4, 4).transpose(0, 1, 3, 2, 4)   # E, rb, cb, 128, 4
+    t = t.reshape(E, RP // 128, CP // 4, 4, 32, 4).transpose(0, 1, 2, 4, 3, 5)  # rows as (4, 32) -> (32, 4)
+    return t.reshape(-1)
+
+
+def test_blocked_layout_hand_lines():
+    # dense[r, c] = r: line b of the tile is rows b, b+32, b+64, b+96, each
+    # repeated for its four columns.
+    R, C = 128, 4
+    dense = np.repeat(np.arange(R, dtype=np.uint8)[:, None], C, axis=1)[None]
+    out, st = oracle.decode_blocked(oracle.encode(oracle.NVFP4, dense))
+    assert st == oracle.OK and out.size == 512
+    assert out[:16].tolist() == [0] * 4 + [32] * 4 + [64] * 4 + [96] * 4
+    assert out[16:32].tolist() == [1] * 4 + [33] * 4 + [65] * 4 + [97] * 4
+    assert out[496:].tolist() == [31] * 4 + [63] * 4 + [95] * 4 + [127] * 4
+    # dense[r, c] = c: every 4-byte group is 0 1 2 3.
+    dense = np.tile(np.arange(C, dtype=np.uint8), (R, 1))[None]
+    out, _ = oracle.decode_blocked(oracle.encode(oracle.NVFP4, dense))
+    assert (out.reshape(-1, 4) == np.arange(4)).all()
+    # Two column blocks (C = 8): tile (row block 0, column block 1) follows
+    # tile 0 and holds columns 4..7.
+    dense = np.tile(np.arange(8, dtype=np.uint8), (R, 1))[None]
+    out, _ = oracle.decode_blocked(oracle.encode(oracle.NVFP4, dense))
+    assert (out[:512].reshape(-1, 4) == np.arange(4)).all()
+    assert (out[512:].reshape(-1, 4) == np.arange(4, 8)).all()
+
+
+@pytest.mark.parametrize("kind,E,R,C", [(0, 2, 128, 4), (0, 3, 200, 7), (0, 2, 256, 100), (1, 2, 130, 160),
+                                        (0, 1, 1, 1), (1, 3, 64, 33)])
+def test_blocked_layout_equals_reshape_form_and_pads_zero(kind, E, R, C):
+    w = 14 if kind == oracle.NVFP4 else 1
+    dense = synth.random_rows(E + R + C, E * R, C, spread=w + 3, replace_p=0.1).reshape(E, R, C)
+    enc = oracle.encode(kind, dense)
+    out, st = oracle.decode_blocked(enc, out=np.full(oracle.blocked_bytes(E, R, C), 0xAB, np.uint8))
+    assert st == oracle.OK
+    assert np.array_equal(out, _reshape_form(dense))
+    # Every byte written once: the padding is zero, the rest a permutation.
+    ones = np.full_like(dense, 0xFF)
+    po, _ = oracle.decode_blocked(oracle.encode(kind, ones))
+    assert int((po == 0xFF).sum()) == dense.size and int((po == 0).sum()) == po.size - dense.size
+
+
+def test_blocked_row_blocks_and_routing_leave_other_tiles():
+    E, R, C = 3, 300, 12                        # row blocks [0,128) [128,256) [256,300)+pad
+    dense = synth.random_rows(9, E * R, C, spread=17, replace_p=0.1).reshape(E, R, C)
+    enc = oracle.encode(oracle.NVFP4, dense)
+    full, _ = oracle.decode_blocked(enc)
+    per_expert = full.size // E
+    tile_rows = 3 * 512                         # bytes of one row block (3 column blocks)
+    start = np.array([0, 1, 1, 4], np.int64)   # experts 0 and 2
+    for lo, hi in [(128, 256), (128, R), (0, 128), (256, R)]:
+        out, st = oracle.decode_blocked(enc, start, np.full(full.size, 0x5A, np.uint8), rows=(lo, hi))
+        assert st == oracle.OK
+        want = np.full(full.size, 0x5A, np.uint8)
+        for e in (0, 2):
+            a = e * per_expert + (lo // 128) * tile_rows
+            b = e * per_expert + (-(-hi // 128)) * tile_rows
+            want[a:b] = full[a:b]
+        assert np.array_equal(out, want), (lo, hi)
+    for bad in [(1, 128), (0, 100), (128, 128), (0, R + 1)]:
+        assert oracle.decode_blocked(enc, None, None, rows=bad)[1] == oracle.ERR_ARG
