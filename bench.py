@@ -281,6 +281,14 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
     rec("gate_half_all", durs, stack_traffic(gate, rows_active=512 * 512))
     del hc, hw
 
+    # the gate stack decoded straight into the block-scaled GEMM scale layout,
+    # rotating over 4 copies (4 x 80 MB > L2)
+    bc = [gate] + [clone_stack(torch, gate) for _ in range(3)]
+    bw = [torch.empty(csf.blocked_bytes(gate), dtype=torch.uint8, device="cuda") for _ in range(4)]
+    durs = timed_steps(torch, lambda i: csf.decode(bc[i % 4], bw[i % 4], layout=csf.LAYOUT_BLOCKED), 400, 20)
+    rec("gate_blocked_layout", durs, stack_traffic(gate))
+    del bc, bw
+
     # paired gate + down
     down_dense = torch.from_numpy(synth.down_stack(seed=0)).cuda()
     down = csf.prepare(down_dense, csf.NVFP4)

@@ -70,7 +70,7 @@
 extern "C" {
 #endif
 
-#define CSF_ABI_VERSION 2
+#define CSF_ABI_VERSION 3
 
 typedef enum {
     CSF_OK = 0,
@@ -105,6 +105,7 @@ typedef struct {
     uint64_t escapes;         /* MXFP4 escape plane rounded up to 16; 0 for NVFP4 */
     uint64_t exc_index;       /* 4*(rows+1) */
     uint64_t prepare_scratch; /* scratch for csf_prepare */
+    uint64_t blocked;         /* a workspace in CSF_LAYOUT_BLOCKED: E * (R up to 128) * (C up to 4) */
 } csf_sizes_t;
 
 /*
@@ -220,13 +221,34 @@ csf_status csf_decode_pair(const csf_stack *gate, uint8_t *gate_ws, size_t gate_
                            const csf_stack *down, uint8_t *down_ws, size_t down_ws_bytes,
                            const void *expert_start, int expert_start_is_int64, void *stream);
 
+/*
+ * Workspace layouts of csf_decode_rows and csf_expand.
+ *   CSF_LAYOUT_ROWS     row-major [E][R][C], the layout of csf_decode.
+ *   CSF_LAYOUT_BLOCKED  the scale-operand layout that Blackwell block-scaled
+ *       GEMMs (tcgen05 block scaling, cuBLASLt VEC16_UE4M3 / VEC32_UE8M0
+ *       scales) read, written directly so that no layout pass runs before
+ *       the GEMM ([FK] measurement paragraph: decode staging before the GEMM
+ *       is the cost).  Per expert, its R x C scales padded to RP = R rounded
+ *       up to 128 rows and CP = C rounded up to 4 columns, cut into 128 x 4
+ *       tiles of 512 bytes; tiles in row-block-major order (column blocks
+ *       innermost); scale (r, c) of a tile at byte
+ *       (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4.  Experts follow each
+ *       other, RP * CP bytes apart.  Padding bytes are written 0.  Needs a
+ *       16-byte aligned workspace of csf_sizes().blocked bytes, row ranges on
+ *       128-row boundaries (row_hi may also be R), and C <= 1024.
+ */
+#define CSF_LAYOUT_ROWS 0
+#define CSF_LAYOUT_BLOCKED 1
+
 /* One stack of a csf_decode_rows call and the rows of each expert it writes. */
 typedef struct {
     const csf_stack *stack; /* num_exc set */
-    uint8_t *ws;            /* device workspace, >= E*R*C bytes, [E][R][C], any byte alignment */
+    uint8_t *ws;            /* device workspace: ROWS >= E*R*C bytes, [E][R][C], any byte alignment;
+                               BLOCKED >= csf_sizes().blocked bytes, 16-byte aligned */
     size_t ws_bytes;
     int32_t row_lo;         /* rows row_lo <= r < row_hi of each selected expert are written; */
     int32_t row_hi;         /* 0 <= row_lo < row_hi <= R */
+    int32_t layout;         /* CSF_LAYOUT_ROWS or CSF_LAYOUT_BLOCKED; every part of a call alike */
 } csf_decode_part;
 
 /*
@@ -242,9 +264,12 @@ typedef struct {
  *                     experts.
  *   expert_start      as csf_decode (NULL: every expert).
  * Errors: CSF_ERR_ARG (bad part count, NULL stack, empty or out-of-range
- * rows, differing expert counts, and the csf_decode cases), CSF_ERR_SIZE,
- * CSF_ERR_UNSUPPORTED (E > 8192 with routing or a partial row range; the
- * per-expert work list lives in shared memory), CSF_ERR_CUDA.
+ * rows, differing expert counts or layouts, an unknown layout, a blocked
+ * workspace not 16-byte aligned or rows off its 128-row boundaries, and the
+ * csf_decode cases), CSF_ERR_SIZE, CSF_ERR_UNSUPPORTED (E > 8192 with
+ * routing, or with a partial row range in the row-major layout: the
+ * per-expert work list lives in shared memory; C > 1024 in the blocked
+ * layout), CSF_ERR_CUDA.
  */
 csf_status csf_decode_rows(const csf_decode_part *parts, int num_parts,
                            const void *expert_start, int expert_start_is_int64, void *stream);

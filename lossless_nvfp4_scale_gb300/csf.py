@@ -13,6 +13,7 @@ Typical use::
     csf.decode(stack, ws, expert_start=start_i32_cuda)    # routed experts only
     csf.decode_pair(gate, down, gate_ws, down_ws, expert_start)
     csf.decode(stack, ws, rows=(0, R // 2))               # gate half of fused gate/up
+    sf = csf.decode(stack, layout=csf.LAYOUT_BLOCKED)     # GEMM scale-operand layout
     ev = csf.expand_scales([(gate, gate_ws), (down, down_ws)], side_stream, after=last_read)
     torch.cuda.current_stream().wait_event(ev)            # before the call that reads them
 """
@@ -31,6 +32,8 @@ MXFP4 = 1
 DEV_ERR_CORRUPT = 0x1
 DEV_ERR_CAPACITY = 0x2
 DEV_ERR_TIMEOUT = 0x4
+LAYOUT_ROWS = 0      # row-major [E][R][C]
+LAYOUT_BLOCKED = 1   # 128 x 4 tiled scale-operand layout of block-scaled GEMMs
 
 _c_i32 = ctypes.c_int32
 _c_u64 = ctypes.c_uint64
@@ -43,7 +46,7 @@ class Geometry(ctypes.Structure):
 
 class Sizes(ctypes.Structure):
     _fields_ = [("dense", _c_u64), ("base", _c_u64), ("offsets", _c_u64), ("escapes", _c_u64),
-                ("exc_index", _c_u64), ("prepare_scratch", _c_u64)]
+                ("exc_index", _c_u64), ("prepare_scratch", _c_u64), ("blocked", _c_u64)]
 
 
 class CStack(ctypes.Structure):
@@ -54,7 +57,7 @@ class CStack(ctypes.Structure):
 
 class CDecodePart(ctypes.Structure):
     _fields_ = [("stack", ctypes.POINTER(CStack)), ("ws", _c_vp), ("ws_bytes", ctypes.c_size_t),
-                ("row_lo", _c_i32), ("row_hi", _c_i32)]
+                ("row_lo", _c_i32), ("row_hi", _c_i32), ("layout", _c_i32)]
 
 
 class CsfError(RuntimeError):
@@ -248,27 +251,35 @@ def _check_es(stack: Stack, expert_start):
         raise CsfError("expert_start must have E+1 entries")
 
 
-def _ws_for(stack: Stack, ws, what: str) -> torch.Tensor:
+def blocked_bytes(stack: Stack) -> int:
+    """Workspace bytes of a stack in the scale-operand layout (LAYOUT_BLOCKED)."""
+    return sizes(stack.kind, stack.E, stack.R, stack.C)["blocked"]
+
+
+def _ws_for(stack: Stack, ws, what: str, layout: int = LAYOUT_ROWS) -> torch.Tensor:
     if ws is None:
-        ws = torch.empty(stack.shape, dtype=torch.uint8, device=stack.base.device)
+        if layout == LAYOUT_BLOCKED:
+            ws = torch.empty(blocked_bytes(stack), dtype=torch.uint8, device=stack.base.device)
+        else:
+            ws = torch.empty(stack.shape, dtype=torch.uint8, device=stack.base.device)
     if ws.dtype != torch.uint8 or not ws.is_cuda or not ws.is_contiguous():
         raise CsfError(f"{what}: workspaces must be contiguous uint8 CUDA tensors")
     return ws
 
 
-def _parts(parts):
+def _parts(parts, layout=LAYOUT_ROWS):
     """Marshal (stack, ws, (lo, hi) or None) triples into csf_decode_part
     structs; returns the array and the stack structs it points to."""
     cs = [p[0].cstruct() for p in parts]
     arr = (CDecodePart * len(parts))()
     for i, ((stack, ws, rows), c) in enumerate(zip(parts, cs)):
         lo, hi = (0, stack.R) if rows is None else rows
-        arr[i] = CDecodePart(ctypes.pointer(c), ws.data_ptr(), ws.numel(), lo, hi)
+        arr[i] = CDecodePart(ctypes.pointer(c), ws.data_ptr(), ws.numel(), lo, hi, layout)
     return arr, cs
 
 
-def _decode_rows(parts, expert_start, stream):
-    arr, _keep = _parts(parts)
+def _decode_rows(parts, expert_start, stream, layout=LAYOUT_ROWS):
+    arr, _keep = _parts(parts, layout)
     ptr, is64 = _es(expert_start)
     _check(lib.csf_decode_rows(arr, len(parts), ptr, is64, _stream(stream)), "csf_decode_rows")
 
@@ -283,16 +294,17 @@ def _event_handle(ev, stream) -> int:
 
 
 def expand_scales(parts, stream=None, after: torch.cuda.Event | None = None,
-                  done: torch.cuda.Event | None = None) -> torch.cuda.Event | bool:
+                  done: torch.cuda.Event | None = None, layout: int = LAYOUT_ROWS) -> torch.cuda.Event | bool:
     """Ahead-of-call expansion (csf_expand): decode every expert of the given
     stacks into their workspaces on `stream` (a side stream, typically),
     after `after` (recorded by the previous reader of the workspaces), and
-    record `done` for the consumer to wait on.
+    record `done` for the consumer to wait on.  `layout` = LAYOUT_BLOCKED
+    writes the GEMM scale-operand layout.
 
     `parts` is a list of (stack, ws) or (stack, ws, (lo, hi)); entries whose
     stack is None (scales that are not compressed) are skipped, and False is
     returned when nothing is left to expand."""
-    todo = [(p[0], _ws_for(p[0], p[1], "expand_scales"), p[2] if len(p) > 2 else None)
+    todo = [(p[0], _ws_for(p[0], p[1], "expand_scales", layout), p[2] if len(p) > 2 else None)
             for p in parts if p[0] is not None]
     if not todo:
         return False
@@ -308,7 +320,7 @@ def expand_scales(parts, stream=None, after: torch.cuda.Event | None = None,
     done_h = _event_handle(done, s)
     for i in range(0, len(todo), 2):
         chunk = todo[i:i + 2]
-        arr, _keep = _parts(chunk)
+        arr, _keep = _parts(chunk, layout)
         last = i + 2 >= len(todo)
         _check(lib.csf_expand(arr, len(chunk), after_h if i == 0 else None, done_h if last else None,
                               s.cuda_stream), "csf_expand")
@@ -316,14 +328,16 @@ def expand_scales(parts, stream=None, after: torch.cuda.Event | None = None,
 
 
 def decode(stack: Stack, ws: torch.Tensor | None = None, expert_start: torch.Tensor | None = None,
-           stream=None, rows: tuple[int, int] | None = None) -> torch.Tensor:
+           stream=None, rows: tuple[int, int] | None = None, layout: int = LAYOUT_ROWS) -> torch.Tensor:
     """Decode into `ws` (uint8 CUDA, >= E*R*C bytes, any byte offset).  With
     `expert_start` only experts with routed tokens are written; with
-    `rows=(lo, hi)` only rows lo <= r < hi of each of them (csf_decode_rows)."""
-    ws = _ws_for(stack, ws, "decode")
+    `rows=(lo, hi)` only rows lo <= r < hi of each of them (csf_decode_rows).
+    `layout=LAYOUT_BLOCKED` writes the 128 x 4 tiled scale-operand layout of
+    block-scaled GEMMs (flat, blocked_bytes(stack), 16-byte aligned)."""
+    ws = _ws_for(stack, ws, "decode", layout)
     _check_es(stack, expert_start)
-    if rows is not None:
-        _decode_rows([(stack, ws, rows)], expert_start, stream)
+    if rows is not None or layout != LAYOUT_ROWS:
+        _decode_rows([(stack, ws, rows)], expert_start, stream, layout)
         return ws
     ptr, is64 = _es(expert_start)
     cs = stack.cstruct()
@@ -335,14 +349,14 @@ def decode(stack: Stack, ws: torch.Tensor | None = None, expert_start: torch.Ten
 def decode_pair(gate: Stack, down: Stack, gate_ws: torch.Tensor | None = None,
                 down_ws: torch.Tensor | None = None, expert_start: torch.Tensor | None = None,
                 stream=None, gate_rows: tuple[int, int] | None = None,
-                down_rows: tuple[int, int] | None = None):
+                down_rows: tuple[int, int] | None = None, layout: int = LAYOUT_ROWS):
     """Decode a gate(/up) and a down stack in one launch with shared routing;
     `gate_rows`/`down_rows` restrict each to a row range of every expert."""
-    gate_ws = _ws_for(gate, gate_ws, "decode_pair")
-    down_ws = _ws_for(down, down_ws, "decode_pair")
+    gate_ws = _ws_for(gate, gate_ws, "decode_pair", layout)
+    down_ws = _ws_for(down, down_ws, "decode_pair", layout)
     _check_es(gate, expert_start)
-    if gate_rows is not None or down_rows is not None:
-        _decode_rows([(gate, gate_ws, gate_rows), (down, down_ws, down_rows)], expert_start, stream)
+    if gate_rows is not None or down_rows is not None or layout != LAYOUT_ROWS:
+        _decode_rows([(gate, gate_ws, gate_rows), (down, down_ws, down_rows)], expert_start, stream, layout)
         return gate_ws, down_ws
     ptr, is64 = _es(expert_start)
     g, d = gate.cstruct(), down.cstruct()

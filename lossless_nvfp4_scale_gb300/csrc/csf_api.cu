@@ -109,6 +109,12 @@ csf_status fill_stack(const csf_stack *s, uint8_t *ws, size_t ws_bytes, DecStack
     return CSF_OK;
 }
 
+uint64_t blocked_bytes(const csf_geometry *g) {
+    const uint64_t RP = ((uint64_t)g->rows + kTileRows - 1) / kTileRows * kTileRows;
+    const uint64_t CP = ((uint64_t)g->cols + 3) / 4 * 4;
+    return (uint64_t)g->num_experts * RP * CP;
+}
+
 uint64_t units_full(const DecStack &d) { return (d.rows + d.rb - 1) / d.rb; }
 
 uint64_t units_all_experts(const DecStack &d, int E) {
@@ -126,7 +132,12 @@ struct DecodeLaunch {
     size_t smem;
     int grid;
     bool per_expert;
+    bool blocked;
 };
+
+// Largest C of the blocked layout: a 128-row item buffer of 128*C bytes
+// plus the per-warp staging stays within the shared memory of one block.
+constexpr int32_t kBlockedMaxCols = 1024;
 
 csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *expert_start, int es64,
                        DecodeLaunch *L) {
@@ -134,11 +145,24 @@ csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *exp
     DecParams &p = L->p;
     std::memset(&p, 0, sizeof p);
     bool whole = true;
+    const int32_t layout = parts[0].layout;
+    if (layout != CSF_LAYOUT_ROWS && layout != CSF_LAYOUT_BLOCKED) return CSF_ERR_ARG;
+    const bool blocked = layout == CSF_LAYOUT_BLOCKED;
+    int32_t cmax = 0;
     for (int i = 0; i < nparts; ++i) {
         const csf_decode_part &q = parts[i];
+        if (q.layout != layout) return CSF_ERR_ARG;
         csf_status st = fill_stack(q.stack, q.ws, q.ws_bytes, &p.st[i]);
         if (st != CSF_OK) return st;
         if (q.row_lo < 0 || q.row_lo >= q.row_hi || q.row_hi > q.stack->g.rows) return CSF_ERR_ARG;
+        if (blocked) {
+            if (!aligned16(q.ws)) return CSF_ERR_ARG;
+            if (q.row_lo % kTileRows != 0 || (q.row_hi % kTileRows != 0 && q.row_hi != q.stack->g.rows))
+                return CSF_ERR_ARG;
+            if (q.ws_bytes < blocked_bytes(&q.stack->g)) return CSF_ERR_SIZE;
+            if (q.stack->g.cols > kBlockedMaxCols) return CSF_ERR_UNSUPPORTED;
+            if (q.stack->g.cols > cmax) cmax = q.stack->g.cols;
+        }
         p.st[i].r_lo = q.row_lo;
         p.st[i].r_hi = q.row_hi;
         const int32_t rb = p.st[i].rb;
@@ -155,11 +179,37 @@ csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *exp
     p.expert_start = expert_start;
     p.es64 = es64 ? 1 : 0;
     const bool per_expert = expert_start != nullptr || !whole;
-    if (per_expert && p.E > kMaxRoutedExperts) return CSF_ERR_UNSUPPORTED;
+    if (blocked ? expert_start != nullptr : per_expert)
+        if (p.E > kMaxRoutedExperts) return CSF_ERR_UNSUPPORTED;
 
     DeviceInfo di;
     csf_status st = device_info(&di);
     if (st != CSF_OK) return st;
+    L->blocked = blocked;
+    if (blocked) {
+        // Items of 256 rows while their buffer stays small, else 128 rows.
+        const uint32_t ir = 256u * (uint32_t)cmax + 32u <= 64u * 1024u ? 256u : (uint32_t)kTileRows;
+        const uint32_t act = expert_start ? (4u * (uint32_t)p.E + 15u) & ~15u : 0u;
+        p.item_rows = ir;
+        p.tile_off = act;
+        const size_t smem = act + (((size_t)ir * (size_t)cmax + 32 + 15) & ~(size_t)15);
+        int occ = 0;
+        if (decode_blocked_occupancy(smem, &occ) != cudaSuccess) {
+            cudaGetLastError();
+            return CSF_ERR_CUDA;
+        }
+        if (occ < 1) return CSF_ERR_UNSUPPORTED;
+        uint64_t items = 0;
+        for (int i = 0; i < nparts; ++i)
+            items += (uint64_t)p.E * (((uint64_t)(p.st[i].r_hi - p.st[i].r_lo) + ir - 1) / ir);
+        uint64_t grid = (uint64_t)di.sms * (uint64_t)occ;
+        if (items < grid) grid = items;
+        if (grid < 1) grid = 1;
+        L->smem = smem;
+        L->grid = (int)grid;
+        L->per_expert = true;
+        return CSF_OK;
+    }
     size_t smem = 0;
     int occ = di.occ_full;
     uint64_t units = 0;
@@ -187,7 +237,10 @@ csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *exp
 }
 
 csf_status launch(const DecodeLaunch &L, void *stream) {
-    if (launch_decode(L.p, L.grid, L.smem, L.per_expert, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    const cudaError_t e = L.blocked
+                              ? launch_decode_blocked(L.p, L.grid, L.smem, static_cast<cudaStream_t>(stream))
+                              : launch_decode(L.p, L.grid, L.smem, L.per_expert, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return CSF_ERR_CUDA;
     }
@@ -209,6 +262,7 @@ csf_decode_part whole_part(const csf_stack *s, uint8_t *ws, size_t ws_bytes) {
     q.ws_bytes = ws_bytes;
     q.row_lo = 0;
     q.row_hi = s ? s->g.rows : 0;
+    q.layout = CSF_LAYOUT_ROWS;
     return q;
 }
 
@@ -245,6 +299,7 @@ csf_status csf_sizes(const csf_geometry *g, csf_sizes_t *out) {
     }
     out->exc_index = 4 * (rows + 1);
     out->prepare_scratch = prepare_scratch_bytes(g, rows);
+    out->blocked = blocked_bytes(g);
     return CSF_OK;
 }
 

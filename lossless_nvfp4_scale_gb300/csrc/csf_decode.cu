@@ -107,6 +107,30 @@ __device__ __forceinline__ void store32(uint8_t *ws, int align, uint32_t p, cons
     }
 }
 
+__device__ __forceinline__ void sts_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
+__device__ __forceinline__ void sts_u8(uint32_t a, uint32_t v) {
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// Shared-memory twin of store32: local elements [p, p+32) at shared address
+// sa0 + p (sa0 + p is 16-byte aligned), only bytes inside [lo, hi).
+__device__ __forceinline__ void sstore32(uint32_t sa0, uint32_t p, const uint32_t *w, uint32_t lo, uint32_t hi) {
+    const uint32_t a = sa0 + p;
+    if (p >= lo && p + 32 <= hi) {
+        sts_v4(a, w[0], w[1], w[2], w[3]);
+        sts_v4(a + 16, w[4], w[5], w[6], w[7]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const uint32_t q = p + j;
+            if (q >= lo && q < hi) sts_u8(a + j, (w[j >> 2] >> (8 * (j & 3))) & 0xFFu);
+        }
+    }
+}
+
 // base + offset, byte-wise mod 256, for offsets below 0x80 (the low 7 bits
 // are added, bit 7 is folded back with XOR, so no carry crosses a byte).
 __device__ __forceinline__ uint32_t add_base(uint32_t bw, uint32_t off) {
@@ -159,9 +183,12 @@ __device__ __forceinline__ void base_words_general(uint32_t (&bw)[NW], uint32_t 
 // ------------------------------------------------------------------ NVFP4
 
 // Decode rows [row_a, row_b) of an NVFP4 stack (row_a*C a multiple of 64),
-// storing only global elements in [lo, hi).  Whole warp.
+// storing only global elements in [lo, hi).  Whole warp.  SMEM: the bytes go
+// to shared memory instead of the workspace, element row_a*C + p at shared
+// address sdst + p (sdst + p is 32-byte aligned for p % 32 == 0).
+template <bool SMEM>
 __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b, uint64_t lo, uint64_t hi,
-                              int lane, uint8_t *stage) {
+                              int lane, uint8_t *stage, uint32_t sdst) {
     const uint32_t C = (uint32_t)S.C;
     const uint64_t sa = row_a * C;
     const uint32_t nel = (uint32_t)(row_b * C - sa);
@@ -174,7 +201,7 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
     uint8_t *ws = S.ws + sa;
     const uint32_t lo_l = (uint32_t)(lo - sa);
     const uint32_t hi_l = (uint32_t)(hi - sa);
-    const bool fast = lo_l == 0 && hi_l == nel && S.ws_align >= 32;
+    const bool fast = lo_l == 0 && hi_l == nel && (SMEM || S.ws_align >= 32);
     const bool v8ok = S.off_align32 != 0;
     const uint32_t nexc = (uint32_t)S.num_exc;
     bool bad = false;
@@ -341,7 +368,12 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                 out[4 * s] = v.x; out[4 * s + 1] = v.y; out[4 * s + 2] = v.z; out[4 * s + 3] = v.w;
             }
         }
-        if (nv == kLaneNv && fast) {
+        if constexpr (SMEM) {
+            if (nv > 0) {
+                sstore32(sdst, p, out, lo_l, hi_l);
+                if (nv > 32) sstore32(sdst, p + 32, out + 8, lo_l, hi_l);
+            }
+        } else if (nv == kLaneNv && fast) {
             st_v8(ws + p, out);
             st_v8(ws + p + 32, out + 8);
         } else if (nv > 0) {
@@ -355,9 +387,11 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
 
 // ------------------------------------------------------------------ MXFP4
 
-// Decode rows [row_a, row_b) of an MXFP4 stack (row_a*C a multiple of 128).
+// Decode rows [row_a, row_b) of an MXFP4 stack (row_a*C a multiple of 128);
+// SMEM and sdst as in segment_nvfp4.
+template <bool SMEM>
 __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b, uint64_t lo, uint64_t hi,
-                              int lane, uint8_t *stage) {
+                              int lane, uint8_t *stage, uint32_t sdst) {
     const uint32_t C = (uint32_t)S.C;
     const uint64_t sa = row_a * C;
     const uint32_t nel = (uint32_t)(row_b * C - sa);
@@ -369,7 +403,7 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
     uint8_t *ws = S.ws + sa;
     const uint32_t lo_l = (uint32_t)(lo - sa);
     const uint32_t hi_l = (uint32_t)(hi - sa);
-    const bool fast = lo_l == 0 && hi_l == nel && S.ws_align >= 32;
+    const bool fast = lo_l == 0 && hi_l == nel && (SMEM || S.ws_align >= 32);
     const uint32_t nexc = (uint32_t)S.num_exc;
     bool bad = false;
     const uint32_t gs = ((uint32_t)lane & 7u) << 4;          // 16-byte slot swizzle (bank spread)
@@ -494,8 +528,13 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                     out[4 * h] = v.x; out[4 * h + 1] = v.y; out[4 * h + 2] = v.z; out[4 * h + 3] = v.w;
                 }
                 const uint32_t pg = p + 32u * gi;
-                if (nv == kLaneMx && fast) st_v8(ws + pg, out);
-                else if (32 * gi < nv) store32(ws, S.ws_align, pg, out, lo_l, hi_l);
+                if constexpr (SMEM) {
+                    if (32 * gi < nv) sstore32(sdst, pg, out, lo_l, hi_l);
+                } else if (nv == kLaneMx && fast) {
+                    st_v8(ws + pg, out);
+                } else if (32 * gi < nv) {
+                    store32(ws, S.ws_align, pg, out, lo_l, hi_l);
+                }
             }
         }
     }
@@ -686,28 +725,178 @@ __global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel
             hi = min(row_b, r1) * C;
         }
         if (S.kind == CSF_NVFP4)
-            segment_nvfp4(S, row_a, row_b, lo, hi, lane, stage);
+            segment_nvfp4<false>(S, row_a, row_b, lo, hi, lane, stage, 0u);
         else
-            segment_mxfp4(S, row_a, row_b, lo, hi, lane, stage);
+            segment_mxfp4<false>(S, row_a, row_b, lo, hi, lane, stage, 0u);
         u += cnt;
+    }
+}
+
+// ------------------------------------------------ scale-operand layout
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+// Decode into the scale-operand layout of Blackwell block-scaled GEMMs: per
+// expert, the R x C scales padded to 128-row / 4-column multiples and cut
+// into 128 x 4 tiles of 512 bytes (row blocks outer, column blocks inner);
+// inside a tile, 16-byte line b holds rows b, b+32, b+64, b+96 with four
+// columns each.  A block item is `item_rows` rows of one expert: the warps
+// decode its units into a shared-memory buffer (row-major, as the flat
+// stream), then the block writes the item's tiles with one 16-byte store per
+// line, zero in the padding.  Items of inactive experts never exist.
+__global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_blocked_kernel(const __grid_constant__ DecParams P) {
+    extern __shared__ __align__(16) uint8_t dsm[];
+    __shared__ __align__(16) uint8_t s_stage[kWarps][kStageBytes];
+    __shared__ uint32_t s_cnt[kWarps];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    uint32_t *act = reinterpret_cast<uint32_t *>(dsm);
+    const uint32_t tile_sa = (uint32_t)__cvta_generic_to_shared(dsm + P.tile_off);
+
+    uint32_t n_act = (uint32_t)P.E;
+    if (P.expert_start != nullptr) {
+        n_act = 0;
+        for (int e0 = 0; e0 < P.E; e0 += kThreads) {
+            const int e = e0 + threadIdx.x;
+            bool a = false;
+            if (e < P.E) {
+                if (P.es64) {
+                    const long long *st = static_cast<const long long *>(P.expert_start);
+                    a = __ldg(st + e + 1) > __ldg(st + e);
+                } else {
+                    const int *st = static_cast<const int *>(P.expert_start);
+                    a = __ldg(st + e + 1) > __ldg(st + e);
+                }
+            }
+            const uint32_t bal = __ballot_sync(kFull, a);
+            if (lane == 0) s_cnt[warp] = __popc(bal);
+            __syncthreads();
+            uint32_t bn = n_act, tn = 0;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                if (w < warp) bn += s_cnt[w];
+                tn += s_cnt[w];
+            }
+            if (a) act[bn + __popc(bal & lanemask_lt())] = (uint32_t)e;
+            n_act += tn;
+            __syncthreads();
+        }
+    }
+    const uint32_t IR = P.item_rows;
+    const uint32_t I0 = ((uint32_t)(P.st[0].r_hi - P.st[0].r_lo) + IR - 1) / IR;
+    const uint32_t I1 = P.nstacks > 1 ? ((uint32_t)(P.st[1].r_hi - P.st[1].r_lo) + IR - 1) / IR : 0u;
+    const uint64_t it0 = (uint64_t)n_act * I0;
+    const uint64_t total = it0 + (uint64_t)n_act * I1;
+
+    for (uint64_t it = blockIdx.x; it < total; it += gridDim.x) {
+        const int s = it < it0 ? 0 : 1;
+        const DecStack &S = P.st[s];
+        const uint32_t Is = s ? I1 : I0;
+        const uint64_t li = s ? it - it0 : it;
+        const uint32_t j = (uint32_t)(li / Is);
+        const uint32_t k = (uint32_t)(li - (uint64_t)j * Is);
+        const uint64_t e = P.expert_start != nullptr ? act[j] : j;
+        const uint64_t R = (uint64_t)S.R, C = (uint64_t)S.C, rb = (uint64_t)S.rb;
+        const uint64_t r0 = e * R + (uint64_t)S.r_lo + (uint64_t)k * IR;
+        const uint64_t r1 = min(r0 + IR, e * R + (uint64_t)S.r_hi);
+        // Element x of the stack lands at tile_sa + (x - x0): 32-byte pieces of
+        // the flat stream stay 32-byte aligned in shared memory.
+        const uint64_t x0 = (r0 * C) & ~31ull;
+        const uint64_t ua = r0 / rb, nu = (r1 + rb - 1) / rb - ua;
+        const uint64_t wa = ua + nu * (uint64_t)warp / kWarps, wb = ua + nu * (uint64_t)(warp + 1) / kWarps;
+        if (wa < wb) {
+            const uint64_t row_a = wa * rb, row_b = min(wb * rb, S.rows);
+            const uint64_t lo = max(row_a, r0) * C, hi = min(row_b, r1) * C;
+            const uint32_t sdst = tile_sa + (uint32_t)(row_a * C - x0);   // modulo 2^32
+            if (S.kind == CSF_NVFP4)
+                segment_nvfp4<true>(S, row_a, row_b, lo, hi, lane, s_stage[warp], sdst);
+            else
+                segment_mxfp4<true>(S, row_a, row_b, lo, hi, lane, s_stage[warp], sdst);
+        }
+        __syncthreads();
+
+        const uint32_t Ci = (uint32_t)C;
+        const uint32_t ncb = (Ci + 3) / 4;
+        const uint32_t nrow = (uint32_t)(r1 - r0);
+        const uint32_t nblk = (nrow + kTileRows - 1) / kTileRows;
+        const uint32_t rblk0 = (uint32_t)((r0 - e * R) / kTileRows);
+        const uint64_t RP = (R + kTileRows - 1) / kTileRows * kTileRows;
+        uint8_t *eo = S.ws + e * RP * (uint64_t)(4 * ncb);
+        const uint32_t toff = (uint32_t)(r0 * C - x0);
+        const uint32_t nline = nblk * ncb * 32;
+        for (uint32_t ln = threadIdx.x; ln < nline; ln += kThreads) {
+            const uint32_t b = ln & 31, t = ln >> 5;
+            const uint32_t blk = t / ncb, cb = t - blk * ncb;
+            uint32_t w[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const uint32_t rl = blk * kTileRows + 32u * a + b;
+                uint32_t v = 0;
+                if (rl < nrow) {
+                    const uint32_t off = tile_sa + toff + rl * Ci + 4 * cb;
+                    if ((Ci & 3) == 0) {
+                        v = lds_u32(off);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (4 * cb + q < Ci) v |= lds_u8(off + q) << (8 * q);
+                    }
+                }
+                w[a] = v;
+            }
+            *reinterpret_cast<uint4 *>(eo + ((uint64_t)(rblk0 + blk) * ncb + cb) * 512 + 16 * b) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        __syncthreads();
     }
 }
 
 }  // namespace
 
+// Dynamic shared memory beyond the default window (48 KB with the static
+// part) needs an opt-in, before the occupancy query as well as the launch.
+template <typename K>
+cudaError_t allow_smem(K kernel, size_t smem) {
+    if (smem == 0) return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+cudaError_t decode_blocked_occupancy(size_t smem, int *blocks_per_sm) {
+    cudaError_t e = allow_smem(decode_blocked_kernel, smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_blocked_kernel, kThreads, smem);
+}
+
+cudaError_t launch_decode_blocked(const DecParams &p, int grid, size_t smem, cudaStream_t s) {
+    cudaError_t e = allow_smem(decode_blocked_kernel, smem);
+    if (e != cudaSuccess) return e;
+    decode_blocked_kernel<<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t decode_occupancy(bool per_expert, size_t smem, int *blocks_per_sm) {
-    if (per_expert)
+    if (per_expert) {
+        cudaError_t e = allow_smem(decode_kernel<true>, smem);
+        if (e != cudaSuccess) return e;
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<true>, kThreads, smem);
+    }
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<false>, kThreads, smem);
 }
 
 cudaError_t launch_decode(const DecParams &p, int grid, size_t smem, bool per_expert, cudaStream_t s) {
     if (per_expert) {
-        if (smem > 16 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
-            if (e != cudaSuccess) return e;
-        }
+        cudaError_t e = allow_smem(decode_kernel<true>, smem);
+        if (e != cudaSuccess) return e;
         decode_kernel<true><<<grid, kThreads, smem, s>>>(p);
     } else {
         decode_kernel<false><<<grid, kThreads, 0, s>>>(p);

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(csf):
 
 
 def test_abi_version_and_status_strings(csf):
-    assert csf.lib.csf_abi_version() == 2
+    assert csf.lib.csf_abi_version() == 3
     for code, text in [(0, "ok"), (1, "invalid argument"), (2, "buffer too small"),
                        (3, "unsupported geometry"), (4, "CUDA error")]:
         assert csf.lib.csf_status_string(code).decode() == text
@@ -50,6 +50,7 @@ def test_sizes(csf, kind, E, R, C):
     assert sz["offsets"] == (packed + 15) // 16 * 16
     assert sz["escapes"] == (0 if kind == 0 else sz["offsets"])
     assert sz["prepare_scratch"] >= 16 + 8
+    assert sz["blocked"] == E * (-(-R // 128) * 128) * (-(-C // 4) * 4)
 
 
 def test_sizes_rejects_bad_geometry(csf):
@@ -131,3 +132,26 @@ def test_expand_argument_checks_before_cuda(csf):
     small = (csf.CDecodePart * 1)()
     small[0] = csf.CDecodePart(ctypes.pointer(st), 16, 639, 0, 10)
     assert csf.lib.csf_expand(small, 1, None, None, None) == 2
+
+
+def test_blocked_layout_argument_checks_before_cuda(csf):
+    # The blocked layout's own checks return before any CUDA call.
+    g = csf.Geometry(0, 2, 256, 100)
+    st = csf.CStack(g, 16, 16, None, 16, 16, 0, None)
+    nb = csf.sizes(0, 2, 256, 100)["blocked"]
+
+    def one(ws=16, nbytes=nb, lo=0, hi=256, layout=csf.LAYOUT_BLOCKED, stack=st):
+        arr = (csf.CDecodePart * 1)()
+        arr[0] = csf.CDecodePart(ctypes.pointer(stack), ws, nbytes, lo, hi, layout)
+        return csf.lib.csf_decode_rows(arr, 1, None, 0, None)
+
+    assert one(ws=24) == 1                       # workspace not 16-byte aligned
+    assert one(lo=64) == 1 and one(hi=200) == 1  # rows off the 128-row boundaries
+    assert one(nbytes=nb - 1) == 2               # smaller than the blocked size
+    assert one(layout=7) == 1                    # unknown layout
+    wide = csf.CStack(csf.Geometry(0, 1, 128, 1025), 16, 16, None, 16, 16, 0, None)
+    assert one(stack=wide, nbytes=1 << 24, hi=128) == 3
+    mixed = (csf.CDecodePart * 2)()
+    mixed[0] = csf.CDecodePart(ctypes.pointer(st), 16, nb, 0, 256, csf.LAYOUT_BLOCKED)
+    mixed[1] = csf.CDecodePart(ctypes.pointer(st), 16, nb, 0, 256, csf.LAYOUT_ROWS)
+    assert csf.lib.csf_decode_rows(mixed, 2, None, 0, None) == 1

@@ -131,6 +131,26 @@ def test_routed_runs_of_consecutive_experts(csf, kind, E, R, C):
     assert up.errors() == 0
 
 
+@pytest.mark.parametrize("E", [1300, 8192])
+def test_routed_many_experts_varying_units(csf, E):
+    # Experts whose unit counts differ (R not a multiple of the unit rows)
+    # keep per-expert prefix arrays in shared memory: 12*E + 8 bytes on top of
+    # the static staging buffers, past the default 48 KB window at E = 1300.
+    R, C = 5, 7
+    dense = _small_dense(0, E, R, C, seed=E)
+    enc = oracle.encode(0, dense)
+    up = csf.upload(enc)
+    counts = np.zeros(E, np.int64)
+    counts[np.arange(0, E, 97)] = 1
+    counts[E - 1] = 2
+    start = np.concatenate([[0], np.cumsum(counts)])
+    ws = torch.full(dense.shape, 0xFF, dtype=torch.uint8, device="cuda")
+    csf.decode(up, ws, expert_start=torch.from_numpy(start.astype(np.int32)).cuda())
+    want, _ = oracle.decode(enc, start, np.full(dense.shape, 0xFF, np.uint8))
+    assert np.array_equal(_np(ws), want)
+    assert up.errors() == 0
+
+
 def test_routed_edge_cases(csf):
     dense = _small_dense(0, 8, 16, 100, seed=3)
     enc = oracle.encode(0, dense)
