@@ -234,8 +234,8 @@ csf_status csf_decode_pair(const csf_stack *gate, uint8_t *gate_ws, size_t gate_
  *       innermost); scale (r, c) of a tile at byte
  *       (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4.  Experts follow each
  *       other, RP * CP bytes apart.  Padding bytes are written 0.  Needs a
- *       16-byte aligned workspace of csf_sizes().blocked bytes, row ranges on
- *       128-row boundaries (row_hi may also be R), and C <= 1024.
+ *       16-byte aligned workspace of csf_sizes().blocked bytes and row
+ *       ranges on 128-row boundaries (row_hi may also be R).
  */
 #define CSF_LAYOUT_ROWS 0
 #define CSF_LAYOUT_BLOCKED 1
@@ -268,8 +268,7 @@ typedef struct {
  * workspace not 16-byte aligned or rows off its 128-row boundaries, and the
  * csf_decode cases), CSF_ERR_SIZE, CSF_ERR_UNSUPPORTED (E > 8192 with
  * routing, or with a partial row range in the row-major layout: the
- * per-expert work list lives in shared memory; C > 1024 in the blocked
- * layout), CSF_ERR_CUDA.
+ * per-expert work list lives in shared memory), CSF_ERR_CUDA.
  */
 csf_status csf_decode_rows(const csf_decode_part *parts, int num_parts,
                            const void *expert_start, int expert_start_is_int64, void *stream);

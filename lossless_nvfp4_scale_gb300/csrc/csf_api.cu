@@ -135,9 +135,6 @@ struct DecodeLaunch {
     bool blocked;
 };
 
-// Largest C of the blocked layout: a 128-row item buffer of 128*C bytes
-// plus the per-warp staging stays within the shared memory of one block.
-constexpr int32_t kBlockedMaxCols = 1024;
 
 csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *expert_start, int es64,
                        DecodeLaunch *L) {
@@ -148,7 +145,6 @@ csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *exp
     const int32_t layout = parts[0].layout;
     if (layout != CSF_LAYOUT_ROWS && layout != CSF_LAYOUT_BLOCKED) return CSF_ERR_ARG;
     const bool blocked = layout == CSF_LAYOUT_BLOCKED;
-    int32_t cmax = 0;
     for (int i = 0; i < nparts; ++i) {
         const csf_decode_part &q = parts[i];
         if (q.layout != layout) return CSF_ERR_ARG;
@@ -160,8 +156,6 @@ csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *exp
             if (q.row_lo % kTileRows != 0 || (q.row_hi % kTileRows != 0 && q.row_hi != q.stack->g.rows))
                 return CSF_ERR_ARG;
             if (q.ws_bytes < blocked_bytes(&q.stack->g)) return CSF_ERR_SIZE;
-            if (q.stack->g.cols > kBlockedMaxCols) return CSF_ERR_UNSUPPORTED;
-            if (q.stack->g.cols > cmax) cmax = q.stack->g.cols;
         }
         p.st[i].r_lo = q.row_lo;
         p.st[i].r_hi = q.row_hi;
@@ -187,23 +181,21 @@ csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *exp
     if (st != CSF_OK) return st;
     L->blocked = blocked;
     if (blocked) {
-        // Items of 256 rows while their buffer stays small, else 128 rows.
-        const uint32_t ir = 256u * (uint32_t)cmax + 32u <= 64u * 1024u ? 256u : (uint32_t)kTileRows;
-        const uint32_t act = expert_start ? (4u * (uint32_t)p.E + 15u) & ~15u : 0u;
-        p.item_rows = ir;
-        p.tile_off = act;
-        const size_t smem = act + (((size_t)ir * (size_t)cmax + 32 + 15) & ~(size_t)15);
+        // One warp per 128-row block of an expert; the routed active list in
+        // dynamic shared memory.
+        const size_t smem = expert_start ? 4ull * (uint64_t)p.E : 0;
         int occ = 0;
-        if (decode_blocked_occupancy(smem, &occ) != cudaSuccess) {
+        if (decode_tiles_occupancy(smem, &occ) != cudaSuccess) {
             cudaGetLastError();
             return CSF_ERR_CUDA;
         }
         if (occ < 1) return CSF_ERR_UNSUPPORTED;
         uint64_t items = 0;
         for (int i = 0; i < nparts; ++i)
-            items += (uint64_t)p.E * (((uint64_t)(p.st[i].r_hi - p.st[i].r_lo) + ir - 1) / ir);
+            items += (uint64_t)p.E * (((uint64_t)(p.st[i].r_hi - p.st[i].r_lo) + kTileRows - 1) / kTileRows);
         uint64_t grid = (uint64_t)di.sms * (uint64_t)occ;
-        if (items < grid) grid = items;
+        const uint64_t need = (items + kTileBlockWarps - 1) / kTileBlockWarps;
+        if (need < grid) grid = need;
         if (grid < 1) grid = 1;
         L->smem = smem;
         L->grid = (int)grid;
@@ -238,7 +230,7 @@ csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *exp
 
 csf_status launch(const DecodeLaunch &L, void *stream) {
     const cudaError_t e = L.blocked
-                              ? launch_decode_blocked(L.p, L.grid, L.smem, static_cast<cudaStream_t>(stream))
+                              ? launch_decode_tiles(L.p, L.grid, L.smem, static_cast<cudaStream_t>(stream))
                               : launch_decode(L.p, L.grid, L.smem, L.per_expert, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();

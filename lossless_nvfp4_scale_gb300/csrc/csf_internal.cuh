@@ -58,8 +58,6 @@ struct DecParams {
     const void *expert_start;   // null: every expert
     int32_t es64;
     int32_t uniform;            // every stack has R % rb == 0: unit -> expert is a division
-    uint32_t item_rows;         // scale-operand layout: rows decoded per block item (128 or 256)
-    uint32_t tile_off;          // scale-operand layout: dynamic smem offset of the item buffer
 };
 
 struct PrepParams {
@@ -97,10 +95,12 @@ inline int32_t unit_rows(int32_t C, int chunk) {
 
 cudaError_t launch_decode(const DecParams &p, int grid, size_t smem, bool routed, cudaStream_t s);
 cudaError_t decode_occupancy(bool routed, size_t smem, int *blocks_per_sm);
-// Decode into the 128 x 4 tiled scale-operand layout of block-scaled GEMMs.
+// Decode into the 128 x 4 tiled scale-operand layout of block-scaled GEMMs
+// (one warp per 128-row block of an expert).
 constexpr int kTileRows = 128;
-cudaError_t launch_decode_blocked(const DecParams &p, int grid, size_t smem, cudaStream_t s);
-cudaError_t decode_blocked_occupancy(size_t smem, int *blocks_per_sm);
+constexpr int kTileBlockWarps = 4;   // warps per block
+cudaError_t launch_decode_tiles(const DecParams &p, int grid, size_t smem, cudaStream_t s);
+cudaError_t decode_tiles_occupancy(size_t smem, int *blocks_per_sm);
 
 cudaError_t launch_prepare(const PrepParams &p, size_t smem, cudaStream_t s);
 void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity,

@@ -149,8 +149,6 @@ def test_blocked_layout_argument_checks_before_cuda(csf):
     assert one(lo=64) == 1 and one(hi=200) == 1  # rows off the 128-row boundaries
     assert one(nbytes=nb - 1) == 2               # smaller than the blocked size
     assert one(layout=7) == 1                    # unknown layout
-    wide = csf.CStack(csf.Geometry(0, 1, 128, 1025), 16, 16, None, 16, 16, 0, None)
-    assert one(stack=wide, nbytes=1 << 24, hi=128) == 3
     mixed = (csf.CDecodePart * 2)()
     mixed[0] = csf.CDecodePart(ctypes.pointer(st), 16, nb, 0, 256, csf.LAYOUT_BLOCKED)
     mixed[1] = csf.CDecodePart(ctypes.pointer(st), 16, nb, 0, 256, csf.LAYOUT_ROWS)

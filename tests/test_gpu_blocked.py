@@ -35,7 +35,8 @@ def _dense(kind, E, R, C, seed, replace_p=0.08):
 
 
 SHAPES = [(0, 1, 1, 1), (0, 2, 128, 4), (0, 3, 200, 7), (0, 2, 256, 100), (0, 3, 300, 50), (0, 2, 1000, 100),
-          (0, 2, 640, 12), (0, 1, 129, 255), (0, 2, 130, 600), (1, 2, 130, 160), (1, 3, 64, 33), (1, 2, 512, 160)]
+          (0, 2, 640, 12), (0, 1, 129, 255), (0, 2, 130, 600), (1, 2, 130, 160), (1, 3, 64, 33), (1, 2, 512, 160),
+          (0, 1, 128, 2000), (1, 2, 100, 17)]
 
 
 @pytest.mark.parametrize("kind,E,R,C", SHAPES)
