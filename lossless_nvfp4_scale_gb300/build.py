@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libcsf.so")
-SOURCES = ["csf_api.cu", "csf_decode.cu", "csf_prepare.cu", "csf_prepare_static.cu"]
+SOURCES = ["csf_api.cu", "csf_decode.cu", "csf_tiles.cu", "csf_prepare.cu", "csf_prepare_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -31,7 +31,8 @@ def nvcc() -> str:
 
 def _inputs():
     files = [os.path.join(CSRC, s) for s in SOURCES]
-    files += [os.path.join(CSRC, "csf_internal.cuh"), os.path.join(INCLUDE, "csf.h")]
+    files += [os.path.join(CSRC, "csf_internal.cuh"), os.path.join(CSRC, "csf_device.cuh"),
+              os.path.join(INCLUDE, "csf.h")]
     return files
 
 
