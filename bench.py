@@ -211,7 +211,7 @@ def run_own(args, rank, world, torch, dist):
     }
     result["clocks"] = clk.summary()
     if rank == 0 and not args.skip_rows:
-        result["rows"] = measure_rows(torch, csf, synth, gate, gate_dense, hbm)
+        result["rows"] = measure_rows(torch, csf, synth, gate, gate_dense, hbm, args.steps)
     if rank == 0:
         result["e2e"] = measure_e2e(torch, csf, gate, gate_dense)
         if not args.skip_cpu:
@@ -249,8 +249,14 @@ def profiled_traffic():
     return None
 
 
-def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
+def measure_rows(torch, csf, synth, gate, gate_dense, hbm, max_steps):
+    """Side figures of the other rows; each row times its default number of
+    steps, fewer when the run asks for fewer (short profiling runs)."""
     rows = {}
+
+    def n(k):
+        return max(16, min(k, max_steps))
+
     E = 512
     start = torch.from_numpy(synth.routing(E=E, active=8, tokens=64, seed=0)).cuda()
     active = int((start[1:] > start[:-1]).sum().item())
@@ -266,17 +272,17 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
 
     # routed 8 of 512: latency-bound, 1.25 MB, L2-warm like the pages' warm
     # graph figure; reported next to an empty-launch floor
-    durs = timed_steps(torch, lambda i: csf.decode(gate, ws, expert_start=start), 400, 20)
+    durs = timed_steps(torch, lambda i: csf.decode(gate, ws, expert_start=start), n(400), 20)
     rec("routed_8of512", durs, stack_traffic(gate, rows_active=active * 1024), {"l2": "warm"})
     z = torch.zeros(1, device="cuda")
-    floor = timed_steps(torch, lambda i: z.add_(1), 400, 20)
+    floor = timed_steps(torch, lambda i: z.add_(1), n(400), 20)
     rows["routed_8of512"]["empty_launch_floor_us"] = round(1e3 * floor[0] / floor[1], 3)
 
     # gate half of every expert (rows [0, R/2): the stack read as fused
     # gate/up), rotating over 4 copies (4 x 40 MB of inputs > L2)
     hc = [gate] + [clone_stack(torch, gate) for _ in range(3)]
     hw = [torch.empty_like(gate_dense) for _ in range(4)]
-    durs = timed_steps(torch, lambda i: csf.decode(hc[i % 4], hw[i % 4], rows=(0, 512)), 400, 20)
+    durs = timed_steps(torch, lambda i: csf.decode(hc[i % 4], hw[i % 4], rows=(0, 512)), n(400), 20)
     assert torch.equal(hw[0][:, :512], gate_dense[:, :512])
     rec("gate_half_all", durs, stack_traffic(gate, rows_active=512 * 512))
     del hc, hw
@@ -285,7 +291,7 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
     # rotating over 4 copies (4 x 80 MB > L2)
     bc = [gate] + [clone_stack(torch, gate) for _ in range(3)]
     bw = [torch.empty(csf.blocked_bytes(gate), dtype=torch.uint8, device="cuda") for _ in range(4)]
-    durs = timed_steps(torch, lambda i: csf.decode(bc[i % 4], bw[i % 4], layout=csf.LAYOUT_BLOCKED), 400, 20)
+    durs = timed_steps(torch, lambda i: csf.decode(bc[i % 4], bw[i % 4], layout=csf.LAYOUT_BLOCKED), n(400), 20)
     rec("gate_blocked_layout", durs, stack_traffic(gate))
     del bc, bw
 
@@ -296,10 +302,10 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
     g2, d2 = clone_stack(torch, gate), clone_stack(torch, down)
     gws2, dws2 = torch.empty_like(gate_dense), torch.empty_like(down_dense)
     pairs = [(gate, down, gws, dws), (g2, d2, gws2, dws2)]
-    durs = timed_steps(torch, lambda i: csf.decode_pair(*pairs[i % 2]), 200, 10)
+    durs = timed_steps(torch, lambda i: csf.decode_pair(*pairs[i % 2]), n(200), 10)
     assert torch.equal(gws, gate_dense) and torch.equal(dws, down_dense)
     rec("pair_full", durs, stack_traffic(gate) + stack_traffic(down))
-    durs = timed_steps(torch, lambda i: csf.decode_pair(gate, down, gws, dws, expert_start=start), 400, 20)
+    durs = timed_steps(torch, lambda i: csf.decode_pair(gate, down, gws, dws, expert_start=start), n(400), 20)
     rec("pair_routed_8of512", durs,
         stack_traffic(gate, rows_active=active * 1024) + stack_traffic(down, rows_active=active * 2048),
         {"l2": "warm"})
@@ -333,7 +339,7 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
         return f
 
     def us(fn):
-        t = timed_steps(torch, fn, 200, 10)
+        t = timed_steps(torch, fn, n(200), 10)
         return 1e3 * t[0] / t[1]
 
     ue = us(lambda i: csf.expand_scales([(gate, gws), (down, dws)]))
@@ -351,7 +357,7 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
     psts = [csf.empty_stack(csf.NVFP4, E_, R_, C_, exc_capacity=gate.dense_bytes) for _ in range(2)]
     scrs = [csf.prepare_scratch(csf.NVFP4, E_, R_, C_) for _ in range(2)]
     dens = [gate_dense, gate_dense.clone()]                 # 2 rotating copies: 2 x 82 MB > L2
-    durs = timed_steps(torch, lambda i: csf.prepare_async(dens[i % 2], psts[i % 2], scrs[i % 2]), 100, 5)
+    durs = timed_steps(torch, lambda i: csf.prepare_async(dens[i % 2], psts[i % 2], scrs[i % 2]), n(100), 5)
     sb = gate.stream_bytes()
     rec("prepare_gate", durs, gate.dense_bytes + sb["offsets"] + sb["base"] + sb["exc_index"] + sb["exc_bytes"])
     del psts, scrs, dens
@@ -362,7 +368,7 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
     E_, R_, C_ = mx.shape
     pst = csf.empty_stack(csf.MXFP4, E_, R_, C_, exc_capacity=mx.dense_bytes)
     scr = csf.prepare_scratch(csf.MXFP4, E_, R_, C_)
-    durs = timed_steps(torch, lambda i: csf.prepare_async(mx_dense, pst, scr), 50, 5)
+    durs = timed_steps(torch, lambda i: csf.prepare_async(mx_dense, pst, scr), n(50), 5)
     sb = mx.stream_bytes()
     rec("prepare_mxfp4", durs, mx.dense_bytes + sb["offsets"] + sb["escapes"] + sb["base"] + sb["exc_index"]
         + sb["exc_bytes"], {"exception_rate": round(mx.num_exc / mx.dense_bytes, 4)})
@@ -370,7 +376,7 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm):
     mx2 = clone_stack(torch, mx)
     mws = [torch.empty_like(mx_dense), torch.empty_like(mx_dense)]
     mcs = [mx, mx2]
-    durs = timed_steps(torch, lambda i: csf.decode(mcs[i % 2], mws[i % 2]), 100, 5)
+    durs = timed_steps(torch, lambda i: csf.decode(mcs[i % 2], mws[i % 2]), n(100), 5)
     assert torch.equal(mws[0], mx_dense)
     rec("decode_mxfp4", durs, stack_traffic(mx))
     return rows
