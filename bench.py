@@ -239,8 +239,8 @@ def profiled_traffic():
         info = {}
         with open(os.path.join(ROOT, "profiles", "decode_gate_512x1024x100.md")) as f:
             for ln in f:
-                if ":" in ln and ln.startswith("- "):
-                    k, v = ln[2:].split(":", 1)
+                if ": " in ln and ln.startswith("- "):
+                    k, v = ln[2:].split(": ", 1)
                     info[k.strip()] = v.strip().strip("`")
         if info.get("csf_decode.cu sha256[:16]") == digest:
             return float(info["dram bytes per launch"])
