@@ -195,3 +195,28 @@ def test_blocked_scales_drive_a_real_nvfp4_gemm(csf):
     flat = torch.from_numpy(sb_dense.reshape(-1).copy()).cuda().view(torch.float8_e4m3fn)
     d2 = _nvfp4_gemm(a, b_t, sa, flat).float().cpu().numpy().astype(np.float64)
     assert np.linalg.norm(d2 - ref) / np.linalg.norm(ref) > 0.1
+
+
+def test_blocked_corrupt_index_sets_error_word(csf):
+    # Corruptions planted on the CPU, as in the row-major test: one row's
+    # index step off by one, and a stream shorter than the index says.
+    for kind in (0, 1):
+        dense = _dense(kind, 4, 64, 8, seed=kind)
+        enc = oracle.encode(kind, dense)
+        assert enc["num_exc"] > 10
+        bad = dict(enc)
+        bad["exc_index"] = enc["exc_index"].copy()
+        bad["exc_index"][100:] += 1
+        assert oracle.check(bad) == oracle.ERR_CORRUPT
+        up = csf.upload(bad)
+        csf.decode(up, layout=csf.LAYOUT_BLOCKED)
+        assert up.errors() & csf.DEV_ERR_CORRUPT
+        bad = dict(enc)
+        bad["num_exc"] = enc["num_exc"] - 3
+        bad["exc_bytes"] = enc["exc_bytes"][:-3]
+        up = csf.upload(bad)
+        csf.decode(up, layout=csf.LAYOUT_BLOCKED)
+        assert up.errors() & csf.DEV_ERR_CORRUPT
+        good = csf.upload(enc)
+        csf.decode(good, layout=csf.LAYOUT_BLOCKED)
+        assert good.errors() == 0
