@@ -107,6 +107,30 @@ __device__ __forceinline__ void store32(uint8_t *ws, int align, uint32_t p, cons
     }
 }
 
+__device__ __forceinline__ void sts_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
+__device__ __forceinline__ void sts_u8(uint32_t a, uint32_t v) {
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// Shared-memory twin of store32: local elements [p, p+32) at shared address
+// sa0 + p (16-byte aligned), only the bytes inside [lo, hi).
+__device__ __forceinline__ void sstore32(uint32_t sa0, uint32_t p, const uint32_t *w, uint32_t lo, uint32_t hi) {
+    const uint32_t a = sa0 + p;
+    if (p >= lo && p + 32 <= hi) {
+        sts_v4(a, w[0], w[1], w[2], w[3]);
+        sts_v4(a + 16, w[4], w[5], w[6], w[7]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const uint32_t q = p + j;
+            if (q >= lo && q < hi) sts_u8(a + j, (w[j >> 2] >> (8 * (j & 3))) & 0xFFu);
+        }
+    }
+}
+
 // Mask of the bytes of word k (elements 4k..4k+3 of a run) that lie at or
 // after element b of the run.
 __device__ __forceinline__ uint32_t bytes_from(int b, int k) {
@@ -149,9 +173,13 @@ __device__ __forceinline__ void base_words_general(uint32_t (&bw)[NW], uint32_t 
 // ------------------------------------------------------------------ NVFP4
 
 // Decode rows [row_a, row_b) of an NVFP4 stack (row_a*C a multiple of 64),
-// storing only global elements in [lo, hi).  Whole warp.
+// storing only global elements in [lo, hi).  Whole warp.  SMEM: the bytes go
+// to shared memory instead, element row_a*C + p at shared address sdst + p
+// (16-byte aligned for p % 32 == 0), and exceptions are patched there in
+// place (no staging); `stage` is then unused.
+template <bool SMEM>
 __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b, uint64_t lo, uint64_t hi,
-                              int lane, uint8_t *stage) {
+                              int lane, uint8_t *stage, uint32_t sdst) {
     const uint32_t C = (uint32_t)S.C;
     const uint64_t sa = row_a * C;
     const uint32_t nel = (uint32_t)(row_b * C - sa);
@@ -302,6 +330,35 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
         uint32_t tot;
         uint32_t xl = X + warp_excl_scan(cnt, lane, tot);
         X += tot;
+        if constexpr (SMEM) {
+            // Write the chunk, then patch its exceptions in place.
+            if (nv > 0) {
+                sstore32(sdst, p, out, lo_l, hi_l);
+                if (nv > 32) sstore32(sdst, p + 32, out + 8, lo_l, hi_l);
+            }
+            if (cnt) {
+                if (xl <= nexc && cnt <= nexc - xl) {
+                    const uint8_t *ep = S.exc_bytes + xl;
+                    uint32_t f = f0;
+                    while (f) {
+                        const uint32_t j = p + (uint32_t)(__ffs(f) - 1);
+                        const uint32_t v = __ldg(ep++);
+                        if (j >= lo_l && j < hi_l) sts_u8(sdst + j, v);
+                        f &= f - 1;
+                    }
+                    f = f1;
+                    while (f) {
+                        const uint32_t j = p + (uint32_t)(__ffs(f) + 31);
+                        const uint32_t v = __ldg(ep++);
+                        if (j >= lo_l && j < hi_l) sts_u8(sdst + j, v);
+                        f &= f - 1;
+                    }
+                } else {
+                    bad = true;
+                }
+            }
+            continue;
+        }
         if (__any_sync(kFull, cnt != 0)) {
 #pragma unroll
             for (int s = 0; s < 4; ++s)
@@ -345,9 +402,11 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
 
 // ------------------------------------------------------------------ MXFP4
 
-// Decode rows [row_a, row_b) of an MXFP4 stack (row_a*C a multiple of 128).
+// Decode rows [row_a, row_b) of an MXFP4 stack (row_a*C a multiple of 128);
+// SMEM and sdst as in segment_nvfp4.
+template <bool SMEM>
 __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b, uint64_t lo, uint64_t hi,
-                              int lane, uint8_t *stage) {
+                              int lane, uint8_t *stage, uint32_t sdst) {
     const uint32_t C = (uint32_t)S.C;
     const uint64_t sa = row_a * C;
     const uint32_t nel = (uint32_t)(row_b * C - sa);
@@ -451,11 +510,15 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                         out[k] = add_base(bw[k], (nib * 0x00204081u) & 0x01010101u);
                     }
                 }
+                if constexpr (SMEM) {
+                    if (32 * gi < nv) sstore32(sdst, p + 32u * gi, out, lo_l, hi_l);
+                } else {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int s = 2 * gi + h;
-                    *reinterpret_cast<uint4 *>(my + ((16 * s) ^ gs)) =
-                        make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
+                    for (int h = 0; h < 2; ++h) {
+                        const int s = 2 * gi + h;
+                        *reinterpret_cast<uint4 *>(my + ((16 * s) ^ gs)) =
+                            make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
+                    }
                 }
                 qg += 32;
                 while (qg >= C) { qg -= C; ++rg; }
@@ -467,7 +530,13 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                     for (int gi = 0; gi < 4; ++gi) {
                         uint32_t f = xw[gi];
                         while (f) {
-                            my[(32u * gi + (uint32_t)(__ffs(f) - 1)) ^ gs] = __ldg(ep++);
+                            if constexpr (SMEM) {
+                                const uint32_t j = p + 32u * gi + (uint32_t)(__ffs(f) - 1);
+                                const uint32_t v = __ldg(ep++);
+                                if (j >= lo_l && j < hi_l) sts_u8(sdst + j, v);   // patched in place
+                            } else {
+                                my[(32u * gi + (uint32_t)(__ffs(f) - 1)) ^ gs] = __ldg(ep++);
+                            }
                             f &= f - 1;
                         }
                     }
@@ -475,6 +544,7 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                     bad = true;
                 }
             }
+            if constexpr (SMEM) continue;
 #pragma unroll
             for (int gi = 0; gi < 4; ++gi) {
                 uint32_t out[8];
@@ -676,14 +746,152 @@ __global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel
             hi = min(row_b, r1) * C;
         }
         if (S.kind == CSF_NVFP4)
-            segment_nvfp4(S, row_a, row_b, lo, hi, lane, stage);
+            segment_nvfp4<false>(S, row_a, row_b, lo, hi, lane, stage, 0u);
         else
-            segment_mxfp4(S, row_a, row_b, lo, hi, lane, stage);
+            segment_mxfp4<false>(S, row_a, row_b, lo, hi, lane, stage, 0u);
         u += cnt;
     }
 }
 
+// ------------------------------ scale-operand layout, a 128-row block per block
+
+#ifndef CSF_BLOCKS_MIN_BLOCKS
+#define CSF_BLOCKS_MIN_BLOCKS 12
+#endif
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+// Decode into the 128 x 4 tiled scale-operand layout of block-scaled GEMMs
+// (see csf_tiles.cu for the layout): a block of kBlkWarps warps takes one
+// 128-row block of an expert; each warp decodes its share of the rows with
+// the row-major segment code into the block's shared-memory buffer
+// (exceptions patched in place); then the warps write the block's tiles,
+// lane b assembling line b of a tile from rows b, b+32, b+64, b+96, so every
+// tile leaves as one coalesced 512-byte warp store.  Rows whose first unit
+// starts before the warp's share are decoded whole and clipped.
+__global__ void __launch_bounds__(kBlkThreads, CSF_BLOCKS_MIN_BLOCKS) decode_blocks_kernel(const __grid_constant__ DecParams P) {
+    extern __shared__ __align__(16) uint8_t dsm[];
+    __shared__ uint32_t s_cnt[kBlkWarps];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    uint32_t *act = reinterpret_cast<uint32_t *>(dsm);
+    uint8_t *buf = dsm + P.buf_off;
+    const uint32_t buf_sa = (uint32_t)__cvta_generic_to_shared(buf);
+
+    uint32_t n_act = (uint32_t)P.E;
+    if (P.expert_start != nullptr) {
+        n_act = 0;
+        for (int e0 = 0; e0 < P.E; e0 += kBlkThreads) {
+            const int e = e0 + threadIdx.x;
+            bool a = false;
+            if (e < P.E) {
+                if (P.es64) {
+                    const long long *st = static_cast<const long long *>(P.expert_start);
+                    a = __ldg(st + e + 1) > __ldg(st + e);
+                } else {
+                    const int *st = static_cast<const int *>(P.expert_start);
+                    a = __ldg(st + e + 1) > __ldg(st + e);
+                }
+            }
+            const uint32_t bal = __ballot_sync(kFull, a);
+            if (lane == 0) s_cnt[warp] = __popc(bal);
+            __syncthreads();
+            uint32_t bn = n_act, tn = 0;
+#pragma unroll
+            for (int w = 0; w < kBlkWarps; ++w) {
+                if (w < warp) bn += s_cnt[w];
+                tn += s_cnt[w];
+            }
+            if (a) act[bn + __popc(bal & lanemask_lt())] = (uint32_t)e;
+            n_act += tn;
+            __syncthreads();
+        }
+    }
+    const uint32_t B0 = (uint32_t)(P.st[0].r_hi - P.st[0].r_lo + kTileRows - 1) / kTileRows;
+    const uint32_t B1 = P.nstacks > 1 ? (uint32_t)(P.st[1].r_hi - P.st[1].r_lo + kTileRows - 1) / kTileRows : 0u;
+    const uint64_t it0 = (uint64_t)n_act * B0;
+    const uint64_t total = it0 + (uint64_t)n_act * B1;
+    constexpr uint32_t kShare = kTileRows / kBlkWarps;                     // rows decoded per warp
+    for (uint64_t it = blockIdx.x; it < total; it += gridDim.x) {
+        const int s = it < it0 ? 0 : 1;
+        const DecStack &S = P.st[s];
+        const uint32_t Bs = s ? B1 : B0;
+        const uint64_t li = s ? it - it0 : it;
+        const uint32_t j = (uint32_t)(li / Bs);
+        const uint32_t t = (uint32_t)(li - (uint64_t)j * Bs);
+        const uint64_t e = P.expert_start != nullptr ? act[j] : j;
+        const uint64_t R = (uint64_t)S.R, C = (uint64_t)S.C, rb = (uint64_t)S.rb;
+        const uint32_t rl0 = (uint32_t)S.r_lo + t * kTileRows;          // expert-local first row
+        const uint64_t r0 = e * R + rl0;
+        const uint64_t r1 = min(r0 + kTileRows, e * R + (uint64_t)S.r_hi);
+        // Element x of the stack lands at buf + (x - x0); 32-byte pieces of the
+        // flat stream stay 32-byte aligned.
+        const uint64_t x0 = (r0 * C) & ~31ull;
+        const uint64_t rs = r0 + (uint64_t)warp * kShare;
+        const uint64_t re = min(rs + kShare, r1);
+        if (rs < re) {
+            const uint64_t row_a = rs / rb * rb, row_b = min((re + rb - 1) / rb * rb, S.rows);
+            const uint32_t sdst = buf_sa + (uint32_t)(row_a * C - x0);  // modulo 2^32
+            if (S.kind == CSF_NVFP4)
+                segment_nvfp4<true>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
+            else
+                segment_mxfp4<true>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
+        }
+        __syncthreads();
+
+        const uint32_t Ci = (uint32_t)C;
+        const uint32_t ncb = (Ci + 3) / 4;
+        const uint32_t nrow = (uint32_t)(r1 - r0);
+        const uint64_t RP = (R + kTileRows - 1) / kTileRows * kTileRows;
+        uint8_t *line = S.ws + e * RP * (4ull * ncb) + (uint64_t)(rl0 / kTileRows) * ncb * 512 + 16u * (uint32_t)lane;
+        const uint32_t src = buf_sa + (uint32_t)(r0 * C - x0) + (uint32_t)lane * Ci;
+        for (uint32_t cb = (uint32_t)warp; cb < ncb; cb += kBlkWarps) {
+            uint32_t w[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                uint32_t v = 0;
+                if ((uint32_t)lane + 32u * a < nrow) {
+                    const uint32_t off = src + 32u * a * Ci + 4 * cb;
+                    if ((Ci & 3) == 0) {
+                        v = lds_u32(off);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (4 * cb + q < Ci) v |= lds_u8(off + q) << (8 * q);
+                    }
+                }
+                w[a] = v;
+            }
+            *reinterpret_cast<uint4 *>(line + (uint64_t)cb * 512) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
+
+cudaError_t decode_blocks_occupancy(size_t smem, int *blocks_per_sm) {
+    cudaError_t e = cudaFuncSetAttribute(decode_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_blocks_kernel, kBlkThreads, smem);
+}
+
+cudaError_t launch_decode_blocks(const DecParams &p, int grid, size_t smem, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(decode_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    decode_blocks_kernel<<<grid, kBlkThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
 
 // Dynamic shared memory beyond the default window (48 KB with the static
 // part) needs an opt-in, before the occupancy query as well as the launch.

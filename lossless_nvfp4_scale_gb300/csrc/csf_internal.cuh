@@ -58,6 +58,8 @@ struct DecParams {
     const void *expert_start;   // null: every expert
     int32_t es64;
     int32_t uniform;            // every stack has R % rb == 0: unit -> expert is a division
+    uint32_t buf_off;           // scale-operand layout by blocks: dynamic smem offset of the 128-row buffer
+    uint32_t buf_bytes;         // bytes of that buffer
 };
 
 struct PrepParams {
@@ -99,6 +101,15 @@ cudaError_t decode_occupancy(bool routed, size_t smem, int *blocks_per_sm);
 // (one warp per 128-row block of an expert).
 constexpr int kTileRows = 128;
 constexpr int kTileBlockWarps = 4;   // warps per block
+// Same layout, one thread block per 128-row block, decoded by the row-major
+// segment code into a shared-memory buffer (csf_decode.cu).
+#ifndef CSF_BLK_WARPS
+#define CSF_BLK_WARPS 2
+#endif
+constexpr int kBlkWarps = CSF_BLK_WARPS;
+constexpr int kBlkThreads = 32 * kBlkWarps;
+cudaError_t launch_decode_blocks(const DecParams &p, int grid, size_t smem, cudaStream_t s);
+cudaError_t decode_blocks_occupancy(size_t smem, int *blocks_per_sm);
 cudaError_t launch_decode_tiles(const DecParams &p, int grid, size_t smem, cudaStream_t s);
 cudaError_t decode_tiles_occupancy(size_t smem, int *blocks_per_sm);
 

@@ -1,7 +1,9 @@
 // CSF decode into the scale-operand layout of Blackwell block-scaled GEMMs
 // (sm_103a): the 128 x 4 tiled layout that tcgen05 block scaling and
 // cuBLASLt's VEC16_UE4M3 / VEC32_UE8M0 scale factors read, so that no layout
-// pass runs between the decode and the GEMM.
+// pass runs between the decode and the GEMM.  This kernel works line by line
+// in registers and serves rows wider than the shared-memory buffers of
+// decode_blocks_kernel (csf_decode.cu) allow.
 //
 // Pages followed (cited by title and paragraph; they have no numbered
 // sections):
