@@ -124,3 +124,38 @@ def test_expansion_inside_a_cuda_graph(csf):
         graph.replay()
         torch.cuda.synchronize()
         assert np.array_equal(outg.cpu().numpy(), g1) and np.array_equal(outd.cpu().numpy(), d1)
+
+
+def test_concurrent_host_threads_on_separate_streams(csf):
+    # Several host threads call the library at once, each on its own stream
+    # with its own stacks and workspaces (the library's per-device state is
+    # set up once under a lock; calls share nothing else).
+    import threading
+    layers = [_layer(csf, 20 + k, E=8, I=64, Rd=64) for k in range(4)]
+    results = [None] * len(layers)
+    errors = []
+
+    def work(k):
+        try:
+            (g, sg), (d, sd) = layers[k]
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for _ in range(20):
+                    gws, dws = csf.decode_pair(sg, sd)
+                    half = csf.decode(sg, rows=(0, g.shape[1] // 2))
+            stream.synchronize()
+            results[k] = (gws.cpu().numpy(), dws.cpu().numpy(), half.cpu().numpy())
+        except Exception as exc:   # reported below
+            errors.append(exc)
+
+    torch.cuda.synchronize()                            # uploads done before other streams read them
+    threads = [threading.Thread(target=work, args=(k,)) for k in range(len(layers))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for k, ((g, _), (d, _)) in enumerate(layers):
+        gw, dw, half = results[k]
+        assert np.array_equal(gw, g) and np.array_equal(dw, d)
+        assert np.array_equal(half[:, :g.shape[1] // 2], g[:, :g.shape[1] // 2])
