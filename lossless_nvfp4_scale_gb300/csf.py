@@ -304,6 +304,8 @@ def expand_scales(parts, stream=None, after: torch.cuda.Event | None = None,
     `parts` is a list of (stack, ws) or (stack, ws, (lo, hi)); entries whose
     stack is None (scales that are not compressed) are skipped, and False is
     returned when nothing is left to expand."""
+    if any(p[0] is not None and p[1] is None for p in parts):
+        raise CsfError("expand_scales: every compressed stack needs the workspace it expands into")
     todo = [(p[0], _ws_for(p[0], p[1], "expand_scales", layout), p[2] if len(p) > 2 else None)
             for p in parts if p[0] is not None]
     if not todo:

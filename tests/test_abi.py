@@ -153,3 +153,13 @@ def test_blocked_layout_argument_checks_before_cuda(csf):
     mixed[0] = csf.CDecodePart(ctypes.pointer(st), 16, nb, 0, 256, csf.LAYOUT_BLOCKED)
     mixed[1] = csf.CDecodePart(ctypes.pointer(st), 16, nb, 0, 256, csf.LAYOUT_ROWS)
     assert csf.lib.csf_decode_rows(mixed, 2, None, 0, None) == 1
+
+
+def test_expand_scales_needs_the_workspace(csf):
+    # Host-side check of the binding: a compressed stack without its
+    # workspace is an error (no CUDA call is made).
+    class Fake:
+        pass
+    with pytest.raises(csf.CsfError, match="workspace"):
+        csf.expand_scales([(Fake(), None)])
+    assert csf.expand_scales([(None, None)]) is False
