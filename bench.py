@@ -277,6 +277,10 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm, max_steps):
     z = torch.zeros(1, device="cuda")
     floor = timed_steps(torch, lambda i: z.add_(1), n(400), 20)
     rows["routed_8of512"]["empty_launch_floor_us"] = round(1e3 * floor[0] / floor[1], 3)
+    # the same persistent grid with no active expert: launch, routing prologue, nothing to decode
+    none = torch.zeros(E + 1, dtype=start.dtype, device="cuda")
+    floor = timed_steps(torch, lambda i: csf.decode(gate, ws, expert_start=none), n(400), 20)
+    rows["routed_8of512"]["no_active_expert_us"] = round(1e3 * floor[0] / floor[1], 3)
 
     # gate half of every expert (rows [0, R/2): the stack read as fused
     # gate/up), rotating over 4 copies (4 x 40 MB of inputs > L2)
@@ -430,9 +434,33 @@ def cpu_baseline(synth, budget_s=8.0):
         reps += 1
     assert st == oracle.OK and np.array_equal(out, dense)
     gbs = reps * dense.size / t / 1e9
+    # Encode (the CPU counterpart of the GPU prepare), timed separately.
+    ereps, et = 0, 0.0
+    while et < budget_s / 4:
+        t0 = time.perf_counter()
+        oracle.encode(oracle.NVFP4, dense)
+        et += time.perf_counter() - t0
+        ereps += 1
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{E} of the 512 experts ({dense.size / 1e6:.1f} MB dense), {reps} decodes, "
-                      f"{t:.1f} s, 1 thread; us per 512-expert stack = {1e6 * 512 / E * t / reps:.0f}"}
+                      f"{t:.1f} s, 1 thread; us per 512-expert stack = {1e6 * 512 / E * t / reps:.0f}",
+            "encode_GB_s": round(ereps * dense.size / et / 1e9, 4),
+            "host": {"cpu": cpu_model(), "nproc": os.cpu_count()}}
+
+
+def cpu_model() -> str:
+    """CPU model string of the host, from /proc/cpuinfo (x86 `model name`, Arm
+    `CPU part` and implementer otherwise)."""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model", "Hardware"):
+        for ln in info:
+            if ln.startswith(key) and ":" in ln:
+                return ln.split(":", 1)[1].strip()
+    parts = sorted({ln.split(":", 1)[1].strip() for ln in info if ln.startswith(("CPU implementer", "CPU part"))})
+    return "arm " + " ".join(parts) if parts else "unknown"
 
 
 def run_reference(args):
