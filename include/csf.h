@@ -255,8 +255,9 @@ typedef struct {
  * Decode only a range of rows of each expert ([B478] pairing commit message:
  * decode only the gate halves that a fused gate/up consumer reads).  For a
  * fused gate/up stack with R = 2*I rows per expert, the gate half is rows
- * [0, I).  The workspace keeps the [E][R][C] layout: rows outside the range,
- * and the planes of experts that expert_start leaves inactive, are not
+ * [0, I).  The workspace keeps its whole-stack layout (row-major [E][R][C],
+ * or the blocked layout below, chosen per call by `layout`): rows outside the
+ * range, and the planes of experts that expert_start leaves inactive, are not
  * touched.  One or two parts (for example the gate half of a gate/up stack
  * and the whole down stack) decode in ONE launch with the same routing.
  *
