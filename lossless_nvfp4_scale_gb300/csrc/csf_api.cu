@@ -133,7 +133,7 @@ struct DecodeLaunch {
     int grid;
     bool per_expert;
     bool blocked;
-    bool warp_blocks;
+    bool buffered;
 };
 
 #ifndef CSF_BLOCKS_MAX_COLS
@@ -186,25 +186,26 @@ csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *exp
     csf_status st = device_info(&di);
     if (st != CSF_OK) return st;
     L->blocked = blocked;
-    L->warp_blocks = false;
+    L->buffered = false;
     if (blocked) {
-        // One warp per 128-row block of an expert; the routed active list in
-        // dynamic shared memory.  Rows up to kBlocksMaxCols bytes are decoded
-        // into a shared-memory buffer per warp (decode_blocks_kernel), wider
-        // rows line by line in registers (decode_tiles_kernel).
+        // Work per 128-row block of an expert; the routed active list in
+        // dynamic shared memory.  Rows up to kBlocksMaxCols bytes: one thread
+        // block per 128-row block, decoded into its shared-memory buffer
+        // (decode_blocks_kernel).  Wider rows: one warp per 128-row block,
+        // line by line in registers (decode_tiles_kernel).
         int32_t cmax = 0;
         for (int i = 0; i < nparts; ++i)
             if (p.st[i].C > cmax) cmax = p.st[i].C;
         const size_t act = expert_start ? (4ull * (uint64_t)p.E + 15) & ~(size_t)15 : 0;
-        L->warp_blocks = cmax <= kBlocksMaxCols;
+        L->buffered = cmax <= kBlocksMaxCols;
         size_t smem = act;
-        if (L->warp_blocks) {
+        if (L->buffered) {
             p.buf_off = (uint32_t)act;
             p.buf_bytes = (uint32_t)(((size_t)kTileRows * (size_t)cmax + 32 + 15) & ~(size_t)15);
             smem += p.buf_bytes;
         }
         int occ = 0;
-        const cudaError_t oe = L->warp_blocks ? decode_blocks_occupancy(smem, &occ) : decode_tiles_occupancy(smem, &occ);
+        const cudaError_t oe = L->buffered ? decode_blocks_occupancy(smem, &occ) : decode_tiles_occupancy(smem, &occ);
         if (oe != cudaSuccess) {
             cudaGetLastError();
             return CSF_ERR_CUDA;
@@ -214,7 +215,7 @@ csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *exp
         for (int i = 0; i < nparts; ++i)
             items += (uint64_t)p.E * (((uint64_t)(p.st[i].r_hi - p.st[i].r_lo) + kTileRows - 1) / kTileRows);
         uint64_t grid = (uint64_t)di.sms * (uint64_t)occ;
-        const uint64_t per_block = L->warp_blocks ? 1 : kTileBlockWarps;   // 128-row blocks per thread block
+        const uint64_t per_block = L->buffered ? 1 : kTileBlockWarps;   // 128-row blocks per thread block
         const uint64_t need = (items + per_block - 1) / per_block;
         if (need < grid) grid = need;
         if (grid < 1) grid = 1;
@@ -252,7 +253,7 @@ csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *exp
 csf_status launch(const DecodeLaunch &L, void *stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const cudaError_t e = !L.blocked     ? launch_decode(L.p, L.grid, L.smem, L.per_expert, st)
-                          : L.warp_blocks ? launch_decode_blocks(L.p, L.grid, L.smem, st)
+                          : L.buffered ? launch_decode_blocks(L.p, L.grid, L.smem, st)
                                           : launch_decode_tiles(L.p, L.grid, L.smem, st);
     if (e != cudaSuccess) {
         cudaGetLastError();
