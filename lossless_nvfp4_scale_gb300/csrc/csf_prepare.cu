@@ -556,6 +556,29 @@ __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_con
             }
             return cd;
         };
+        // The same codes for a whole word at once (SWAR): per byte d = x - base
+        // without borrows between bytes, and bit 7 of `o` set for the bytes
+        // outside [base, base + w] (d > w, or x below base: the byte's borrow).
+        const uint32_t B4 = base * 0x01010101u, W1 = (w + 1) * 0x01010101u;
+        auto code4w = [&](uint32_t x) {
+            const uint32_t H = 0x80808080u;
+            const uint32_t d = ((x | H) - (B4 & ~H)) ^ ((x ^ ~B4) & H);
+            const uint32_t bo = ((~x & B4) | (~(x ^ B4) & d)) & H;
+            const uint32_t o = ((((d | H) - W1) | d) | bo) & H;
+#pragma unroll
+            for (uint32_t j = 0; j < 4; ++j)               // exceptions, in element order
+                if (o & (0x80u << (8 * j))) s_exc[pos++] = (uint8_t)(x >> (8 * j));
+            const uint32_t ob = o >> 7;                    // 1 in each outside byte
+            if (nv) {
+                const uint32_t c = (d & ~(ob * 0xFFu)) | (ob * 0x0Fu);    // outside -> escape code 15
+                const uint32_t t = c | (c >> 4);
+                return __byte_perm(t, 0u, 0x4420);         // nibble j = element j
+            }
+            // bit 0 of each byte -> bits 0..3 (offset bits, 0 for exceptions), escape bits -> 4..7
+            const uint32_t ofb = (((d & ~ob) & 0x01010101u) * 0x01020408u) >> 24;
+            const uint32_t esb = (ob * 0x01020408u) >> 24;
+            return ofb | (esb << 4);
+        };
         uint32_t acc = 0, ax = 0;
         auto flush = [&](bool force) {
             if (nv) {
@@ -573,7 +596,7 @@ __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_con
             // Whole words; groups of 4 never straddle an output word.
             const uint32_t *rw = reinterpret_cast<const uint32_t *>(row);
             for (uint32_t k = 0; k < C / 4; ++k) {
-                const uint32_t cd = code4(rw[k], 4);
+                const uint32_t cd = code4w(rw[k]);
                 if (nv) acc |= cd << (4 * (el & 7u));
                 else { acc |= (cd & 0xFu) << (el & 31u); ax |= (cd >> 4) << (el & 31u); }
                 el += 4;
