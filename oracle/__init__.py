@@ -73,6 +73,14 @@ def _load():
         lib.csfo_decode_blocked.restype = ctypes.c_int
         lib.csfo_blocked_bytes.argtypes = [_i64, _i64, _i64]
         lib.csfo_blocked_bytes.restype = ctypes.c_uint64
+        lib.csfo_tiled_code_bytes.argtypes = [ctypes.c_int, _i64, _i64, _i64]
+        lib.csfo_tiled_code_bytes.restype = ctypes.c_uint64
+        lib.csfo_tiled_pack.argtypes = [ctypes.c_int, _i64, _i64, _i64, _u8p, _u8p, _u8p, _u32p, _u8p,
+                                        ctypes.c_uint64, _u8p, _u8p, _u32p, _u8p, ctypes.c_uint64, _u64p]
+        lib.csfo_tiled_pack.restype = ctypes.c_int
+        lib.csfo_tiled_decode.argtypes = [ctypes.c_int, _i64, _i64, _i64, _u8p, _u8p, _u32p, _u8p,
+                                          ctypes.c_uint64, _i64p, _u8p]
+        lib.csfo_tiled_decode.restype = ctypes.c_int
         lib.csfo_check.argtypes = [ctypes.c_int, _i64, _i64, _i64, _u8p, _u8p,
                                    _u32p, ctypes.c_uint64]
         lib.csfo_check.restype = ctypes.c_int
@@ -168,6 +176,46 @@ def decode_blocked(enc: dict, expert_start=None, out: np.ndarray | None = None, 
                                      _ptr(enc["escapes"] if enc["escapes"].size else None, _u8p),
                                      _ptr(enc["exc_index"], _u32p), _ptr(exc, _u8p),
                                      enc["num_exc"], _ptr(es, _i64p), lo, hi, _ptr(out, _u8p))
+    return out, st
+
+
+def tiled_pack(enc: dict) -> dict:
+    """Tile-packed form of a CSF stack (codes, bases and exceptions in the
+    order of the block-scaled GEMM scale tiles; see csf_oracle.c)."""
+    kind = enc["kind"]
+    E, R, C = enc["shape"]
+    nrb, ncb = -(-R // 128), -(-C // 4)
+    codes = np.zeros(int(_load().csfo_tiled_code_bytes(kind, E, R, C)), np.uint8)
+    bases = np.zeros(E * nrb * 128, np.uint8)
+    tile_index = np.zeros(E * nrb * ncb + 1, np.uint32)
+    cap = max(enc["num_exc"], 1)
+    t_exc = np.zeros(cap, np.uint8)
+    num = ctypes.c_uint64()
+    exc = enc["exc_bytes"] if enc["exc_bytes"].size else np.zeros(1, np.uint8)
+    st = _load().csfo_tiled_pack(kind, E, R, C, _ptr(enc["base"], _u8p), _ptr(enc["offsets"], _u8p),
+                                 _ptr(enc["escapes"] if enc["escapes"].size else None, _u8p),
+                                 _ptr(enc["exc_index"], _u32p), _ptr(exc, _u8p), enc["num_exc"],
+                                 _ptr(codes, _u8p), _ptr(bases, _u8p), _ptr(tile_index, _u32p),
+                                 _ptr(t_exc, _u8p), cap, ctypes.byref(num))
+    if st != OK:
+        raise RuntimeError(f"oracle tiled_pack failed with status {st}")
+    return {"kind": kind, "shape": (E, R, C), "codes": codes, "bases": bases, "tile_index": tile_index,
+            "exc_bytes": t_exc[:num.value].copy(), "num_exc": num.value}
+
+
+def tiled_decode(tp: dict, expert_start=None, out: np.ndarray | None = None):
+    """Decode a tile-packed stack into the block-scaled GEMM scale layout;
+    returns (out, status).  Tiles of inactive experts keep their bytes."""
+    E, R, C = tp["shape"]
+    if out is None:
+        out = np.zeros(blocked_bytes(E, R, C), np.uint8)
+    es = None
+    if expert_start is not None:
+        es = np.ascontiguousarray(np.asarray(expert_start, dtype=np.int64))
+    exc = tp["exc_bytes"] if tp["exc_bytes"].size else np.zeros(1, np.uint8)
+    st = _load().csfo_tiled_decode(tp["kind"], E, R, C, _ptr(tp["codes"], _u8p), _ptr(tp["bases"], _u8p),
+                                   _ptr(tp["tile_index"], _u32p), _ptr(exc, _u8p), tp["num_exc"],
+                                   _ptr(es, _i64p), _ptr(out, _u8p))
     return out, st
 
 

@@ -315,6 +315,145 @@ int csfo_decode_blocked(int kind, int64_t E, int64_t R, int64_t C,
 }
 
 /*
+ * Tile-packed CSF: the same per-row bases and codes, stored in the order of
+ * the block-scaled GEMM scale layout so that any 128 x 4 tile decodes on its
+ * own (the stage-readable packed storage that the expand_scales commit
+ * message describes for pipeline stages; its layout is not on the pages, so
+ * this one is a design of this library).  Per expert, tiles as in
+ * blocked_offset: tile t = row block rb * (CP/4) + column block cb.  Inside a
+ * tile, position q = 16*b + 4*a + c (line b, row r = 128*rb + b + 32*a,
+ * column 4*cb + c), the same order as the tile's bytes in the blocked layout.
+ *   codes   NVFP4: 256 bytes per tile, position q in byte q/2 (even q in the
+ *           low nibble), nibble = offset 0..14 or 15 for an exception.
+ *           MXFP4: 128 bytes per tile, an offset bit plane (bytes 0..63,
+ *           position q at bit q%8 of byte q/8) then an escape bit plane
+ *           (bytes 64..127).  Padding positions (r >= R or c >= C) code 0.
+ *   bases   128 bytes per row block, byte 4*b + a = base of row
+ *           128*rb + b + 32*a (0 for padding rows).
+ *   tile_index  E*T + 1 u32: exclusive prefix of the tiles' exception counts.
+ *   exc_bytes   each tile's exceptions in position order.
+ * Packed from a CSF stack: decoded first, then every position recoded against
+ * its row's base, so the codes equal the CSF codes of the same elements.
+ */
+uint64_t csfo_tiled_code_bytes(int kind, int64_t E, int64_t R, int64_t C)
+{
+    uint64_t T = (uint64_t)((R + 127) / 128) * (uint64_t)((C + 3) / 4);
+    return (uint64_t)E * T * (kind == CSFO_NVFP4 ? 256u : 128u);
+}
+
+int csfo_tiled_pack(int kind, int64_t E, int64_t R, int64_t C,
+                    const uint8_t *base, const uint8_t *offsets, const uint8_t *escapes,
+                    const uint32_t *exc_index, const uint8_t *exc_bytes, uint64_t num_exc,
+                    uint8_t *codes, uint8_t *bases, uint32_t *tile_index, uint8_t *t_exc,
+                    uint64_t t_exc_capacity, uint64_t *t_num_exc)
+{
+    if ((kind != CSFO_NVFP4 && kind != CSFO_MXFP4) || E < 1 || R < 1 || C < 1)
+        return CSFO_ERR_ARG;
+    int w = window_width(kind);
+    int64_t nrb = (R + 127) / 128, ncb = (C + 3) / 4;
+    uint64_t per_tile = kind == CSFO_NVFP4 ? 256u : 128u;
+    uint8_t *dense = (uint8_t *)malloc((size_t)(E * R * C));
+    if (!dense)
+        return CSFO_ERR_ARG;
+    int status = csfo_decode(kind, E, R, C, base, offsets, escapes, exc_index, exc_bytes, num_exc, NULL, 0, R,
+                             dense);
+    memset(codes, 0, (size_t)csfo_tiled_code_bytes(kind, E, R, C));
+    memset(bases, 0, (size_t)(E * nrb * 128));
+    uint64_t n = 0;        /* exceptions written so far */
+    uint64_t tile = 0;
+    for (int64_t e = 0; e < E; ++e) {
+        for (int64_t rb = 0; rb < nrb; ++rb) {
+            for (int64_t b = 0; b < 32; ++b)
+                for (int64_t a = 0; a < 4; ++a) {
+                    int64_t r = 128 * rb + b + 32 * a;
+                    if (r < R)
+                        bases[(e * nrb + rb) * 128 + 4 * b + a] = base[e * R + r];
+                }
+            for (int64_t cb = 0; cb < ncb; ++cb, ++tile) {
+                tile_index[tile] = (uint32_t)n;
+                uint8_t *tc = codes + tile * per_tile;
+                for (int64_t q = 0; q < 512; ++q) {
+                    int64_t b = q / 16, a = (q / 4) % 4, c = 4 * cb + q % 4;
+                    int64_t r = 128 * rb + b + 32 * a;
+                    if (r >= R || c >= C)
+                        continue;                          /* padding: code 0 */
+                    uint64_t row = (uint64_t)e * (uint64_t)R + (uint64_t)r;
+                    unsigned v = dense[row * (uint64_t)C + (uint64_t)c], bs = base[row];
+                    int inside = v >= bs && v - bs <= (unsigned)w;
+                    if (!inside) {
+                        if (n < t_exc_capacity)
+                            t_exc[n] = (uint8_t)v;
+                        else
+                            status = CSFO_ERR_CAPACITY;
+                        n += 1;
+                    }
+                    if (kind == CSFO_NVFP4) {
+                        nibble_put(tc, (uint64_t)q, inside ? v - bs : 15u);
+                    } else {
+                        bit_put(tc, (uint64_t)q, inside ? v - bs : 0u);
+                        bit_put(tc + 64, (uint64_t)q, inside ? 0u : 1u);
+                    }
+                }
+            }
+        }
+    }
+    tile_index[tile] = (uint32_t)n;
+    *t_num_exc = n;
+    free(dense);
+    return status;
+}
+
+/*
+ * Decode a tile-packed stack into the block-scaled GEMM scale layout (same
+ * bytes as csfo_decode_blocked of the CSF stack it was packed from).
+ * expert_start as in csfo_decode.  An exception reference past num_exc
+ * writes 0 and returns CSFO_ERR_CORRUPT.
+ */
+int csfo_tiled_decode(int kind, int64_t E, int64_t R, int64_t C,
+                      const uint8_t *codes, const uint8_t *bases, const uint32_t *tile_index,
+                      const uint8_t *t_exc, uint64_t num_exc, const int64_t *expert_start, uint8_t *out)
+{
+    if ((kind != CSFO_NVFP4 && kind != CSFO_MXFP4) || E < 1 || R < 1 || C < 1)
+        return CSFO_ERR_ARG;
+    int64_t nrb = (R + 127) / 128, ncb = (C + 3) / 4;
+    uint64_t per_tile = kind == CSFO_NVFP4 ? 256u : 128u;
+    int status = CSFO_OK;
+    for (int64_t e = 0; e < E; ++e) {
+        if (expert_start != NULL && !(expert_start[e + 1] > expert_start[e]))
+            continue;
+        for (int64_t rb = 0; rb < nrb; ++rb) {
+            for (int64_t cb = 0; cb < ncb; ++cb) {
+                uint64_t tile = ((uint64_t)e * (uint64_t)nrb + (uint64_t)rb) * (uint64_t)ncb + (uint64_t)cb;
+                const uint8_t *tc = codes + tile * per_tile;
+                uint64_t k = tile_index[tile];
+                for (int64_t q = 0; q < 512; ++q) {
+                    int64_t b = q / 16, a = (q / 4) % 4, c = 4 * cb + q % 4;
+                    int64_t r = 128 * rb + b + 32 * a;
+                    uint8_t v = 0;
+                    int esc = kind == CSFO_NVFP4 ? nibble_get(tc, (uint64_t)q) == 15u
+                                                 : bit_get(tc + 64, (uint64_t)q) == 1u;
+                    if (esc) {
+                        if (k < num_exc) {
+                            v = t_exc[k];
+                        } else {
+                            status = CSFO_ERR_CORRUPT;
+                        }
+                        k += 1;
+                    } else {
+                        unsigned off = kind == CSFO_NVFP4 ? nibble_get(tc, (uint64_t)q) : bit_get(tc, (uint64_t)q);
+                        v = (uint8_t)((bases[(e * nrb + rb) * 128 + 4 * b + a] + off) & 0xFFu);
+                    }
+                    out[blocked_offset(R, C, e, r, c)] = (r < R && c < C) ? v : 0;
+                }
+                if (k != tile_index[tile + 1])
+                    status = CSFO_ERR_CORRUPT;
+            }
+        }
+    }
+    return status;
+}
+
+/*
  * Well-formedness of a stack's index: exc_index[0] == 0, each row's index
  * step equals the number of escapes in that row, and the last entry equals
  * num_exc.  Returns CSFO_OK or CSFO_ERR_CORRUPT.

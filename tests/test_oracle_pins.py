@@ -364,3 +364,62 @@ def test_blocked_row_blocks_and_routing_leave_other_tiles():
         assert np.array_equal(out, want), (lo, hi)
     for bad in [(1, 128), (0, 100), (128, 128), (0, R + 1)]:
         assert oracle.decode_blocked(enc, None, None, rows=bad)[1] == oracle.ERR_ARG
+
+
+# ------------------------------------------------ tile-packed (stage-readable)
+# The same per-row bases and codes stored in GEMM-tile order: inside a 128 x 4
+# tile, position q = 16*b + 4*a + c is row b + 32*a, column c (the tile's byte
+# order in the blocked layout); bases in the same line order per row block.
+
+def test_tiled_hand_worked_tile():
+    R, C = 128, 4
+    base = 0x20 + (np.arange(R) % 8)
+    dense = (base[:, None] + np.arange(C)[None, :]).astype(np.uint8)
+    dense[33, 2] = 0xFF                                  # row 33 = line 1, a = 1; column 2 -> q = 22
+    enc = oracle.encode(oracle.NVFP4, dense[None])
+    assert enc["base"].tolist() == base.tolist()
+    tp = oracle.tiled_pack(enc)
+    # codes: nibbles 0 1 2 3 per line-row group -> bytes 0x10 0x32, except q = 22 (escape 15)
+    want = np.tile(np.array([0x10, 0x32], np.uint8), 128)
+    want[11] = 0x3F
+    assert np.array_equal(tp["codes"], want)
+    # bases in line order: byte 4*b + a = base of row b + 32*a
+    assert tp["bases"].tolist() == [0x20 + (b % 8) for b in range(32) for a in range(4)]
+    assert tp["tile_index"].tolist() == [0, 1] and tp["exc_bytes"].tolist() == [0xFF]
+
+
+def test_tiled_mxfp4_bits():
+    R, C = 128, 8                                        # two column tiles
+    dense = np.full((R, C), 120, np.uint8)
+    dense[:, 1] = 121                                    # offset bit 1 in column 1
+    dense[5, 6] = 7                                      # exception: row 5 (line 5, a = 0), tile 1, c = 2
+    enc = oracle.encode(oracle.MXFP4, dense[None])
+    tp = oracle.tiled_pack(enc)
+    t0, t1 = tp["codes"][:128], tp["codes"][128:]
+    # tile 0: offset bit set at every q with q % 4 == 1 -> 0x22 in every byte; no escapes
+    assert (t0[:64] == 0x22).all() and not t0[64:].any()
+    # tile 1 (columns 4..7): no offsets; escape at q = 16*5 + 2 = 82 -> byte 10, bit 2
+    assert not t1[:64].any()
+    esc = np.zeros(64, np.uint8)
+    esc[10] = 0x04
+    assert np.array_equal(t1[64:], esc)
+    assert tp["tile_index"].tolist() == [0, 0, 1] and tp["exc_bytes"].tolist() == [7]
+
+
+@pytest.mark.parametrize("kind,E,R,C", [(0, 3, 200, 7), (0, 2, 256, 100), (1, 2, 130, 160), (1, 3, 64, 33),
+                                        (0, 1, 1, 1), (0, 2, 300, 50)])
+def test_tiled_round_trip_equals_blocked_decode(kind, E, R, C):
+    w = W[kind]
+    dense = synth.random_rows(R + C, E * R, C, spread=w + 5, replace_p=0.1).reshape(E, R, C)
+    enc = oracle.encode(kind, dense)
+    tp = oracle.tiled_pack(enc)
+    assert tp["num_exc"] == enc["num_exc"]
+    assert sorted(tp["exc_bytes"].tolist()) == sorted(enc["exc_bytes"].tolist())
+    nb = oracle.blocked_bytes(E, R, C)
+    out, st = oracle.tiled_decode(tp, None, np.full(nb, 0xAB, np.uint8))
+    want, _ = oracle.decode_blocked(enc)
+    assert st == oracle.OK and np.array_equal(out, want)
+    start = np.concatenate([[0], np.cumsum(np.arange(E) % 2)]).astype(np.int64)   # odd experts
+    out, _ = oracle.tiled_decode(tp, start, np.full(nb, 0xAB, np.uint8))
+    want, _ = oracle.decode_blocked(enc, start, np.full(nb, 0xAB, np.uint8))
+    assert np.array_equal(out, want)
