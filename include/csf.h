@@ -70,7 +70,7 @@
 extern "C" {
 #endif
 
-#define CSF_ABI_VERSION 3
+#define CSF_ABI_VERSION 4
 
 typedef enum {
     CSF_OK = 0,
@@ -106,6 +106,9 @@ typedef struct {
     uint64_t exc_index;       /* 4*(rows+1) */
     uint64_t prepare_scratch; /* scratch for csf_prepare */
     uint64_t blocked;         /* a workspace in CSF_LAYOUT_BLOCKED: E * (R up to 128) * (C up to 4) */
+    uint64_t tiled_codes;     /* csf_tiled codes: 256 (NVFP4) or 128 (MXFP4) bytes a tile */
+    uint64_t tiled_bases;     /* csf_tiled bases: 128 bytes per expert and 128-row block */
+    uint64_t tiled_index;     /* csf_tiled tile_index: 4 * (tiles + 1) */
 } csf_sizes_t;
 
 /*
@@ -301,6 +304,63 @@ csf_status csf_decode_rows(const csf_decode_part *parts, int num_parts,
  * (a wait may already be enqueued when the launch or the record fails).
  */
 csf_status csf_expand(const csf_decode_part *parts, int num_parts, void *after, void *done, void *stream);
+
+/*
+ * Tile-packed CSF: a stage-readable form of a CSF stack ([B478] commit message
+ * on packed experts prepared from CSF checkpoints, whose scales stay as
+ * compressed storage that each GEMM pipeline stage rebuilds in shared memory;
+ * the pages give no record layout, so this one is the library's).  The same
+ * per-row bases and codes, stored in the order of the block-scaled GEMM scale
+ * tiles (CSF_LAYOUT_BLOCKED), so that any 128 x 4 tile decodes on its own with
+ * no walk along its rows.  Per expert: nrb = ceil(R/128) row blocks, ncb =
+ * ceil(C/4) column blocks, T = nrb * ncb tiles, tile t = rb * ncb + cb.
+ *   codes       NVFP4: 256 bytes a tile; position q = 16*b + 4*a + c (row
+ *               128*rb + b + 32*a, column 4*cb + c) in byte q/2, even q in the
+ *               low nibble; nibble 0..14 = offset, 15 = exception.  MXFP4:
+ *               128 bytes a tile, offset bits (bytes 0..63, position q at bit
+ *               q%8 of byte q/8) then escape bits (bytes 64..127).  Padding
+ *               positions (row >= R or column >= C) code 0.
+ *   bases       128 bytes per expert and row block, byte 4*b + a = base of
+ *               row 128*rb + b + 32*a (0 past R).
+ *   tile_index  E*T + 1 uint32: exclusive prefix of the tiles' exception
+ *               counts, the total last.
+ *   exc_bytes   each tile's exceptions in position order (num_exc bytes,
+ *               readable rounded up to 16).
+ * Sizes: csf_sizes().tiled_codes / tiled_bases / tiled_index.
+ */
+typedef struct {
+    csf_geometry g;
+    uint8_t *codes;       /* 16-byte aligned */
+    uint8_t *bases;       /* 16-byte aligned */
+    uint32_t *tile_index;
+    uint8_t *exc_bytes;
+    uint64_t num_exc;     /* host copy: the CSF stack's num_exc (same exceptions, tile order) */
+    uint32_t *error_word; /* optional device word for CSF_DEV_ERR_* bits; may be NULL */
+} csf_tiled;
+
+/*
+ * Convert a CSF stack to its tile-packed form on the GPU (three kernels:
+ * per-tile exception counts, their scan into tile_index, then codes, bases
+ * and exceptions).  `exc_capacity` = bytes at dst->exc_bytes (src->num_exc
+ * suffices); exceptions past it are dropped and CSF_DEV_ERR_CAPACITY set.  A
+ * CSF index that disagrees with the escape codes sets CSF_DEV_ERR_CORRUPT.
+ * dst->num_exc is not written (it equals src->num_exc).  The stacks must have
+ * the same geometry.
+ * Errors: CSF_ERR_ARG (NULL or misaligned buffers, geometries differ),
+ * CSF_ERR_UNSUPPORTED (more than 2^32 - 1 exceptions), CSF_ERR_CUDA.
+ */
+csf_status csf_tiled_pack(const csf_stack *src, csf_tiled *dst, uint64_t exc_capacity, void *stream);
+
+/*
+ * Decode a tile-packed stack into the block-scaled GEMM scale layout
+ * (CSF_LAYOUT_BLOCKED, same bytes as csf_decode_rows of the CSF stack with
+ * that layout), one warp per tile.  ws: 16-byte aligned, csf_sizes().blocked
+ * bytes.  expert_start as csf_decode: tiles of inactive experts are not
+ * touched.  Errors: CSF_ERR_ARG, CSF_ERR_SIZE, CSF_ERR_UNSUPPORTED (routing
+ * with E > 8192), CSF_ERR_CUDA.
+ */
+csf_status csf_tiled_decode(const csf_tiled *t, uint8_t *ws, size_t ws_bytes,
+                            const void *expert_start, int expert_start_is_int64, void *stream);
 
 #ifdef __cplusplus
 }

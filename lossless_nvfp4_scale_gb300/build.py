@@ -18,7 +18,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libcsf.so")
-SOURCES = ["csf_api.cu", "csf_decode.cu", "csf_tiles.cu", "csf_prepare.cu", "csf_prepare_static.cu"]
+SOURCES = ["csf_api.cu", "csf_decode.cu", "csf_tiles.cu", "csf_tiled.cu", "csf_prepare.cu",
+           "csf_prepare_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -14,6 +14,8 @@ Typical use::
     csf.decode_pair(gate, down, gate_ws, down_ws, expert_start)
     csf.decode(stack, ws, rows=(0, R // 2))               # gate half of fused gate/up
     sf = csf.decode(stack, layout=csf.LAYOUT_BLOCKED)     # GEMM scale-operand layout
+    tp = csf.tiled_pack(stack)                            # stage-readable tile-packed form
+    sf = csf.tiled_decode(tp)                             # same bytes as the line above
     ev = csf.expand_scales([(gate, gate_ws), (down, down_ws)], side_stream, after=last_read)
     torch.cuda.current_stream().wait_event(ev)            # before the call that reads them
 """
@@ -46,7 +48,8 @@ class Geometry(ctypes.Structure):
 
 class Sizes(ctypes.Structure):
     _fields_ = [("dense", _c_u64), ("base", _c_u64), ("offsets", _c_u64), ("escapes", _c_u64),
-                ("exc_index", _c_u64), ("prepare_scratch", _c_u64), ("blocked", _c_u64)]
+                ("exc_index", _c_u64), ("prepare_scratch", _c_u64), ("blocked", _c_u64),
+                ("tiled_codes", _c_u64), ("tiled_bases", _c_u64), ("tiled_index", _c_u64)]
 
 
 class CStack(ctypes.Structure):
@@ -58,6 +61,11 @@ class CStack(ctypes.Structure):
 class CDecodePart(ctypes.Structure):
     _fields_ = [("stack", ctypes.POINTER(CStack)), ("ws", _c_vp), ("ws_bytes", ctypes.c_size_t),
                 ("row_lo", _c_i32), ("row_hi", _c_i32), ("layout", _c_i32)]
+
+
+class CTiled(ctypes.Structure):
+    _fields_ = [("g", Geometry), ("codes", _c_vp), ("bases", _c_vp), ("tile_index", _c_vp),
+                ("exc_bytes", _c_vp), ("num_exc", _c_u64), ("error_word", _c_vp)]
 
 
 class CsfError(RuntimeError):
@@ -88,6 +96,10 @@ def _load():
     lib.csf_decode_rows.restype = ctypes.c_int
     lib.csf_expand.argtypes = [ctypes.POINTER(CDecodePart), ctypes.c_int, _c_vp, _c_vp, _c_vp]
     lib.csf_expand.restype = ctypes.c_int
+    lib.csf_tiled_pack.argtypes = [ctypes.POINTER(CStack), ctypes.POINTER(CTiled), _c_u64, _c_vp]
+    lib.csf_tiled_pack.restype = ctypes.c_int
+    lib.csf_tiled_decode.argtypes = [ctypes.POINTER(CTiled), _c_vp, ctypes.c_size_t, _c_vp, ctypes.c_int, _c_vp]
+    lib.csf_tiled_decode.restype = ctypes.c_int
     return lib
 
 
@@ -366,3 +378,63 @@ def decode_pair(gate: Stack, down: Stack, gate_ws: torch.Tensor | None = None,
                                ctypes.byref(d), down_ws.data_ptr(), down_ws.numel(),
                                ptr, is64, _stream(stream)), "csf_decode_pair")
     return gate_ws, down_ws
+
+
+@dataclass
+class Tiled:
+    """A tile-packed stack in device memory (csf_tiled: stage-readable, each
+    128 x 4 scale tile decodes on its own)."""
+    kind: int
+    E: int
+    R: int
+    C: int
+    codes: torch.Tensor
+    bases: torch.Tensor
+    tile_index: torch.Tensor    # int32 storage of the uint32 index
+    exc_bytes: torch.Tensor
+    num_exc: int
+    error_word: torch.Tensor
+
+    @property
+    def shape(self):
+        return (self.E, self.R, self.C)
+
+    def cstruct(self) -> CTiled:
+        return CTiled(Geometry(self.kind, self.E, self.R, self.C), self.codes.data_ptr(), self.bases.data_ptr(),
+                      self.tile_index.data_ptr(), self.exc_bytes.data_ptr(), self.num_exc,
+                      self.error_word.data_ptr())
+
+    def errors(self) -> int:
+        return int(self.error_word.item())
+
+
+def tiled_pack(stack: Stack, stream=None) -> Tiled:
+    """Convert a CSF stack to its tile-packed form on the GPU (csf_tiled_pack)."""
+    sz = sizes(stack.kind, stack.E, stack.R, stack.C)
+    dev = stack.base.device
+    u8 = dict(dtype=torch.uint8, device=dev)
+    t = Tiled(stack.kind, stack.E, stack.R, stack.C,
+              codes=torch.empty(sz["tiled_codes"], **u8), bases=torch.empty(_pad16(sz["tiled_bases"]), **u8),
+              tile_index=torch.empty(sz["tiled_index"] // 4, dtype=torch.int32, device=dev),
+              exc_bytes=torch.zeros(_pad16(stack.num_exc), **u8), num_exc=stack.num_exc,
+              error_word=torch.zeros(1, dtype=torch.int32, device=dev))
+    cs, ct = stack.cstruct(), t.cstruct()
+    _check(lib.csf_tiled_pack(ctypes.byref(cs), ctypes.byref(ct), stack.num_exc, _stream(stream)), "csf_tiled_pack")
+    return t
+
+
+def tiled_decode(t: Tiled, ws: torch.Tensor | None = None, expert_start: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """Decode a tile-packed stack into the block-scaled GEMM scale layout
+    (flat uint8 of csf_sizes().blocked bytes, 16-byte aligned)."""
+    if ws is None:
+        ws = torch.empty(sizes(t.kind, t.E, t.R, t.C)["blocked"], dtype=torch.uint8, device=t.codes.device)
+    if ws.dtype != torch.uint8 or not ws.is_cuda or not ws.is_contiguous():
+        raise CsfError("tiled_decode: ws must be a contiguous uint8 CUDA tensor")
+    if expert_start is not None and expert_start.numel() != t.E + 1:
+        raise CsfError("expert_start must have E+1 entries")
+    ptr, is64 = _es(expert_start)
+    ct = t.cstruct()
+    _check(lib.csf_tiled_decode(ctypes.byref(ct), ws.data_ptr(), ws.numel(), ptr, is64, _stream(stream)),
+           "csf_tiled_decode")
+    return ws

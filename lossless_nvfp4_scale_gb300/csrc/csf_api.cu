@@ -315,6 +315,11 @@ csf_status csf_sizes(const csf_geometry *g, csf_sizes_t *out) {
     out->exc_index = 4 * (rows + 1);
     out->prepare_scratch = prepare_scratch_bytes(g, rows);
     out->blocked = blocked_bytes(g);
+    const uint64_t nrb = ((uint64_t)g->rows + kTileRows - 1) / kTileRows, ncb = ((uint64_t)g->cols + 3) / 4;
+    const uint64_t tiles = (uint64_t)g->num_experts * nrb * ncb;
+    out->tiled_codes = tiles * (g->kind == CSF_NVFP4 ? 256u : 128u);
+    out->tiled_bases = (uint64_t)g->num_experts * nrb * 128u;
+    out->tiled_index = 4 * (tiles + 1);
     return CSF_OK;
 }
 
@@ -395,6 +400,101 @@ csf_status csf_expand(const csf_decode_part *parts, int num_parts, void *after, 
     st = launch(L, stream);
     if (st != CSF_OK) return st;
     if (done && cudaEventRecord(static_cast<cudaEvent_t>(done), s) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    return CSF_OK;
+}
+
+csf_status csf_tiled_pack(const csf_stack *src, csf_tiled *dst, uint64_t exc_capacity, void *stream) {
+    if (!src || !dst) return CSF_ERR_ARG;
+    uint64_t n = 0, rows = 0;
+    csf_status st = geometry(&src->g, &n, &rows);
+    if (st != CSF_OK) return st;
+    const csf_geometry &g = src->g;
+    if (dst->g.kind != g.kind || dst->g.num_experts != g.num_experts || dst->g.rows != g.rows ||
+        dst->g.cols != g.cols)
+        return CSF_ERR_ARG;
+    if (!dst->codes || !dst->bases || !dst->tile_index || !aligned16(dst->codes) || !aligned16(dst->bases))
+        return CSF_ERR_ARG;
+    if (exc_capacity > 0 && !dst->exc_bytes) return CSF_ERR_ARG;
+    if (src->num_exc > 0xFFFFFFFFull) return CSF_ERR_UNSUPPORTED;
+    // The source read through the decode's stack view (its workspace unused).
+    DecStack S;
+    uint8_t dummy = 0;
+    st = fill_stack(src, &dummy, n, &S);
+    if (st != CSF_OK) return st;
+    S.err = dst->error_word;
+    TiledOut O;
+    O.codes = dst->codes;
+    O.bases = dst->bases;
+    O.tile_index = dst->tile_index;
+    O.exc_bytes = dst->exc_bytes;
+    O.exc_capacity = exc_capacity;
+    O.err = dst->error_word;
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != CSF_OK) return st;
+    const uint64_t items = (uint64_t)g.num_experts * (((uint64_t)g.rows + kTileRows - 1) / kTileRows);
+    uint64_t grid = (items + 3) / 4;                       // 4 warps a block, one (expert, row block) each
+    const uint64_t cap = (uint64_t)di.sms * 16;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    if (launch_tiled_pack(S, O, (int)grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    return CSF_OK;
+}
+
+csf_status csf_tiled_decode(const csf_tiled *t, uint8_t *ws, size_t ws_bytes, const void *expert_start,
+                            int expert_start_is_int64, void *stream) {
+    if (!t || !ws) return CSF_ERR_ARG;
+    uint64_t n = 0, rows = 0;
+    csf_status st = geometry(&t->g, &n, &rows);
+    if (st != CSF_OK) return st;
+    const csf_geometry &g = t->g;
+    if (!t->codes || !t->bases || !t->tile_index || !aligned16(t->codes) || !aligned16(t->bases) || !aligned16(ws))
+        return CSF_ERR_ARG;
+    if (t->num_exc > 0 && !t->exc_bytes) return CSF_ERR_ARG;
+    if (t->num_exc > 0xFFFFFFFFull) return CSF_ERR_ARG;
+    if (ws_bytes < blocked_bytes(&g)) return CSF_ERR_SIZE;
+    if (expert_start && g.num_experts > kMaxRoutedExperts) return CSF_ERR_UNSUPPORTED;
+    DecStack S;
+    std::memset(&S, 0, sizeof S);
+    S.ws = ws;
+    S.err = t->error_word;
+    S.rows = rows;
+    S.n = n;
+    S.R = g.rows;
+    S.C = g.cols;
+    S.kind = g.kind;
+    TiledIn I;
+    std::memset(&I, 0, sizeof I);
+    I.codes = t->codes;
+    I.bases = t->bases;
+    I.tile_index = t->tile_index;
+    I.exc_bytes = t->exc_bytes;
+    I.num_exc = t->num_exc;
+    I.expert_start = expert_start;
+    I.es64 = expert_start_is_int64 ? 1 : 0;
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != CSF_OK) return st;
+    const size_t smem = expert_start ? 4ull * (uint64_t)g.num_experts : 0;
+    int occ = 0;
+    if (tiled_decode_occupancy(g.kind, smem, &occ) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    if (occ < 1) occ = 1;
+    const uint64_t tiles = (uint64_t)g.num_experts * (((uint64_t)g.rows + kTileRows - 1) / kTileRows) *
+                           (((uint64_t)g.cols + 3) / 4);
+    uint64_t grid = (uint64_t)di.sms * (uint64_t)occ;
+    const uint64_t need = (tiles + 3) / 4;
+    if (need < grid) grid = need;
+    if (grid < 1) grid = 1;
+    if (launch_tiled_decode(S, I, (int)grid, smem, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return CSF_ERR_CUDA;
     }

@@ -113,6 +113,31 @@ cudaError_t decode_blocks_occupancy(size_t smem, int *blocks_per_sm);
 cudaError_t launch_decode_tiles(const DecParams &p, int grid, size_t smem, cudaStream_t s);
 cudaError_t decode_tiles_occupancy(size_t smem, int *blocks_per_sm);
 
+// Tile-packed CSF (csf_tiled.cu).
+struct TiledOut {
+    uint8_t *codes;
+    uint8_t *bases;
+    uint32_t *tile_index;
+    uint8_t *exc_bytes;
+    uint64_t exc_capacity;
+    uint32_t *err;          // may be null
+};
+
+struct TiledIn {
+    const uint8_t *codes;
+    const uint8_t *bases;
+    const uint32_t *tile_index;
+    const uint8_t *exc_bytes;
+    uint64_t num_exc;
+    const void *expert_start;   // null: every expert
+    int32_t es64;
+    int32_t pad_;
+};
+
+cudaError_t launch_tiled_pack(const DecStack &S, const TiledOut &O, int grid, cudaStream_t s);
+cudaError_t tiled_decode_occupancy(int kind, size_t smem, int *blocks_per_sm);
+cudaError_t launch_tiled_decode(const DecStack &S, const TiledIn &I, int grid, size_t smem, cudaStream_t s);
+
 cudaError_t launch_prepare(const PrepParams &p, size_t smem, cudaStream_t s);
 void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity,
                       void *scratch, uint64_t rows, uint64_t n);

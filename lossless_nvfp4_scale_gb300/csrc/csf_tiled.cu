@@ -1,0 +1,432 @@
+// Tile-packed CSF on sm_103a: the same per-row bases and codes as a CSF stack,
+// stored in the order of the block-scaled GEMM scale tiles so that every
+// 128 x 4 tile decodes on its own (stage-readable storage), plus the
+// conversion from a CSF stack and the decode into the tiled scale layout.
+//
+// Pages followed (cited by title and paragraph; they have no numbered
+// sections):
+//   "NVFP4-CSF: expand_scales() for ahead-of-call scale expansion (canonical
+//     twin of #477)": commit message on packed experts prepared from CSF
+//     checkpoints that keep their scales as stage-readable compressed
+//     storage, which each pipeline stage rebuilds in shared memory (no record
+//     layout given: the layout below is this library's).
+//   "finegrained-kernels: decode losslessly compressed NVFP4 scales (CSF)":
+//     format paragraph (base byte per row, 4-bit offsets, exception stream).
+//
+// Layout (per expert: nrb = ceil(R/128) row blocks, ncb = ceil(C/4) column
+// blocks, T = nrb*ncb tiles, tile t = rb*ncb + cb; global tile = e*T + t):
+//   codes   NVFP4 256 bytes a tile, MXFP4 128 (offset plane, then escape
+//           plane, 64 bytes each); position q = 16*b + 4*a + c of a tile is
+//           row 128*rb + b + 32*a, column 4*cb + c; padding positions code 0.
+//   bases   128 bytes a row block, byte 4*b + a = base of row b + 32*a.
+//   tile_index  E*T + 1 u32, exclusive prefix of the tiles' exception counts.
+//   exc_bytes   each tile's exceptions in position order.
+// Lane b of a warp owns line b of a tile (positions 16b .. 16b+15): 8 code
+// bytes (NVFP4) and 4 base bytes, exactly the 16 bytes of line b of the tile
+// in the block-scaled layout, which sits at byte 512*(global tile) + 16*b.
+#include "csf_device.cuh"
+#include "csf_internal.cuh"
+
+namespace csfk {
+namespace {
+
+using dev::add_base;
+using dev::flag;
+using dev::kFull;
+using dev::lanemask_lt;
+
+constexpr int kTlWarps = 4;
+constexpr int kTlThreads = 32 * kTlWarps;
+
+__device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, int lane, uint32_t &total) {
+    uint32_t x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, x, d);
+        if (lane >= d) x += y;
+    }
+    total = __shfl_sync(kFull, x, 31);
+    return x - v;
+}
+
+// Bits [pos, pos + 64) of an LSB-first packed plane of `bytes` bytes (8-byte
+// aligned, `bytes` a multiple of 8); words past the end read as 0.
+__device__ __forceinline__ uint64_t plane_bits(const uint8_t *plane, uint64_t pos, uint64_t bytes) {
+    const uint64_t w = pos >> 6;
+    const uint32_t sh = (uint32_t)pos & 63u;
+    const unsigned long long *p = reinterpret_cast<const unsigned long long *>(plane);
+    const uint64_t a = (w + 1) * 8 <= bytes ? __ldg(p + w) : 0ull;
+    const uint64_t b = (sh != 0 && (w + 2) * 8 <= bytes) ? __ldg(p + w + 1) : 0ull;
+    return sh ? (a >> sh) | (b << (64 - sh)) : a;
+}
+
+struct Geo {
+    uint32_t R, C, nrb, ncb, T;
+};
+
+__device__ __forceinline__ Geo geo_of(const DecStack &S) {
+    Geo g;
+    g.R = (uint32_t)S.R;
+    g.C = (uint32_t)S.C;
+    g.nrb = (g.R + kTileRows - 1) / kTileRows;
+    g.ncb = (g.C + 3) / 4;
+    g.T = g.nrb * g.ncb;
+    return g;
+}
+
+// ------------------------------------------------------------------ pack
+
+// The CSF codes of columns [4cb, 4cb+4) of one row: NVFP4 four nibbles in
+// bits 0..15 and their escape flags in bits 16..19; MXFP4 four offset bits
+// in bits 0..3 and four escape bits in 16..19.  Columns past C read 0.
+template <int KIND>
+__device__ __forceinline__ uint32_t csf_cols4(const DecStack &S, uint64_t row, uint32_t cb, uint32_t C) {
+    const uint64_t el = row * C + 4u * cb;
+    const uint32_t cv = min(4u, C - 4u * cb);
+    if (KIND == CSF_NVFP4) {
+        uint32_t n = (uint32_t)plane_bits(S.offsets, 4 * el, S.off_bytes) & 0xFFFFu;
+        n &= cv >= 4 ? 0xFFFFu : (1u << (4 * cv)) - 1;
+        const uint32_t f = n & (n >> 1) & (n >> 2) & (n >> 3) & 0x1111u;      // nibble == 15 -> bit 4j
+        const uint32_t e4 = (f & 1u) | ((f >> 3) & 2u) | ((f >> 6) & 4u) | ((f >> 9) & 8u);
+        return n | (e4 << 16);
+    }
+    const uint32_t m = cv >= 4 ? 0xFu : (1u << cv) - 1;
+    const uint32_t o4 = (uint32_t)plane_bits(S.offsets, el, S.off_bytes) & m;
+    const uint32_t x4 = (uint32_t)plane_bits(S.escapes, el, S.off_bytes) & m;
+    return o4 | (x4 << 16);
+}
+
+// One warp per (expert, row block): walk its column tiles in order.  PASS 0
+// writes each tile's exception count to tile_index; PASS 1 writes the codes,
+// the bases and the exceptions (tile_index already scanned).
+template <int KIND, int PASS>
+__global__ void __launch_bounds__(kTlThreads) tiled_pack_kernel(const __grid_constant__ DecStack S,
+                                                                 const __grid_constant__ TiledOut O) {
+    const int lane = threadIdx.x & 31;
+    const Geo g = geo_of(S);
+    const uint64_t items = (uint64_t)S.rows / g.R * g.nrb;                 // E * nrb
+    const uint64_t nw = (uint64_t)gridDim.x * kTlWarps;
+    const uint32_t nexc = (uint32_t)S.num_exc;
+    for (uint64_t it = (uint64_t)blockIdx.x * kTlWarps + (threadIdx.x >> 5); it < items; it += nw) {
+        const uint64_t e = it / g.nrb;
+        const uint32_t rb = (uint32_t)(it - e * g.nrb);
+        uint64_t row[4];
+        bool ok[4];
+        uint32_t X[4] = {0, 0, 0, 0};
+        uint32_t bw = 0;
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const uint32_t rl = rb * kTileRows + (uint32_t)lane + 32u * a;
+            ok[a] = rl < g.R;
+            row[a] = e * g.R + rl;
+            if (PASS == 1 && ok[a]) {
+                X[a] = __ldg(S.exc_index + row[a]);
+                bw |= (uint32_t)__ldg(S.base + row[a]) << (8 * a);
+            }
+        }
+        if (PASS == 1)
+            reinterpret_cast<uint32_t *>(O.bases)[(e * g.nrb + rb) * 32 + lane] = bw;
+        bool bad = false;
+        for (uint32_t cb = 0; cb < g.ncb; ++cb) {
+            const uint64_t tile = e * g.T + (uint64_t)rb * g.ncb + cb;
+            uint32_t v[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) v[a] = ok[a] ? csf_cols4<KIND>(S, row[a], cb, g.C) : 0u;
+            uint32_t cnt = 0;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) cnt += __popc(v[a] >> 16);
+            uint32_t tot;
+            const uint32_t pre = warp_excl_scan(cnt, lane, tot);
+            if (PASS == 0) {
+                if (lane == 0) O.tile_index[tile] = tot;
+                continue;
+            }
+            if (KIND == CSF_NVFP4) {
+                const uint64_t code = (uint64_t)(v[0] & 0xFFFFu) | ((uint64_t)(v[1] & 0xFFFFu) << 16) |
+                                      ((uint64_t)(v[2] & 0xFFFFu) << 32) | ((uint64_t)(v[3] & 0xFFFFu) << 48);
+                reinterpret_cast<unsigned long long *>(O.codes + tile * 256)[lane] = code;
+            } else {
+                const uint32_t ob = (v[0] & 0xFu) | ((v[1] & 0xFu) << 4) | ((v[2] & 0xFu) << 8) |
+                                    ((v[3] & 0xFu) << 12);
+                const uint32_t xb = ((v[0] >> 16) & 0xFu) | (((v[1] >> 16) & 0xFu) << 4) |
+                                    (((v[2] >> 16) & 0xFu) << 8) | (((v[3] >> 16) & 0xFu) << 12);
+                reinterpret_cast<uint16_t *>(O.codes + tile * 128)[lane] = (uint16_t)ob;
+                reinterpret_cast<uint16_t *>(O.codes + tile * 128 + 64)[lane] = (uint16_t)xb;
+            }
+            // Exceptions in position order: row a, then column; the CSF byte of
+            // a row's k-th exception in this tile is at X[a] + k.
+            uint64_t dst = (uint64_t)O.tile_index[tile] + pre;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                uint32_t f = v[a] >> 16;
+                while (f) {
+                    uint32_t byte = 0;
+                    if (X[a] < nexc) byte = __ldg(S.exc_bytes + X[a]);
+                    else bad = true;
+                    if (dst < O.exc_capacity) O.exc_bytes[dst] = (uint8_t)byte;
+                    else flag(O.err, CSF_DEV_ERR_CAPACITY);
+                    ++X[a];
+                    ++dst;
+                    f &= f - 1;
+                }
+            }
+        }
+        if (PASS == 1) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                if (ok[a] && X[a] != __ldg(S.exc_index + row[a] + 1)) bad = true;
+            if (__any_sync(kFull, bad) && lane == 0) flag(S.err, CSF_DEV_ERR_CORRUPT);
+        }
+    }
+}
+
+// Exclusive scan of tile_index[0..n) in place, total in tile_index[n]; one
+// block of 1024 threads, each scanning a contiguous chunk.
+__global__ void __launch_bounds__(1024) tiled_scan_kernel(uint32_t *idx, uint64_t n, uint32_t *err) {
+    __shared__ uint32_t s_sum[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint64_t per = (n + 1023) / 1024;
+    const uint64_t lo = min((uint64_t)tid * per, n), hi = min(lo + per, n);
+    uint64_t local = 0;
+    for (uint64_t i = lo; i < hi; ++i) local += idx[i];
+    uint32_t wt;
+    const uint32_t wx = warp_excl_scan((uint32_t)local, lane, wt);
+    if (lane == 0) s_sum[warp] = wt;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t t;
+        const uint32_t x = warp_excl_scan(s_sum[lane], lane, t);
+        s_sum[lane] = x;
+        if (lane == 0 && tid == 0) idx[n] = t;   // total (every exception fits u32: checked on the host)
+    }
+    __syncthreads();
+    uint32_t run = s_sum[warp] + wx;
+    for (uint64_t i = lo; i < hi; ++i) {
+        const uint32_t c = idx[i];
+        idx[i] = run;
+        run += c;
+    }
+    (void)err;
+}
+
+// ---------------------------------------------------------------- decode
+
+// The raw inputs of one tile for lane b: its 8 code bytes (NVFP4) or 2 + 2
+// plane bytes (MXFP4), its 4 row bases, and the tile's index entries.
+struct TileRaw {
+    uint64_t code;
+    uint32_t bw;
+    uint32_t x0, x1;     // tile_index[tile], tile_index[tile + 1] (lane 0 only)
+};
+
+// `tile` is the global tile, `rbg` the global row block (expert * nrb + rb).
+template <int KIND>
+__device__ __forceinline__ TileRaw tile_load(const TiledIn &I, uint64_t tile, uint64_t rbg, int lane) {
+    TileRaw r;
+    r.bw = __ldg(reinterpret_cast<const uint32_t *>(I.bases) + rbg * 32 + lane);
+    if (KIND == CSF_NVFP4) {
+        r.code = __ldg(reinterpret_cast<const unsigned long long *>(I.codes + tile * 256) + lane);
+    } else {
+        const uint16_t *c16 = reinterpret_cast<const uint16_t *>(I.codes + tile * 128);
+        r.code = (uint64_t)__ldg(c16 + lane) | ((uint64_t)__ldg(c16 + 32 + lane) << 32);
+    }
+    r.x0 = r.x1 = 0;
+    if (lane == 0) {
+        r.x0 = __ldg(I.tile_index + tile);
+        r.x1 = __ldg(I.tile_index + tile + 1);
+    }
+    return r;
+}
+
+// One tile from its raw inputs, whole warp: lane b writes line b (16 bytes)
+// at dst + 16*b.  `line` is the lane's own 16-byte shared-memory slot, where
+// it patches its exceptions byte by byte; `edge` says that the tile holds
+// padding (rows past R or columns past C), which is written as 0.  Returns
+// true when the tile's index disagrees with its codes.
+template <int KIND>
+__device__ __forceinline__ bool tile_finish(const TiledIn &I, const Geo &g, uint32_t rb, uint32_t cb, bool edge,
+                                            const TileRaw &r, uint8_t *dst, uint4 *line, int lane) {
+    const uint32_t bw = r.bw;
+    uint32_t w0, w1, w2, w3, cnt;
+    uint64_t f;                                                 // escape flags: bit 4j (NVFP4) / bit j (MXFP4)
+    if (KIND == CSF_NVFP4) {
+        const uint32_t x0 = (uint32_t)r.code, x1 = (uint32_t)(r.code >> 32);
+        const uint32_t l0 = x0 & 0x0F0F0F0Fu, h0 = (x0 >> 4) & 0x0F0F0F0Fu;
+        const uint32_t l1 = x1 & 0x0F0F0F0Fu, h1 = (x1 >> 4) & 0x0F0F0F0Fu;
+        w0 = __byte_perm(l0, h0, 0x5140);
+        w1 = __byte_perm(l0, h0, 0x7362);
+        w2 = __byte_perm(l1, h1, 0x5140);
+        w3 = __byte_perm(l1, h1, 0x7362);
+        const uint32_t f0 = x0 & (x0 >> 1) & (x0 >> 2) & (x0 >> 3) & 0x11111111u;
+        const uint32_t f1 = x1 & (x1 >> 1) & (x1 >> 2) & (x1 >> 3) & 0x11111111u;
+        cnt = __popc(f0) + __popc(f1);
+        f = (uint64_t)f0 | ((uint64_t)f1 << 32);
+    } else {
+        const uint32_t o16 = (uint32_t)r.code & 0xFFFFu, x16 = (uint32_t)(r.code >> 32) & 0xFFFFu;
+        w0 = ((o16 & 0xFu) * 0x00204081u) & 0x01010101u;          // bit i -> byte i
+        w1 = (((o16 >> 4) & 0xFu) * 0x00204081u) & 0x01010101u;
+        w2 = (((o16 >> 8) & 0xFu) * 0x00204081u) & 0x01010101u;
+        w3 = ((o16 >> 12) * 0x00204081u) & 0x01010101u;
+        f = x16;
+        cnt = __popc(x16);
+    }
+    // row bases, byte a of bw for word a, added byte by byte modulo 256
+    w0 = add_base(__byte_perm(bw, 0, 0x0000), w0);
+    w1 = add_base(__byte_perm(bw, 0, 0x1111), w1);
+    w2 = add_base(__byte_perm(bw, 0, 0x2222), w2);
+    w3 = add_base(__byte_perm(bw, 0, 0x3333), w3);
+    uint32_t tot;
+    const uint32_t pre = warp_excl_scan(cnt, lane, tot);
+    const uint32_t X = __shfl_sync(kFull, r.x0, 0);
+    bool bad = false;
+    if (cnt) {
+        // Lane-private patch: no other lane reads or writes this slot.
+        *line = make_uint4(w0, w1, w2, w3);
+        uint8_t *lb = reinterpret_cast<uint8_t *>(line);
+        uint32_t k = X + pre;
+        do {
+            const uint32_t j = KIND == CSF_NVFP4 ? (uint32_t)(__ffsll((long long)f) - 1) >> 2
+                                                 : (uint32_t)(__ffsll((long long)f) - 1);
+            f &= f - 1;
+            uint8_t v = 0;
+            if (k < (uint32_t)I.num_exc) v = __ldg(I.exc_bytes + k);
+            else bad = true;
+            ++k;
+            lb[j] = v;
+        } while (f);
+        const uint4 q = *line;
+        w0 = q.x; w1 = q.y; w2 = q.z; w3 = q.w;
+    }
+    if (edge) {
+        const uint32_t rl = rb * kTileRows + (uint32_t)lane;
+        const uint32_t cv = min(4u, g.C - 4u * cb);
+        const uint32_t cm = cv >= 4 ? 0xFFFFFFFFu : (1u << (8 * cv)) - 1;
+        w0 = rl < g.R ? w0 & cm : 0u;
+        w1 = rl + 32 < g.R ? w1 & cm : 0u;
+        w2 = rl + 64 < g.R ? w2 & cm : 0u;
+        w3 = rl + 96 < g.R ? w3 & cm : 0u;
+    }
+    *reinterpret_cast<uint4 *>(dst + 16u * (uint32_t)lane) = make_uint4(w0, w1, w2, w3);
+    if (lane == 0 && X + tot != r.x1) bad = true;
+    return bad;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kTlThreads) tiled_decode_kernel(const __grid_constant__ DecStack S,
+                                                                   const __grid_constant__ TiledIn I) {
+    extern __shared__ __align__(16) uint32_t act[];
+    __shared__ uint32_t s_cnt[kTlWarps];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const Geo g = geo_of(S);
+    const uint32_t E = (uint32_t)(S.rows / g.R);
+    uint32_t n_act = E;
+    if (I.expert_start != nullptr) {
+        n_act = 0;
+        for (uint32_t e0 = 0; e0 < E; e0 += kTlThreads) {
+            const uint32_t e = e0 + threadIdx.x;
+            bool a = false;
+            if (e < E) {
+                if (I.es64) {
+                    const long long *st = static_cast<const long long *>(I.expert_start);
+                    a = __ldg(st + e + 1) > __ldg(st + e);
+                } else {
+                    const int *st = static_cast<const int *>(I.expert_start);
+                    a = __ldg(st + e + 1) > __ldg(st + e);
+                }
+            }
+            const uint32_t bal = __ballot_sync(kFull, a);
+            if (lane == 0) s_cnt[warp] = __popc(bal);
+            __syncthreads();
+            uint32_t bn = n_act, tn = 0;
+#pragma unroll
+            for (int w = 0; w < kTlWarps; ++w) {
+                if (w < warp) bn += s_cnt[w];
+                tn += s_cnt[w];
+            }
+            if (a) act[bn + __popc(bal & lanemask_lt())] = e;
+            n_act += tn;
+            __syncthreads();
+        }
+    }
+    const uint64_t total = (uint64_t)n_act * g.T;
+    const uint64_t nw = (uint64_t)gridDim.x * kTlWarps;
+    const uint64_t w = (uint64_t)blockIdx.x * kTlWarps + warp;
+    // A contiguous range of tiles per warp, walked with running counters
+    // (active expert j, tile t = rb*ncb + cb, global tile and row block); the
+    // next tile's inputs are fetched while the current one is expanded.
+    __shared__ uint4 s_line[kTlWarps][32];
+    uint4 *line = &s_line[warp][lane];
+    const uint32_t full_rb = g.R / kTileRows, full_cb = g.C / 4;  // row / column blocks without padding
+    bool bad = false;
+    const uint64_t it0 = total * w / nw;
+    uint32_t n = (uint32_t)(total * (w + 1) / nw - it0);
+    uint32_t j = (uint32_t)(it0 / g.T);
+    uint32_t t = (uint32_t)(it0 - (uint64_t)j * g.T);
+    uint32_t rb = t / g.ncb, cb = t - rb * g.ncb;
+    uint64_t e = I.expert_start != nullptr && n ? act[j] : j;
+    uint64_t tile = e * g.T + t, rbg = e * g.nrb + rb;
+    TileRaw cur;
+    if (n) cur = tile_load<KIND>(I, tile, rbg, lane);
+    for (; n; --n) {
+        uint32_t jn = j, tn = t + 1, rbn = rb, cbn = cb + 1;
+        uint64_t tilen = tile + 1, rbgn = rbg;
+        if (cbn == g.ncb) { cbn = 0; ++rbn; ++rbgn; }
+        if (tn == g.T) {
+            tn = 0; rbn = 0; cbn = 0; ++jn;
+            if (I.expert_start != nullptr && n > 1) {
+                const uint64_t en = act[jn];
+                tilen = en * g.T;
+                rbgn = en * g.nrb;
+            }
+        }
+        TileRaw nxt;
+        if (n > 1) nxt = tile_load<KIND>(I, tilen, rbgn, lane);
+        const bool edge = rb >= full_rb || cb >= full_cb;
+        bad |= tile_finish<KIND>(I, g, rb, cb, edge, cur, S.ws + tile * 512, line, lane);
+        cur = nxt;
+        j = jn; t = tn; rb = rbn; cb = cbn; tile = tilen; rbg = rbgn;
+    }
+    if (__any_sync(kFull, bad) && lane == 0) flag(S.err, CSF_DEV_ERR_CORRUPT);
+}
+
+}  // namespace
+
+cudaError_t launch_tiled_pack(const DecStack &S, const TiledOut &O, int grid, cudaStream_t s) {
+    if (S.kind == CSF_NVFP4) {
+        tiled_pack_kernel<CSF_NVFP4, 0><<<grid, kTlThreads, 0, s>>>(S, O);
+    } else {
+        tiled_pack_kernel<CSF_MXFP4, 0><<<grid, kTlThreads, 0, s>>>(S, O);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const uint64_t n = S.rows / (uint64_t)S.R * (((uint64_t)S.R + kTileRows - 1) / kTileRows) *
+                       (((uint64_t)S.C + 3) / 4);
+    tiled_scan_kernel<<<1, 1024, 0, s>>>(O.tile_index, n, O.err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (S.kind == CSF_NVFP4) {
+        tiled_pack_kernel<CSF_NVFP4, 1><<<grid, kTlThreads, 0, s>>>(S, O);
+    } else {
+        tiled_pack_kernel<CSF_MXFP4, 1><<<grid, kTlThreads, 0, s>>>(S, O);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t tiled_decode_occupancy(int kind, size_t smem, int *blocks_per_sm) {
+    if (kind == CSF_NVFP4)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tiled_decode_kernel<CSF_NVFP4>,
+                                                             kTlThreads, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tiled_decode_kernel<CSF_MXFP4>, kTlThreads,
+                                                         smem);
+}
+
+cudaError_t launch_tiled_decode(const DecStack &S, const TiledIn &I, int grid, size_t smem, cudaStream_t s) {
+    if (S.kind == CSF_NVFP4)
+        tiled_decode_kernel<CSF_NVFP4><<<grid, kTlThreads, smem, s>>>(S, I);
+    else
+        tiled_decode_kernel<CSF_MXFP4><<<grid, kTlThreads, smem, s>>>(S, I);
+    return cudaGetLastError();
+}
+
+}  // namespace csfk

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(csf):
 
 
 def test_abi_version_and_status_strings(csf):
-    assert csf.lib.csf_abi_version() == 3
+    assert csf.lib.csf_abi_version() == 4
     for code, text in [(0, "ok"), (1, "invalid argument"), (2, "buffer too small"),
                        (3, "unsupported geometry"), (4, "CUDA error")]:
         assert csf.lib.csf_status_string(code).decode() == text
@@ -51,6 +51,9 @@ def test_sizes(csf, kind, E, R, C):
     assert sz["escapes"] == (0 if kind == 0 else sz["offsets"])
     assert sz["prepare_scratch"] >= 16 + 8
     assert sz["blocked"] == E * (-(-R // 128) * 128) * (-(-C // 4) * 4)
+    tiles = E * (-(-R // 128)) * (-(-C // 4))
+    assert sz["tiled_codes"] == tiles * (256 if kind == 0 else 128)
+    assert sz["tiled_bases"] == E * (-(-R // 128)) * 128 and sz["tiled_index"] == 4 * (tiles + 1)
 
 
 def test_sizes_rejects_bad_geometry(csf):
