@@ -249,6 +249,12 @@ def profiled_traffic():
     return None
 
 
+def tiled_bytes(t):
+    """Bytes of a tile-packed stack that a full decode reads: codes, bases,
+    tile index and exception bytes."""
+    return t.codes.numel() + t.bases.numel() + 4 * t.tile_index.numel() + t.num_exc
+
+
 def measure_rows(torch, csf, synth, gate, gate_dense, hbm, max_steps):
     """Side figures of the other rows; each row times its default number of
     steps, fewer when the run asks for fewer (short profiling runs)."""
@@ -297,7 +303,18 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm, max_steps):
     bw = [torch.empty(csf.blocked_bytes(gate), dtype=torch.uint8, device="cuda") for _ in range(4)]
     durs = timed_steps(torch, lambda i: csf.decode(bc[i % 4], bw[i % 4], layout=csf.LAYOUT_BLOCKED), n(400), 20)
     rec("gate_blocked_layout", durs, stack_traffic(gate))
-    del bc, bw
+
+    # the same scales kept tile-packed (stage-readable: each 128 x 4 tile
+    # decodes alone) and decoded into the same layout; the pack runs once per
+    # stack at load time and is reported beside it
+    tps = [csf.tiled_pack(c) for c in bc]
+    durs = timed_steps(torch, lambda i: csf.tiled_decode(tps[i % 4], bw[i % 4]), n(400), 20)
+    assert torch.equal(bw[0], csf.decode(gate, layout=csf.LAYOUT_BLOCKED))
+    packed = tiled_bytes(tps[0])
+    pk = timed_steps(torch, lambda i: csf.tiled_pack(bc[i % 4]), n(20), 3)
+    rec("gate_tiled_packed", durs, packed + bw[0].numel(),
+        {"packed_MB": round(packed / 1e6, 3), "pack_us": round(1e3 * pk[0] / pk[1], 1)})
+    del bc, bw, tps
 
     # paired gate + down
     down_dense = torch.from_numpy(synth.down_stack(seed=0)).cuda()

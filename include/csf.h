@@ -339,9 +339,11 @@ typedef struct {
 } csf_tiled;
 
 /*
- * Convert a CSF stack to its tile-packed form on the GPU (three kernels:
- * per-tile exception counts, their scan into tile_index, then codes, bases
- * and exceptions).  `exc_capacity` = bytes at dst->exc_bytes (src->num_exc
+ * Convert a CSF stack to its tile-packed form on the GPU (one kernel, one
+ * warp per expert and 128-row block).  A row block's exceptions take the same
+ * range of the stream as in the CSF stack, from the CSF index of its first
+ * row, so tile_index follows from that index and a running count over the
+ * block's tiles.  `exc_capacity` = bytes at dst->exc_bytes (src->num_exc
  * suffices); exceptions past it are dropped and CSF_DEV_ERR_CAPACITY set.  A
  * CSF index that disagrees with the escape codes sets CSF_DEV_ERR_CORRUPT.
  * dst->num_exc is not written (it equals src->num_exc).  The stacks must have
@@ -354,7 +356,8 @@ csf_status csf_tiled_pack(const csf_stack *src, csf_tiled *dst, uint64_t exc_cap
 /*
  * Decode a tile-packed stack into the block-scaled GEMM scale layout
  * (CSF_LAYOUT_BLOCKED, same bytes as csf_decode_rows of the CSF stack with
- * that layout), one warp per tile.  ws: 16-byte aligned, csf_sizes().blocked
+ * that layout); each warp decodes a contiguous range of tiles, one tile at a
+ * time, every tile on its own.  ws: 16-byte aligned, csf_sizes().blocked
  * bytes.  expert_start as csf_decode: tiles of inactive experts are not
  * touched.  Errors: CSF_ERR_ARG, CSF_ERR_SIZE, CSF_ERR_UNSUPPORTED (routing
  * with E > 8192), CSF_ERR_CUDA.

@@ -96,10 +96,12 @@ __device__ __forceinline__ uint32_t csf_cols4(const DecStack &S, uint64_t row, u
     return o4 | (x4 << 16);
 }
 
-// One warp per (expert, row block): walk its column tiles in order.  PASS 0
-// writes each tile's exception count to tile_index; PASS 1 writes the codes,
-// the bases and the exceptions (tile_index already scanned).
-template <int KIND, int PASS>
+// One warp per (expert, row block), walking its column tiles in order.  A
+// row block is a run of consecutive rows, so its exceptions fill the same
+// range of the tile-ordered stream as of the row-major CSF stream, starting
+// at the CSF index of its first row; within it the tiles follow one another
+// (a running sum over the walk), so no scan pass is needed.
+template <int KIND>
 __global__ void __launch_bounds__(kTlThreads) tiled_pack_kernel(const __grid_constant__ DecStack S,
                                                                  const __grid_constant__ TiledOut O) {
     const int lane = threadIdx.x & 31;
@@ -107,6 +109,7 @@ __global__ void __launch_bounds__(kTlThreads) tiled_pack_kernel(const __grid_con
     const uint64_t items = (uint64_t)S.rows / g.R * g.nrb;                 // E * nrb
     const uint64_t nw = (uint64_t)gridDim.x * kTlWarps;
     const uint32_t nexc = (uint32_t)S.num_exc;
+    if (blockIdx.x == 0 && threadIdx.x == 0) O.tile_index[items * g.ncb] = __ldg(S.exc_index + S.rows);
     for (uint64_t it = (uint64_t)blockIdx.x * kTlWarps + (threadIdx.x >> 5); it < items; it += nw) {
         const uint64_t e = it / g.nrb;
         const uint32_t rb = (uint32_t)(it - e * g.nrb);
@@ -119,16 +122,16 @@ __global__ void __launch_bounds__(kTlThreads) tiled_pack_kernel(const __grid_con
             const uint32_t rl = rb * kTileRows + (uint32_t)lane + 32u * a;
             ok[a] = rl < g.R;
             row[a] = e * g.R + rl;
-            if (PASS == 1 && ok[a]) {
+            if (ok[a]) {
                 X[a] = __ldg(S.exc_index + row[a]);
                 bw |= (uint32_t)__ldg(S.base + row[a]) << (8 * a);
             }
         }
-        if (PASS == 1)
-            reinterpret_cast<uint32_t *>(O.bases)[(e * g.nrb + rb) * 32 + lane] = bw;
+        reinterpret_cast<uint32_t *>(O.bases)[it * 32 + lane] = bw;
+        uint32_t run = __shfl_sync(kFull, X[0], 0);                          // index of the block's first row
         bool bad = false;
         for (uint32_t cb = 0; cb < g.ncb; ++cb) {
-            const uint64_t tile = e * g.T + (uint64_t)rb * g.ncb + cb;
+            const uint64_t tile = it * g.ncb + cb;
             uint32_t v[4];
 #pragma unroll
             for (int a = 0; a < 4; ++a) v[a] = ok[a] ? csf_cols4<KIND>(S, row[a], cb, g.C) : 0u;
@@ -137,10 +140,7 @@ __global__ void __launch_bounds__(kTlThreads) tiled_pack_kernel(const __grid_con
             for (int a = 0; a < 4; ++a) cnt += __popc(v[a] >> 16);
             uint32_t tot;
             const uint32_t pre = warp_excl_scan(cnt, lane, tot);
-            if (PASS == 0) {
-                if (lane == 0) O.tile_index[tile] = tot;
-                continue;
-            }
+            if (lane == 0) O.tile_index[tile] = run;
             if (KIND == CSF_NVFP4) {
                 const uint64_t code = (uint64_t)(v[0] & 0xFFFFu) | ((uint64_t)(v[1] & 0xFFFFu) << 16) |
                                       ((uint64_t)(v[2] & 0xFFFFu) << 32) | ((uint64_t)(v[3] & 0xFFFFu) << 48);
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kTlThreads) tiled_pack_kernel(const __grid_con
             }
             // Exceptions in position order: row a, then column; the CSF byte of
             // a row's k-th exception in this tile is at X[a] + k.
-            uint64_t dst = (uint64_t)O.tile_index[tile] + pre;
+            uint64_t dst = (uint64_t)run + pre;
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
                 uint32_t f = v[a] >> 16;
@@ -170,43 +170,14 @@ __global__ void __launch_bounds__(kTlThreads) tiled_pack_kernel(const __grid_con
                     f &= f - 1;
                 }
             }
+            run += tot;
         }
-        if (PASS == 1) {
+        // every row's exceptions accounted for: the index and the codes agree
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
-                if (ok[a] && X[a] != __ldg(S.exc_index + row[a] + 1)) bad = true;
-            if (__any_sync(kFull, bad) && lane == 0) flag(S.err, CSF_DEV_ERR_CORRUPT);
-        }
+        for (int a = 0; a < 4; ++a)
+            if (ok[a] && X[a] != __ldg(S.exc_index + row[a] + 1)) bad = true;
+        if (__any_sync(kFull, bad) && lane == 0) flag(S.err, CSF_DEV_ERR_CORRUPT);
     }
-}
-
-// Exclusive scan of tile_index[0..n) in place, total in tile_index[n]; one
-// block of 1024 threads, each scanning a contiguous chunk.
-__global__ void __launch_bounds__(1024) tiled_scan_kernel(uint32_t *idx, uint64_t n, uint32_t *err) {
-    __shared__ uint32_t s_sum[32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint64_t per = (n + 1023) / 1024;
-    const uint64_t lo = min((uint64_t)tid * per, n), hi = min(lo + per, n);
-    uint64_t local = 0;
-    for (uint64_t i = lo; i < hi; ++i) local += idx[i];
-    uint32_t wt;
-    const uint32_t wx = warp_excl_scan((uint32_t)local, lane, wt);
-    if (lane == 0) s_sum[warp] = wt;
-    __syncthreads();
-    if (warp == 0) {
-        uint32_t t;
-        const uint32_t x = warp_excl_scan(s_sum[lane], lane, t);
-        s_sum[lane] = x;
-        if (lane == 0 && tid == 0) idx[n] = t;   // total (every exception fits u32: checked on the host)
-    }
-    __syncthreads();
-    uint32_t run = s_sum[warp] + wx;
-    for (uint64_t i = lo; i < hi; ++i) {
-        const uint32_t c = idx[i];
-        idx[i] = run;
-        run += c;
-    }
-    (void)err;
 }
 
 // ---------------------------------------------------------------- decode
@@ -393,23 +364,10 @@ __global__ void __launch_bounds__(kTlThreads) tiled_decode_kernel(const __grid_c
 }  // namespace
 
 cudaError_t launch_tiled_pack(const DecStack &S, const TiledOut &O, int grid, cudaStream_t s) {
-    if (S.kind == CSF_NVFP4) {
-        tiled_pack_kernel<CSF_NVFP4, 0><<<grid, kTlThreads, 0, s>>>(S, O);
-    } else {
-        tiled_pack_kernel<CSF_MXFP4, 0><<<grid, kTlThreads, 0, s>>>(S, O);
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const uint64_t n = S.rows / (uint64_t)S.R * (((uint64_t)S.R + kTileRows - 1) / kTileRows) *
-                       (((uint64_t)S.C + 3) / 4);
-    tiled_scan_kernel<<<1, 1024, 0, s>>>(O.tile_index, n, O.err);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    if (S.kind == CSF_NVFP4) {
-        tiled_pack_kernel<CSF_NVFP4, 1><<<grid, kTlThreads, 0, s>>>(S, O);
-    } else {
-        tiled_pack_kernel<CSF_MXFP4, 1><<<grid, kTlThreads, 0, s>>>(S, O);
-    }
+    if (S.kind == CSF_NVFP4)
+        tiled_pack_kernel<CSF_NVFP4><<<grid, kTlThreads, 0, s>>>(S, O);
+    else
+        tiled_pack_kernel<CSF_MXFP4><<<grid, kTlThreads, 0, s>>>(S, O);
     return cudaGetLastError();
 }
 

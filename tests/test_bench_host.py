@@ -33,3 +33,15 @@ def test_profiled_traffic_ignores_a_stale_summary(tmp_path, monkeypatch):
     fresh = hashlib.sha256(b"// kernel v2\n").hexdigest()[:16]
     (tmp_path / "profiles" / "decode_gate_512x1024x100.md").write_text(summary.format(fresh))
     assert bench.profiled_traffic() == 1234.0
+
+
+def test_tiled_bytes_counts_every_stream_of_the_packed_gate():
+    """512 x 1024 x 100 NVFP4: 102,400 tiles of 256 code bytes, 4,096 row blocks
+    of 128 base bytes, a 102,401-entry u32 tile index, plus the exceptions."""
+    import types
+    E, R, C, exc = 512, 1024, 100, 984_000
+    tiles = E * (R // 128) * (C // 4)
+    t = types.SimpleNamespace(codes=types.SimpleNamespace(numel=lambda: tiles * 256),
+                              bases=types.SimpleNamespace(numel=lambda: E * (R // 128) * 128),
+                              tile_index=types.SimpleNamespace(numel=lambda: tiles + 1), num_exc=exc)
+    assert bench.tiled_bytes(t) == tiles * 256 + E * 8 * 128 + 4 * (tiles + 1) + exc

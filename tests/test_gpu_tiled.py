@@ -34,7 +34,7 @@ SHAPES = [(0, 1, 1, 1), (0, 2, 128, 4), (0, 3, 200, 7), (0, 2, 256, 100), (0, 3,
 
 
 @pytest.mark.parametrize("kind,E,R,C", SHAPES)
-@pytest.mark.parametrize("routed", [False, True])
+@pytest.mark.parametrize("routed", [False, np.int64, np.int32])
 def test_tiled_pack_and_decode(csf, kind, E, R, C, routed):
     w = 14 if kind == 0 else 1
     dense = synth.random_rows(E + R + C, E * R, C, spread=w + 5, replace_p=0.1).reshape(E, R, C)
@@ -48,7 +48,7 @@ def test_tiled_pack_and_decode(csf, kind, E, R, C, routed):
     nb = oracle.blocked_bytes(E, R, C)
     start = None
     if routed:
-        start = np.concatenate([[0], np.cumsum((np.arange(E) % 2 == 0) * 3)]).astype(np.int64)
+        start = np.concatenate([[0], np.cumsum((np.arange(E) % 2 == 0) * 3)]).astype(routed)
     ws = torch.full((nb,), 0xA5, dtype=torch.uint8, device="cuda")
     csf.tiled_decode(t, ws, expert_start=None if start is None else torch.from_numpy(start).cuda())
     want, st = oracle.tiled_decode(tp, start, np.full(nb, 0xA5, np.uint8))
@@ -88,3 +88,16 @@ def test_tiled_corrupt_inputs_set_the_error_word(csf):
     good.error_word.zero_()
     csf.tiled_decode(good)
     assert good.errors() == 0
+
+
+@pytest.mark.parametrize("dtype", [np.int32, np.int64])
+def test_tiled_decode_no_active_expert_writes_nothing(csf, dtype):
+    dense = synth.random_rows(5, 3 * 130, 20, spread=19, replace_p=0.1).reshape(3, 130, 20)
+    enc = oracle.encode(0, dense)
+    t = csf.tiled_pack(csf.upload(enc))
+    nb = oracle.blocked_bytes(3, 130, 20)
+    ws = torch.full((nb,), 0x5A, dtype=torch.uint8, device="cuda")
+    start = torch.from_numpy(np.full(4, 7, dtype)).cuda()
+    csf.tiled_decode(t, ws, expert_start=start)
+    assert bool((ws == 0x5A).all())
+    assert t.errors() == 0
