@@ -15,7 +15,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     bool init = false;
     int sms = 0;
-    int occ_full = 0;
+    int occ_full[3] = {0, 0, 0};   // full-stack decode, per DecodeKinds
 };
 
 std::mutex g_mu;
@@ -30,12 +30,17 @@ csf_status device_info(DeviceInfo *out) {
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceInfo &d = g_dev[dev];
     if (!d.init) {
-        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            decode_occupancy(false, 0, &d.occ_full) != cudaSuccess) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
             cudaGetLastError();
             return CSF_ERR_CUDA;
         }
-        if (d.occ_full < 1) d.occ_full = 1;
+        for (int k = 0; k < 3; ++k) {
+            if (decode_occupancy(false, k, 0, &d.occ_full[k]) != cudaSuccess) {
+                cudaGetLastError();
+                return CSF_ERR_CUDA;
+            }
+            if (d.occ_full[k] < 1) d.occ_full[k] = 1;
+        }
         d.init = true;
     }
     *out = d;
@@ -225,13 +230,14 @@ csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *exp
         return CSF_OK;
     }
     size_t smem = 0;
-    int occ = di.occ_full;
+    const int kinds = decode_kinds(p);
+    int occ = di.occ_full[kinds];
     uint64_t units = 0;
     if (per_expert) {
         // Active list (E words); prefix arrays (2 x (E+1) words) unless uniform.
         smem = p.uniform ? (expert_start ? 4ull * (uint64_t)p.E : 0)
                          : 4ull * ((uint64_t)p.E + 2ull * ((uint64_t)p.E + 1));
-        if (decode_occupancy(true, smem, &occ) != cudaSuccess) {
+        if (decode_occupancy(true, kinds, smem, &occ) != cudaSuccess) {
             cudaGetLastError();
             return CSF_ERR_CUDA;
         }

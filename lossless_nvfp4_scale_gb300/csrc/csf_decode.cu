@@ -172,12 +172,28 @@ __device__ __forceinline__ void base_words_general(uint32_t (&bw)[NW], uint32_t 
 
 // ------------------------------------------------------------------ NVFP4
 
+// True when NVFP4 rows [row_a, row_b) can take the word-wise expansion: C a
+// multiple of 4 and at least one lane chunk (so a chunk holds at most one row
+// boundary, on a word boundary), and no base above 240 (base + 15 <= 255, so a
+// plain 32-bit add cannot carry from one byte into the next).  Whole warp;
+// the bases are read again by the decode itself, from L1.
+__device__ __forceinline__ bool words_case(const DecStack &S, uint64_t row_a, uint64_t row_b, int lane) {
+    if ((S.C & 3) != 0 || S.C < kLaneNv) return false;
+    // The decode also reads the base of the row after a chunk's last row
+    // (row_b, when it exists): include it.
+    const uint64_t end = min(row_b + 1, (uint64_t)S.rows);
+    bool high = false;
+    for (uint64_t r = row_a + (uint64_t)lane; r < end; r += 32) high |= __ldg(S.base + r) > 240u;
+    return !__any_sync(kFull, high);
+}
+
 // Decode rows [row_a, row_b) of an NVFP4 stack (row_a*C a multiple of 64),
 // storing only global elements in [lo, hi).  Whole warp.  SMEM: the bytes go
 // to shared memory instead, element row_a*C + p at shared address sdst + p
 // (16-byte aligned for p % 32 == 0), and exceptions are patched there in
-// place (no staging); `stage` is then unused.
-template <bool SMEM>
+// place (no staging); `stage` is then unused.  WORDS: the caller has checked
+// words_case() for these rows, so only its expansion is compiled into the loop.
+template <bool SMEM, bool WORDS>
 __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b, uint64_t lo, uint64_t hi,
                               int lane, uint8_t *stage, uint32_t sdst) {
     const uint32_t C = (uint32_t)S.C;
@@ -251,7 +267,20 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
         const int nv = cc < nch ? (int)min(nel - p, (uint32_t)kLaneNv) : 0;
         const int b = (int)(C - cq);                           // elements to the next row start
         uint32_t out[16], fl[8];
-        if (C >= kLaneNv) {
+        if constexpr (WORDS) {
+            // Row boundaries fall on whole words and base + 15 <= 255 for every
+            // row of the segment: one base select and a plain add per word.
+            const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u;
+            const int kb = b >> 2;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t x = cw[i];
+                const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
+                fl[i] = escape_flags8(lo4, hi4);
+                out[2 * i] = (2 * i >= kb ? B : A) + __byte_perm(lo4, hi4, 0x5140);
+                out[2 * i + 1] = (2 * i + 1 >= kb ? B : A) + __byte_perm(lo4, hi4, 0x7362);
+            }
+        } else if (C >= kLaneNv) {
             // At most one row boundary in the 64 elements: bytes at or after
             // element b take row B's base.
             const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u;
@@ -577,8 +606,10 @@ __device__ __forceinline__ uint32_t units_of_expert(const DecStack &S, uint32_t 
 #endif
 
 // PER_EXPERT: the work list is built per selected expert (routing, row
-// ranges); otherwise it covers the whole stacks.
-template <bool PER_EXPERT>
+// ranges); otherwise it covers the whole stacks.  KINDS (DecodeKinds): the
+// segment decoders compiled in, so that a launch of one kind carries no code
+// of the other.
+template <bool PER_EXPERT, int KINDS>
 __global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel(const __grid_constant__ DecParams P) {
     extern __shared__ __align__(16) uint32_t smem[];
     __shared__ __align__(16) uint8_t s_stage[kWarps][kStageBytes];
@@ -745,10 +776,14 @@ __global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel
             lo = max(row_a, r0) * C;
             hi = min(row_b, r1) * C;
         }
-        if (S.kind == CSF_NVFP4)
-            segment_nvfp4<false>(S, row_a, row_b, lo, hi, lane, stage, 0u);
-        else
+        if (KINDS == kKindsNv || (KINDS == kKindsBoth && S.kind == CSF_NVFP4)) {
+            if (words_case(S, row_a, row_b, lane))
+                segment_nvfp4<false, true>(S, row_a, row_b, lo, hi, lane, stage, 0u);
+            else
+                segment_nvfp4<false, false>(S, row_a, row_b, lo, hi, lane, stage, 0u);
+        } else {
             segment_mxfp4<false>(S, row_a, row_b, lo, hi, lane, stage, 0u);
+        }
         u += cnt;
     }
 }
@@ -842,9 +877,12 @@ __global__ void __launch_bounds__(kBlkThreads, CSF_BLOCKS_MIN_BLOCKS) decode_blo
         if (rs < re) {
             const uint64_t row_a = rs / rb * rb, row_b = min((re + rb - 1) / rb * rb, S.rows);
             const uint32_t sdst = buf_sa + (uint32_t)(row_a * C - x0);  // modulo 2^32
-            if (S.kind == CSF_NVFP4)
-                segment_nvfp4<true>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
-            else
+            if (S.kind == CSF_NVFP4) {
+                if (words_case(S, row_a, row_b, lane))
+                    segment_nvfp4<true, true>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
+                else
+                    segment_nvfp4<true, false>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
+            } else
                 segment_mxfp4<true>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
         }
         __syncthreads();
@@ -901,24 +939,44 @@ cudaError_t allow_smem(K kernel, size_t smem) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-cudaError_t decode_occupancy(bool per_expert, size_t smem, int *blocks_per_sm) {
-    if (per_expert) {
-        cudaError_t e = allow_smem(decode_kernel<true>, smem);
-        if (e != cudaSuccess) return e;
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<true>, kThreads, smem);
-    }
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<false>, kThreads, smem);
+template <bool PER_EXPERT, int KINDS>
+cudaError_t occupancy_of(size_t smem, int *blocks_per_sm) {
+    cudaError_t e = allow_smem(decode_kernel<PER_EXPERT, KINDS>, smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<PER_EXPERT, KINDS>, kThreads,
+                                                         smem);
+}
+
+template <bool PER_EXPERT>
+cudaError_t occupancy_kinds(int kinds, size_t smem, int *blocks_per_sm) {
+    if (kinds == kKindsNv) return occupancy_of<PER_EXPERT, kKindsNv>(smem, blocks_per_sm);
+    if (kinds == kKindsMx) return occupancy_of<PER_EXPERT, kKindsMx>(smem, blocks_per_sm);
+    return occupancy_of<PER_EXPERT, kKindsBoth>(smem, blocks_per_sm);
+}
+
+cudaError_t decode_occupancy(bool per_expert, int kinds, size_t smem, int *blocks_per_sm) {
+    return per_expert ? occupancy_kinds<true>(kinds, smem, blocks_per_sm)
+                      : occupancy_kinds<false>(kinds, smem, blocks_per_sm);
+}
+
+template <bool PER_EXPERT, int KINDS>
+cudaError_t launch_of(const DecParams &p, int grid, size_t smem, cudaStream_t s) {
+    cudaError_t e = allow_smem(decode_kernel<PER_EXPERT, KINDS>, smem);
+    if (e != cudaSuccess) return e;
+    decode_kernel<PER_EXPERT, KINDS><<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <bool PER_EXPERT>
+cudaError_t launch_kinds(const DecParams &p, int grid, size_t smem, cudaStream_t s) {
+    const int k = decode_kinds(p);
+    if (k == kKindsNv) return launch_of<PER_EXPERT, kKindsNv>(p, grid, smem, s);
+    if (k == kKindsMx) return launch_of<PER_EXPERT, kKindsMx>(p, grid, smem, s);
+    return launch_of<PER_EXPERT, kKindsBoth>(p, grid, smem, s);
 }
 
 cudaError_t launch_decode(const DecParams &p, int grid, size_t smem, bool per_expert, cudaStream_t s) {
-    if (per_expert) {
-        cudaError_t e = allow_smem(decode_kernel<true>, smem);
-        if (e != cudaSuccess) return e;
-        decode_kernel<true><<<grid, kThreads, smem, s>>>(p);
-    } else {
-        decode_kernel<false><<<grid, kThreads, 0, s>>>(p);
-    }
-    return cudaGetLastError();
+    return per_expert ? launch_kinds<true>(p, grid, smem, s) : launch_kinds<false>(p, grid, smem, s);
 }
 
 }  // namespace csfk

@@ -95,8 +95,16 @@ inline int32_t unit_rows(int32_t C, int chunk) {
     return chunk / g;
 }
 
+// Which segment decoders a row-major decode launch compiles in: NVFP4 only,
+// MXFP4 only, or both (a pair of stacks of different kinds).
+enum DecodeKinds { kKindsNv = 0, kKindsMx = 1, kKindsBoth = 2 };
+inline int decode_kinds(const DecParams &p) {
+    const int k0 = p.st[0].kind;
+    if (p.nstacks > 1 && p.st[1].kind != k0) return kKindsBoth;
+    return k0 == CSF_NVFP4 ? kKindsNv : kKindsMx;
+}
 cudaError_t launch_decode(const DecParams &p, int grid, size_t smem, bool routed, cudaStream_t s);
-cudaError_t decode_occupancy(bool routed, size_t smem, int *blocks_per_sm);
+cudaError_t decode_occupancy(bool routed, int kinds, size_t smem, int *blocks_per_sm);
 // Decode into the 128 x 4 tiled scale-operand layout of block-scaled GEMMs
 // (one warp per 128-row block of an expert).
 constexpr int kTileRows = 128;

@@ -457,3 +457,41 @@ def test_full_mxfp4_prepare_and_decode(csf):
     mask = torch.zeros(384, dtype=torch.bool, device="cuda")
     mask[active] = True
     assert torch.equal(ws[mask], d[mask]) and bool((ws[~mask] == 0xFF).all())
+
+
+def _low_and_high_base_stack(seed, E, R, C, high_experts):
+    # Rows centred low (bases well under 240) except in `high_experts`, whose
+    # rows sit at the top of the byte range (bases above 240, values that
+    # reach 255); 3% random bytes everywhere.
+    rng = np.random.default_rng(seed)
+    centre = rng.integers(0x20, 0x60, size=(E, R, 1))
+    centre[list(high_experts)] = rng.integers(241, 250, size=(len(high_experts), R, 1))
+    vals = np.minimum(centre + rng.integers(0, 15, size=(E, R, C)), 255)
+    repl = rng.integers(0, 256, size=(E, R, C))
+    return np.where(rng.random((E, R, C)) < 0.03, repl, vals).astype(np.uint8)
+
+
+@pytest.mark.parametrize("C", [64, 68, 100])
+def test_word_wise_and_general_segments_in_one_launch(csf, C):
+    # With C a multiple of 4 and at least 64, a warp segment whose bases are
+    # all <= 240 takes the word-wise expansion and the others the general one;
+    # both kinds of segment meet in every launch below.
+    E, R = 6, 300
+    dense = _low_and_high_base_stack(11 + C, E, R, C, high_experts=(3, 5))
+    enc = oracle.encode(0, dense)
+    assert (enc["base"] > 240).any() and (enc["base"] <= 240).any()
+    st = csf.upload(enc)
+    assert np.array_equal(_np(csf.decode(st)), dense)
+    start = torch.from_numpy(np.array([0, 1, 1, 4, 6, 6, 9], np.int32)).cuda()    # experts 0, 2, 3, 5
+    ws = torch.full(dense.shape, 0xFF, dtype=torch.uint8, device="cuda")
+    csf.decode(st, ws, expert_start=start)
+    want, status = oracle.decode(enc, start.cpu().numpy(), np.full(dense.shape, 0xFF, np.uint8))
+    assert status == oracle.OK and np.array_equal(_np(ws), want)
+    ws = torch.full(dense.shape, 0xFF, dtype=torch.uint8, device="cuda")
+    csf.decode(st, ws, rows=(0, 150))
+    want, status = oracle.decode(enc, None, np.full(dense.shape, 0xFF, np.uint8), rows=(0, 150))
+    assert status == oracle.OK and np.array_equal(_np(ws), want)
+    sf = csf.decode(st, layout=csf.LAYOUT_BLOCKED)
+    want, status = oracle.decode_blocked(enc)
+    assert status == oracle.OK and np.array_equal(_np(sf), want)
+    assert st.errors() == 0
