@@ -43,6 +43,8 @@
 //   * A unit whose rows straddle an expert or range boundary (R*C not a
 //     multiple of the lane chunk) is decoded whole but stored only inside the
 //     selected rows.
+#include <type_traits>
+
 #include "csf_device.cuh"
 #include "csf_internal.cuh"
 
@@ -191,9 +193,10 @@ __device__ __forceinline__ bool words_case(const DecStack &S, uint64_t row_a, ui
 // storing only global elements in [lo, hi).  Whole warp.  SMEM: the bytes go
 // to shared memory instead, element row_a*C + p at shared address sdst + p
 // (16-byte aligned for p % 32 == 0), and exceptions are patched there in
-// place (no staging); `stage` is then unused.  WORDS: the caller has checked
-// words_case() for these rows, so only its expansion is compiled into the loop.
-template <bool SMEM, bool WORDS>
+// place (no staging); `stage` is then unused.  The loop is compiled twice:
+// once with only the word-wise expansion, taken when words_case() holds for
+// the segment, and once general.
+template <bool SMEM>
 __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b, uint64_t lo, uint64_t hi,
                               int lane, uint8_t *stage, uint32_t sdst) {
     const uint32_t C = (uint32_t)S.C;
@@ -250,43 +253,31 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
     uint32_t X = 0, Xend = 0;
     if (lane == 0) X = __ldg(S.exc_index + row_a);
     if (lane == 1) Xend = __ldg(S.exc_index + row_b);
+    // The base check's loads leave together with the first piece as well.
+    const bool words = words_case(S, row_a, row_b, lane);
     X = __shfl_sync(kFull, X, 0);
 
-    for (uint32_t cb = 0; cb < nch; cb += 32) {
-        const uint32_t cc = cb + lane;
-        uint32_t cw[8];
+    auto run = [&](auto words_tag) {
+        constexpr bool WORDS = decltype(words_tag)::value;
+        for (uint32_t cb = 0; cb < nch; cb += 32) {
+            const uint32_t cc = cb + lane;
+            uint32_t cw[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cw[i] = w[i];
-        const uint32_t cA = bA, cB = bB, cD = bD, cq = q, crr = rr;
-        q += S.step_q;
-        rr += S.step_r;
-        if (q >= C) { q -= C; ++rr; }
-        if (cb + 32 < nch) load(cc + 32, rr);                // prefetch the next piece
+            for (int i = 0; i < 8; ++i) cw[i] = w[i];
+            const uint32_t cA = bA, cB = bB, cD = bD, cq = q, crr = rr;
+            q += S.step_q;
+            rr += S.step_r;
+            if (q >= C) { q -= C; ++rr; }
+            if (cb + 32 < nch) load(cc + 32, rr);                // prefetch the next piece
 
-        const uint32_t p = cc * kLaneNv;
-        const int nv = cc < nch ? (int)min(nel - p, (uint32_t)kLaneNv) : 0;
-        const int b = (int)(C - cq);                           // elements to the next row start
-        uint32_t out[16], fl[8];
-        if constexpr (WORDS) {
-            // Row boundaries fall on whole words and base + 15 <= 255 for every
-            // row of the segment: one base select and a plain add per word.
-            const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u;
-            const int kb = b >> 2;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t x = cw[i];
-                const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
-                fl[i] = escape_flags8(lo4, hi4);
-                out[2 * i] = (2 * i >= kb ? B : A) + __byte_perm(lo4, hi4, 0x5140);
-                out[2 * i + 1] = (2 * i + 1 >= kb ? B : A) + __byte_perm(lo4, hi4, 0x7362);
-            }
-        } else if (C >= kLaneNv) {
-            // At most one row boundary in the 64 elements: bytes at or after
-            // element b take row B's base.
-            const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u;
-            if (cA <= 240u && cB <= 240u && (C & 3u) == 0) {
-                // Row boundaries fall on whole words (C % 4 == 0) and base + 15
-                // <= 255 (a plain add cannot carry between bytes).
+            const uint32_t p = cc * kLaneNv;
+            const int nv = cc < nch ? (int)min(nel - p, (uint32_t)kLaneNv) : 0;
+            const int b = (int)(C - cq);                           // elements to the next row start
+            uint32_t out[16], fl[8];
+            if constexpr (WORDS) {
+                // Row boundaries fall on whole words and base + 15 <= 255 for every
+                // row of the segment: one base select and a plain add per word.
+                const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u;
                 const int kb = b >> 2;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -296,140 +287,181 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                     out[2 * i] = (2 * i >= kb ? B : A) + __byte_perm(lo4, hi4, 0x5140);
                     out[2 * i + 1] = (2 * i + 1 >= kb ? B : A) + __byte_perm(lo4, hi4, 0x7362);
                 }
-            } else if (cA <= 240u && cB <= 240u) {
-                // base + 15 <= 255: a plain add cannot carry between bytes.
+            } else if (C >= kLaneNv) {
+                // At most one row boundary in the 64 elements: bytes at or after
+                // element b take row B's base.
+                const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u;
+                if (cA <= 240u && cB <= 240u && (C & 3u) == 0) {
+                    // Row boundaries fall on whole words (C % 4 == 0) and base + 15
+                    // <= 255 (a plain add cannot carry between bytes).
+                    const int kb = b >> 2;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t x = cw[i];
+                        const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
+                        fl[i] = escape_flags8(lo4, hi4);
+                        out[2 * i] = (2 * i >= kb ? B : A) + __byte_perm(lo4, hi4, 0x5140);
+                        out[2 * i + 1] = (2 * i + 1 >= kb ? B : A) + __byte_perm(lo4, hi4, 0x7362);
+                    }
+                } else if (cA <= 240u && cB <= 240u) {
+                    // base + 15 <= 255: a plain add cannot carry between bytes.
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t x = cw[i];
+                        const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
+                        fl[i] = escape_flags8(lo4, hi4);
+                        const uint32_t m0 = bytes_from(b, 2 * i), m1 = bytes_from(b, 2 * i + 1);
+                        out[2 * i] = ((A & ~m0) | (B & m0)) + __byte_perm(lo4, hi4, 0x5140);
+                        out[2 * i + 1] = ((A & ~m1) | (B & m1)) + __byte_perm(lo4, hi4, 0x7362);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t x = cw[i];
+                        const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
+                        fl[i] = escape_flags8(lo4, hi4);
+                        const uint32_t m0 = bytes_from(b, 2 * i), m1 = bytes_from(b, 2 * i + 1);
+                        out[2 * i] = add_base((A & ~m0) | (B & m0), __byte_perm(lo4, hi4, 0x5140));
+                        out[2 * i + 1] = add_base((A & ~m1) | (B & m1), __byte_perm(lo4, hi4, 0x7362));
+                    }
+                }
+            } else if (C >= 32) {
+                // At most two row boundaries in the 64 elements (at b and b + C).
+                const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u, D = cD * 0x01010101u;
+                const int b2 = b + (int)C;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const uint32_t x = cw[i];
                     const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
                     fl[i] = escape_flags8(lo4, hi4);
-                    const uint32_t m0 = bytes_from(b, 2 * i), m1 = bytes_from(b, 2 * i + 1);
-                    out[2 * i] = ((A & ~m0) | (B & m0)) + __byte_perm(lo4, hi4, 0x5140);
-                    out[2 * i + 1] = ((A & ~m1) | (B & m1)) + __byte_perm(lo4, hi4, 0x7362);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int k = 2 * i + h;
+                        const uint32_t m1 = bytes_from(b, k), m2 = bytes_from(b2, k);
+                        const uint32_t bw = (((A & ~m1) | (B & m1)) & ~m2) | (D & m2);
+                        const uint32_t o = __byte_perm(lo4, hi4, h ? 0x7362 : 0x5140);
+                        out[k] = (cA <= 240u && cB <= 240u && cD <= 240u) ? bw + o : add_base(bw, o);
+                    }
                 }
             } else {
+                uint32_t bw[16];
+                base_words_general<16>(bw, cA, b, S.base, row_a + crr + 1, S.rows, C);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const uint32_t x = cw[i];
                     const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
                     fl[i] = escape_flags8(lo4, hi4);
-                    const uint32_t m0 = bytes_from(b, 2 * i), m1 = bytes_from(b, 2 * i + 1);
-                    out[2 * i] = add_base((A & ~m0) | (B & m0), __byte_perm(lo4, hi4, 0x5140));
-                    out[2 * i + 1] = add_base((A & ~m1) | (B & m1), __byte_perm(lo4, hi4, 0x7362));
+                    out[2 * i] = add_base(bw[2 * i], __byte_perm(lo4, hi4, 0x5140));
+                    out[2 * i + 1] = add_base(bw[2 * i + 1], __byte_perm(lo4, hi4, 0x7362));
                 }
             }
-        } else if (C >= 32) {
-            // At most two row boundaries in the 64 elements (at b and b + C).
-            const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u, D = cD * 0x01010101u;
-            const int b2 = b + (int)C;
+            // Element-ordered escape masks: bit j of f_h <-> element 32h + j.
+            uint32_t f0 = __byte_perm(__byte_perm(fl[0], fl[1], 0x0040), __byte_perm(fl[2], fl[3], 0x0040), 0x5410);
+            uint32_t f1 = __byte_perm(__byte_perm(fl[4], fl[5], 0x0040), __byte_perm(fl[6], fl[7], 0x0040), 0x5410);
+            if (nv < kLaneNv) {
+                f0 &= nv >= 32 ? 0xFFFFFFFFu : (nv == 0 ? 0u : 0xFFFFFFFFu >> (32 - nv));
+                f1 &= nv <= 32 ? 0u : 0xFFFFFFFFu >> (64 - nv);
+            }
+            const uint32_t cnt = __popc(f0) + __popc(f1);
+            uint32_t tot;
+            uint32_t xl = X + warp_excl_scan(cnt, lane, tot);
+            X += tot;
+            if constexpr (SMEM) {
+                // Write the chunk, then patch its exceptions in place.
+                if (nv > 0) {
+                    sstore32(sdst, p, out, lo_l, hi_l);
+                    if (nv > 32) sstore32(sdst, p + 32, out + 8, lo_l, hi_l);
+                }
+                if (cnt) {
+                    if (xl <= nexc && cnt <= nexc - xl) {
+                        const uint8_t *ep = S.exc_bytes + xl;
+                        uint32_t f = f0;
+                        while (f) {
+                            const uint32_t j = p + (uint32_t)(__ffs(f) - 1);
+                            const uint32_t v = __ldg(ep++);
+                            if (j >= lo_l && j < hi_l) sts_u8(sdst + j, v);
+                            f &= f - 1;
+                        }
+                        f = f1;
+                        while (f) {
+                            const uint32_t j = p + (uint32_t)(__ffs(f) + 31);
+                            const uint32_t v = __ldg(ep++);
+                            if (j >= lo_l && j < hi_l) sts_u8(sdst + j, v);
+                            f &= f - 1;
+                        }
+                    } else {
+                        bad = true;
+                    }
+                }
+                continue;
+            }
+            if (__any_sync(kFull, cnt != 0)) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t x = cw[i];
-                const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
-                fl[i] = escape_flags8(lo4, hi4);
+                for (int s = 0; s < 4; ++s)
+                    *reinterpret_cast<uint4 *>(my + ((16 * s) ^ gs)) =
+                        make_uint4(out[4 * s], out[4 * s + 1], out[4 * s + 2], out[4 * s + 3]);
+                if (cnt) {
+                    if (xl <= nexc && cnt <= nexc - xl) {
+                        // The lane's exceptions are consecutive in the stream.
+                        const uint8_t *ep = S.exc_bytes + xl;
+                        uint32_t f = f0;
+                        while (f) {
+                            my[(uint32_t)(__ffs(f) - 1) ^ gs] = __ldg(ep++);
+                            f &= f - 1;
+                        }
+                        f = f1;
+                        while (f) {
+                            my[(uint32_t)(__ffs(f) + 31) ^ gs] = __ldg(ep++);
+                            f &= f - 1;
+                        }
+                    } else {
+                        bad = true;   // index points past the stream: leave the bytes, report
+                    }
+                }
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int k = 2 * i + h;
-                    const uint32_t m1 = bytes_from(b, k), m2 = bytes_from(b2, k);
-                    const uint32_t bw = (((A & ~m1) | (B & m1)) & ~m2) | (D & m2);
-                    const uint32_t o = __byte_perm(lo4, hi4, h ? 0x7362 : 0x5140);
-                    out[k] = (cA <= 240u && cB <= 240u && cD <= 240u) ? bw + o : add_base(bw, o);
+                for (int s = 0; s < 4; ++s) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(my + ((16 * s) ^ gs));
+                    out[4 * s] = v.x; out[4 * s + 1] = v.y; out[4 * s + 2] = v.z; out[4 * s + 3] = v.w;
                 }
             }
-        } else {
-            uint32_t bw[16];
-            base_words_general<16>(bw, cA, b, S.base, row_a + crr + 1, S.rows, C);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t x = cw[i];
-                const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
-                fl[i] = escape_flags8(lo4, hi4);
-                out[2 * i] = add_base(bw[2 * i], __byte_perm(lo4, hi4, 0x5140));
-                out[2 * i + 1] = add_base(bw[2 * i + 1], __byte_perm(lo4, hi4, 0x7362));
+            if (nv == kLaneNv && fast) {
+                st_v8(ws + p, out);
+                st_v8(ws + p + 32, out + 8);
+            } else if (nv > 0) {
+                store32(ws, S.ws_align, p, out, lo_l, hi_l);
+                if (nv > 32) store32(ws, S.ws_align, p + 32, out + 8, lo_l, hi_l);
             }
         }
-        // Element-ordered escape masks: bit j of f_h <-> element 32h + j.
-        uint32_t f0 = __byte_perm(__byte_perm(fl[0], fl[1], 0x0040), __byte_perm(fl[2], fl[3], 0x0040), 0x5410);
-        uint32_t f1 = __byte_perm(__byte_perm(fl[4], fl[5], 0x0040), __byte_perm(fl[6], fl[7], 0x0040), 0x5410);
-        if (nv < kLaneNv) {
-            f0 &= nv >= 32 ? 0xFFFFFFFFu : (nv == 0 ? 0u : 0xFFFFFFFFu >> (32 - nv));
-            f1 &= nv <= 32 ? 0u : 0xFFFFFFFFu >> (64 - nv);
-        }
-        const uint32_t cnt = __popc(f0) + __popc(f1);
-        uint32_t tot;
-        uint32_t xl = X + warp_excl_scan(cnt, lane, tot);
-        X += tot;
-        if constexpr (SMEM) {
-            // Write the chunk, then patch its exceptions in place.
-            if (nv > 0) {
-                sstore32(sdst, p, out, lo_l, hi_l);
-                if (nv > 32) sstore32(sdst, p + 32, out + 8, lo_l, hi_l);
-            }
-            if (cnt) {
-                if (xl <= nexc && cnt <= nexc - xl) {
-                    const uint8_t *ep = S.exc_bytes + xl;
-                    uint32_t f = f0;
-                    while (f) {
-                        const uint32_t j = p + (uint32_t)(__ffs(f) - 1);
-                        const uint32_t v = __ldg(ep++);
-                        if (j >= lo_l && j < hi_l) sts_u8(sdst + j, v);
-                        f &= f - 1;
-                    }
-                    f = f1;
-                    while (f) {
-                        const uint32_t j = p + (uint32_t)(__ffs(f) + 31);
-                        const uint32_t v = __ldg(ep++);
-                        if (j >= lo_l && j < hi_l) sts_u8(sdst + j, v);
-                        f &= f - 1;
-                    }
-                } else {
-                    bad = true;
-                }
-            }
-            continue;
-        }
-        if (__any_sync(kFull, cnt != 0)) {
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-                *reinterpret_cast<uint4 *>(my + ((16 * s) ^ gs)) =
-                    make_uint4(out[4 * s], out[4 * s + 1], out[4 * s + 2], out[4 * s + 3]);
-            if (cnt) {
-                if (xl <= nexc && cnt <= nexc - xl) {
-                    // The lane's exceptions are consecutive in the stream.
-                    const uint8_t *ep = S.exc_bytes + xl;
-                    uint32_t f = f0;
-                    while (f) {
-                        my[(uint32_t)(__ffs(f) - 1) ^ gs] = __ldg(ep++);
-                        f &= f - 1;
-                    }
-                    f = f1;
-                    while (f) {
-                        my[(uint32_t)(__ffs(f) + 31) ^ gs] = __ldg(ep++);
-                        f &= f - 1;
-                    }
-                } else {
-                    bad = true;   // index points past the stream: leave the bytes, report
-                }
-            }
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(my + ((16 * s) ^ gs));
-                out[4 * s] = v.x; out[4 * s + 1] = v.y; out[4 * s + 2] = v.z; out[4 * s + 3] = v.w;
-            }
-        }
-        if (nv == kLaneNv && fast) {
-            st_v8(ws + p, out);
-            st_v8(ws + p + 32, out + 8);
-        } else if (nv > 0) {
-            store32(ws, S.ws_align, p, out, lo_l, hi_l);
-            if (nv > 32) store32(ws, S.ws_align, p + 32, out + 8, lo_l, hi_l);
-        }
-    }
+    };
+    if (words)
+        run(std::true_type{});
+    else
+        run(std::false_type{});
     if (lane == 1 && Xend != X) bad = true;
     if (__any_sync(kFull, bad) && lane == 0) flag(S.err, CSF_DEV_ERR_CORRUPT);
 }
 
 // ------------------------------------------------------------------ MXFP4
+
+// Patch the escapes flagged in f (bit i -> staged element jb + i) with the
+// next bytes of the exception stream, two per trip: the two loads are
+// independent.  Used where exceptions are dense (MXFP4); with a few per lane
+// chunk (NVFP4) the one-per-trip loop is faster.
+__device__ __forceinline__ void patch_two(uint8_t *my, uint32_t gs, uint32_t jb, uint32_t f, const uint8_t *&ep) {
+    while (f) {
+        const uint32_t j0 = jb + (uint32_t)(__ffs(f) - 1);
+        f &= f - 1;
+        const bool two = f != 0;
+        const uint32_t j1 = jb + (uint32_t)(__ffs(f) - 1);   // unused unless two
+        f &= f - 1;
+        const uint8_t v0 = __ldg(ep);
+        uint8_t v1 = 0;
+        if (two) v1 = __ldg(ep + 1);
+        my[j0 ^ gs] = v0;
+        if (two) my[j1 ^ gs] = v1;
+        ep += two ? 2 : 1;
+    }
+}
 
 // Decode rows [row_a, row_b) of an MXFP4 stack (row_a*C a multiple of 128);
 // SMEM and sdst as in segment_nvfp4.
@@ -558,33 +590,35 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
 #pragma unroll
                     for (int gi = 0; gi < 4; ++gi) {
                         uint32_t f = xw[gi];
-                        while (f) {
-                            if constexpr (SMEM) {
+                        if constexpr (SMEM) {
+                            while (f) {
                                 const uint32_t j = p + 32u * gi + (uint32_t)(__ffs(f) - 1);
                                 const uint32_t v = __ldg(ep++);
                                 if (j >= lo_l && j < hi_l) sts_u8(sdst + j, v);   // patched in place
-                            } else {
-                                my[(32u * gi + (uint32_t)(__ffs(f) - 1)) ^ gs] = __ldg(ep++);
+                                f &= f - 1;
                             }
-                            f &= f - 1;
+                        } else {
+                            patch_two(my, gs, 32u * gi, f, ep);
                         }
                     }
                 } else {
                     bad = true;
                 }
             }
-            if constexpr (SMEM) continue;
+            if constexpr (!SMEM) {
+                // reload the patched lane chunk and store it
 #pragma unroll
-            for (int gi = 0; gi < 4; ++gi) {
-                uint32_t out[8];
+                for (int gi = 0; gi < 4; ++gi) {
+                    uint32_t out[8];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(my + ((16 * (2 * gi + h)) ^ gs));
-                    out[4 * h] = v.x; out[4 * h + 1] = v.y; out[4 * h + 2] = v.z; out[4 * h + 3] = v.w;
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(my + ((16 * (2 * gi + h)) ^ gs));
+                        out[4 * h] = v.x; out[4 * h + 1] = v.y; out[4 * h + 2] = v.z; out[4 * h + 3] = v.w;
+                    }
+                    const uint32_t pg = p + 32u * gi;
+                    if (nv == kLaneMx && fast) st_v8(ws + pg, out);
+                    else if (32 * gi < nv) store32(ws, S.ws_align, pg, out, lo_l, hi_l);
                 }
-                const uint32_t pg = p + 32u * gi;
-                if (nv == kLaneMx && fast) st_v8(ws + pg, out);
-                else if (32 * gi < nv) store32(ws, S.ws_align, pg, out, lo_l, hi_l);
             }
         }
     }
@@ -777,10 +811,7 @@ __global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel
             hi = min(row_b, r1) * C;
         }
         if (KINDS == kKindsNv || (KINDS == kKindsBoth && S.kind == CSF_NVFP4)) {
-            if (words_case(S, row_a, row_b, lane))
-                segment_nvfp4<false, true>(S, row_a, row_b, lo, hi, lane, stage, 0u);
-            else
-                segment_nvfp4<false, false>(S, row_a, row_b, lo, hi, lane, stage, 0u);
+            segment_nvfp4<false>(S, row_a, row_b, lo, hi, lane, stage, 0u);
         } else {
             segment_mxfp4<false>(S, row_a, row_b, lo, hi, lane, stage, 0u);
         }
@@ -878,10 +909,7 @@ __global__ void __launch_bounds__(kBlkThreads, CSF_BLOCKS_MIN_BLOCKS) decode_blo
             const uint64_t row_a = rs / rb * rb, row_b = min((re + rb - 1) / rb * rb, S.rows);
             const uint32_t sdst = buf_sa + (uint32_t)(row_a * C - x0);  // modulo 2^32
             if (S.kind == CSF_NVFP4) {
-                if (words_case(S, row_a, row_b, lane))
-                    segment_nvfp4<true, true>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
-                else
-                    segment_nvfp4<true, false>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
+                segment_nvfp4<true>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
             } else
                 segment_mxfp4<true>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
         }
