@@ -210,7 +210,7 @@ csf_status plan_decode(const csf_decode_part *parts, int nparts, const void *exp
             smem += p.buf_bytes;
         }
         int occ = 0;
-        const cudaError_t oe = L->buffered ? decode_blocks_occupancy(smem, &occ) : decode_tiles_occupancy(smem, &occ);
+        const cudaError_t oe = L->buffered ? decode_blocks_occupancy(p, smem, &occ) : decode_tiles_occupancy(smem, &occ);
         if (oe != cudaSuccess) {
             cudaGetLastError();
             return CSF_ERR_CUDA;

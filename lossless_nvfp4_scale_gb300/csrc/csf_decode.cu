@@ -195,8 +195,9 @@ __device__ __forceinline__ bool words_case(const DecStack &S, uint64_t row_a, ui
 // (16-byte aligned for p % 32 == 0), and exceptions are patched there in
 // place (no staging); `stage` is then unused.  The loop is compiled twice:
 // once with only the word-wise expansion, taken when words_case() holds for
-// the segment, and once general.
-template <bool SMEM>
+// the segment, and once general; WORDS_OK = false (no stack of the launch
+// can take the word-wise loop) compiles the general loop alone.
+template <bool SMEM, bool WORDS_OK>
 __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b, uint64_t lo, uint64_t hi,
                               int lane, uint8_t *stage, uint32_t sdst) {
     const uint32_t C = (uint32_t)S.C;
@@ -254,7 +255,7 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
     if (lane == 0) X = __ldg(S.exc_index + row_a);
     if (lane == 1) Xend = __ldg(S.exc_index + row_b);
     // The base check's loads leave together with the first piece as well.
-    const bool words = words_case(S, row_a, row_b, lane);
+    const bool words = WORDS_OK && words_case(S, row_a, row_b, lane);
     X = __shfl_sync(kFull, X, 0);
 
     auto run = [&](auto words_tag) {
@@ -433,10 +434,14 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
             }
         }
     };
-    if (words)
-        run(std::true_type{});
-    else
+    if constexpr (WORDS_OK) {
+        if (words)
+            run(std::true_type{});
+        else
+            run(std::false_type{});
+    } else {
         run(std::false_type{});
+    }
     if (lane == 1 && Xend != X) bad = true;
     if (__any_sync(kFull, bad) && lane == 0) flag(S.err, CSF_DEV_ERR_CORRUPT);
 }
@@ -811,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel
             hi = min(row_b, r1) * C;
         }
         if (KINDS == kKindsNv || (KINDS == kKindsBoth && S.kind == CSF_NVFP4)) {
-            segment_nvfp4<false>(S, row_a, row_b, lo, hi, lane, stage, 0u);
+            segment_nvfp4<false, true>(S, row_a, row_b, lo, hi, lane, stage, 0u);
         } else {
             segment_mxfp4<false>(S, row_a, row_b, lo, hi, lane, stage, 0u);
         }
@@ -845,7 +850,10 @@ __device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
 // lane b assembling line b of a tile from rows b, b+32, b+64, b+96, so every
 // tile leaves as one coalesced 512-byte warp store.  Rows whose first unit
 // starts before the warp's share are decoded whole and clipped.
-__global__ void __launch_bounds__(kBlkThreads, CSF_BLOCKS_MIN_BLOCKS) decode_blocks_kernel(const __grid_constant__ DecParams P) {
+// KINDS (DecodeKinds) and WORDS_OK as for decode_kernel and segment_nvfp4.
+template <int KINDS, bool WORDS_OK>
+__global__ void __launch_bounds__(kBlkThreads, CSF_BLOCKS_MIN_BLOCKS)
+    decode_blocks_kernel(const __grid_constant__ DecParams P) {
     extern __shared__ __align__(16) uint8_t dsm[];
     __shared__ uint32_t s_cnt[kBlkWarps];
     const int lane = threadIdx.x & 31;
@@ -908,9 +916,9 @@ __global__ void __launch_bounds__(kBlkThreads, CSF_BLOCKS_MIN_BLOCKS) decode_blo
         if (rs < re) {
             const uint64_t row_a = rs / rb * rb, row_b = min((re + rb - 1) / rb * rb, S.rows);
             const uint32_t sdst = buf_sa + (uint32_t)(row_a * C - x0);  // modulo 2^32
-            if (S.kind == CSF_NVFP4) {
-                segment_nvfp4<true>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
-            } else
+            if (KINDS == kKindsNv || (KINDS == kKindsBoth && S.kind == CSF_NVFP4))
+                segment_nvfp4<true, WORDS_OK>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
+            else
                 segment_mxfp4<true>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
         }
         __syncthreads();
@@ -946,17 +954,39 @@ __global__ void __launch_bounds__(kBlkThreads, CSF_BLOCKS_MIN_BLOCKS) decode_blo
 
 }  // namespace
 
-cudaError_t decode_blocks_occupancy(size_t smem, int *blocks_per_sm) {
-    cudaError_t e = cudaFuncSetAttribute(decode_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+// The blocked-layout instance a launch needs: its kinds, and whether any
+// NVFP4 stack of it can take the word-wise loop (C % 4 == 0, C >= 64).
+template <int KINDS, bool WORDS_OK>
+cudaError_t blocks_of(const DecParams *p, int grid, size_t smem, cudaStream_t s, int *blocks_per_sm) {
+    cudaError_t e = cudaFuncSetAttribute(decode_blocks_kernel<KINDS, WORDS_OK>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_blocks_kernel, kBlkThreads, smem);
+    if (blocks_per_sm)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_blocks_kernel<KINDS, WORDS_OK>,
+                                                             kBlkThreads, smem);
+    decode_blocks_kernel<KINDS, WORDS_OK><<<grid, kBlkThreads, smem, s>>>(*p);
+    return cudaGetLastError();
+}
+
+cudaError_t blocks_dispatch(const DecParams &p, int grid, size_t smem, cudaStream_t s, int *blocks_per_sm) {
+    const int k = decode_kinds(p);
+    bool words = false;
+    for (int i = 0; i < p.nstacks; ++i)
+        if (p.st[i].kind == CSF_NVFP4 && p.st[i].C % 4 == 0 && p.st[i].C >= kLaneNv) words = true;
+    if (k == kKindsMx) return blocks_of<kKindsMx, false>(&p, grid, smem, s, blocks_per_sm);
+    if (k == kKindsNv)
+        return words ? blocks_of<kKindsNv, true>(&p, grid, smem, s, blocks_per_sm)
+                     : blocks_of<kKindsNv, false>(&p, grid, smem, s, blocks_per_sm);
+    return words ? blocks_of<kKindsBoth, true>(&p, grid, smem, s, blocks_per_sm)
+                 : blocks_of<kKindsBoth, false>(&p, grid, smem, s, blocks_per_sm);
+}
+
+cudaError_t decode_blocks_occupancy(const DecParams &p, size_t smem, int *blocks_per_sm) {
+    return blocks_dispatch(p, 0, smem, nullptr, blocks_per_sm);
 }
 
 cudaError_t launch_decode_blocks(const DecParams &p, int grid, size_t smem, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(decode_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    decode_blocks_kernel<<<grid, kBlkThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return blocks_dispatch(p, grid, smem, s, nullptr);
 }
 
 // Dynamic shared memory beyond the default window (48 KB with the static

@@ -117,7 +117,7 @@ constexpr int kTileBlockWarps = 4;   // warps per block
 constexpr int kBlkWarps = CSF_BLK_WARPS;
 constexpr int kBlkThreads = 32 * kBlkWarps;
 cudaError_t launch_decode_blocks(const DecParams &p, int grid, size_t smem, cudaStream_t s);
-cudaError_t decode_blocks_occupancy(size_t smem, int *blocks_per_sm);
+cudaError_t decode_blocks_occupancy(const DecParams &p, size_t smem, int *blocks_per_sm);
 cudaError_t launch_decode_tiles(const DecParams &p, int grid, size_t smem, cudaStream_t s);
 cudaError_t decode_tiles_occupancy(size_t smem, int *blocks_per_sm);
 
