@@ -174,18 +174,20 @@ __device__ __forceinline__ void base_words_general(uint32_t (&bw)[NW], uint32_t 
 
 // ------------------------------------------------------------------ NVFP4
 
-// True when NVFP4 rows [row_a, row_b) can take the word-wise expansion: C a
-// multiple of 4 and at least one lane chunk (so a chunk holds at most one row
-// boundary, on a word boundary), and no base above 240 (base + 15 <= 255, so a
-// plain 32-bit add cannot carry from one byte into the next).  Whole warp;
-// the bases are read again by the decode itself, from L1.
-__device__ __forceinline__ bool words_case(const DecStack &S, uint64_t row_a, uint64_t row_b, int lane) {
-    if ((S.C & 3) != 0 || S.C < kLaneNv) return false;
+// True when rows [row_a, row_b) can take the word-wise expansion: C a multiple
+// of 4 and at least one lane chunk (so a chunk holds at most one row boundary,
+// on a word boundary), and no base above `limit` (240 for NVFP4, 254 for
+// MXFP4: base + largest code <= 255, so a plain 32-bit add cannot carry from
+// one byte into the next).  Whole warp; the bases are read again by the decode
+// itself, from L1.
+__device__ __forceinline__ bool words_case(const DecStack &S, uint64_t row_a, uint64_t row_b, int lane, int chunk,
+                                           uint32_t limit) {
+    if ((S.C & 3) != 0 || S.C < chunk) return false;
     // The decode also reads the base of the row after a chunk's last row
     // (row_b, when it exists): include it.
     const uint64_t end = min(row_b + 1, (uint64_t)S.rows);
     bool high = false;
-    for (uint64_t r = row_a + (uint64_t)lane; r < end; r += 32) high |= __ldg(S.base + r) > 240u;
+    for (uint64_t r = row_a + (uint64_t)lane; r < end; r += 32) high |= __ldg(S.base + r) > limit;
     return !__any_sync(kFull, high);
 }
 
@@ -255,7 +257,7 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
     if (lane == 0) X = __ldg(S.exc_index + row_a);
     if (lane == 1) Xend = __ldg(S.exc_index + row_b);
     // The base check's loads leave together with the first piece as well.
-    const bool words = WORDS_OK && words_case(S, row_a, row_b, lane);
+    const bool words = WORDS_OK && words_case(S, row_a, row_b, lane, kLaneNv, 240u);
     X = __shfl_sync(kFull, X, 0);
 
     auto run = [&](auto words_tag) {
@@ -469,8 +471,9 @@ __device__ __forceinline__ void patch_two(uint8_t *my, uint32_t gs, uint32_t jb,
 }
 
 // Decode rows [row_a, row_b) of an MXFP4 stack (row_a*C a multiple of 128);
-// SMEM and sdst as in segment_nvfp4.
-template <bool SMEM>
+// SMEM, sdst and WORDS_OK as in segment_nvfp4 (word-wise: C % 4 == 0, C >= 128
+// and no base above 254).
+template <bool SMEM, bool WORDS_OK>
 __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b, uint64_t lo, uint64_t hi,
                               int lane, uint8_t *stage, uint32_t sdst) {
     const uint32_t C = (uint32_t)S.C;
@@ -509,8 +512,11 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
     uint32_t X = 0, Xend = 0;                                  // as in segment_nvfp4
     if (lane == 0) X = __ldg(S.exc_index + row_a);
     if (lane == 1) Xend = __ldg(S.exc_index + row_b);
+    const bool words = WORDS_OK && words_case(S, row_a, row_b, lane, kLaneMx, 254u);
     X = __shfl_sync(kFull, X, 0);
 
+    auto run = [&](auto words_tag) {
+    constexpr bool WORDS = decltype(words_tag)::value;
     for (uint32_t cb = 0; cb < nch; cb += 32) {
         const uint32_t cc = cb + lane;
         const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
@@ -539,6 +545,16 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
 #pragma unroll
             for (int gi = 0; gi < 4; ++gi) {
                 uint32_t out[8];
+                if constexpr (WORDS) {
+                    // Row B starts at word kb of the chunk (none when kb >= 32).
+                    const uint32_t A4 = cA * 0x01010101u, B4 = cB * 0x01010101u;
+                    const int kb = (int)(C - cq) >> 2;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t nib = (ow[gi] >> (4 * k)) & 0xFu;
+                        out[k] = (8 * gi + k >= kb ? B4 : A4) + ((nib * 0x00204081u) & 0x01010101u);
+                    }
+                } else {
                 const int bg = (int)(C - qg);                  // elements to the next row start
                 const uint32_t A = rg == crr ? cA
                                  : (rg == crr + 1 ? cB : (rg < rows_left ? (uint32_t)__ldg(bases + rg) : 0u));
@@ -575,6 +591,7 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                         const uint32_t nib = (ow[gi] >> (4 * k)) & 0xFu;
                         out[k] = add_base(bw[k], (nib * 0x00204081u) & 0x01010101u);
                     }
+                }
                 }
                 if constexpr (SMEM) {
                     if (32 * gi < nv) sstore32(sdst, p + 32u * gi, out, lo_l, hi_l);
@@ -626,6 +643,15 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                 }
             }
         }
+    }
+    };
+    if constexpr (WORDS_OK) {
+        if (words)
+            run(std::true_type{});
+        else
+            run(std::false_type{});
+    } else {
+        run(std::false_type{});
     }
     if (lane == 1 && Xend != X) bad = true;
     if (__any_sync(kFull, bad) && lane == 0) flag(S.err, CSF_DEV_ERR_CORRUPT);
@@ -818,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel
         if (KINDS == kKindsNv || (KINDS == kKindsBoth && S.kind == CSF_NVFP4)) {
             segment_nvfp4<false, true>(S, row_a, row_b, lo, hi, lane, stage, 0u);
         } else {
-            segment_mxfp4<false>(S, row_a, row_b, lo, hi, lane, stage, 0u);
+            segment_mxfp4<false, true>(S, row_a, row_b, lo, hi, lane, stage, 0u);
         }
         u += cnt;
     }
@@ -919,7 +945,7 @@ __global__ void __launch_bounds__(kBlkThreads, CSF_BLOCKS_MIN_BLOCKS)
             if (KINDS == kKindsNv || (KINDS == kKindsBoth && S.kind == CSF_NVFP4))
                 segment_nvfp4<true, WORDS_OK>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
             else
-                segment_mxfp4<true>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
+                segment_mxfp4<true, WORDS_OK>(S, row_a, row_b, rs * C, re * C, lane, buf, sdst);
         }
         __syncthreads();
 
@@ -955,7 +981,8 @@ __global__ void __launch_bounds__(kBlkThreads, CSF_BLOCKS_MIN_BLOCKS)
 }  // namespace
 
 // The blocked-layout instance a launch needs: its kinds, and whether any
-// NVFP4 stack of it can take the word-wise loop (C % 4 == 0, C >= 64).
+// stack of it can take the word-wise loop (C % 4 == 0 and C at least the
+// lane chunk: 64 NVFP4, 128 MXFP4).
 template <int KINDS, bool WORDS_OK>
 cudaError_t blocks_of(const DecParams *p, int grid, size_t smem, cudaStream_t s, int *blocks_per_sm) {
     cudaError_t e = cudaFuncSetAttribute(decode_blocks_kernel<KINDS, WORDS_OK>,
@@ -972,8 +999,10 @@ cudaError_t blocks_dispatch(const DecParams &p, int grid, size_t smem, cudaStrea
     const int k = decode_kinds(p);
     bool words = false;
     for (int i = 0; i < p.nstacks; ++i)
-        if (p.st[i].kind == CSF_NVFP4 && p.st[i].C % 4 == 0 && p.st[i].C >= kLaneNv) words = true;
-    if (k == kKindsMx) return blocks_of<kKindsMx, false>(&p, grid, smem, s, blocks_per_sm);
+        if (p.st[i].C % 4 == 0 && p.st[i].C >= (p.st[i].kind == CSF_NVFP4 ? kLaneNv : kLaneMx)) words = true;
+    if (k == kKindsMx)
+        return words ? blocks_of<kKindsMx, true>(&p, grid, smem, s, blocks_per_sm)
+                     : blocks_of<kKindsMx, false>(&p, grid, smem, s, blocks_per_sm);
     if (k == kKindsNv)
         return words ? blocks_of<kKindsNv, true>(&p, grid, smem, s, blocks_per_sm)
                      : blocks_of<kKindsNv, false>(&p, grid, smem, s, blocks_per_sm);

@@ -495,3 +495,34 @@ def test_word_wise_and_general_segments_in_one_launch(csf, C):
     want, status = oracle.decode_blocked(enc)
     assert status == oracle.OK and np.array_equal(_np(sf), want)
     assert st.errors() == 0
+
+
+def _mx_low_and_high_base_stack(seed, E, R, C, high_experts):
+    # MXFP4-shaped rows: base + {0, 1} for 85% of entries, else random; bases
+    # low except in `high_experts`, whose rows centre on 254 / 255 (bases
+    # above 254 reach the general loop).
+    rng = np.random.default_rng(seed)
+    centre = rng.integers(100, 130, size=(E, R, 1))
+    centre[list(high_experts)] = rng.integers(254, 256, size=(len(high_experts), R, 1))
+    vals = np.minimum(centre + rng.integers(0, 2, size=(E, R, C)), 255)
+    repl = rng.integers(0, 256, size=(E, R, C))
+    return np.where(rng.random((E, R, C)) < 0.15, repl, vals).astype(np.uint8)
+
+
+@pytest.mark.parametrize("C", [64, 128, 132, 160])
+def test_mxfp4_word_wise_and_general_segments_in_one_launch(csf, C):
+    E, R = 5, 260
+    dense = _mx_low_and_high_base_stack(23 + C, E, R, C, high_experts=(1, 4))
+    enc = oracle.encode(1, dense)
+    assert (enc["base"] > 254).any() and (enc["base"] <= 254).any()
+    st = csf.upload(enc)
+    assert np.array_equal(_np(csf.decode(st)), dense)
+    start = torch.from_numpy(np.array([0, 2, 3, 3, 5, 8], np.int64)).cuda()       # experts 0, 1, 3, 4
+    ws = torch.full(dense.shape, 0xFF, dtype=torch.uint8, device="cuda")
+    csf.decode(st, ws, expert_start=start)
+    want, status = oracle.decode(enc, start.cpu().numpy(), np.full(dense.shape, 0xFF, np.uint8))
+    assert status == oracle.OK and np.array_equal(_np(ws), want)
+    sf = csf.decode(st, layout=csf.LAYOUT_BLOCKED)
+    want, status = oracle.decode_blocked(enc)
+    assert status == oracle.OK and np.array_equal(_np(sf), want)
+    assert st.errors() == 0
