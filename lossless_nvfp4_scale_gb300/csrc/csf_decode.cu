@@ -332,20 +332,28 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                 // At most two row boundaries in the 64 elements (at b and b + C).
                 const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u, D = cD * 0x01010101u;
                 const int b2 = b + (int)C;
+                // One branch per chunk (bases above 240 are rare): plain adds,
+                // or carry-free byte adds.
+                auto two_rows = [&](auto plain) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t x = cw[i];
-                    const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
-                    fl[i] = escape_flags8(lo4, hi4);
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t x = cw[i];
+                        const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
+                        fl[i] = escape_flags8(lo4, hi4);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int k = 2 * i + h;
-                        const uint32_t m1 = bytes_from(b, k), m2 = bytes_from(b2, k);
-                        const uint32_t bw = (((A & ~m1) | (B & m1)) & ~m2) | (D & m2);
-                        const uint32_t o = __byte_perm(lo4, hi4, h ? 0x7362 : 0x5140);
-                        out[k] = (cA <= 240u && cB <= 240u && cD <= 240u) ? bw + o : add_base(bw, o);
+                        for (int h = 0; h < 2; ++h) {
+                            const int k = 2 * i + h;
+                            const uint32_t m1 = bytes_from(b, k), m2 = bytes_from(b2, k);
+                            const uint32_t bw = (((A & ~m1) | (B & m1)) & ~m2) | (D & m2);
+                            const uint32_t o = __byte_perm(lo4, hi4, h ? 0x7362 : 0x5140);
+                            out[k] = decltype(plain)::value ? bw + o : add_base(bw, o);
+                        }
                     }
-                }
+                };
+                if (cA <= 240u && cB <= 240u && cD <= 240u)
+                    two_rows(std::true_type{});
+                else
+                    two_rows(std::false_type{});
             } else {
                 uint32_t bw[16];
                 base_words_general<16>(bw, cA, b, S.base, row_a + crr + 1, S.rows, C);

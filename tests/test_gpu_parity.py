@@ -471,11 +471,13 @@ def _low_and_high_base_stack(seed, E, R, C, high_experts):
     return np.where(rng.random((E, R, C)) < 0.03, repl, vals).astype(np.uint8)
 
 
-@pytest.mark.parametrize("C", [64, 68, 100])
+@pytest.mark.parametrize("C", [20, 50, 64, 66, 68, 100])
 def test_word_wise_and_general_segments_in_one_launch(csf, C):
-    # With C a multiple of 4 and at least 64, a warp segment whose bases are
-    # all <= 240 takes the word-wise expansion and the others the general one;
-    # both kinds of segment meet in every launch below.
+    # A warp segment whose bases are all <= 240 takes plain adds: the
+    # word-wise expansion when C is a multiple of 4 and at least 64, else the
+    # plain-add variant of the general expansion (C < 32, 32 <= C < 64, and
+    # C >= 64 with boundaries inside words); segments with a higher base take
+    # the general loop.  Both kinds of segment meet in every launch below.
     E, R = 6, 300
     dense = _low_and_high_base_stack(11 + C, E, R, C, high_experts=(3, 5))
     enc = oracle.encode(0, dense)
