@@ -134,6 +134,27 @@ def timed_steps(torch, fn, steps, warmup, per_graph=16):
     return e0.elapsed_time(e1), reps * per_graph
 
 
+def single_launches(torch, fn, n, flush):
+    """`n` launches of `fn`, each timed alone with CUDA events on the launching
+    stream after `flush` (a buffer of twice the L2 size) is read, outside the
+    events.  Reading it evicts every line, and any write-back of dirty lines
+    happens before the start event, so each launch starts from a cold, clean
+    L2.  The flush also keeps the stream busy while the host enqueues the
+    start event and the launch, so the events bracket the kernel only.
+    Returns the per-launch times in ms (three untimed launches first)."""
+    out = []
+    for i in range(n + 3):
+        flush.sum()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn(i)
+        e1.record()
+        out.append((e0, e1))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in out[3:]]
+
+
 def reduce_max(torch, dist, value, device):
     """Maximum of a per-rank float over all ranks (the job's time is its slowest
     rank's); no data-path collective exists, this is timing only."""
@@ -287,6 +308,22 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm, max_steps):
     none = torch.zeros(E + 1, dtype=start.dtype, device="cuda")
     floor = timed_steps(torch, lambda i: csf.decode(gate, ws, expert_start=none), n(400), 20)
     rows["routed_8of512"]["no_active_expert_us"] = round(1e3 * floor[0] / floor[1], 3)
+
+    # the gate decode one launch at a time: L2 flushed (a 258 MB read) before
+    # each launch (median of 50), and warm (one copy decoded back to back, so its 80 MB
+    # stay largely in the 129 MB L2; may exceed the HBM bound)
+    flush = torch.ones(2 * 129 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda")
+    ts = sorted(single_launches(torch, lambda i: csf.decode(gate, ws), 50, flush))
+    med = ts[len(ts) // 2]
+    alg = stack_traffic(gate)
+    rows["gate_single_launch"] = {"l2": "flushed (2 x L2 read)", "n": len(ts), "median_us": round(1e3 * med, 3),
+                                  "p10_us": round(1e3 * ts[len(ts) // 10], 3),
+                                  "p90_us": round(1e3 * ts[(9 * len(ts)) // 10], 3),
+                                  "GB_s": round(alg / (med / 1e3) / 1e9, 1),
+                                  "hbm_frac": round(alg / (med / 1e3) / 1e9 / hbm, 4)}
+    del flush
+    durs = timed_steps(torch, lambda i: csf.decode(gate, ws), n(400), 20)
+    rec("gate_warm", durs, alg, {"l2": "warm"})
 
     # gate half of every expert (rows [0, R/2): the stack read as fused
     # gate/up), rotating over 4 copies (4 x 40 MB of inputs > L2)
