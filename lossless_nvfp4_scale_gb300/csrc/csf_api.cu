@@ -342,7 +342,8 @@ csf_status csf_prepare(const uint8_t *dense, csf_stack *out, uint64_t exc_capaci
     if ((reinterpret_cast<uintptr_t>(scratch) & 7u) != 0) return CSF_ERR_ARG;
     if (g.cols >= 65536) return CSF_ERR_UNSUPPORTED;
     const int32_t tr = prepare_tile_rows(g.kind, g.cols);
-    const size_t smem = prepare_smem_bytes(g.kind, g.cols, tr);
+    const bool staged = prepare_stages_rows(g.kind, g.cols, dense);
+    const size_t smem = prepare_smem_bytes(g.kind, g.cols, tr, staged);
     if (smem > 200 * 1024 || (uint64_t)tr * g.cols >= (1ull << 24)) return CSF_ERR_UNSUPPORTED;
     const uint64_t need = prepare_scratch_bytes(&g, rows);
     if (scratch_bytes < need) return CSF_ERR_SIZE;
@@ -360,7 +361,7 @@ csf_status csf_prepare(const uint8_t *dense, csf_stack *out, uint64_t exc_capaci
         return CSF_ERR_CUDA;
     }
     PrepParams p;
-    make_prep_params(p, dense, *out, exc_capacity, scratch, rows, n);
+    make_prep_params(p, dense, *out, exc_capacity, scratch, rows, n, staged);
     if (launch_prepare(p, smem, s) != cudaSuccess) {
         cudaGetLastError();
         return CSF_ERR_CUDA;

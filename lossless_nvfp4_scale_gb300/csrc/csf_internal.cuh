@@ -84,7 +84,7 @@ struct PrepParams {
     uint32_t smem_dense;         // byte sizes of the dynamic smem regions
     uint32_t smem_planes;
     int32_t stride;              // row stride of the staged tile (row-wise kernel)
-    int32_t pad_;
+    int32_t stage;               // row-wise kernel: stage the tile in shared memory (else read rows from L1/L2)
 };
 
 // Rows per unit so that a unit's first element starts a whole chunk.
@@ -148,8 +148,9 @@ cudaError_t launch_tiled_decode(const DecStack &S, const TiledIn &I, int grid, s
 
 cudaError_t launch_prepare(const PrepParams &p, size_t smem, cudaStream_t s);
 void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity,
-                      void *scratch, uint64_t rows, uint64_t n);
-size_t prepare_smem_bytes(int32_t kind, int32_t C, int32_t tr);
+                      void *scratch, uint64_t rows, uint64_t n, bool staged);
+size_t prepare_smem_bytes(int32_t kind, int32_t C, int32_t tr, bool staged);
+bool prepare_stages_rows(int32_t kind, int32_t C, const void *dense);
 int32_t prepare_tile_rows(int32_t kind, int32_t C);
 
 }  // namespace csfk

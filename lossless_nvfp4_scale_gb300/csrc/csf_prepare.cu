@@ -376,7 +376,11 @@ constexpr int kRowTile = 128;
 // (byte prefix sums for NVFP4, neighbour sums for MXFP4), and the packed
 // 16-bit key (count << 8 | 255 - value) whose maximum is the most bytes with
 // the smallest value.  The histogram area is reused to stage the tile's
-// exception bytes in row-major order for one coalesced copy-out.
+// exception bytes in row-major order for one coalesced copy-out.  The tile's
+// dense rows are staged in shared memory with one coalesced read, unless that
+// would leave fewer than 4 blocks per SM (prepare_stages_rows): then each
+// thread reads its row in place, as 4-byte words through L1.
+template <bool STAGE>
 __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_constant__ PrepParams P) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ unsigned int s_tile;
@@ -408,12 +412,13 @@ __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_con
     const uint64_t e0 = r0 * C;
     const uint32_t ne = (uint32_t)nr * C;
 
-    // 1. Zero the histograms and planes; stage the rows at `stride`.
+    // 1. Zero the histograms and planes; stage the rows at `stride` (unless
+    //    the rows are read in place: C % 4 == 0, 4-byte aligned dense).
     for (int i = tid; i < 64 * kRowTile / 4; i += kRowTile)
         reinterpret_cast<uint4 *>(s_hist)[i] = make_uint4(0, 0, 0, 0);
     for (uint32_t i = tid; i < P.smem_planes / 16; i += kRowTile)
         reinterpret_cast<uint4 *>(s_planes)[i] = make_uint4(0, 0, 0, 0);
-    {
+    if (STAGE) {
         const uint8_t *src = P.dense + e0;
         if (stride == C) {
             uint32_t done = 0;
@@ -451,7 +456,7 @@ __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_con
     // 2. Base byte and exception count of this thread's row.
     uint32_t base = 0, count = 0;
     if (tid < nr) {
-        const uint8_t *row = s_dense + tid * stride;
+        const uint8_t *row = STAGE ? s_dense + tid * stride : P.dense + (r0 + (uint64_t)tid) * C;
         uint32_t *h = s_hist + tid;
         uint32_t occ = 0;
         // Shared-memory reductions (no returned value): increments of the same
@@ -460,7 +465,7 @@ __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_con
             atomicAdd(h + (v >> 2) * kRowTile, 1u << ((v & 3u) << 3));
             occ |= 1u << (v >> 3);
         };
-        if ((stride & 3u) == 0) {
+        if (!STAGE || (stride & 3u) == 0) {
             const uint32_t *rw = reinterpret_cast<const uint32_t *>(row);
             for (uint32_t k = 0; k < C / 4; ++k) {
                 const uint32_t x = rw[k];
@@ -533,7 +538,7 @@ __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_con
 
     // 5. Pack this row's planes; stage its exceptions at their tile position.
     if (tid < nr) {
-        const uint8_t *row = s_dense + tid * stride;
+        const uint8_t *row = STAGE ? s_dense + tid * stride : P.dense + (r0 + (uint64_t)tid) * C;
         uint32_t pos = pre;
         uint32_t el = (uint32_t)tid * C;   // tile-local element index
         const uint32_t w = nv ? 14u : 1u;
@@ -592,7 +597,7 @@ __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_con
                 acc = ax = 0;
             }
         };
-        if ((stride & 3u) == 0 && (el & 3u) == 0) {
+        if ((!STAGE || (stride & 3u) == 0) && (el & 3u) == 0) {
             // Whole words; groups of 4 never straddle an output word.
             const uint32_t *rw = reinterpret_cast<const uint32_t *>(row);
             for (uint32_t k = 0; k < C / 4; ++k) {
@@ -682,16 +687,36 @@ static uint32_t planes_bytes(int32_t kind, uint64_t te) {
     return kind == CSF_NVFP4 ? round16((te + 1) / 2) : 2 * round16((te + 7) / 8);
 }
 
-size_t prepare_smem_bytes(int32_t kind, int32_t C, int32_t tr) {
+size_t prepare_smem_bytes(int32_t kind, int32_t C, int32_t tr, bool staged) {
     const uint64_t te = (uint64_t)tr * C;
     if (rows_path(C))
-        return 256u * kRowTile + round16((uint64_t)kRowTile * rows_stride(C)) + planes_bytes(kind, te) + kRowTile +
-               4u * kRowTile;
+        return 256u * kRowTile + (staged ? round16((uint64_t)kRowTile * rows_stride(C)) : 0u) +
+               planes_bytes(kind, te) + kRowTile + 4u * kRowTile;
     return (size_t)round16(te) + planes_bytes(kind, te) + kWarps * 256 * 4 + (size_t)tr * 4 + round16(tr);
 }
 
+// The row-wise kernel stages its tile in shared memory (one coalesced read of
+// the dense rows) when 4 or more blocks per SM still fit; otherwise, and only
+// for rows it can read as aligned 4-byte words, each thread reads its row in
+// place.  Measured on the gate (C = 100: 4 blocks staged) staging is faster
+// (121 against 139 us); on MXFP4 384 x 2048 x 160 (3 blocks staged, 5 not)
+// reading in place is (272 against 343 us).
+bool prepare_stages_rows(int32_t kind, int32_t C, const void *dense) {
+    if (!rows_path(C)) return true;
+    if (C % 4 != 0 || (reinterpret_cast<uintptr_t>(dense) & 3u) != 0) return true;
+    const size_t smem = prepare_smem_bytes(kind, C, kRowTile, true);
+    int occ = 0;
+    if (cudaFuncSetAttribute(prepare_rows_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, prepare_rows_kernel<true>, kRowTile, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return occ >= 4;
+}
+
 void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity,
-                      void *scratch, uint64_t rows, uint64_t n) {
+                      void *scratch, uint64_t rows, uint64_t n, bool staged) {
     const csf_geometry &g = out.g;
     const int32_t tr = prepare_tile_rows(g.kind, g.cols);
     std::memset(&p, 0, sizeof p);
@@ -715,16 +740,17 @@ void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out,
     p.dense_aligned = (reinterpret_cast<uintptr_t>(dense) & 15u) == 0 ? 1 : 0;
     const uint64_t te = (uint64_t)tr * g.cols;
     p.stride = rows_path(g.cols) ? rows_stride(g.cols) : g.cols;
-    p.smem_dense = rows_path(g.cols) ? round16((uint64_t)kRowTile * p.stride) : round16(te);
+    p.stage = staged ? 1 : 0;
+    p.smem_dense = rows_path(g.cols) ? (staged ? round16((uint64_t)kRowTile * p.stride) : 0u) : round16(te);
     p.smem_planes = planes_bytes(g.kind, te);
 }
 
 cudaError_t launch_prepare(const PrepParams &p, size_t smem, cudaStream_t s) {
     if (rows_path(p.C)) {
-        cudaError_t e = cudaFuncSetAttribute(prepare_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        const auto kernel = p.stage ? prepare_rows_kernel<true> : prepare_rows_kernel<false>;
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        prepare_rows_kernel<<<(unsigned)p.num_tiles, kRowTile, smem, s>>>(p);
+        kernel<<<(unsigned)p.num_tiles, kRowTile, smem, s>>>(p);
         return cudaGetLastError();
     }
     if (smem > 48 * 1024) {

@@ -72,7 +72,8 @@ extern "C" csf_status csf_prepare_static(const uint8_t *dense, csf_stack *out, u
     if (g.kind == CSF_MXFP4 && (!out->escapes || !aligned16(out->escapes))) return CSF_ERR_ARG;
     if (exc_capacity > 0 && !out->exc_bytes) return CSF_ERR_ARG;
     const int32_t tr = prepare_tile_rows(g.kind, g.cols);
-    const size_t smem = prepare_smem_bytes(g.kind, g.cols, tr);
+    const bool staged = prepare_stages_rows(g.kind, g.cols, dense);
+    const size_t smem = prepare_smem_bytes(g.kind, g.cols, tr, staged);
     if (smem > 200 * 1024 || (uint64_t)tr * g.cols >= (1ull << 24)) return CSF_ERR_UNSUPPORTED;
     const uint64_t tiles = (rows + tr - 1) / tr;
     const uint64_t need = 16 + 8 * tiles;
@@ -94,7 +95,7 @@ extern "C" csf_status csf_prepare_static(const uint8_t *dense, csf_stack *out, u
         return CSF_ERR_CUDA;
     }
     PrepParams p;
-    make_prep_params(p, dense, *out, exc_capacity, scratch, rows, n);
+    make_prep_params(p, dense, *out, exc_capacity, scratch, rows, n, staged);
     if (launch_prepare(p, smem, s) != cudaSuccess) {
         cudaGetLastError();
         return CSF_ERR_CUDA;

@@ -528,3 +528,22 @@ def test_mxfp4_word_wise_and_general_segments_in_one_launch(csf, C):
     want, status = oracle.decode_blocked(enc)
     assert status == oracle.OK and np.array_equal(_np(sf), want)
     assert st.errors() == 0
+
+
+@pytest.mark.parametrize("kind,E,R,C", [(0, 3, 150, 128), (0, 2, 130, 200), (0, 2, 70, 252), (1, 3, 150, 160),
+                                        (1, 2, 100, 200)])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_prepare_rows_read_in_place_or_staged(csf, kind, E, R, C, offset):
+    # Wide rows of C % 4 == 0 leave too few blocks per SM with the tile staged
+    # in shared memory, so each thread reads its row in place; a dense pointer
+    # one byte off alignment takes the staged path.  Both give the oracle's
+    # streams, with a ragged last tile of rows.
+    dense = _small_dense(kind, E, R, C, seed=C + 17 * E)
+    enc = oracle.encode(kind, dense)
+    buf = torch.zeros(dense.size + offset, dtype=torch.uint8, device="cuda")
+    d = buf[offset:].view(E, R, C)
+    d.copy_(_dense_cuda(dense))
+    st = csf.prepare(d, kind)
+    torch.cuda.synchronize()
+    assert st.errors() == 0
+    assert_stack_matches(st, enc)
