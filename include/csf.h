@@ -365,6 +365,19 @@ csf_status csf_tiled_pack(const csf_stack *src, csf_tiled *dst, uint64_t exc_cap
 csf_status csf_tiled_decode(const csf_tiled *t, uint8_t *ws, size_t ws_bytes,
                             const void *expert_start, int expert_start_is_int64, void *stream);
 
+/*
+ * Failure-detection self-test of the prepare's bounded waits, synchronous.
+ * Runs the prepare kernel on a small internal stack (512 x 8 NVFP4, four
+ * 128-row tiles) whose first tile no block ever takes, so the next tile's
+ * decoupled look-back waits on a status word that nothing writes; with a poll
+ * limit of 4096 the wait gives up, the kernel finishes, and the device error
+ * word of the run is written to *error_word (CSF_DEV_ERR_TIMEOUT expected).
+ * Nothing faults or hangs, and the context stays usable.  Allocates and frees
+ * its own device memory on its own stream.
+ * Errors: CSF_ERR_ARG (NULL), CSF_ERR_CUDA.
+ */
+csf_status csf_selftest_lookback_timeout(uint32_t *error_word);
+
 #ifdef __cplusplus
 }
 #endif

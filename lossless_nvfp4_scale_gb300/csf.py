@@ -100,6 +100,8 @@ def _load():
     lib.csf_tiled_pack.restype = ctypes.c_int
     lib.csf_tiled_decode.argtypes = [ctypes.POINTER(CTiled), _c_vp, ctypes.c_size_t, _c_vp, ctypes.c_int, _c_vp]
     lib.csf_tiled_decode.restype = ctypes.c_int
+    lib.csf_selftest_lookback_timeout.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.csf_selftest_lookback_timeout.restype = ctypes.c_int
     return lib
 
 
@@ -438,3 +440,13 @@ def tiled_decode(t: Tiled, ws: torch.Tensor | None = None, expert_start: torch.T
     _check(lib.csf_tiled_decode(ctypes.byref(ct), ws.data_ptr(), ws.numel(), ptr, is64, _stream(stream)),
            "csf_tiled_decode")
     return ws
+
+
+def selftest_lookback_timeout() -> int:
+    """Run the library's failure-detection self-test of the prepare's bounded
+    look-back wait (a small internal stack whose first tile is never taken) and
+    return the device error word of that run; CSF_DEV_ERR_TIMEOUT is set when
+    the wait gave up as designed.  Synchronous."""
+    word = ctypes.c_uint32(0)
+    _check(lib.csf_selftest_lookback_timeout(ctypes.byref(word)), "csf_selftest_lookback_timeout")
+    return int(word.value)

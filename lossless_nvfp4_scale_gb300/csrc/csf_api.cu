@@ -508,4 +508,53 @@ csf_status csf_tiled_decode(const csf_tiled *t, uint8_t *ws, size_t ws_bytes, co
     return CSF_OK;
 }
 
+csf_status csf_selftest_lookback_timeout(uint32_t *error_word) {
+    if (!error_word) return CSF_ERR_ARG;
+    *error_word = 0;
+    // A 512 x 8 NVFP4 stack: four 128-row tiles.  The ticket counter starts at
+    // 1, so no block takes tile 0 and tile 1's look-back waits on a status word
+    // that nothing writes; with a short poll limit the wait gives up.
+    csf_stack st;
+    std::memset(&st, 0, sizeof st);
+    st.g.kind = CSF_NVFP4;
+    st.g.num_experts = 1;
+    st.g.rows = 512;
+    st.g.cols = 8;
+    const uint64_t rows = 512, n = 512 * 8;
+    const int32_t tr = prepare_tile_rows(st.g.kind, st.g.cols);
+    const size_t smem = prepare_smem_bytes(st.g.kind, st.g.cols, tr, true);
+    const uint64_t need = prepare_scratch_bytes(&st.g, rows);
+    uint8_t *mem = nullptr;
+    // dense 4096 B, base 512 B, offsets 2048 B, index 513 x 4 B, exceptions 4096 B, error word, scratch
+    const size_t off_dense = 0, off_base = 4096, off_offsets = 4608, off_index = 6656, off_exc = 8720,
+                 off_err = 12816, off_scratch = 12832;
+    if (cudaMalloc(&mem, off_scratch + need) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    cudaStream_t s = nullptr;
+    csf_status ret = CSF_OK;
+    const uint32_t one = 1;
+    PrepParams p;
+    st.base = mem + off_base;
+    st.offsets = mem + off_offsets;
+    st.exc_index = reinterpret_cast<uint32_t *>(mem + off_index);
+    st.exc_bytes = mem + off_exc;
+    st.error_word = reinterpret_cast<uint32_t *>(mem + off_err);
+    make_prep_params(p, mem + off_dense, st, 4096, mem + off_scratch, rows, n, true);
+    p.spin_limit = 4096;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaMemsetAsync(mem, 0, off_scratch + need, s) != cudaSuccess ||
+        cudaMemcpyAsync(mem + off_scratch, &one, sizeof one, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        launch_prepare(p, smem, s) != cudaSuccess ||
+        cudaMemcpyAsync(error_word, st.error_word, sizeof *error_word, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        ret = CSF_ERR_CUDA;
+    }
+    if (s) cudaStreamDestroy(s);
+    cudaFree(mem);
+    return ret;
+}
+
 }  // extern "C"

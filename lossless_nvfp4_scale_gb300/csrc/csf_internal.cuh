@@ -85,6 +85,8 @@ struct PrepParams {
     uint32_t smem_planes;
     int32_t stride;              // row stride of the staged tile (row-wise kernel)
     int32_t stage;               // row-wise kernel: stage the tile in shared memory (else read rows from L1/L2)
+    uint32_t spin_limit;         // polls before a look-back wait gives up (CSF_DEV_ERR_TIMEOUT)
+    uint32_t pad2_;
 };
 
 // Rows per unit so that a unit's first element starts a whole chunk.

@@ -44,7 +44,7 @@ constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr unsigned long long kFlagAgg = 1ull << 62;
 constexpr unsigned long long kFlagIncl = 2ull << 62;
 constexpr unsigned long long kValMask = (1ull << 62) - 1;
-constexpr int kSpinLimit = 1 << 22;   // polls before a look-back wait gives up
+constexpr uint32_t kSpinLimit = 1u << 22;   // polls before a look-back wait gives up (default)
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
@@ -102,9 +102,9 @@ __device__ unsigned long long lookback_exclusive(const PrepParams &P, uint64_t t
             unsigned long long v = kFlagIncl;   // before tile 0: inclusive zero
             if (idx >= 0) {
                 v = ld_acquire(&P.status[idx]);
-                int spins = 0;
+                uint32_t spins = 0;
                 while ((v >> 62) == 0) {
-                    if (++spins > kSpinLimit) { timed_out = true; v = kFlagAgg; break; }
+                    if (++spins > P.spin_limit) { timed_out = true; v = kFlagAgg; break; }
                     __nanosleep(64);
                     v = ld_acquire(&P.status[idx]);
                 }
@@ -741,6 +741,7 @@ void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out,
     const uint64_t te = (uint64_t)tr * g.cols;
     p.stride = rows_path(g.cols) ? rows_stride(g.cols) : g.cols;
     p.stage = staged ? 1 : 0;
+    p.spin_limit = kSpinLimit;
     p.smem_dense = rows_path(g.cols) ? (staged ? round16((uint64_t)kRowTile * p.stride) : 0u) : round16(te);
     p.smem_planes = planes_bytes(g.kind, te);
 }
