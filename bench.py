@@ -39,6 +39,7 @@ METRIC = "CSF decode µs & dense-scale GB/s per 512-expert stack; % of HBM roofl
 WORKLOAD = "gate 512x1024x100 NVFP4-CSF full-stack decode"
 FALLBACK_HBM_GBS = 6800.0
 ROTATE = 4           # stack/workspace copies (working set > L2)
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e nominal bandwidth (context beside the measured copy peak)
 
 
 def peak_hbm():
@@ -226,6 +227,7 @@ def run_own(args, rank, world, torch, dist):
         "us_per_stack": round(1e3 * ms_per_step, 3),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "peak_source": peak_kind,
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": profiled_traffic(), "algorithmic_bytes": int(alg)},
         "gpu_launches": steps,
         "wall_s": round(wall, 3),
