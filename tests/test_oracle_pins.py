@@ -264,19 +264,42 @@ def test_stream_sizes_closed_form(kind, E, R, C):
     assert enc["offsets"].size == sz["offsets"] and enc["base"].size == E * R
 
 
+def _golden_sizes():
+    """The size figures printed on the finegrained-kernels page (size
+    paragraph), from tests/golden/csf_sizes.txt: name -> (dense, compressed)."""
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "csf_sizes.txt")
+    out = {}
+    with open(path) as f:
+        for ln in f:
+            if ln.strip() and not ln.startswith("#"):
+                name, dense, comp, _unit = ln.split("\t")
+                out[name] = (float(dense), float(comp))
+    return out
+
+
 def test_size_against_pages_figures():
     # The size paragraph reports 28.68 MB (gate, C=100) and 27.99 MB (down,
     # C=50) for 52.43 MB dense per 512-expert stack.  Offsets (N/2) plus one
     # base byte per row must not exceed those, which a byte-per-scale or
     # 8-bit-offset layout would; the rest is the exception stream: the
     # implied exception rates must be "a few percent".
+    g = _golden_sizes()
     dense_bytes = 512 * 1024 * 100
-    for reported, C in ((28.68e6, 100), (27.99e6, 50)):
+    assert abs(g["gate_stack"][0] * 1e6 - dense_bytes) < 0.01e6
+    assert abs(g["down_stack"][0] * 1e6 - dense_bytes) < 0.01e6
+    for (_, reported_mb), C in ((g["gate_stack"], 100), (g["down_stack"], 50)):
+        reported = reported_mb * 1e6
         rows = dense_bytes // C
         fixed = dense_bytes / 2 + rows
         assert fixed < reported
         rate = (reported - fixed) / dense_bytes
         assert 0.005 < rate < 0.05
+    # The whole checkpoint's planes (gate, up and down of every layer) shrink
+    # from 7.03 to 3.69 GiB: above the 4-bit floor of one half, by less than a
+    # base byte per 16 scales plus a few percent of exceptions.
+    dense, comp = g["all_planes"]
+    assert 0.5 < comp / dense < 0.5 + 1 / 16 + 0.05
     # A synthetic gate-shaped stack at a few percent exceptions lands in the
     # pages' 53-55% band, and its size is the closed form exactly.
     dense = synth.gate_stack(E=8, replace_p=0.039)
