@@ -789,7 +789,23 @@ __global__ void __launch_bounds__(kThreads, CSF_DECODE_MIN_BLOCKS) decode_kernel
     const uint64_t W = (uint64_t)gridDim.x * kWarps;
     const uint64_t w = (uint64_t)blockIdx.x * kWarps + warp;
     uint64_t u = T * w / W;
-    const uint64_t ub = T * (w + 1) / W;
+    uint64_t ub = T * (w + 1) / W;
+    if (PER_EXPERT && P.uniform && P.nstacks == 1 && n_act > 0 && W >= n_act && W < (1u << 13) &&
+        P.st[0].upe < (1u << 19) && !(P.st[0].r_lo == 0 && P.st[0].r_hi == P.st[0].R)) {
+        // A row range of every selected expert (segments cannot run on from
+        // one expert to the next): whole warps per expert, so that no warp's
+        // range straddles two experts and pays a second segment start.  With
+        // fewer than 2^13 warps and 2^19 units per expert every product below
+        // fits in 32 bits.
+        const uint32_t U = P.st[0].upe, wpe = (uint32_t)W / n_act, j = (uint32_t)w / wpe;
+        if (j >= n_act) {
+            u = ub = 0;
+        } else {
+            const uint32_t k = (uint32_t)w - j * wpe;
+            u = (uint64_t)j * U + U * k / wpe;
+            ub = (uint64_t)j * U + U * (k + 1) / wpe;
+        }
+    }
     while (u < ub) {
         const int s = (u < T0) ? 0 : 1;
         const DecStack &S = P.st[s];
