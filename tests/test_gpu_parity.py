@@ -547,3 +547,37 @@ def test_prepare_rows_read_in_place_or_staged(csf, kind, E, R, C, offset):
     torch.cuda.synchronize()
     assert st.errors() == 0
     assert_stack_matches(st, enc)
+
+
+@pytest.mark.parametrize("Cm", [160, 33])
+@pytest.mark.parametrize("routed", [False, True])
+@pytest.mark.parametrize("layout", ["rows", "blocked"])
+@pytest.mark.parametrize("half", [False, True])
+def test_pair_of_different_kinds(csf, Cm, routed, layout, half):
+    # A pair may mix kinds (an NVFP4 stack and an MXFP4 one, different R and C):
+    # the launch runs the kernel instance that holds both segment decoders,
+    # whole-stack or per expert (routing, the gate half of a fused stack).
+    E = 5
+    gu = _small_dense(0, E, 256, 100, seed=31)                 # fused gate/up, gate half decoded
+    mx = _small_dense(1, E, 300, Cm, seed=32)
+    genc, menc = oracle.encode(0, gu), oracle.encode(1, mx)
+    g_up, m_up = csf.upload(genc), csf.upload(menc)
+    start = np.array([0, 1, 1, 4, 4, 6], np.int32) if routed else None
+    es = None if start is None else torch.from_numpy(start).cuda()
+    gr = (0, 128) if half else None
+    if layout == "rows":
+        gws = torch.full(gu.shape, 0x3C, dtype=torch.uint8, device="cuda")
+        mws = torch.full(mx.shape, 0x3C, dtype=torch.uint8, device="cuda")
+        csf.decode_pair(g_up, m_up, gws, mws, expert_start=es, gate_rows=gr)
+        gw, gs = oracle.decode(genc, start, np.full(gu.shape, 0x3C, np.uint8), rows=gr)
+        mw, ms = oracle.decode(menc, start, np.full(mx.shape, 0x3C, np.uint8))
+    else:
+        gws = torch.full((oracle.blocked_bytes(E, 256, 100),), 0x3C, dtype=torch.uint8, device="cuda")
+        mws = torch.full((oracle.blocked_bytes(E, 300, Cm),), 0x3C, dtype=torch.uint8, device="cuda")
+        csf.decode_pair(g_up, m_up, gws, mws, expert_start=es, gate_rows=gr, layout=csf.LAYOUT_BLOCKED)
+        gw, gs = oracle.decode_blocked(genc, start, np.full(gws.numel(), 0x3C, np.uint8), rows=gr)
+        mw, ms = oracle.decode_blocked(menc, start, np.full(mws.numel(), 0x3C, np.uint8))
+    assert gs == oracle.OK and ms == oracle.OK
+    assert np.array_equal(_np(gws).ravel(), gw.ravel())
+    assert np.array_equal(_np(mws).ravel(), mw.ravel())
+    assert g_up.errors() == 0 and m_up.errors() == 0
