@@ -36,7 +36,7 @@ def _dense(kind, E, R, C, seed, replace_p=0.08):
 
 SHAPES = [(0, 1, 1, 1), (0, 2, 128, 4), (0, 3, 200, 7), (0, 2, 256, 100), (0, 3, 300, 50), (0, 2, 1000, 100),
           (0, 2, 640, 12), (0, 1, 129, 255), (0, 2, 130, 600), (1, 2, 130, 160), (1, 3, 64, 33), (1, 2, 512, 160),
-          (0, 1, 128, 2000), (1, 2, 100, 17)]
+          (0, 1, 128, 2000), (1, 2, 100, 17), (1, 2, 130, 300), (1, 1, 200, 1000)]
 
 
 @pytest.mark.parametrize("kind,E,R,C", SHAPES)
@@ -54,7 +54,8 @@ def test_blocked_matches_oracle_poisoned(csf, kind, E, R, C):
     assert up.errors() == 0
 
 
-@pytest.mark.parametrize("kind,E,R,C", [(0, 4, 300, 100), (1, 3, 384, 160), (0, 5, 512, 50)])
+@pytest.mark.parametrize("kind,E,R,C", [(0, 4, 300, 100), (1, 3, 384, 160), (0, 5, 512, 50), (0, 3, 384, 400),
+                                        (1, 3, 300, 520)])
 @pytest.mark.parametrize("routed", [False, True])
 def test_blocked_row_blocks_and_routing(csf, kind, E, R, C, routed):
     dense = _dense(kind, E, R, C, seed=R + C)
