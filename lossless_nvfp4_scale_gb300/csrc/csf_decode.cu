@@ -330,8 +330,13 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                 }
             } else if (C >= 32) {
                 // At most two row boundaries in the 64 elements (at b and b + C).
-                const uint32_t A = cA * 0x01010101u, B = cB * 0x01010101u, D = cD * 0x01010101u;
-                const int b2 = b + (int)C;
+                // The three row bases sit in bytes 0..2 of P3.  For 8 elements
+                // at a time, nibble j of `rows` is the row (0, 1 or 2) of
+                // element j: a 1 from each boundary at or before it, as clamped
+                // funnel shifts of 0x11111111; a byte permute of P3 by it gives
+                // a word's four bases.
+                const uint32_t P3 = cA | (cB << 8) | (cD << 16);
+                const int s1 = 4 * b, s2 = 4 * (b + (int)C);
                 // One branch per chunk (bases above 240 are rare): plain adds,
                 // or carry-free byte adds.
                 auto two_rows = [&](auto plain) {
@@ -340,14 +345,12 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                         const uint32_t x = cw[i];
                         const uint32_t lo4 = x & 0x0F0F0F0Fu, hi4 = (x >> 4) & 0x0F0F0F0Fu;
                         fl[i] = escape_flags8(lo4, hi4);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int k = 2 * i + h;
-                            const uint32_t m1 = bytes_from(b, k), m2 = bytes_from(b2, k);
-                            const uint32_t bw = (((A & ~m1) | (B & m1)) & ~m2) | (D & m2);
-                            const uint32_t o = __byte_perm(lo4, hi4, h ? 0x7362 : 0x5140);
-                            out[k] = decltype(plain)::value ? bw + o : add_base(bw, o);
-                        }
+                        const uint32_t rows = __funnelshift_lc(0u, 0x11111111u, (uint32_t)max(s1 - 32 * i, 0)) +
+                                              __funnelshift_lc(0u, 0x11111111u, (uint32_t)max(s2 - 32 * i, 0));
+                        const uint32_t bw0 = __byte_perm(P3, 0, rows), bw1 = __byte_perm(P3, 0, rows >> 16);
+                        const uint32_t o0 = __byte_perm(lo4, hi4, 0x5140), o1 = __byte_perm(lo4, hi4, 0x7362);
+                        out[2 * i] = decltype(plain)::value ? bw0 + o0 : add_base(bw0, o0);
+                        out[2 * i + 1] = decltype(plain)::value ? bw1 + o1 : add_base(bw1, o1);
                     }
                 };
                 if (cA <= 240u && cB <= 240u && cD <= 240u)
