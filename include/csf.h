@@ -50,7 +50,9 @@
  *   - All buffer pointers are DEVICE pointers owned by the caller; the library
  *     never allocates or frees device memory.  Calls are asynchronous on
  *     `stream` (a cudaStream_t; NULL = the legacy default stream) and never
- *     synchronise the host.
+ *     synchronise the host.  The one exception is the self-test
+ *     csf_selftest_lookback_timeout, which allocates, runs and synchronises
+ *     on its own.
  *   - The return value reports argument and launch errors only.  Data errors
  *     found on the device (a corrupt index, a full exception buffer, a bounded
  *     wait that gave up) are OR-ed into the optional device word
