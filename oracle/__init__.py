@@ -2,7 +2,8 @@
 
 Plain, slow, single-threaded reference of what the CSF method computes
 (encode, decode, routed and row-range decode, decode into the block-scaled
-GEMM scale layout, index check), written in plain C
+GEMM scale layout, the tile-packed form and its decode, index check), written
+in plain C
 (``csf_oracle.c``) and reached through ``ctypes``.  Only the test suite, the
 smoke check and the benchmark's CPU-baseline leg may import this package.  It
 shares no code with the CUDA library, and the product path never routes

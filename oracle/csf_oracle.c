@@ -41,6 +41,10 @@
  *     written (the gate half of a fused gate/up expert is rows [0, R/2)).
  *   - blocked decode: the same bytes placed in the 128 x 4 tiled scale-operand
  *     layout of block-scaled GEMMs (see blocked_offset), padding written 0.
+ *   - tile-packed form: the same bases, codes and exception bytes reordered so
+ *     that each 128 x 4 tile of that layout decodes on its own ([B478] commit
+ *     message on stage-readable compressed scales; layout in csfo_tiled_pack),
+ *     and its decode into the blocked layout.
  */
 #include <stdint.h>
 #include <stdlib.h>
