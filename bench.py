@@ -355,9 +355,16 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm, max_steps):
         {"packed_MB": round(packed / 1e6, 3), "pack_us": round(1e3 * pk[0] / pk[1], 1)})
     del bc, bw, tps
 
-    # paired gate + down
+    # the down stack alone (C = 50: lane chunks span up to three rows), then
+    # paired with the gate
     down_dense = torch.from_numpy(synth.down_stack(seed=0)).cuda()
     down = csf.prepare(down_dense, csf.NVFP4)
+    dc = [down] + [clone_stack(torch, down) for _ in range(3)]
+    dw = [torch.empty_like(down_dense) for _ in range(4)]
+    durs = timed_steps(torch, lambda i: csf.decode(dc[i % 4], dw[i % 4]), n(400), 20)
+    assert torch.equal(dw[0], down_dense)
+    rec("decode_down", durs, stack_traffic(down))
+    del dc, dw
     gws, dws = torch.empty_like(gate_dense), torch.empty_like(down_dense)
     g2, d2 = clone_stack(torch, gate), clone_stack(torch, down)
     gws2, dws2 = torch.empty_like(gate_dense), torch.empty_like(down_dense)
