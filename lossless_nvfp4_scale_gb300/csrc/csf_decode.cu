@@ -32,14 +32,22 @@
 //   * Lanes read 256-bit pieces of the offset stream (coalesced across the
 //     warp), prefetching the next piece while the current one is expanded
 //     with byte permutes (NVFP4) or a bit-to-byte spreading multiply (MXFP4)
-//     and carry-free byte adds of the row bases.
+//     and the row bases added byte by byte.  A segment whose bases cannot
+//     carry out of a byte, with row boundaries on word boundaries, runs a
+//     loop instance that holds only the word-wise expansion (one base select
+//     and a plain 32-bit add per word); other segments run the general loop.
+//     Chunks spanning three rows (32 <= C < 64) take each word's bases with
+//     one byte permute of the three packed bases.
 //   * Escapes are patched in a lane-private, bank-swizzled shared-memory slot
 //     (one byte store each); each 32 dense bytes leave with one 256-bit store.
 //   * Per-expert mode (routing and/or row ranges): every block compacts the
 //     active experts of `expert_start` (all experts without it) into shared
 //     memory with ballots and prefix sums, each with the units that hold its
 //     rows [r_lo, r_hi); units of inactive experts and of rows outside the
-//     range never exist, so those workspace bytes are never written.
+//     range never exist, so those workspace bytes are never written.  With a
+//     partial row range every expert gets whole warps.
+//   * The kernel is instantiated per kind (NVFP4, MXFP4, or both for a
+//     mixed pair), so a launch carries only the decoders it uses.
 //   * A unit whose rows straddle an expert or range boundary (R*C not a
 //     multiple of the lane chunk) is decoded whole but stored only inside the
 //     selected rows.
