@@ -43,33 +43,39 @@ _c_vp = ctypes.c_void_p
 
 
 class Geometry(ctypes.Structure):
+    """csf_geometry: kind, experts E, rows R per expert, scale bytes C per row."""
     _fields_ = [("kind", _c_i32), ("num_experts", _c_i32), ("rows", _c_i32), ("cols", _c_i32)]
 
 
 class Sizes(ctypes.Structure):
+    """csf_sizes_t: allocation sizes in bytes for one geometry."""
     _fields_ = [("dense", _c_u64), ("base", _c_u64), ("offsets", _c_u64), ("escapes", _c_u64),
                 ("exc_index", _c_u64), ("prepare_scratch", _c_u64), ("blocked", _c_u64),
                 ("tiled_codes", _c_u64), ("tiled_bases", _c_u64), ("tiled_index", _c_u64)]
 
 
 class CStack(ctypes.Structure):
+    """csf_stack: the device buffers of a compressed stack."""
     _fields_ = [("g", Geometry), ("base", _c_vp), ("offsets", _c_vp), ("escapes", _c_vp),
                 ("exc_index", _c_vp), ("exc_bytes", _c_vp), ("num_exc", _c_u64),
                 ("error_word", _c_vp)]
 
 
 class CDecodePart(ctypes.Structure):
+    """csf_decode_part: one stack of a row-range or expansion call."""
     _fields_ = [("stack", ctypes.POINTER(CStack)), ("ws", _c_vp), ("ws_bytes", ctypes.c_size_t),
                 ("row_lo", _c_i32), ("row_hi", _c_i32), ("layout", _c_i32)]
 
 
 class CTiled(ctypes.Structure):
+    """csf_tiled: the device buffers of a tile-packed stack."""
     _fields_ = [("g", Geometry), ("codes", _c_vp), ("bases", _c_vp), ("tile_index", _c_vp),
                 ("exc_bytes", _c_vp), ("num_exc", _c_u64), ("error_word", _c_vp)]
 
 
 class CsfError(RuntimeError):
-    pass
+    """A csf_* call returned an error status, or its arguments were rejected
+    before the call."""
 
 
 def _load():
@@ -119,6 +125,7 @@ def _stream(stream) -> int:
 
 
 def sizes(kind: int, E: int, R: int, C: int) -> dict:
+    """csf_sizes for a geometry, as a dict of field name -> bytes."""
     g = Geometry(kind, E, R, C)
     out = Sizes()
     _check(lib.csf_sizes(ctypes.byref(g), ctypes.byref(out)), "csf_sizes")
@@ -188,6 +195,8 @@ def empty_stack(kind: int, E: int, R: int, C: int, exc_capacity: int = 0, device
 
 
 def prepare_scratch(kind: int, E: int, R: int, C: int, device=None) -> torch.Tensor:
+    """A device scratch buffer for prepare_async (its contents need no
+    initialisation: each prepare clears what it uses on its stream)."""
     n = sizes(kind, E, R, C)["prepare_scratch"]
     return torch.empty(_pad16(n), dtype=torch.uint8, device=device if device is not None else "cuda")
 
