@@ -446,3 +446,27 @@ def test_tiled_round_trip_equals_blocked_decode(kind, E, R, C):
     out, _ = oracle.tiled_decode(tp, start, np.full(nb, 0xAB, np.uint8))
     want, _ = oracle.decode_blocked(enc, start, np.full(nb, 0xAB, np.uint8))
     assert np.array_equal(out, want)
+
+
+@pytest.mark.parametrize("kind,E,R,C", [(0, 3, 300, 50), (1, 2, 260, 33), (0, 2, 128, 100)])
+def test_tiled_row_block_ranges_match_csf(kind, E, R, C):
+    # A 128-row block is a run of consecutive rows, so its exceptions take the
+    # same range of the tile-ordered stream as of CSF's row-major one: the
+    # tile index at a block's first tile is the CSF index at its first row,
+    # and the bytes in that range are the same bytes, reordered.  (The GPU
+    # conversion from CSF relies on this to place each block without a scan.)
+    w = W[kind]
+    dense = synth.random_rows(E * R + C, E * R, C, spread=w + 7, replace_p=0.12).reshape(E, R, C)
+    enc = oracle.encode(kind, dense)
+    tp = oracle.tiled_pack(enc)
+    nrb, ncb = -(-R // 128), -(-C // 4)
+    T = nrb * ncb
+    for e in range(E):
+        for rb in range(nrb):
+            r0 = e * R + 128 * rb
+            r1 = e * R + min(128 * (rb + 1), R)
+            lo, hi = int(enc["exc_index"][r0]), int(enc["exc_index"][r1])
+            t0 = e * T + rb * ncb
+            assert int(tp["tile_index"][t0]) == lo
+            assert int(tp["tile_index"][t0 + ncb]) == hi
+            assert sorted(tp["exc_bytes"][lo:hi].tolist()) == sorted(enc["exc_bytes"][lo:hi].tolist())
