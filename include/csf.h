@@ -186,9 +186,12 @@ csf_status csf_prepare(const uint8_t *dense, csf_stack *out, uint64_t exc_capaci
  * and the results are the same bytes.
  *
  * The first call on each device looks up the array's device address (with
- * that device current) and caches it; make that first call before any stream
- * capture.  Every call shares the one array and clears the part it uses on
- * `stream` first: calls that overlap on the GPU race, so order them.
+ * that device current) and caches it under the id of the current CUDA
+ * context; make that first call before any stream capture.  A device reset
+ * (cudaDeviceReset) destroys the context and the array with it: the next call
+ * runs in a new context and looks the address up again, as a first call.
+ * Every call shares the one array and clears the part it uses on `stream`
+ * first: calls that overlap on the GPU race, so order them.
  * Errors: as csf_prepare, plus CSF_ERR_SIZE when the geometry needs more than
  * CSF_STATIC_SCRATCH_BYTES of scratch (16 + 8 bytes per tile of rows; tiles
  * are 128 rows when C <= 255, so about 4 million rows).

@@ -8,6 +8,70 @@
 
 using namespace csfk;
 
+namespace csfk {
+
+csf_status check_geometry(const csf_geometry *g, uint64_t *n, uint64_t *rows) {
+    if (!g) return CSF_ERR_ARG;
+    if (g->kind != CSF_NVFP4 && g->kind != CSF_MXFP4) return CSF_ERR_ARG;
+    if (g->num_experts < 1 || g->rows < 1 || g->cols < 1) return CSF_ERR_ARG;
+    const uint64_t r = (uint64_t)g->num_experts * (uint64_t)g->rows;
+    const uint64_t e = r * (uint64_t)g->cols;
+    if (r >= (1ull << 31) || e >= (1ull << 40) || g->cols >= (1 << 24)) return CSF_ERR_UNSUPPORTED;
+    *n = e;
+    *rows = r;
+    return CSF_OK;
+}
+
+static bool is_aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+csf_status prepare_check(const uint8_t *dense, const csf_stack *out, uint64_t exc_capacity, PrepPlan *plan) {
+    if (!dense || !out) return CSF_ERR_ARG;
+    csf_status st = check_geometry(&out->g, &plan->n, &plan->rows);
+    if (st != CSF_OK) return st;
+    const csf_geometry &g = out->g;
+    if (!out->base || !out->offsets || !out->exc_index || !is_aligned16(out->offsets)) return CSF_ERR_ARG;
+    if (g.kind == CSF_MXFP4 && (!out->escapes || !is_aligned16(out->escapes))) return CSF_ERR_ARG;
+    if (exc_capacity > 0 && !out->exc_bytes) return CSF_ERR_ARG;
+    if (g.cols >= 65536) return CSF_ERR_UNSUPPORTED;
+    const int32_t tr = prepare_tile_rows(g.kind, g.cols);
+    if ((uint64_t)tr * g.cols >= (1ull << 24)) return CSF_ERR_UNSUPPORTED;
+    plan->scratch_bytes = 16 + 8 * ((plan->rows + tr - 1) / tr);
+    plan->staged = true;
+    plan->smem = 0;
+    return CSF_OK;
+}
+
+csf_status prepare_configure(const uint8_t *dense, const csf_geometry &g, PrepPlan *plan) {
+    const int32_t tr = prepare_tile_rows(g.kind, g.cols);
+    plan->staged = prepare_stages_rows(g.kind, g.cols, dense);
+    plan->smem = prepare_smem_bytes(g.kind, g.cols, tr, plan->staged);
+    if (plan->smem > 200 * 1024) return CSF_ERR_UNSUPPORTED;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, dense) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_ARG;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return CSF_ERR_ARG;
+    return CSF_OK;
+}
+
+csf_status prepare_enqueue(const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity, void *scratch,
+                           const PrepPlan &plan, cudaStream_t s) {
+    if (cudaMemsetAsync(scratch, 0, plan.scratch_bytes, s) != cudaSuccess) {   // ticket and status words start at 0
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    PrepParams p;
+    make_prep_params(p, dense, out, exc_capacity, scratch, plan.rows, plan.n, plan.staged);
+    if (launch_prepare(p, plan.smem, s) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    return CSF_OK;
+}
+
+}  // namespace csfk
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -51,18 +115,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 uint64_t round16(uint64_t v) { return (v + 15) & ~15ull; }
 
-csf_status geometry(const csf_geometry *g, uint64_t *n, uint64_t *rows) {
-    if (!g) return CSF_ERR_ARG;
-    if (g->kind != CSF_NVFP4 && g->kind != CSF_MXFP4) return CSF_ERR_ARG;
-    if (g->num_experts < 1 || g->rows < 1 || g->cols < 1) return CSF_ERR_ARG;
-    const uint64_t r = (uint64_t)g->num_experts * (uint64_t)g->rows;
-    const uint64_t e = r * (uint64_t)g->cols;
-    if (r >= (1ull << 31) || e >= (1ull << 40) || g->cols >= (1 << 24)) return CSF_ERR_UNSUPPORTED;
-    *n = e;
-    *rows = r;
-    return CSF_OK;
-}
+csf_status geometry(const csf_geometry *g, uint64_t *n, uint64_t *rows) { return check_geometry(g, n, rows); }
 
+// Look-back scratch of a prepare: a ticket counter (16 bytes) and one 8-byte
+// status word per tile of rows.
 uint64_t prepare_scratch_bytes(const csf_geometry *g, uint64_t rows) {
     const int32_t tr = prepare_tile_rows(g->kind, g->cols);
     const uint64_t tiles = (rows + tr - 1) / tr;
@@ -331,42 +387,15 @@ csf_status csf_sizes(const csf_geometry *g, csf_sizes_t *out) {
 
 csf_status csf_prepare(const uint8_t *dense, csf_stack *out, uint64_t exc_capacity, void *scratch,
                        size_t scratch_bytes, void *stream) {
-    if (!dense || !out || !scratch) return CSF_ERR_ARG;
-    uint64_t n = 0, rows = 0;
-    csf_status st = geometry(&out->g, &n, &rows);
+    if (!scratch) return CSF_ERR_ARG;
+    PrepPlan plan;
+    csf_status st = prepare_check(dense, out, exc_capacity, &plan);
     if (st != CSF_OK) return st;
-    const csf_geometry &g = out->g;
-    if (!out->base || !out->offsets || !out->exc_index || !aligned16(out->offsets)) return CSF_ERR_ARG;
-    if (g.kind == CSF_MXFP4 && (!out->escapes || !aligned16(out->escapes))) return CSF_ERR_ARG;
-    if (exc_capacity > 0 && !out->exc_bytes) return CSF_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(scratch) & 7u) != 0) return CSF_ERR_ARG;
-    if (g.cols >= 65536) return CSF_ERR_UNSUPPORTED;
-    const int32_t tr = prepare_tile_rows(g.kind, g.cols);
-    const bool staged = prepare_stages_rows(g.kind, g.cols, dense);
-    const size_t smem = prepare_smem_bytes(g.kind, g.cols, tr, staged);
-    if (smem > 200 * 1024 || (uint64_t)tr * g.cols >= (1ull << 24)) return CSF_ERR_UNSUPPORTED;
-    const uint64_t need = prepare_scratch_bytes(&g, rows);
-    if (scratch_bytes < need) return CSF_ERR_SIZE;
-
-    cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, dense) != cudaSuccess) {
-        cudaGetLastError();
-        return CSF_ERR_ARG;
-    }
-    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return CSF_ERR_ARG;
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) {
-        cudaGetLastError();
-        return CSF_ERR_CUDA;
-    }
-    PrepParams p;
-    make_prep_params(p, dense, *out, exc_capacity, scratch, rows, n, staged);
-    if (launch_prepare(p, smem, s) != cudaSuccess) {
-        cudaGetLastError();
-        return CSF_ERR_CUDA;
-    }
-    return CSF_OK;
+    if (scratch_bytes < plan.scratch_bytes) return CSF_ERR_SIZE;
+    st = prepare_configure(dense, out->g, &plan);
+    if (st != CSF_OK) return st;
+    return prepare_enqueue(dense, *out, exc_capacity, scratch, plan, static_cast<cudaStream_t>(stream));
 }
 
 csf_status csf_decode(const csf_stack *s, uint8_t *ws, size_t ws_bytes, const void *expert_start,

@@ -148,6 +148,26 @@ cudaError_t launch_tiled_pack(const DecStack &S, const TiledOut &O, int grid, cu
 cudaError_t tiled_decode_occupancy(int kind, size_t smem, int *blocks_per_sm);
 cudaError_t launch_tiled_decode(const DecStack &S, const TiledIn &I, int grid, size_t smem, cudaStream_t s);
 
+// Geometry checks shared by every entry point: sets N = E*R*C and rows = E*R.
+csf_status check_geometry(const csf_geometry *g, uint64_t *n, uint64_t *rows);
+
+// A checked prepare, shared by csf_prepare and csf_prepare_static:
+// prepare_check makes the host-only argument checks and sizes the look-back
+// scratch (no CUDA call); prepare_configure picks the launch configuration
+// (it may query the device); prepare_enqueue clears the scratch on `s` and
+// launches the kernel.
+struct PrepPlan {
+    uint64_t n;
+    uint64_t rows;
+    uint64_t scratch_bytes;   // ticket counter + one look-back word per tile
+    bool staged;
+    size_t smem;
+};
+csf_status prepare_check(const uint8_t *dense, const csf_stack *out, uint64_t exc_capacity, PrepPlan *plan);
+csf_status prepare_configure(const uint8_t *dense, const csf_geometry &g, PrepPlan *plan);
+csf_status prepare_enqueue(const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity, void *scratch,
+                           const PrepPlan &plan, cudaStream_t s);
+
 cudaError_t launch_prepare(const PrepParams &p, size_t smem, cudaStream_t s);
 void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity,
                       void *scratch, uint64_t rows, uint64_t n, bool staged);

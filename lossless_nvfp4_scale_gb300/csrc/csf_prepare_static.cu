@@ -12,13 +12,18 @@
 // passes the dense input and every output buffer.
 //
 // The array is CSF_STATIC_SCRATCH_BYTES (256 KiB) and exists on every GPU that
-// loads the library until the process exits.  Its host-side name is only a
-// stand-in for the device symbol, so the first call on each device looks up
-// the device address with cudaGetSymbolAddress (with that device current)
-// and caches it; make that first call before any stream capture.  Every call
-// shares the one array and clears the part it uses on the caller's stream
-// before the kernel, so calls that overlap on the GPU (different streams
-// without ordering) race and must not be issued.
+// loads the library, in every CUDA context the library's module is loaded
+// into, until that context is destroyed.  Its host-side name is only a
+// stand-in for the device symbol, so the first call in each context (normally
+// once per device, with that device current) looks up the device address with
+// cudaGetSymbolAddress and caches it under the context's unique id; make that
+// first call before any stream capture.  A device reset destroys the context:
+// the next call sees a new context id and looks the address up again rather
+// than reuse a stale one.  Every call shares the one array and clears the part
+// it uses on the caller's stream before the kernel, so calls that overlap on
+// the GPU (different streams without ordering) race and must not be issued.
+#include <cuda.h>
+
 #include <cstring>
 #include <mutex>
 
@@ -30,75 +35,88 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_prepare_scratch[CSF_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices];
+// Driver calls that name the current context, fetched through the runtime
+// (no link against the driver library).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
 
-// Device address of g_prepare_scratch on the current device (set up once per
-// device, with that device current).
+constexpr int kSlots = 64;
+struct Slot {
+    unsigned long long ctx_id;   // 0: empty
+    void *ptr;
+};
+
+std::mutex g_mu;
+Slot g_slots[kSlots];
+int g_next = 0;
+CtxGetCurrentFn g_get_current = nullptr;
+CtxGetIdFn g_get_id = nullptr;
+
+bool driver_calls() {
+    if (g_get_current && g_get_id) return true;
+    void *a = nullptr, *b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) != cudaSuccess ||
+        qa != cudaDriverEntryPointSuccess || qb != cudaDriverEntryPointSuccess || !a || !b) {
+        cudaGetLastError();
+        return false;
+    }
+    g_get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+    g_get_id = reinterpret_cast<CtxGetIdFn>(b);
+    return true;
+}
+
+// Unique id of the context current on this thread; 0 when none is current.
+bool current_context_id(unsigned long long *id) {
+    CUcontext ctx = nullptr;
+    if (g_get_current(&ctx) != CUDA_SUCCESS) return false;
+    *id = 0;
+    if (ctx == nullptr) return true;
+    return g_get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_prepare_scratch in the current context: looked up once
+// per context (with its device current) and cached under the context id.
 csf_status static_scratch(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!driver_calls()) return CSF_ERR_CUDA;
+    unsigned long long id = 0;
+    if (!current_context_id(&id)) return CSF_ERR_CUDA;
+    if (id != 0)
+        for (const Slot &s : g_slots)
+            if (s.ctx_id == id) {
+                *out = s.ptr;
+                return CSF_OK;
+            }
+    // Set-up: this runtime call also makes the device's primary context
+    // current when no context was, so the id is read again afterwards.
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_prepare_scratch);
+    if (e != cudaSuccess || p == nullptr) {
         cudaGetLastError();
         return CSF_ERR_CUDA;
     }
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_prepare_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return CSF_ERR_CUDA;
-        }
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    if (!current_context_id(&id) || id == 0) return CSF_ERR_CUDA;
+    g_slots[g_next] = Slot{id, p};
+    g_next = (g_next + 1) % kSlots;
+    *out = p;
     return CSF_OK;
 }
-
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
 extern "C" csf_status csf_prepare_static(const uint8_t *dense, csf_stack *out, uint64_t exc_capacity, void *stream) {
-    if (!dense || !out) return CSF_ERR_ARG;
-    const csf_geometry &g = out->g;
-    if (g.kind != CSF_NVFP4 && g.kind != CSF_MXFP4) return CSF_ERR_ARG;
-    if (g.num_experts < 1 || g.rows < 1 || g.cols < 1) return CSF_ERR_ARG;
-    const uint64_t rows = (uint64_t)g.num_experts * (uint64_t)g.rows;
-    const uint64_t n = rows * (uint64_t)g.cols;
-    if (rows >= (1ull << 31) || n >= (1ull << 40) || g.cols >= 65536) return CSF_ERR_UNSUPPORTED;
-    if (!out->base || !out->offsets || !out->exc_index || !aligned16(out->offsets)) return CSF_ERR_ARG;
-    if (g.kind == CSF_MXFP4 && (!out->escapes || !aligned16(out->escapes))) return CSF_ERR_ARG;
-    if (exc_capacity > 0 && !out->exc_bytes) return CSF_ERR_ARG;
-    const int32_t tr = prepare_tile_rows(g.kind, g.cols);
-    const bool staged = prepare_stages_rows(g.kind, g.cols, dense);
-    const size_t smem = prepare_smem_bytes(g.kind, g.cols, tr, staged);
-    if (smem > 200 * 1024 || (uint64_t)tr * g.cols >= (1ull << 24)) return CSF_ERR_UNSUPPORTED;
-    const uint64_t tiles = (rows + tr - 1) / tr;
-    const uint64_t need = 16 + 8 * tiles;
-    if (need > CSF_STATIC_SCRATCH_BYTES) return CSF_ERR_SIZE;   // stack too large for the built-in scratch
-
-    cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, dense) != cudaSuccess) {
-        cudaGetLastError();
-        return CSF_ERR_ARG;
-    }
-    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return CSF_ERR_ARG;
-
-    void *scratch = nullptr;
-    csf_status st = static_scratch(&scratch);
+    // Host-only checks first: a geometry the built-in scratch cannot hold is
+    // refused before any CUDA call.
+    PrepPlan plan;
+    csf_status st = prepare_check(dense, out, exc_capacity, &plan);
     if (st != CSF_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) {   // ticket and status words start at zero
-        cudaGetLastError();
-        return CSF_ERR_CUDA;
-    }
-    PrepParams p;
-    make_prep_params(p, dense, *out, exc_capacity, scratch, rows, n, staged);
-    if (launch_prepare(p, smem, s) != cudaSuccess) {
-        cudaGetLastError();
-        return CSF_ERR_CUDA;
-    }
-    return CSF_OK;
+    if (plan.scratch_bytes > CSF_STATIC_SCRATCH_BYTES) return CSF_ERR_SIZE;   // too large for the built-in scratch
+    st = prepare_configure(dense, out->g, &plan);
+    if (st != CSF_OK) return st;
+    void *scratch = nullptr;
+    st = static_scratch(&scratch);
+    if (st != CSF_OK) return st;
+    return prepare_enqueue(dense, *out, exc_capacity, scratch, plan, static_cast<cudaStream_t>(stream));
 }

@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(csf):
     names = declared_functions()
-    assert {"csf_prepare", "csf_decode", "csf_decode_pair", "csf_sizes"} <= set(names)
+    assert {"csf_prepare", "csf_prepare_static", "csf_decode", "csf_decode_pair", "csf_sizes"} <= set(names)
     lib = ctypes.CDLL(build.LIB)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/csf.h but not exported"
@@ -166,3 +166,19 @@ def test_expand_scales_needs_the_workspace(csf):
     with pytest.raises(csf.CsfError, match="workspace"):
         csf.expand_scales([(Fake(), None)])
     assert csf.expand_scales([(None, None)]) is False
+
+
+def test_static_prepare_host_checks(csf):
+    # The allocation-free prepare checks its arguments on the host before any
+    # CUDA call: NULLs are refused, and so is a geometry whose look-back words
+    # (16 + 8 per 128-row tile) exceed the built-in 256 KiB array.
+    fn = csf.lib.csf_prepare_static
+    fn.argtypes = [ctypes.c_void_p, ctypes.POINTER(csf.CStack), ctypes.c_uint64, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    assert fn(None, None, 0, None) == 1
+    g = csf.Geometry(0, 8192, 1024, 100)
+    st = csf.CStack(g, 256, 256, None, 256, 256, 0, None)
+    assert fn(256, ctypes.byref(st), 0, None) == 2
+    g = csf.Geometry(0, 4, 64, 8)
+    st = csf.CStack(g, 256, 256, None, 256, 256, 0, None)
+    assert fn(None, ctypes.byref(st), 0, None) == 1

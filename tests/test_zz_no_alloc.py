@@ -17,6 +17,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from lossless_nvfp4_scale_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -66,6 +67,12 @@ def test_static_prepare_matches_prepare_on_two_calls(csf, kind, shape):
     dense = torch.from_numpy(dense_np).cuda()
     ref = csf.prepare(dense, kind)                     # the existing entry point
     sb = ref.stream_bytes()
+    if shape[0] < 384:
+        # small stacks: the existing entry point's streams are also the oracle's
+        enc = oracle.encode(kind, dense_np)
+        assert ref.num_exc == enc["num_exc"]
+        assert np.array_equal(_np(ref.offsets[:enc["offsets"].size]), enc["offsets"])
+        assert np.array_equal(_np(ref.exc_bytes[:ref.num_exc]), enc["exc_bytes"][:enc["num_exc"]])
     for call in range(2):
         st = _static_prepare(csf, dense, kind)
         assert st.errors() == 0, f"call {call}: device error {st.errors():#x}"
