@@ -16,8 +16,10 @@ workspace rotate over 4 copies (321 MB > 129 MB L2), so every step reads and
 writes HBM.  nvidia-smi samples clocks during the timed region.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-Under torchrun every rank decodes its own stack (weak scaling, no collective
-on the data path); rank 0 prints one JSON line.
+Under torchrun the ranks split the 512 experts into contiguous ranges, each
+rank preparing and decoding its own sub-stack (strong scaling; --replicas
+gives every rank a whole stack instead, weak scaling); no collective on the
+data path; rank 0 prints one JSON line.
 """
 from __future__ import annotations
 
@@ -106,11 +108,15 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def timed_steps(torch, fn, steps, warmup, per_graph=16):
-    """Run `fn(i)` `warmup` times eagerly, capture `per_graph` calls into a CUDA
-    graph, then replay it back to back for at least `steps` calls with CUDA
-    events only around the whole timed region (on the launching stream).
-    Returns (total_ms, steps_done)."""
+def timed_steps(torch, fn, steps, warmup, per_graph=16, hold_s=0.0):
+    """Run `fn(i)` `warmup` times eagerly, capture the calls into CUDA graphs
+    (`per_graph` calls each, plus one graph for the remainder) and replay them
+    back to back for exactly `steps` calls, with CUDA events only around the
+    whole timed region (on the launching stream).  Each graph is replayed once,
+    untimed, before the region (its first launch uploads it).  With `hold_s`
+    > 0 the full graph is then replayed again, untimed, for that long, so a
+    clock sampler running around this call sees the same kernel under load.
+    Returns (total_ms, steps)."""
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
@@ -118,21 +124,34 @@ def timed_steps(torch, fn, steps, warmup, per_graph=16):
             fn(i)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for i in range(per_graph):
-            fn(i)
-    reps = max(1, -(-steps // per_graph))
-    g.replay()
+    full, rem = divmod(steps, per_graph)
+    graphs = []
+    for count, reps in ((per_graph, full), (rem, 1 if rem else 0)):
+        if reps == 0:
+            continue
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(count):
+                fn(i)
+        g.replay()
+        graphs.append((g, reps))
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(reps):
-        g.replay()
+    for g, reps in graphs:
+        for _ in range(reps):
+            g.replay()
     e1.record()
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1), reps * per_graph
+    if hold_s > 0 and graphs:
+        g = graphs[0][0]
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < hold_s:
+            for _ in range(64):
+                g.replay()
+            torch.cuda.synchronize()
+    return e0.elapsed_time(e1), steps
 
 
 def single_launches(torch, fn, n, flush):
@@ -164,29 +183,38 @@ def reduce_max(torch, dist, value, device):
     return float(t.item())
 
 
-def stack_traffic(st, rows_active=None):
-    """Algorithmic bytes of one decode: packed streams read + dense written.
-    Routed: only the active experts' share (their index entries are 8 bytes a
-    warp segment and are not counted)."""
+def stack_traffic(st, rows_active=None, index=True):
+    """Algorithmic bytes of one decode: packed streams read (offsets, escape
+    plane, bases, exception bytes and, with `index`, the per-row exception
+    index) + dense bytes written.  Routed: only the active experts' share.
+    The kernel itself reads the index only at the two ends of each warp
+    segment; `index=False` gives that read set."""
     sb = st.stream_bytes()
     total_rows = st.E * st.R
     frac = 1.0 if rows_active is None else rows_active / total_rows
-    read = (sb["offsets"] + sb["escapes"] + sb["base"]) * frac
+    read = (sb["offsets"] + sb["escapes"] + sb["base"] + (sb["exc_index"] if index else 0)) * frac
     exc = sb["exc_bytes"] * frac
     return read + exc + st.dense_bytes * frac
 
 
 def run_own(args, rank, world, torch, dist):
-    from lossless_nvfp4_scale_gb300 import build as b, synth
+    from lossless_nvfp4_scale_gb300 import build as b, shard, synth
     b.ensure_built()
     from lossless_nvfp4_scale_gb300 import csf
 
     dev = torch.cuda.current_device()
     hbm, peak_kind = peak_hbm()
-    seed = rank
+    # N > 1: the ranks split the 512 experts of one stack into contiguous
+    # ranges (expert parallel, strong scaling); --replicas gives every rank a
+    # whole stack of its own instead (weak scaling).  No data-path collective.
+    split = world > 1 and not args.replicas
+    E_all = 512
+    e0, e1 = shard.expert_range(E_all, world, rank) if split else (0, E_all)
 
     # ---- headline: full gate decode -------------------------------------
-    gate_dense = torch.from_numpy(synth.gate_stack(seed=seed)).cuda()
+    full = synth.gate_stack(seed=0 if split else rank)
+    gate_dense = torch.from_numpy(np.ascontiguousarray(shard.shard_dense(full, e0, e1))).cuda()
+    del full
     gate = csf.prepare(gate_dense, csf.NVFP4)
     copies = [gate] + [clone_stack(torch, gate) for _ in range(ROTATE - 1)]
     wss = [torch.empty_like(gate_dense) for _ in range(ROTATE)]
@@ -200,8 +228,7 @@ def run_own(args, rank, world, torch, dist):
     torch.cuda.synchronize()
     with ClockSampler(dev) as clk:
         t0 = time.perf_counter()
-        total_ms, steps = timed_steps(torch, step, args.steps, args.warmup)
-        torch.cuda.synchronize()
+        total_ms, steps = timed_steps(torch, step, args.steps, args.warmup, hold_s=args.clock_hold)
         wall = time.perf_counter() - t0
     if world > 1:
         dist.barrier()
@@ -210,31 +237,50 @@ def run_own(args, rank, world, torch, dist):
     if world > 1:
         total_ms = reduce_max(torch, dist, total_ms, "cuda")
     ms_per_step = total_ms / steps
-    dense_gb = gate.dense_bytes / 1e9
-    value = world * dense_gb * steps / (total_ms / 1e3)
-    alg = stack_traffic(gate)
+    job_dense = (E_all * 1024 * 100) if split else world * gate.dense_bytes
+    value = job_dense / 1e9 * steps / (total_ms / 1e3)
+    alg = stack_traffic(gate)                        # with the per-row index
+    alg_kernel = stack_traffic(gate, index=False)    # what the kernel reads
     achieved = alg / (ms_per_step / 1e3) / 1e9
+    traffic, traffic_src = profiled_traffic()
+    parallelism = (f"expert split x{world}: rank r decodes experts [{e0}, {e1}) of the 512 (no collective)"
+                   if split else (f"replicas x{world} (independent stacks, no collective)" if world > 1 else "single GPU"))
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "higher_is_better": True, "scaling": "strong" if split else "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded gate-shaped stack; the pages' checkpoint streams are not available)",
-        "config": {"workload": WORKLOAD, "experts": 512, "rows": 1024, "cols": 100,
-                   "dense_bytes": gate.dense_bytes, "exceptions": gate.num_exc,
+        "config": {"workload": WORKLOAD, "experts": E_all, "rows": 1024, "cols": 100,
+                   "experts_this_rank": e1 - e0, "dense_bytes": gate.dense_bytes, "exceptions": gate.num_exc,
                    "l2": f"inputs rotate over {ROTATE} stack+workspace copies "
                          f"({ROTATE * alg / 1e6:.0f} MB > 129 MB L2)",
-                   "parallelism": f"replicas x{world} (independent stacks, no collective)"},
+                   "timing": "exactly `steps` decodes replayed from CUDA graphs (16 per graph plus a "
+                             "remainder graph), CUDA events around the whole region",
+                   "parallelism": parallelism},
         "us_per_stack": round(1e3 * ms_per_step, 3),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "peak_source": peak_kind,
-                     "nominal_peak": NOMINAL_HBM_GBS, "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
-                     "traffic": profiled_traffic(), "algorithmic_bytes": int(alg)},
+                     "traffic": traffic, "traffic_source": traffic_src,
+                     "algorithmic_bytes": int(alg),
+                     "algorithmic_bytes_definition": "offsets + bases + exception index + exception bytes "
+                                                     "read, dense bytes written (per-unit figures of the "
+                                                     "measurement plan, actual buffer lengths)",
+                     "kernel_read_set_bytes": int(alg_kernel),
+                     "frac_kernel_read_set": round(alg_kernel / (ms_per_step / 1e3) / 1e9 / hbm, 4),
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4)},
         "gpu_launches": steps,
         "wall_s": round(wall, 3),
     }
     result["clocks"] = clk.summary()
+    result["clocks"]["window"] = (f"sampled every 100 ms from before the timed region through {args.clock_hold} s "
+                                  "of untimed replays of the same graph right after it")
     if rank == 0 and not args.skip_rows:
         result["rows"] = measure_rows(torch, csf, synth, gate, gate_dense, hbm, args.steps)
+        sl = result["rows"].get("gate_single_launch")
+        if sl:
+            result["roofline"]["single_launch_l2_flushed"] = {
+                "median_us": sl["median_us"], "frac": sl["hbm_frac"],
+                "frac_kernel_read_set": round(alg_kernel / (sl["median_us"] / 1e6) / 1e9 / hbm, 4)}
     if rank == 0:
         result["e2e"] = measure_e2e(torch, csf, gate, gate_dense)
         if not args.skip_cpu:
@@ -253,8 +299,9 @@ def clone_stack(torch, st):
 
 
 def profiled_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel source (else null)."""
+    """DRAM bytes per decode launch, read from the committed ncu summary of
+    the gate decode if it was taken on the current kernel source (else null).
+    Returns (bytes or None, a label of where the figure comes from)."""
     import hashlib
     try:
         src = open(os.path.join(ROOT, "lossless_nvfp4_scale_gb300", "csrc", "csf_decode.cu"), "rb").read()
@@ -266,10 +313,12 @@ def profiled_traffic():
                     k, v = ln[2:].split(": ", 1)
                     info[k.strip()] = v.strip().strip("`")
         if info.get("csf_decode.cu sha256[:16]") == digest:
-            return float(info["dram bytes per launch"])
+            return float(info["dram bytes per launch"]), (
+                "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch, from the committed profile "
+                "summary taken on this kernel source (not measured in this run)")
+        return None, "the committed profile summary was taken on another kernel source"
     except Exception:
-        pass
-    return None
+        return None, "no profile summary"
 
 
 def tiled_bytes(t):
@@ -315,15 +364,21 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm, max_steps):
     # each launch (median of 50), and warm (one copy decoded back to back, so its 80 MB
     # stay largely in the 129 MB L2; may exceed the HBM bound)
     flush = torch.ones(2 * 129 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda")
-    ts = sorted(single_launches(torch, lambda i: csf.decode(gate, ws), 50, flush))
-    med = ts[len(ts) // 2]
+
+    def cold(name, fn, alg, extra=None):
+        ts = sorted(single_launches(torch, fn, 50, flush))
+        med = ts[len(ts) // 2]
+        rows[name] = {"l2": "flushed (2 x L2 read before each launch)", "n": len(ts),
+                      "median_us": round(1e3 * med, 3), "p10_us": round(1e3 * ts[len(ts) // 10], 3),
+                      "p90_us": round(1e3 * ts[(9 * len(ts)) // 10], 3), "algorithmic_MB": round(alg / 1e6, 3),
+                      "GB_s": round(alg / (med / 1e3) / 1e9, 1), "hbm_frac": round(alg / (med / 1e3) / 1e9 / hbm, 4)}
+        if extra:
+            rows[name].update(extra)
+
     alg = stack_traffic(gate)
-    rows["gate_single_launch"] = {"l2": "flushed (2 x L2 read)", "n": len(ts), "median_us": round(1e3 * med, 3),
-                                  "p10_us": round(1e3 * ts[len(ts) // 10], 3),
-                                  "p90_us": round(1e3 * ts[(9 * len(ts)) // 10], 3),
-                                  "GB_s": round(alg / (med / 1e3) / 1e9, 1),
-                                  "hbm_frac": round(alg / (med / 1e3) / 1e9 / hbm, 4)}
-    del flush
+    cold("gate_single_launch", lambda i: csf.decode(gate, ws), alg)
+    cold("routed_8of512_cold", lambda i: csf.decode(gate, ws, expert_start=start),
+         stack_traffic(gate, rows_active=active * 1024))
     durs = timed_steps(torch, lambda i: csf.decode(gate, ws), n(400), 20)
     rec("gate_warm", durs, alg, {"l2": "warm"})
 
@@ -373,9 +428,11 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm, max_steps):
     assert torch.equal(gws, gate_dense) and torch.equal(dws, down_dense)
     rec("pair_full", durs, stack_traffic(gate) + stack_traffic(down))
     durs = timed_steps(torch, lambda i: csf.decode_pair(gate, down, gws, dws, expert_start=start), n(400), 20)
-    rec("pair_routed_8of512", durs,
-        stack_traffic(gate, rows_active=active * 1024) + stack_traffic(down, rows_active=active * 2048),
-        {"l2": "warm"})
+    pair_routed_alg = stack_traffic(gate, rows_active=active * 1024) + stack_traffic(down, rows_active=active * 2048)
+    rec("pair_routed_8of512", durs, pair_routed_alg, {"l2": "warm"})
+    cold("pair_routed_8of512_cold", lambda i: csf.decode_pair(gate, down, gws, dws, expert_start=start),
+         pair_routed_alg)
+    del flush
     del g2, d2, gws2, dws2, pairs
 
     # ahead-of-call expansion: the gate + down pair expanded on a side stream
@@ -572,7 +629,7 @@ def cpu_model() -> str:
     return "arm " + " ".join(parts) if parts else "unknown"
 
 
-def run_reference(args):
+def run_reference(args, world=1):
     """The CPU oracle as the reference arm: same metric and workload, each
     step decodes a bounded sample (16 experts) of the gate stack."""
     import oracle
@@ -591,8 +648,8 @@ def run_reference(args):
     sample = f"{E} of the 512 experts per step ({dense.size / 1e6:.2f} MB dense), 1 thread"
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t / args.steps, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+            "higher_is_better": True, "scaling": "strong" if world > 1 else "weak", "vs_baseline": None,
+            "dtype": "u8", "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -606,6 +663,11 @@ def main():
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
     ap.add_argument("--skip-rows", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--replicas", action="store_true",
+                    help="N > 1: every rank decodes a whole stack of its own (weak scaling) instead of "
+                         "its range of the 512 experts")
+    ap.add_argument("--clock-hold", type=float, default=1.0,
+                    help="seconds of untimed replays after the timed region, for the clock record")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -613,7 +675,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args)), flush=True)
+            print(json.dumps(run_reference(args, world)), flush=True)
         return
     import torch
     dist = None
