@@ -84,9 +84,9 @@ struct PrepParams {
     uint32_t smem_dense;         // byte sizes of the dynamic smem regions
     uint32_t smem_planes;
     int32_t stride;              // row stride of the staged tile (row-wise kernel)
-    int32_t stage;               // row-wise kernel: stage the tile in shared memory (else read rows from L1/L2)
-    uint32_t spin_limit;         // polls before a look-back wait gives up (CSF_DEV_ERR_TIMEOUT)
-    uint32_t pad2_;
+    int32_t stage;               // row-wise kernel: how the tile is staged (plain loads, one bulk copy, a copy per row)
+    uint32_t spin_limit;         // polls before a bounded wait gives up (CSF_DEV_ERR_TIMEOUT)
+    uint32_t smem_hist;          // row-wise kernel: bytes of the bins / exception staging region
 };
 
 // Rows per unit so that a unit's first element starts a whole chunk.

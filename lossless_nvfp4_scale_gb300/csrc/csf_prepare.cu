@@ -365,44 +365,247 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const __grid_constant
 
 // ---------------------------------------------------------------- row-wise
 
-// Rows (and threads) per block in the row-wise kernel; a multiple of every
-// chunk-alignment row count (it divides into 32 and 128-element pieces).
+// Rows (and threads) per block in the row-wise kernel (C <= 255); a multiple
+// of every chunk-alignment row count (it divides into 32 and 128-element
+// pieces), so each tile's planes start on a 16-byte boundary.
 constexpr int kRowTile = 128;
+// Relative histogram of a row: 32 bins for the values [a, a + 32) around the
+// row's anchor a, and one bin for every byte outside them.
+constexpr int kBins = 32;
+constexpr int kHistWords = kBins + 1;
+constexpr uint32_t kH = 0x80808080u;   // bit 7 of each byte
 
-// Row-wise prepare for C <= 255 (byte counters cannot overflow).  One thread
-// per row: a thread-private 256-bin histogram of byte counters (word k of
-// thread t at hist[k * kRowTile + t], so a warp's accesses hit 32 banks), an
-// occupancy mask of 8-bin groups, window counts for the occupied words only
-// (byte prefix sums for NVFP4, neighbour sums for MXFP4), and the packed
-// 16-bit key (count << 8 | 255 - value) whose maximum is the most bytes with
-// the smallest value.  The histogram area is reused to stage the tile's
-// exception bytes in row-major order for one coalesced copy-out.  The tile's
-// dense rows are staged in shared memory with one coalesced read, unless that
-// would leave fewer than 4 blocks per SM (prepare_stages_rows): then each
-// thread reads its row in place, as 4-byte words through L1.
-template <bool STAGE>
+// How a thread reads its row's 4-byte words from the staged tile.
+enum RowRead { kRdWord = 0, kRdVec = 1, kRdShift = 2 };
+// How a tile is staged in shared memory.
+enum Stage { kStagePlain = 0, kStageTile = 1, kStageRows = 2 };
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// One bulk copy global -> this block's shared memory (both 16-byte aligned,
+// `bytes` a multiple of 16), completing on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_done(uint64_t *bar) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar))
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the tile's bulk copies; false when the poll limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_done(bar)) return true;
+    return false;
+}
+
+// Median of five bytes: the two middle values of the first four are
+// max(min(p0,p1), min(p2,p3)) and min(max(p0,p1), max(p2,p3)); the median of
+// all five is the median of those two and p4.
+__device__ __forceinline__ uint32_t median5(uint32_t p0, uint32_t p1, uint32_t p2, uint32_t p3, uint32_t p4) {
+    const uint32_t e = max(min(p0, p1), min(p2, p3));
+    const uint32_t f = min(max(p0, p1), max(p2, p3));
+    return max(min(p4, e), min(max(p4, e), f));
+}
+
+// 0xFF in each byte whose bit 7 is set in `f` (f has no other bits set).
+__device__ __forceinline__ uint32_t byte_mask(uint32_t f) { return (f >> 7) * 0xFFu; }
+
+// Byte-wise x - b (mod 256 in each byte, no borrow across bytes) and, in bit
+// 7 of each byte of `below`, whether that byte of x is below b.
+__device__ __forceinline__ uint32_t sub_bytes(uint32_t x, uint32_t B, uint32_t &below) {
+    const uint32_t d = ((x | kH) - (B & ~kH)) ^ ((x ^ ~B) & kH);
+    below = (~x & B) | (~(x ^ B) & d);   // borrow out of bit 7 of each byte
+    return d;
+}
+
+// The row's 4-byte words, read from its staged copy in shared memory.
+template <int RD>
+struct RowWords {
+    const uint8_t *row;
+    const uint32_t *w;   // kRdShift: the aligned word at or below the row start
+    uint32_t sh;         // kRdShift: 8 * (row start % 4)
+    __device__ __forceinline__ explicit RowWords(const uint8_t *r) : row(r) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(r);
+        w = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+        sh = 8u * (uint32_t)(a & 3u);
+    }
+    // word k (bytes 4k .. 4k+3 of the row); kRdShift reads one word past them
+    __device__ __forceinline__ uint32_t word(uint32_t k) const {
+        if (RD == kRdShift) return __funnelshift_r(w[k], w[k + 1], sh);
+        return w[k];
+    }
+    __device__ __forceinline__ uint4 quad(uint32_t q) const {   // kRdVec: words 4q .. 4q+3
+        return reinterpret_cast<const uint4 *>(w)[q];
+    }
+};
+
+// The row's relative histogram: four bytes of a word into the bins of this
+// thread's column (word-sized counters, bank = thread, no conflicts).
+__device__ __forceinline__ void hist_word(uint32_t *hcol, uint32_t x, uint32_t A4) {
+    uint32_t below;
+    const uint32_t d = sub_bytes(x, A4, below);
+    // d >= 32 in a byte: outside [a, a + 32) (bytes below a wrap to >= 32, a <= 224)
+    const uint32_t out = (((d | kH) - 0x20202020u) | d) & kH;
+    const uint32_t m = byte_mask(out);                            // 0xFF in each outside byte
+    const uint32_t bins = (d & ~m) | (0x20202020u & m);           // bin 32 = outside
+    atomicAdd(hcol + (bins & 0xFFu) * kRowTile, 1u);
+    atomicAdd(hcol + __byte_perm(bins, 0, 0x4441) * kRowTile, 1u);
+    atomicAdd(hcol + __byte_perm(bins, 0, 0x4442) * kRowTile, 1u);
+    atomicAdd(hcol + (bins >> 24) * kRowTile, 1u);
+}
+
+__device__ __forceinline__ void hist_byte(uint32_t *hcol, uint32_t v, uint32_t a) {
+    const uint32_t d = v - a;   // below a: wraps far above 32
+    atomicAdd(hcol + min(d, (uint32_t)kBins) * kRowTile, 1u);
+}
+
+// Base rule on the relative histogram h[0..32] (h[32] = bytes outside
+// [a, a + 32)): the best window among those lying inside the bins, and
+// whether that is provably the best window of the whole row.  Returns the
+// packed key (count << 8) | (255 - base), 0 when the proof fails.
+//   Windows [v, v + w] with v < a hold at most out + (bytes in [a, a + w))
+//   (they reach at most w - 1 values into the bins); windows past the bins'
+//   exact range hold at most out + (bytes in the last w bins).  A lower
+//   window must hold strictly fewer bytes than the best (ties go to the
+//   smaller value), a higher one at most as many.
+template <int KIND>
+__device__ __forceinline__ uint32_t window_key(const uint32_t *hcol, uint32_t a, uint32_t C) {
+    constexpr int w = KIND == CSF_NVFP4 ? 14 : 1;
+    constexpr int jmax = kBins - 1 - w;               // last window that lies inside the bins
+    uint32_t h[kHistWords];
+#pragma unroll
+    for (int i = 0; i < kHistWords; ++i) h[i] = hcol[i * kRowTile];
+    const uint32_t out = h[kBins];
+    const bool top = a + kBins == 256;                // the bins reach 255: every window is exact
+    uint32_t best = 0, S = 0, low = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i <= w; ++i) S += h[i];
+#pragma unroll
+    for (int i = 0; i < w; ++i) low += h[i];
+#pragma unroll
+    for (int i = kBins - w; i < kBins; ++i) hi += h[i];
+#pragma unroll
+    for (int j = 0; j <= jmax; ++j) {
+        if (h[j]) best = max(best, (S << 8) | (255u - a - (uint32_t)j));
+        if (j < jmax) S += h[j + w + 1] - h[j];
+    }
+    if (top) {
+        // windows truncated at 255
+        S -= h[jmax];
+#pragma unroll
+        for (int j = jmax + 1; j < kBins; ++j) {
+            if (h[j]) best = max(best, (S << 8) | (255u - a - (uint32_t)j));
+            S -= h[j];
+        }
+    }
+    const uint32_t M = best >> 8;
+    const bool ok_low = a == 0 || out + low < M;
+    const bool ok_high = top || out + hi <= M;
+    (void)C;
+    return ok_low && ok_high ? best : 0u;
+}
+
+// Exact base rule over all 256 values for one row, whole warp (the fallback
+// when the relative histogram cannot prove its answer).  `wh` maps value v to
+// this warp's 256 counters.  Returns the packed key (count << 8) | (255 - base).
+template <int KIND>
+__device__ uint32_t exact_key(const uint8_t *row, uint32_t C, uint32_t *hist, int warp, int lane) {
+    constexpr uint32_t w = KIND == CSF_NVFP4 ? 14u : 1u;
+    auto at = [&](uint32_t v) -> uint32_t * { return hist + (v >> 5) * kRowTile + 32u * warp + (v & 31u); };
+#pragma unroll
+    for (int i = 0; i < 8; ++i) *at((uint32_t)lane + 32u * i) = 0;
+    __syncwarp();
+    for (uint32_t c = lane; c < C; c += 32) atomicAdd(at(row[c]), 1u);
+    __syncwarp();
+    uint32_t hv[8], pre[8], run = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        hv[j] = *at(8u * lane + j);
+        run += hv[j];
+        pre[j] = run;
+    }
+    uint32_t tot;
+    const uint32_t ex = warp_excl_scan(run, lane, tot);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) pre[j] += ex;
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) *at(8u * lane + j) = pre[j];   // inclusive prefix P[v]
+    __syncwarp();
+    uint32_t key = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t v = 8u * lane + j;
+        const uint32_t cnt = *at(min(v + w, 255u)) - (pre[j] - hv[j]);   // P[v + w] - P[v - 1]
+        if (hv[j]) key = max(key, (cnt << 8) | (255u - v));
+    }
+    key = __reduce_max_sync(kFull, key);
+    __syncwarp();
+    return key;
+}
+
+// Row-wise prepare for C <= 255.  One thread per row of a 128-row tile:
+//   1. the tile is staged in shared memory by bulk copies (or plain loads);
+//   2. each thread histograms its row into 32 bins around the median of five
+//      of its bytes, finds the best window inside them and checks the bound
+//      that makes it the row's base (window_key); rows without a proof are
+//      redone exactly by their warp (exact_key);
+//   3. block scan of the exception counts; the tile's total is chained to
+//      the earlier tiles by the decoupled look-back (warp 0), while
+//   4. every thread encodes its row word by word (byte-wise subtract, range
+//      test, nibble or bit gather) into the tile's planes in shared memory,
+//      and stages its exception bytes at their tile positions (the escape
+//      positions of 8 words at a time, walked in element order);
+//   5. bases, index entries, planes and exception bytes leave with coalesced
+//      stores.
+template <int KIND, int RD>
 __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_constant__ PrepParams P) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ unsigned int s_tile;
     __shared__ unsigned long long s_excl;
     __shared__ uint32_t s_wsum[kRowTile / 32];
     __shared__ uint32_t s_total;
+    __shared__ __align__(8) uint64_t s_bar;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const uint32_t C = (uint32_t)P.C;
-    const bool nv = P.kind == CSF_NVFP4;
     const uint32_t stride = (uint32_t)P.stride;
 
-    uint32_t *s_hist = reinterpret_cast<uint32_t *>(smem);            // 64 x kRowTile words
-    uint8_t *s_exc = smem;                                             // after the base pass
-    uint8_t *s_dense = smem + 256 * kRowTile;
+    uint32_t *s_hist = reinterpret_cast<uint32_t *>(smem);          // kHistWords x kRowTile words
+    uint8_t *s_exc = smem;                                           // after the base pass
+    uint8_t *s_dense = smem + P.smem_hist;
     uint8_t *s_planes = s_dense + P.smem_dense;
     uint8_t *s_base = s_planes + P.smem_planes;
     uint32_t *s_pre = reinterpret_cast<uint32_t *>(s_base + kRowTile);
 
-    if (tid == 0) s_tile = atomicAdd(P.ticket, 1u);
+    if (tid == 0) {
+        s_tile = atomicAdd(P.ticket, 1u);
+        if (P.stage != kStagePlain) mbar_init(&s_bar);
+    }
     __syncthreads();
     const uint64_t tile = s_tile;
     if (tile >= P.num_tiles) return;
@@ -412,14 +615,29 @@ __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_con
     const uint64_t e0 = r0 * C;
     const uint32_t ne = (uint32_t)nr * C;
 
-    // 1. Zero the histograms and planes; stage the rows at `stride` (unless
-    //    the rows are read in place: C % 4 == 0, 4-byte aligned dense).
-    for (int i = tid; i < 64 * kRowTile / 4; i += kRowTile)
+    // 1. Stage the rows (row t at t * stride); clear the bins and the planes.
+    const uint8_t *src = P.dense + e0;
+    uint32_t plain_from = 0;   // bytes [plain_from, ne) of a packed tile are loaded plainly
+    if (P.stage == kStageTile) {
+        const uint32_t nb = ne & ~15u;
+        if (tid == 0) {
+            mbar_expect(&s_bar, nb);
+            if (nb) bulk_load(s_dense, src, nb, &s_bar);
+        }
+        plain_from = nb;
+    } else if (P.stage == kStageRows) {
+        if (warp == 0) {
+            if (lane == 0) mbar_expect(&s_bar, ne);
+            __syncwarp();
+            for (int r = lane; r < nr; r += 32) bulk_load(s_dense + (uint32_t)r * stride, src + (uint64_t)r * C, C, &s_bar);
+        }
+        plain_from = ne;
+    }
+    for (uint32_t i = tid; i < (uint32_t)kHistWords * kRowTile / 4; i += kRowTile)
         reinterpret_cast<uint4 *>(s_hist)[i] = make_uint4(0, 0, 0, 0);
     for (uint32_t i = tid; i < P.smem_planes / 16; i += kRowTile)
         reinterpret_cast<uint4 *>(s_planes)[i] = make_uint4(0, 0, 0, 0);
-    if (STAGE) {
-        const uint8_t *src = P.dense + e0;
+    if (P.stage == kStagePlain) {
         if (stride == C) {
             uint32_t done = 0;
             if (P.dense_aligned) {
@@ -430,86 +648,61 @@ __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_con
             }
             for (uint32_t i = done + tid; i < ne; i += kRowTile) s_dense[i] = __ldg(src + i);
         } else {
-            // C % 4 == 0 here: 4-byte words never straddle rows.
-            auto put = [&](uint32_t e, uint32_t w) {
-                const uint32_t row = (uint32_t)(((uint64_t)e * P.magic) >> 40);
-                *reinterpret_cast<uint32_t *>(s_dense + row * stride + (e - row * C)) = w;
-            };
-            uint32_t done = 0;
-            if (P.dense_aligned) {
-                const uint32_t n16 = ne / 16;
-                for (uint32_t i = tid; i < n16; i += kRowTile) {
-                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src) + i);
-                    put(16 * i, v.x); put(16 * i + 4, v.y); put(16 * i + 8, v.z); put(16 * i + 12, v.w);
-                }
-                done = n16 * 16;
-            }
-            for (uint32_t e = done + 4 * tid; e < ne; e += 4 * kRowTile) {
-                const uint32_t w = (uint32_t)__ldg(src + e) | ((uint32_t)__ldg(src + e + 1) << 8) |
-                                   ((uint32_t)__ldg(src + e + 2) << 16) | ((uint32_t)__ldg(src + e + 3) << 24);
-                put(e, w);
+            for (uint32_t i = tid; i < ne; i += kRowTile) {
+                const uint32_t row = (uint32_t)(((uint64_t)i * P.magic) >> 40);
+                s_dense[row * stride + (i - row * C)] = __ldg(src + i);
             }
         }
+    } else {
+        for (uint32_t i = plain_from + tid; i < ne; i += kRowTile) s_dense[i] = __ldg(src + i);
     }
     __syncthreads();
+    if (P.stage != kStagePlain && !mbar_wait(&s_bar, P.spin_limit)) {
+        flag(P.err, CSF_DEV_ERR_TIMEOUT);
+        mbar_wait(&s_bar, P.spin_limit);   // let copies in flight land before the block goes on
+    }
+
+    const bool mine = tid < nr;
+    const uint8_t *rowb = s_dense + (uint32_t)tid * stride;
+    const uint32_t nw = C / 4;                           // whole words of a row
+    const uint32_t tailn = C & 3u;                       // kRdShift only
 
     // 2. Base byte and exception count of this thread's row.
     uint32_t base = 0, count = 0;
-    if (tid < nr) {
-        const uint8_t *row = STAGE ? s_dense + tid * stride : P.dense + (r0 + (uint64_t)tid) * C;
-        uint32_t *h = s_hist + tid;
-        uint32_t occ = 0;
-        // Shared-memory reductions (no returned value): increments of the same
-        // word need no read-after-write chain through this thread.
-        auto add = [&](uint32_t v) {
-            atomicAdd(h + (v >> 2) * kRowTile, 1u << ((v & 3u) << 3));
-            occ |= 1u << (v >> 3);
-        };
-        if (!STAGE || (stride & 3u) == 0) {
-            const uint32_t *rw = reinterpret_cast<const uint32_t *>(row);
-            for (uint32_t k = 0; k < C / 4; ++k) {
-                const uint32_t x = rw[k];
-                add(x & 0xFFu); add((x >> 8) & 0xFFu); add((x >> 16) & 0xFFu); add(x >> 24);
+    uint32_t key = 0;
+    if (mine) {
+        const uint32_t med = median5(rowb[0], rowb[C / 4], rowb[C / 2], rowb[(3 * C) / 4], rowb[C - 1]);
+        const uint32_t a = min(max((int)med - 16, 0), 256 - kBins);
+        const uint32_t A4 = a * 0x01010101u;
+        uint32_t *hcol = s_hist + tid;
+        const RowWords<RD> rw(rowb);
+        if (RD == kRdVec) {
+            for (uint32_t q = 0; q < C / 16; ++q) {
+                const uint4 v = rw.quad(q);
+                hist_word(hcol, v.x, A4);
+                hist_word(hcol, v.y, A4);
+                hist_word(hcol, v.z, A4);
+                hist_word(hcol, v.w, A4);
             }
-            for (uint32_t c = C & ~3u; c < C; ++c) add(row[c]);
         } else {
-            for (uint32_t c = 0; c < C; ++c) add(row[c]);
+            for (uint32_t k = 0; k < nw; ++k) hist_word(hcol, rw.word(k), A4);
+            for (uint32_t c = 4 * nw; c < C; ++c) hist_byte(hcol, rowb[c], a);
         }
-        uint32_t best = 0;
-        while (occ) {
-            const uint32_t g = (uint32_t)(__ffs(occ) - 1);
-            occ &= occ - 1;
-#pragma unroll
-            for (uint32_t m = 2 * g; m < 2 * g + 2; ++m) {
-                const uint32_t hm = h[m * kRowTile];
-                if (hm == 0) continue;
-                uint32_t W;
-                if (nv) {
-                    // window [v, v+14]: byte prefix sums over words m..m+4
-                    const uint32_t q0 = hm * 0x01010101u;
-                    uint32_t c = q0 >> 24;
-                    uint32_t q[4];
-#pragma unroll
-                    for (int i = 1; i <= 4; ++i) {
-                        const uint32_t hw = (m + i < 64) ? h[(m + i) * kRowTile] : 0u;
-                        q[i - 1] = hw * 0x01010101u + c * 0x01010101u;
-                        c = q[i - 1] >> 24;
-                    }
-                    W = __byte_perm(q[2], q[3], 0x5432) - (q0 << 8);
-                } else {
-                    // window [v, v+1]
-                    const uint32_t hn = (m + 1 < 64) ? h[(m + 1) * kRowTile] : 0u;
-                    W = hm + __byte_perm(hm, hn, 0x4321);
-                }
-                const uint32_t f = (((hm & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | hm) & 0x80808080u;
-                const uint32_t Wm = W & (f | (f - (f >> 7)));               // present values only
-                const uint32_t cm = 4u * m;
-                const uint32_t kE = (Wm & 0x00FF00FFu) * 256u + (0x00FD00FFu - cm * 0x00010001u);
-                const uint32_t kO = ((Wm >> 8) & 0x00FF00FFu) * 256u + (0x00FC00FEu - cm * 0x00010001u);
-                best = __vmaxu2(best, __vmaxu2(kE, kO));
-            }
+        key = window_key<KIND>(hcol, a, C);
+    }
+    // rows whose window the bound cannot prove: exact over all 256 values
+    {
+        uint32_t redo = __ballot_sync(kFull, mine && key == 0);
+        __syncwarp();
+        while (redo) {
+            const int src_lane = __ffs(redo) - 1;
+            redo &= redo - 1;
+            const uint32_t k2 = exact_key<KIND>(s_dense + (uint32_t)(32 * warp + src_lane) * stride, C, s_hist,
+                                                warp, lane);
+            if (lane == src_lane) key = k2;
         }
-        const uint32_t key = max(best & 0xFFFFu, best >> 16);
+    }
+    if (mine) {
         base = 255u - (key & 0xFFu);
         count = C - (key >> 8);
         s_base[tid] = (uint8_t)base;
@@ -527,102 +720,91 @@ __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_con
         btot += s_wsum[w];
     }
     const uint32_t pre = boff + wex;
-    if (tid < nr) s_pre[tid] = pre;
+    if (mine) s_pre[tid] = pre;
     if (tid == 0) s_total = btot;
 
-    // 4. Look-back across tiles (warp 0), overlapping the packing below.
+    // 4. Look-back across tiles (warp 0), overlapping the encoding below.
     if (warp == 0) {
         const unsigned long long excl = lookback_exclusive(P, tile, btot, lane);
         if (lane == 0) s_excl = excl;
     }
 
-    // 5. Pack this row's planes; stage its exceptions at their tile position.
-    if (tid < nr) {
-        const uint8_t *row = STAGE ? s_dense + tid * stride : P.dense + (r0 + (uint64_t)tid) * C;
+    // 5. Encode this row into the planes; stage its exceptions.
+    if (mine) {
+        const uint32_t B4 = base * 0x01010101u;
+        const RowWords<RD> rw(rowb);
         uint32_t pos = pre;
-        uint32_t el = (uint32_t)tid * C;   // tile-local element index
-        const uint32_t w = nv ? 14u : 1u;
-        uint32_t *po = reinterpret_cast<uint32_t *>(s_planes);
+        const uint32_t el0 = (uint32_t)tid * C;   // tile-local element index of the row start
+        uint32_t *pw = reinterpret_cast<uint32_t *>(s_planes);
         uint32_t *px = reinterpret_cast<uint32_t *>(s_planes + P.smem_planes / 2);
-        // Codes of 4 elements: NVFP4 nibbles in bits 0..15, MXFP4 offset bits in
-        // bits 0..3 and escape bits in 4..7.
-        auto code4 = [&](uint32_t x, uint32_t nb) {
-            uint32_t cd = 0;
-#pragma unroll
-            for (uint32_t j = 0; j < 4; ++j) {
-                if (j < nb) {
-                    const uint32_t v = (x >> (8 * j)) & 0xFFu;
-                    const uint32_t d = v - base;
-                    const bool inside = v >= base && d <= w;
-                    if (!inside) s_exc[pos++] = (uint8_t)v;
-                    if (nv) cd |= (inside ? d : 15u) << (4 * j);
-                    else cd |= (inside ? (d << j) : (0x10u << j));
-                }
+        uint32_t excm = 0, acc_o = 0, acc_x = 0;
+        // Escape flags of 8 words at a time (bit 4j + i = byte i of word j, so
+        // bit order is element order), then their bytes in order.
+        auto flush_exc = [&](uint32_t k0) {
+            while (excm) {
+                const uint32_t i = (uint32_t)(__ffs(excm) - 1);
+                excm &= excm - 1;
+                s_exc[pos++] = rowb[4 * k0 + i];
             }
-            return cd;
         };
-        // The same codes for a whole word at once (SWAR): per byte d = x - base
-        // without borrows between bytes, and bit 7 of `o` set for the bytes
-        // outside [base, base + w] (d > w, or x below base: the byte's borrow).
-        const uint32_t B4 = base * 0x01010101u, W1 = (w + 1) * 0x01010101u;
-        auto code4w = [&](uint32_t x) {
-            const uint32_t H = 0x80808080u;
-            const uint32_t d = ((x | H) - (B4 & ~H)) ^ ((x ^ ~B4) & H);
-            const uint32_t bo = ((~x & B4) | (~(x ^ B4) & d)) & H;
-            const uint32_t o = ((((d | H) - W1) | d) | bo) & H;
-#pragma unroll
-            for (uint32_t j = 0; j < 4; ++j)               // exceptions, in element order
-                if (o & (0x80u << (8 * j))) s_exc[pos++] = (uint8_t)(x >> (8 * j));
-            const uint32_t ob = o >> 7;                    // 1 in each outside byte
-            if (nv) {
-                const uint32_t c = (d & ~(ob * 0xFFu)) | (ob * 0x0Fu);    // outside -> escape code 15
+        // codes of word k from its bytes x (`valid` = mask of the bytes that
+        // belong to the row: 0xFFFFFFFF except in a tail word)
+        auto encode = [&](uint32_t k, uint32_t x, uint32_t valid) {
+            uint32_t below;
+            const uint32_t d = sub_bytes(x, B4, below);
+            constexpr uint32_t kW1 = KIND == CSF_NVFP4 ? 0x0F0F0F0Fu : 0x02020202u;   // (w + 1) per byte
+            const uint32_t o = ((((d | kH) - kW1) | d | below) & kH) & valid;     // outside [b, b + w]
+            const uint32_t m = byte_mask(o);
+            const uint32_t esc4 = (o * 0x00204081u) >> 28;                        // bit i = byte i outside
+            excm |= esc4 << (4 * (k & 7u));
+            const uint32_t el = el0 + 4 * k;
+            if (KIND == CSF_NVFP4) {
+                const uint32_t c = ((d & ~m) | (0x0F0F0F0Fu & m)) & valid;
                 const uint32_t t = c | (c >> 4);
-                return __byte_perm(t, 0u, 0x4420);         // nibble j = element j
-            }
-            // bit 0 of each byte -> bits 0..3 (offset bits, 0 for exceptions), escape bits -> 4..7
-            const uint32_t ofb = (((d & ~ob) & 0x01010101u) * 0x01020408u) >> 24;
-            const uint32_t esb = (ob * 0x01020408u) >> 24;
-            return ofb | (esb << 4);
-        };
-        uint32_t acc = 0, ax = 0;
-        auto flush = [&](bool force) {
-            if (nv) {
-                if ((el & 7u) == 0 || force) {
-                    if (acc) atomicOr(po + ((el - 1) >> 3), acc);
-                    acc = 0;
+                const uint32_t code = __byte_perm(t, 0, 0x4420);                  // 4 nibbles, element order
+                if (RD != kRdShift) {
+                    reinterpret_cast<uint16_t *>(s_planes)[el >> 2] = (uint16_t)code;
+                } else {
+                    const uint32_t sh = 4 * (el & 7u);
+                    atomicOr(pw + (el >> 3), code << sh);
+                    if (sh > 16 && (code >> (32 - sh)) != 0) atomicOr(pw + (el >> 3) + 1, code >> (32 - sh));
                 }
-            } else if ((el & 31u) == 0 || force) {
-                if (acc) atomicOr(po + ((el - 1) >> 5), acc);
-                if (ax) atomicOr(px + ((el - 1) >> 5), ax);
-                acc = ax = 0;
+            } else {
+                const uint32_t ob4 = (((d & ~m) & 0x01010101u & valid) * 0x10204080u) >> 28;
+                if (RD != kRdShift && (C & 31u) == 0) {
+                    acc_o |= ob4 << (4 * (k & 7u));
+                    acc_x |= esc4 << (4 * (k & 7u));
+                    if ((k & 7u) == 7u) {
+                        pw[(el - 28) >> 5] = acc_o;
+                        px[(el - 28) >> 5] = acc_x;
+                        acc_o = acc_x = 0;
+                    }
+                } else {
+                    const uint32_t sh = el & 31u;
+                    if (ob4) atomicOr(pw + (el >> 5), ob4 << sh);
+                    if (esc4) atomicOr(px + (el >> 5), esc4 << sh);
+                    if (sh > 28) {
+                        if (ob4 >> (32 - sh)) atomicOr(pw + (el >> 5) + 1, ob4 >> (32 - sh));
+                        if (esc4 >> (32 - sh)) atomicOr(px + (el >> 5) + 1, esc4 >> (32 - sh));
+                    }
+                }
             }
+            if ((k & 7u) == 7u) flush_exc(k - 7);
         };
-        if ((!STAGE || (stride & 3u) == 0) && (el & 3u) == 0) {
-            // Whole words; groups of 4 never straddle an output word.
-            const uint32_t *rw = reinterpret_cast<const uint32_t *>(row);
-            for (uint32_t k = 0; k < C / 4; ++k) {
-                const uint32_t cd = code4w(rw[k]);
-                if (nv) acc |= cd << (4 * (el & 7u));
-                else { acc |= (cd & 0xFu) << (el & 31u); ax |= (cd >> 4) << (el & 31u); }
-                el += 4;
-                flush(k == C / 4 - 1 && (C & 3u) == 0);
-            }
-            for (uint32_t c = C & ~3u; c < C; ++c) {
-                const uint32_t cd = code4(row[c], 1);
-                if (nv) acc |= cd << (4 * (el & 7u));
-                else { acc |= (cd & 1u) << (el & 31u); ax |= ((cd >> 4) & 1u) << (el & 31u); }
-                ++el;
-                flush(c == C - 1);
+        if (RD == kRdVec) {
+            for (uint32_t q = 0; q < C / 16; ++q) {
+                const uint4 v = rw.quad(q);
+                encode(4 * q, v.x, 0xFFFFFFFFu);
+                encode(4 * q + 1, v.y, 0xFFFFFFFFu);
+                encode(4 * q + 2, v.z, 0xFFFFFFFFu);
+                encode(4 * q + 3, v.w, 0xFFFFFFFFu);
             }
         } else {
-            for (uint32_t c = 0; c < C; ++c) {
-                const uint32_t cd = code4(row[c], 1);
-                if (nv) acc |= cd << (4 * (el & 7u));
-                else { acc |= (cd & 1u) << (el & 31u); ax |= ((cd >> 4) & 1u) << (el & 31u); }
-                ++el;
-                flush(c == C - 1);
-            }
+            for (uint32_t k = 0; k < nw; ++k) encode(k, rw.word(k), 0xFFFFFFFFu);
+            if (tailn) encode(nw, rw.word(nw), 0xFFFFFFFFu >> (32 - 8 * tailn));
         }
+        const uint32_t kend = nw + (tailn ? 1 : 0);   // words encoded
+        if (kend & 7u) flush_exc(kend & ~7u);
     }
     __syncthreads();
     const unsigned long long excl = s_excl;
@@ -638,7 +820,7 @@ __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_con
         P.exc_index[P.rows] = (uint32_t)all;
         if (all > 0xFFFFFFFFull) flag(P.err, CSF_DEV_ERR_CAPACITY);
     }
-    if (nv) {
+    if (KIND == CSF_NVFP4) {
         const uint32_t nbytes = ((ne + 1) / 2 + 15) & ~15u;
         uint4 *dst = reinterpret_cast<uint4 *>(P.offsets + e0 / 2);
         for (uint32_t i = tid; i < nbytes / 16; i += kRowTile) dst[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
@@ -665,11 +847,21 @@ __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_con
 
 static bool rows_path(int32_t C) { return C <= 255; }
 
-// Smem row stride of the staged tile in the row-wise kernel: rows of C % 4 == 0
-// bytes are read as words, so their word stride is made odd (conflict-free).
+static int row_read(int32_t C) {
+    if (C % 16 == 0) return kRdVec;
+    if (C % 4 == 0) return kRdWord;
+    return kRdShift;
+}
+
+// Smem row stride of the staged tile: rows read as 16-byte vectors get an odd
+// number of 16-byte slots (8 lanes of a quarter warp hit distinct banks),
+// rows read as words an odd number of words; byte-aligned rows stay packed.
 static int32_t rows_stride(int32_t C) {
-    if (C % 4 != 0) return C;
-    return ((C / 4) % 2 == 1) ? C : C + 4;
+    switch (row_read(C)) {
+    case kRdVec: return ((C / 16) % 2 == 1) ? C : C + 16;
+    case kRdWord: return ((C / 4) % 2 == 1) ? C : C + 4;
+    default: return C;
+    }
 }
 
 int32_t prepare_tile_rows(int32_t kind, int32_t C) {
@@ -687,36 +879,35 @@ static uint32_t planes_bytes(int32_t kind, uint64_t te) {
     return kind == CSF_NVFP4 ? round16((te + 1) / 2) : 2 * round16((te + 7) / 8);
 }
 
+// Row-wise kernel: bins (reused for the tile's exception bytes), the staged
+// tile (+16 bytes that a shifted word read may touch), planes, bases, row
+// prefixes.
+static uint32_t rows_hist_bytes(int32_t C) {
+    const uint32_t bins = 4u * kHistWords * kRowTile;
+    const uint32_t exc = round16((uint64_t)kRowTile * C);
+    return bins > exc ? bins : exc;
+}
+
 size_t prepare_smem_bytes(int32_t kind, int32_t C, int32_t tr, bool staged) {
+    (void)staged;
     const uint64_t te = (uint64_t)tr * C;
     if (rows_path(C))
-        return 256u * kRowTile + (staged ? round16((uint64_t)kRowTile * rows_stride(C)) : 0u) +
-               planes_bytes(kind, te) + kRowTile + 4u * kRowTile;
+        return rows_hist_bytes(C) + round16((uint64_t)kRowTile * rows_stride(C) + 16) + planes_bytes(kind, te) +
+               kRowTile + 4u * kRowTile;
     return (size_t)round16(te) + planes_bytes(kind, te) + kWarps * 256 * 4 + (size_t)tr * 4 + round16(tr);
 }
 
-// The row-wise kernel stages its tile in shared memory (one coalesced read of
-// the dense rows) when 4 or more blocks per SM still fit; otherwise, and only
-// for rows it can read as aligned 4-byte words, each thread reads its row in
-// place.  Measured on the gate (C = 100: 4 blocks staged) staging is faster
-// (121 against 139 us); on MXFP4 384 x 2048 x 160 (3 blocks staged, 5 not)
-// reading in place is (272 against 343 us).
+// The row-wise kernel always stages its tile in shared memory.
 bool prepare_stages_rows(int32_t kind, int32_t C, const void *dense) {
-    if (!rows_path(C)) return true;
-    if (C % 4 != 0 || (reinterpret_cast<uintptr_t>(dense) & 3u) != 0) return true;
-    const size_t smem = prepare_smem_bytes(kind, C, kRowTile, true);
-    int occ = 0;
-    if (cudaFuncSetAttribute(prepare_rows_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, prepare_rows_kernel<true>, kRowTile, smem) != cudaSuccess) {
-        cudaGetLastError();
-        return true;
-    }
-    return occ >= 4;
+    (void)kind;
+    (void)C;
+    (void)dense;
+    return true;
 }
 
 void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity,
                       void *scratch, uint64_t rows, uint64_t n, bool staged) {
+    (void)staged;
     const csf_geometry &g = out.g;
     const int32_t tr = prepare_tile_rows(g.kind, g.cols);
     std::memset(&p, 0, sizeof p);
@@ -739,21 +930,39 @@ void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out,
     p.tr = tr;
     p.dense_aligned = (reinterpret_cast<uintptr_t>(dense) & 15u) == 0 ? 1 : 0;
     const uint64_t te = (uint64_t)tr * g.cols;
-    p.stride = rows_path(g.cols) ? rows_stride(g.cols) : g.cols;
-    p.stage = staged ? 1 : 0;
     p.spin_limit = kSpinLimit;
-    p.smem_dense = rows_path(g.cols) ? (staged ? round16((uint64_t)kRowTile * p.stride) : 0u) : round16(te);
     p.smem_planes = planes_bytes(g.kind, te);
+    if (rows_path(g.cols)) {
+        p.stride = rows_stride(g.cols);
+        p.smem_hist = rows_hist_bytes(g.cols);
+        p.smem_dense = round16((uint64_t)kRowTile * p.stride + 16);
+        // Bulk copies need 16-byte aligned sources: the whole tile when rows
+        // are packed, one copy per row when rows are padded (C % 16 == 0).
+        if (!p.dense_aligned) p.stage = kStagePlain;
+        else if (p.stride == g.cols && (te % 16) == 0) p.stage = kStageTile;
+        else if (g.cols % 16 == 0) p.stage = kStageRows;
+        else p.stage = kStagePlain;
+    } else {
+        p.stride = g.cols;
+        p.smem_dense = round16(te);
+        p.stage = kStagePlain;
+    }
+}
+
+template <int KIND>
+static cudaError_t launch_rows(const PrepParams &p, size_t smem, cudaStream_t s) {
+    const int rd = row_read(p.C);
+    const auto kernel = rd == kRdVec    ? prepare_rows_kernel<KIND, kRdVec>
+                        : rd == kRdWord ? prepare_rows_kernel<KIND, kRdWord>
+                                        : prepare_rows_kernel<KIND, kRdShift>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<(unsigned)p.num_tiles, kRowTile, smem, s>>>(p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_prepare(const PrepParams &p, size_t smem, cudaStream_t s) {
-    if (rows_path(p.C)) {
-        const auto kernel = p.stage ? prepare_rows_kernel<true> : prepare_rows_kernel<false>;
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        kernel<<<(unsigned)p.num_tiles, kRowTile, smem, s>>>(p);
-        return cudaGetLastError();
-    }
+    if (rows_path(p.C)) return p.kind == CSF_NVFP4 ? launch_rows<CSF_NVFP4>(p, smem, s) : launch_rows<CSF_MXFP4>(p, smem, s);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;

@@ -530,14 +530,23 @@ def test_mxfp4_word_wise_and_general_segments_in_one_launch(csf, C):
     assert st.errors() == 0
 
 
-@pytest.mark.parametrize("kind,E,R,C", [(0, 3, 150, 128), (0, 2, 130, 200), (0, 2, 70, 252), (1, 3, 150, 160),
-                                        (1, 2, 100, 200)])
+# Row widths that reach every way the prepare kernel reads rows and stages
+# tiles: 16-byte vectors with one bulk copy per tile (C/16 odd) or one per row
+# (C/16 even, padded rows), words with a tile copy (C/4 odd) or plain loads
+# (C/4 even, padded rows), and byte-shifted words for C % 4 != 0; wider rows
+# than 255 bytes take the warp-per-row kernel.
+PREP_WIDTHS = [(0, 3, 150, 48), (0, 3, 150, 128), (0, 2, 130, 200), (0, 2, 70, 252), (0, 3, 131, 100),
+               (0, 2, 140, 8), (0, 2, 133, 72), (0, 3, 129, 7), (0, 2, 150, 50), (0, 2, 135, 255),
+               (0, 2, 60, 256), (1, 3, 150, 160), (1, 2, 100, 200), (1, 2, 140, 96), (1, 2, 131, 100),
+               (1, 3, 129, 33), (1, 2, 140, 8), (1, 2, 50, 300)]
+
+
+@pytest.mark.parametrize("kind,E,R,C", PREP_WIDTHS)
 @pytest.mark.parametrize("offset", [0, 1])
-def test_prepare_rows_read_in_place_or_staged(csf, kind, E, R, C, offset):
-    # Wide rows of C % 4 == 0 leave too few blocks per SM with the tile staged
-    # in shared memory, so each thread reads its row in place; a dense pointer
-    # one byte off alignment takes the staged path.  Both give the oracle's
-    # streams, with a ragged last tile of rows.
+def test_prepare_rows_every_staging_path(csf, kind, E, R, C, offset):
+    # A dense pointer one byte off alignment takes plain loads; aligned ones
+    # take the bulk copies where the row layout allows.  All give the
+    # oracle's streams, with a ragged last tile of rows.
     dense = _small_dense(kind, E, R, C, seed=C + 17 * E)
     enc = oracle.encode(kind, dense)
     buf = torch.zeros(dense.size + offset, dtype=torch.uint8, device="cuda")
@@ -547,6 +556,53 @@ def test_prepare_rows_read_in_place_or_staged(csf, kind, E, R, C, offset):
     torch.cuda.synchronize()
     assert st.errors() == 0
     assert_stack_matches(st, enc)
+
+
+def _adversarial_rows(kind, C, seed):
+    """Rows built against the prepare's fast base search: it histograms each
+    row in 32 bins around the median of the bytes at columns 0, C/4, C/2,
+    3C/4 and C-1, and proves the best window there against the bytes it
+    cannot see.  These rows defeat the anchor or the proof, or sit on the
+    edges of the byte range, so both the fast and the exact paths run."""
+    rng = np.random.default_rng(seed)
+    w = 14 if kind == 0 else 1
+    rows = []
+    probes = sorted({0, C // 4, C // 2, (3 * C) // 4, C - 1})
+    for _ in range(6):
+        rows.append(rng.integers(0, 256, C))                                 # flat: no dominant window
+        b = int(rng.integers(0, 256 - w))
+        r = b + rng.integers(0, w + 1, C)
+        r[probes] = (b + 128 + rng.integers(0, 60, len(probes))) % 256       # every probe an outlier
+        rows.append(r)
+        b1, b2 = int(rng.integers(0, 100)), int(rng.integers(140, 256 - w))
+        half = np.concatenate([b1 + rng.integers(0, w + 1, C // 2), b2 + rng.integers(0, w + 1, C - C // 2)])
+        rows.append(rng.permutation(half))                                    # twin clusters: tie or near tie
+        rows.append(np.clip(255 - rng.integers(0, w + 3, C), 0, 255))          # at the top of the range
+        rows.append(np.clip(rng.integers(0, w + 3, C), 0, 255))                # at the bottom
+        b = int(rng.integers(40, 200))
+        r = b + rng.integers(0, w + 1, C)
+        edge = rng.random(C) < 0.35                                           # many bytes just past the window
+        r[edge] = b + w + 1 + rng.integers(0, 18, edge.sum())
+        low = rng.random(C) < 0.15
+        r[low] = b - 1 - rng.integers(0, 18, low.sum())
+        rows.append(np.clip(r, 0, 255))
+        rows.append(np.full(C, int(rng.integers(0, 256))))                    # constant
+        rows.append((np.arange(C) * 7 + int(rng.integers(0, 256))) % 256)      # every value once or so
+    return np.array(rows, dtype=np.uint8)
+
+
+@pytest.mark.parametrize("kind,C", [(0, 100), (0, 50), (0, 7), (0, 160), (0, 255), (1, 160), (1, 100), (1, 33),
+                                    (1, 5)])
+def test_prepare_adversarial_rows(csf, kind, C):
+    rows = _adversarial_rows(kind, C, seed=C + 1000 * kind)
+    E = 2
+    R = -(-rows.shape[0] // E)
+    dense = np.resize(rows, (E * R, C)).reshape(E, R, C)
+    enc = oracle.encode(kind, dense)
+    st = csf.prepare(_dense_cuda(dense), kind)
+    assert st.errors() == 0
+    assert_stack_matches(st, enc)
+    assert np.array_equal(_np(csf.decode(st)), dense)
 
 
 @pytest.mark.parametrize("Cm", [160, 33])
