@@ -158,11 +158,15 @@ csf_status csf_sizes(const csf_geometry *g, csf_sizes_t *out);
  *                  complete either way, so the caller can re-run with a
  *                  buffer of exc_index[rows] bytes.  E*R*C always suffices.
  *   scratch        device, csf_sizes().prepare_scratch bytes, 8-byte
- *                  aligned; cleared by this call on `stream`.  Calls that
- *                  share a scratch buffer must not overlap on the GPU.
- * Blocks of the kernel pass exception-count prefixes to later blocks through
- * the scratch (a decoupled look-back); every wait is bounded and sets
- * CSF_DEV_ERR_TIMEOUT rather than hang.
+ *                  aligned; needs no initialisation.  Calls that share a
+ *                  scratch buffer must not overlap on the GPU.
+ * Rows of up to 255 bytes take two kernels: the first picks each row's base
+ * and counts its exceptions (per-tile totals go to the scratch), the second
+ * places each tile in the exception stream from the totals before it and
+ * encodes; no block waits on another.  Wider rows take one kernel whose
+ * blocks pass exception-count prefixes to later blocks through the scratch
+ * (a decoupled look-back, cleared by this call on `stream`); every wait is
+ * bounded and sets CSF_DEV_ERR_TIMEOUT rather than hang.
  * Errors: CSF_ERR_ARG (NULL, misaligned planes, dense not in device memory),
  * CSF_ERR_SIZE (scratch too small), CSF_ERR_CUDA.
  */
@@ -372,11 +376,12 @@ csf_status csf_tiled_decode(const csf_tiled *t, uint8_t *ws, size_t ws_bytes,
 
 /*
  * Failure-detection self-test of the prepare's bounded waits, synchronous.
- * Runs the prepare kernel on a small internal stack (512 x 8 NVFP4, four
- * 128-row tiles) whose first tile no block ever takes, so the next tile's
- * decoupled look-back waits on a status word that nothing writes; with a poll
- * limit of 4096 the wait gives up, the kernel finishes, and the device error
- * word of the run is written to *error_word (CSF_DEV_ERR_TIMEOUT expected).
+ * Runs the single-pass prepare kernel of wide rows on a small internal stack
+ * (512 x 300 NVFP4, 48-row tiles) whose first tile no block ever takes, so
+ * the next tiles' decoupled look-backs wait on a status word that nothing
+ * writes; with a poll limit of 4096 the waits give up, the kernel finishes,
+ * and the device error word of the run is written to *error_word
+ * (CSF_DEV_ERR_TIMEOUT expected).
  * Nothing faults or hangs, and the context stays usable.  Allocates and frees
  * its own device memory on its own stream.
  * Errors: CSF_ERR_ARG (NULL), CSF_ERR_CUDA.

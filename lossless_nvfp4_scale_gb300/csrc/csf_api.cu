@@ -57,7 +57,8 @@ csf_status prepare_configure(const uint8_t *dense, const csf_geometry &g, PrepPl
 
 csf_status prepare_enqueue(const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity, void *scratch,
                            const PrepPlan &plan, cudaStream_t s) {
-    if (cudaMemsetAsync(scratch, 0, plan.scratch_bytes, s) != cudaSuccess) {   // ticket and status words start at 0
+    if (prepare_needs_cleared_scratch(out.g.cols) &&
+        cudaMemsetAsync(scratch, 0, plan.scratch_bytes, s) != cudaSuccess) {   // ticket and status words start at 0
         cudaGetLastError();
         return CSF_ERR_CUDA;
     }
@@ -540,23 +541,27 @@ csf_status csf_tiled_decode(const csf_tiled *t, uint8_t *ws, size_t ws_bytes, co
 csf_status csf_selftest_lookback_timeout(uint32_t *error_word) {
     if (!error_word) return CSF_ERR_ARG;
     *error_word = 0;
-    // A 512 x 8 NVFP4 stack: four 128-row tiles.  The ticket counter starts at
-    // 1, so no block takes tile 0 and tile 1's look-back waits on a status word
-    // that nothing writes; with a short poll limit the wait gives up.
+    // A 512 x 300 NVFP4 stack: rows wider than 255 bytes take the single-pass
+    // kernel, whose tiles (48 rows) chain their exception counts through a
+    // decoupled look-back.  The ticket counter starts at 1, so no block takes
+    // tile 0 and the next tiles' look-backs wait on a status word that nothing
+    // writes; with a short poll limit the waits give up.
     csf_stack st;
     std::memset(&st, 0, sizeof st);
     st.g.kind = CSF_NVFP4;
     st.g.num_experts = 1;
     st.g.rows = 512;
-    st.g.cols = 8;
-    const uint64_t rows = 512, n = 512 * 8;
+    st.g.cols = 300;
+    const uint64_t rows = 512, n = 512 * 300;
     const int32_t tr = prepare_tile_rows(st.g.kind, st.g.cols);
-    const size_t smem = prepare_smem_bytes(st.g.kind, st.g.cols, tr, true);
+    const size_t smem = prepare_smem_bytes(st.g.kind, st.g.cols, tr, false);
     const uint64_t need = prepare_scratch_bytes(&st.g, rows);
+    auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    // dense, base, offsets, index, exceptions, error word, scratch
+    const size_t off_dense = 0, off_base = up(off_dense + n), off_offsets = up(off_base + rows),
+                 off_index = up(off_offsets + n / 2), off_exc = up(off_index + 4 * (rows + 1)),
+                 off_err = up(off_exc + n), off_scratch = up(off_err + 16);
     uint8_t *mem = nullptr;
-    // dense 4096 B, base 512 B, offsets 2048 B, index 513 x 4 B, exceptions 4096 B, error word, scratch
-    const size_t off_dense = 0, off_base = 4096, off_offsets = 4608, off_index = 6656, off_exc = 8720,
-                 off_err = 12816, off_scratch = 12832;
     if (cudaMalloc(&mem, off_scratch + need) != cudaSuccess) {
         cudaGetLastError();
         return CSF_ERR_CUDA;
@@ -570,7 +575,7 @@ csf_status csf_selftest_lookback_timeout(uint32_t *error_word) {
     st.exc_index = reinterpret_cast<uint32_t *>(mem + off_index);
     st.exc_bytes = mem + off_exc;
     st.error_word = reinterpret_cast<uint32_t *>(mem + off_err);
-    make_prep_params(p, mem + off_dense, st, 4096, mem + off_scratch, rows, n, true);
+    make_prep_params(p, mem + off_dense, st, n, mem + off_scratch, rows, n, false);
     p.spin_limit = 4096;
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess ||
         cudaMemsetAsync(mem, 0, off_scratch + need, s) != cudaSuccess ||

@@ -71,7 +71,8 @@ struct PrepParams {
     uint8_t *exc_bytes;
     uint32_t *err;               // may be null
     unsigned int *ticket;        // scratch: tile ticket counter (zeroed)
-    unsigned long long *status;  // scratch: one look-back word per tile (zeroed)
+    unsigned long long *status;  // scratch: one look-back word per tile (zeroed; wide rows)
+    uint32_t *tile_total;        // scratch: exception total of each tile (row path)
     uint64_t exc_capacity;
     uint64_t rows;
     uint64_t n;
@@ -87,6 +88,8 @@ struct PrepParams {
     int32_t stage;               // row-wise kernel: how the tile is staged (plain loads, one bulk copy, a copy per row)
     uint32_t spin_limit;         // polls before a bounded wait gives up (CSF_DEV_ERR_TIMEOUT)
     uint32_t smem_hist;          // row-wise kernel: bytes of the bins / exception staging region
+    int32_t nbuf;                // row kernels: tile staging buffers (2: the next tile loads during this one)
+    uint32_t exc_stage;          // encode kernel: bytes of the shared-memory exception stage
 };
 
 // Rows per unit so that a unit's first element starts a whole chunk.
@@ -173,6 +176,7 @@ void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out,
                       void *scratch, uint64_t rows, uint64_t n, bool staged);
 size_t prepare_smem_bytes(int32_t kind, int32_t C, int32_t tr, bool staged);
 bool prepare_stages_rows(int32_t kind, int32_t C, const void *dense);
+bool prepare_needs_cleared_scratch(int32_t C);
 int32_t prepare_tile_rows(int32_t kind, int32_t C);
 
 }  // namespace csfk

@@ -1,6 +1,5 @@
-// CSF prepare kernel for sm_103a: encodes a dense stack (base byte per row,
-// offset / escape planes, exception index, exception stream) in one pass over
-// the dense bytes.
+// CSF prepare kernels for sm_103a: encode a dense stack (base byte per row,
+// offset / escape planes, exception index, exception stream).
 //
 // Pages followed (cited by title and paragraph; no numbered sections):
 //   "finegrained-kernels: decode losslessly compressed NVFP4 scales (CSF)":
@@ -17,22 +16,17 @@
 // exception stream): the smallest byte value present in the row whose window
 // [v, v+w] (w = 14 NVFP4, 1 MXFP4) holds the most of the row's bytes.
 //
-// Per block = one tile of `tr` rows (a whole number of chunk-aligned row
-// groups, so output planes start on 16-byte boundaries):
-//   1. stage the tile's dense bytes in shared memory (one HBM read);
-//   2. one warp per row: 256-bin histogram in shared memory, window counts
-//      (prefix sums for NVFP4, neighbour sums for MXFP4), warp max-reduce of
-//      (count, -value) picks the base; the row's exception count is C minus
-//      the winning window count;
-//   3. all threads pack offset nibbles / bit planes from the staged bytes;
-//   4. block scan of the per-row counts; the tile total is chained to earlier
-//      tiles by a decoupled look-back (Merrill & Garland, "Single-pass
-//      Parallel Prefix Scan with Decoupled Look-back", 2016) over per-tile
-//      status words in caller scratch; tiles take ids from a ticket counter in
-//      start order, so a block only waits on blocks already running; every
-//      wait is bounded and reports CSF_DEV_ERR_TIMEOUT instead of hanging;
-//   5. write base bytes, planes, exc_index and the exception bytes at their
-//      global positions.
+// Rows of up to 255 bytes (every workload of the pages) take two kernels, a
+// base kernel and an encode kernel, with no wait between blocks (see the
+// row-wise section below).  Wider rows take one single-pass kernel
+// (prepare_kernel): per tile of rows, one warp per row picks the base from a
+// 256-bin histogram, all threads pack the planes, and a block scan of the
+// exception counts is chained to the earlier tiles by a decoupled look-back
+// (Merrill & Garland, "Single-pass Parallel Prefix Scan with Decoupled
+// Look-back", 2016) over per-tile status words in caller scratch; tiles take
+// ids from a ticket counter in start order, so a block only waits on blocks
+// already running, and every wait is bounded and reports
+// CSF_DEV_ERR_TIMEOUT instead of hanging.
 #include <cstring>
 
 #include "csf_internal.cuh"
@@ -364,10 +358,26 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const __grid_constant
 
 
 // ---------------------------------------------------------------- row-wise
+//
+// Rows of C <= 255 bytes are prepared by two kernels with no wait between
+// blocks.  The exception stream needs every tile's position, which depends on
+// the exception counts of all earlier tiles; a single pass would make each
+// tile wait for the slowest of the hundreds of tiles in flight before it (a
+// decoupled look-back measured 20 us of the gate stack's 78 us this way).
+//   base kernel    per row: base byte and exception count (into base[] and,
+//                  for now, exc_index[]); per tile: its exception total.
+//   encode kernel  per tile: its offset in the exception stream (the sum of
+//                  the earlier tiles' totals), the rows' exc_index entries
+//                  (offset + block scan of the counts), the offset / escape
+//                  planes, and the exception bytes written straight to their
+//                  final positions.
+// Both are persistent: block b takes tiles b, b + G, b + 2G, ... (G = grid),
+// staging each tile in shared memory with bulk copies while it works on the
+// one before.
 
-// Rows (and threads) per block in the row-wise kernel (C <= 255); a multiple
-// of every chunk-alignment row count (it divides into 32 and 128-element
-// pieces), so each tile's planes start on a 16-byte boundary.
+// Rows (and threads) per block; a multiple of every chunk-alignment row count
+// (it divides into 32 and 128-element pieces), so each tile's planes start on
+// a 16-byte boundary.
 constexpr int kRowTile = 128;
 // Relative histogram of a row: 32 bins for the values [a, a + 32) around the
 // row's anchor a, and one bin for every byte outside them.
@@ -403,20 +413,27 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_done(uint64_t *bar) {
+// Orders this thread's earlier generic-proxy accesses to shared memory before
+// its later bulk copies into it.
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_done(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n selp.u32 %0, 1, 0, p;\n}"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(smem_addr(bar))
+        : "r"(smem_addr(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }
 
-// Bounded wait for the tile's bulk copies; false when the poll limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t limit) {
+// Bounded wait for the phase `parity` of a staging buffer's barrier; false
+// when the poll limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
     for (uint32_t i = 0; i < limit; ++i)
-        if (mbar_done(bar)) return true;
+        if (mbar_done(bar, parity)) return true;
     return false;
 }
 
@@ -443,10 +460,9 @@ __device__ __forceinline__ uint32_t sub_bytes(uint32_t x, uint32_t B, uint32_t &
 // The row's 4-byte words, read from its staged copy in shared memory.
 template <int RD>
 struct RowWords {
-    const uint8_t *row;
     const uint32_t *w;   // kRdShift: the aligned word at or below the row start
     uint32_t sh;         // kRdShift: 8 * (row start % 4)
-    __device__ __forceinline__ explicit RowWords(const uint8_t *r) : row(r) {
+    __device__ __forceinline__ explicit RowWords(const uint8_t *r) {
         const uintptr_t a = reinterpret_cast<uintptr_t>(r);
         w = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
         sh = 8u * (uint32_t)(a & 3u);
@@ -456,8 +472,23 @@ struct RowWords {
         if (RD == kRdShift) return __funnelshift_r(w[k], w[k + 1], sh);
         return w[k];
     }
-    __device__ __forceinline__ uint4 quad(uint32_t q) const {   // kRdVec: words 4q .. 4q+3
-        return reinterpret_cast<const uint4 *>(w)[q];
+    // words 8g .. 8g+7
+    __device__ __forceinline__ void group(uint32_t g, uint32_t (&x)[8]) const {
+        if (RD == kRdVec) {
+            const uint4 a = reinterpret_cast<const uint4 *>(w)[2 * g];
+            const uint4 b = reinterpret_cast<const uint4 *>(w)[2 * g + 1];
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+            x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        } else if (RD == kRdWord) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = w[8 * g + j];
+        } else {
+            uint32_t y[9];
+#pragma unroll
+            for (int j = 0; j < 9; ++j) y[j] = w[8 * g + j];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = __funnelshift_r(y[j], y[j + 1], sh);
+        }
     }
 };
 
@@ -491,7 +522,7 @@ __device__ __forceinline__ void hist_byte(uint32_t *hcol, uint32_t v, uint32_t a
 //   window must hold strictly fewer bytes than the best (ties go to the
 //   smaller value), a higher one at most as many.
 template <int KIND>
-__device__ __forceinline__ uint32_t window_key(const uint32_t *hcol, uint32_t a, uint32_t C) {
+__device__ __forceinline__ uint32_t window_key(const uint32_t *hcol, uint32_t a) {
     constexpr int w = KIND == CSF_NVFP4 ? 14 : 1;
     constexpr int jmax = kBins - 1 - w;               // last window that lies inside the bins
     uint32_t h[kHistWords];
@@ -523,13 +554,12 @@ __device__ __forceinline__ uint32_t window_key(const uint32_t *hcol, uint32_t a,
     const uint32_t M = best >> 8;
     const bool ok_low = a == 0 || out + low < M;
     const bool ok_high = top || out + hi <= M;
-    (void)C;
     return ok_low && ok_high ? best : 0u;
 }
 
 // Exact base rule over all 256 values for one row, whole warp (the fallback
-// when the relative histogram cannot prove its answer).  `wh` maps value v to
-// this warp's 256 counters.  Returns the packed key (count << 8) | (255 - base).
+// when the relative histogram cannot prove its answer), in the warp's own
+// columns of the bins.  Returns the packed key (count << 8) | (255 - base).
 template <int KIND>
 __device__ uint32_t exact_key(const uint8_t *row, uint32_t C, uint32_t *hist, int warp, int lane) {
     constexpr uint32_t w = KIND == CSF_NVFP4 ? 14u : 1u;
@@ -566,134 +596,142 @@ __device__ uint32_t exact_key(const uint8_t *row, uint32_t C, uint32_t *hist, in
     return key;
 }
 
-// Row-wise prepare for C <= 255.  One thread per row of a 128-row tile:
-//   1. the tile is staged in shared memory by bulk copies (or plain loads);
-//   2. each thread histograms its row into 32 bins around the median of five
-//      of its bytes, finds the best window inside them and checks the bound
-//      that makes it the row's base (window_key); rows without a proof are
-//      redone exactly by their warp (exact_key);
-//   3. block scan of the exception counts; the tile's total is chained to
-//      the earlier tiles by the decoupled look-back (warp 0), while
-//   4. every thread encodes its row word by word (byte-wise subtract, range
-//      test, nibble or bit gather) into the tile's planes in shared memory,
-//      and stages its exception bytes at their tile positions (the escape
-//      positions of 8 words at a time, walked in element order);
-//   5. bases, index entries, planes and exception bytes leave with coalesced
-//      stores.
-template <int KIND, int RD>
-__global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_constant__ PrepParams P) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ unsigned int s_tile;
-    __shared__ unsigned long long s_excl;
-    __shared__ uint32_t s_wsum[kRowTile / 32];
-    __shared__ uint32_t s_total;
-    __shared__ __align__(8) uint64_t s_bar;
+// Tile staging shared by the two row kernels: rows of tile t land in a buffer
+// at row * stride.  Bulk copies (one per tile, or one per padded row) are
+// issued by warp 0; with plain staging every thread loads.
+__device__ __forceinline__ uint32_t tile_rows(const PrepParams &P, uint64_t t) {
+    const uint64_t r0 = t * (uint64_t)kRowTile;
+    return (uint32_t)(min(r0 + (uint64_t)kRowTile, P.rows) - r0);
+}
 
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
+__device__ __forceinline__ void stage_issue(const PrepParams &P, uint64_t t, uint8_t *dst, uint64_t *bar, int lane) {
+    const uint32_t C = (uint32_t)P.C;
+    const uint32_t nr = tile_rows(P, t);
+    const uint8_t *src = P.dense + t * (uint64_t)kRowTile * C;
+    if (P.stage == kStageTile) {
+        const uint32_t nb = (nr * C) & ~15u;   // the last tile's tail (< 16 bytes) is loaded plainly
+        if (lane == 0) {
+            fence_proxy_async();
+            mbar_expect(bar, nb);
+            if (nb) bulk_load(dst, src, nb, bar);
+        }
+    } else {
+        if (lane == 0) {
+            fence_proxy_async();
+            mbar_expect(bar, nr * C);
+        }
+        __syncwarp();
+        for (uint32_t r = lane; r < nr; r += 32) bulk_load(dst + r * (uint32_t)P.stride, src + (uint64_t)r * C, C, bar);
+    }
+}
+
+// Makes tile t's rows available in `dst` (whole block): plain loads, or the
+// bulk copies' completion (phase `parity` of `bar`) plus the tail of a packed
+// last tile.
+__device__ __forceinline__ void stage_wait(const PrepParams &P, uint64_t t, uint8_t *dst, uint64_t *bar,
+                                           uint32_t parity, int tid) {
     const uint32_t C = (uint32_t)P.C;
     const uint32_t stride = (uint32_t)P.stride;
-
-    uint32_t *s_hist = reinterpret_cast<uint32_t *>(smem);          // kHistWords x kRowTile words
-    uint8_t *s_exc = smem;                                           // after the base pass
-    uint8_t *s_dense = smem + P.smem_hist;
-    uint8_t *s_planes = s_dense + P.smem_dense;
-    uint8_t *s_base = s_planes + P.smem_planes;
-    uint32_t *s_pre = reinterpret_cast<uint32_t *>(s_base + kRowTile);
-
-    if (tid == 0) {
-        s_tile = atomicAdd(P.ticket, 1u);
-        if (P.stage != kStagePlain) mbar_init(&s_bar);
-    }
-    __syncthreads();
-    const uint64_t tile = s_tile;
-    if (tile >= P.num_tiles) return;
-    const uint64_t r0 = tile * (uint64_t)kRowTile;
-    const uint64_t r1 = min(r0 + (uint64_t)kRowTile, P.rows);
-    const int nr = (int)(r1 - r0);
-    const uint64_t e0 = r0 * C;
-    const uint32_t ne = (uint32_t)nr * C;
-
-    // 1. Stage the rows (row t at t * stride); clear the bins and the planes.
-    const uint8_t *src = P.dense + e0;
-    uint32_t plain_from = 0;   // bytes [plain_from, ne) of a packed tile are loaded plainly
-    if (P.stage == kStageTile) {
-        const uint32_t nb = ne & ~15u;
-        if (tid == 0) {
-            mbar_expect(&s_bar, nb);
-            if (nb) bulk_load(s_dense, src, nb, &s_bar);
-        }
-        plain_from = nb;
-    } else if (P.stage == kStageRows) {
-        if (warp == 0) {
-            if (lane == 0) mbar_expect(&s_bar, ne);
-            __syncwarp();
-            for (int r = lane; r < nr; r += 32) bulk_load(s_dense + (uint32_t)r * stride, src + (uint64_t)r * C, C, &s_bar);
-        }
-        plain_from = ne;
-    }
-    for (uint32_t i = tid; i < (uint32_t)kHistWords * kRowTile / 4; i += kRowTile)
-        reinterpret_cast<uint4 *>(s_hist)[i] = make_uint4(0, 0, 0, 0);
-    for (uint32_t i = tid; i < P.smem_planes / 16; i += kRowTile)
-        reinterpret_cast<uint4 *>(s_planes)[i] = make_uint4(0, 0, 0, 0);
+    const uint32_t ne = tile_rows(P, t) * C;
+    const uint8_t *src = P.dense + t * (uint64_t)kRowTile * C;
     if (P.stage == kStagePlain) {
         if (stride == C) {
             uint32_t done = 0;
             if (P.dense_aligned) {
                 const uint32_t n16 = ne / 16;
                 for (uint32_t i = tid; i < n16; i += kRowTile)
-                    reinterpret_cast<uint4 *>(s_dense)[i] = __ldg(reinterpret_cast<const uint4 *>(src) + i);
+                    reinterpret_cast<uint4 *>(dst)[i] = __ldg(reinterpret_cast<const uint4 *>(src) + i);
                 done = n16 * 16;
             }
-            for (uint32_t i = done + tid; i < ne; i += kRowTile) s_dense[i] = __ldg(src + i);
+            for (uint32_t i = done + tid; i < ne; i += kRowTile) dst[i] = __ldg(src + i);
         } else {
             for (uint32_t i = tid; i < ne; i += kRowTile) {
                 const uint32_t row = (uint32_t)(((uint64_t)i * P.magic) >> 40);
-                s_dense[row * stride + (i - row * C)] = __ldg(src + i);
+                dst[row * stride + (i - row * C)] = __ldg(src + i);
             }
         }
-    } else {
-        for (uint32_t i = plain_from + tid; i < ne; i += kRowTile) s_dense[i] = __ldg(src + i);
+        __syncthreads();
+        return;
+    }
+    if (P.stage == kStageTile && (ne & 15u) != 0) {
+        for (uint32_t i = (ne & ~15u) + tid; i < ne; i += kRowTile) dst[i] = __ldg(src + i);
+        __syncthreads();
+    }
+    if (!mbar_wait(bar, parity, P.spin_limit)) {
+        flag(P.err, CSF_DEV_ERR_TIMEOUT);
+        mbar_wait(bar, parity, P.spin_limit);   // let copies in flight land before going on
+    }
+}
+
+// Base kernel: one thread per row.  Each row is histogrammed into 32 bins
+// around the median of five of its bytes; the best window inside them is its
+// base when the bound of window_key proves it, else the row's warp finds the
+// base exactly over all 256 values (exact_key).  Writes base[row], the row's
+// exception count into exc_index[row] (until the encode kernel replaces it)
+// and the tile's total into the scratch.
+template <int KIND, int RD>
+__global__ void __launch_bounds__(kRowTile) prepare_base_kernel(const __grid_constant__ PrepParams P) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ uint32_t s_wsum[2][kRowTile / 32];
+    __shared__ __align__(8) uint64_t s_bar[2];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const uint32_t C = (uint32_t)P.C;
+    const uint32_t stride = (uint32_t)P.stride;
+    const bool bulk = P.stage != kStagePlain;
+    const bool two = bulk && P.nbuf == 2;
+    const uint64_t G = gridDim.x;
+
+    uint32_t *s_hist = reinterpret_cast<uint32_t *>(smem);          // kHistWords x kRowTile words
+    uint8_t *s_dense0 = smem + P.smem_hist;                          // nbuf staging buffers
+
+    if (tid == 0 && bulk) {
+        mbar_init(&s_bar[0]);
+        mbar_init(&s_bar[1]);
     }
     __syncthreads();
-    if (P.stage != kStagePlain && !mbar_wait(&s_bar, P.spin_limit)) {
-        flag(P.err, CSF_DEV_ERR_TIMEOUT);
-        mbar_wait(&s_bar, P.spin_limit);   // let copies in flight land before the block goes on
-    }
+    if (bulk && warp == 0 && blockIdx.x < P.num_tiles) stage_issue(P, blockIdx.x, s_dense0, &s_bar[0], lane);
 
-    const bool mine = tid < nr;
-    const uint8_t *rowb = s_dense + (uint32_t)tid * stride;
-    const uint32_t nw = C / 4;                           // whole words of a row
-    const uint32_t tailn = C & 3u;                       // kRdShift only
+    const uint32_t nw = C / 4;                       // whole words of a row
+    for (uint32_t k = 0;; ++k) {
+        const uint64_t tile = blockIdx.x + (uint64_t)k * G;
+        if (tile >= P.num_tiles) break;
+        // buffer and barrier of this tile: with two buffers they alternate;
+        // with one, the barrier alternates so that its phases stay in step
+        const int buf = two ? (int)(k & 1u) : 0;
+        const int bar = (int)(k & 1u);
+        uint8_t *s_dense = s_dense0 + (uint32_t)buf * P.smem_dense;
+        if (two && warp == 0 && tile + G < P.num_tiles)
+            stage_issue(P, tile + G, s_dense0 + (uint32_t)(buf ^ 1) * P.smem_dense, &s_bar[bar ^ 1], lane);
+        stage_wait(P, tile, s_dense, &s_bar[bar], (k >> 1) & 1u, tid);
 
-    // 2. Base byte and exception count of this thread's row.
-    uint32_t base = 0, count = 0;
-    uint32_t key = 0;
-    if (mine) {
-        const uint32_t med = median5(rowb[0], rowb[C / 4], rowb[C / 2], rowb[(3 * C) / 4], rowb[C - 1]);
-        const uint32_t a = min(max((int)med - 16, 0), 256 - kBins);
-        const uint32_t A4 = a * 0x01010101u;
-        uint32_t *hcol = s_hist + tid;
-        const RowWords<RD> rw(rowb);
-        if (RD == kRdVec) {
-            for (uint32_t q = 0; q < C / 16; ++q) {
-                const uint4 v = rw.quad(q);
-                hist_word(hcol, v.x, A4);
-                hist_word(hcol, v.y, A4);
-                hist_word(hcol, v.z, A4);
-                hist_word(hcol, v.w, A4);
+        const uint64_t r0 = tile * (uint64_t)kRowTile;
+        const int nr = (int)tile_rows(P, tile);
+        const bool mine = tid < nr;
+        const uint8_t *rowb = s_dense + (uint32_t)tid * stride;
+        uint32_t key = 0;
+        if (mine) {
+            uint32_t *hcol = s_hist + tid;
+#pragma unroll
+            for (int i = 0; i < kHistWords; ++i) hcol[i * kRowTile] = 0;
+            const uint32_t med = median5(rowb[0], rowb[C / 4], rowb[C / 2], rowb[(3 * C) / 4], rowb[C - 1]);
+            const uint32_t a = min(max((int)med - 16, 0), 256 - kBins);
+            const uint32_t A4 = a * 0x01010101u;
+            const RowWords<RD> rw(rowb);
+            for (uint32_t g = 0; g < nw / 8; ++g) {
+                uint32_t x[8];
+                rw.group(g, x);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) hist_word(hcol, x[j], A4);
             }
-        } else {
-            for (uint32_t k = 0; k < nw; ++k) hist_word(hcol, rw.word(k), A4);
+            for (uint32_t q = nw & ~7u; q < nw; ++q) hist_word(hcol, rw.word(q), A4);
             for (uint32_t c = 4 * nw; c < C; ++c) hist_byte(hcol, rowb[c], a);
+            key = window_key<KIND>(hcol, a);
         }
-        key = window_key<KIND>(hcol, a, C);
-    }
-    // rows whose window the bound cannot prove: exact over all 256 values
-    {
+        // rows whose window the bound cannot prove: exact over all 256 values
         uint32_t redo = __ballot_sync(kFull, mine && key == 0);
-        __syncwarp();
         while (redo) {
             const int src_lane = __ffs(redo) - 1;
             redo &= redo - 1;
@@ -701,146 +739,247 @@ __global__ void __launch_bounds__(kRowTile) prepare_rows_kernel(const __grid_con
                                                 warp, lane);
             if (lane == src_lane) key = k2;
         }
-    }
-    if (mine) {
-        base = 255u - (key & 0xFFu);
-        count = C - (key >> 8);
-        s_base[tid] = (uint8_t)base;
-    }
-
-    // 3. Block scan of the per-row counts.
-    uint32_t wtot;
-    const uint32_t wex = warp_excl_scan(count, lane, wtot);
-    if (lane == 0) s_wsum[warp] = wtot;
-    __syncthreads();   // also ends every histogram read: s_exc may overwrite it
-    uint32_t boff = 0, btot = 0;
+        const uint32_t count = mine ? C - (key >> 8) : 0u;
+        const uint32_t wsum = __reduce_add_sync(kFull, count);
+        if (lane == 0) s_wsum[k & 1u][warp] = wsum;
+        __syncthreads();   // the tile's rows are read: its buffer may be refilled
+        if (!two && bulk && warp == 0 && tile + G < P.num_tiles)
+            stage_issue(P, tile + G, s_dense0, &s_bar[bar ^ 1], lane);
+        if (mine) {
+            P.base[r0 + tid] = (uint8_t)(255u - (key & 0xFFu));
+            P.exc_index[r0 + tid] = count;
+        }
+        if (tid == 0) {
+            uint32_t t = 0;
 #pragma unroll
-    for (int w = 0; w < kRowTile / 32; ++w) {
-        if (w < warp) boff += s_wsum[w];
-        btot += s_wsum[w];
+            for (int w = 0; w < kRowTile / 32; ++w) t += s_wsum[k & 1u][w];
+            P.tile_total[tile] = t;
+        }
     }
-    const uint32_t pre = boff + wex;
-    if (mine) s_pre[tid] = pre;
-    if (tid == 0) s_total = btot;
+}
 
-    // 4. Look-back across tiles (warp 0), overlapping the encoding below.
-    if (warp == 0) {
-        const unsigned long long excl = lookback_exclusive(P, tile, btot, lane);
-        if (lane == 0) s_excl = excl;
+// Encode kernel: one thread per row.  The tile's offset in the exception
+// stream is the sum of the earlier tiles' totals (each block keeps a running
+// sum over its tiles); exc_index entries follow from a block scan of the
+// counts; each thread encodes its row word by word (byte-wise subtract, range
+// test, nibble or bit gather) into the tile's planes in shared memory and
+// writes its exception bytes to their positions in the stream (escape
+// positions taken 8 words at a time and walked in element order).
+template <int KIND, int RD>
+__global__ void __launch_bounds__(kRowTile) prepare_encode_kernel(const __grid_constant__ PrepParams P) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ uint32_t s_wsum[2][kRowTile / 32];
+    __shared__ unsigned long long s_part[2][kRowTile / 32];
+    __shared__ __align__(8) uint64_t s_bar[2];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const uint32_t C = (uint32_t)P.C;
+    const uint32_t stride = (uint32_t)P.stride;
+    const bool bulk = P.stage != kStagePlain;
+    const bool two = bulk && P.nbuf == 2;
+    const uint64_t G = gridDim.x;
+
+    uint8_t *s_dense0 = smem;                                        // nbuf staging buffers
+    uint8_t *s_planes = smem + (uint32_t)P.nbuf * P.smem_dense;
+    uint8_t *s_exc = s_planes + P.smem_planes;                       // the tile's exception bytes, in order
+
+    if (tid == 0 && bulk) {
+        mbar_init(&s_bar[0]);
+        mbar_init(&s_bar[1]);
     }
+    for (uint32_t i = tid; i < P.smem_planes / 16; i += kRowTile)
+        reinterpret_cast<uint4 *>(s_planes)[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    if (bulk && warp == 0 && blockIdx.x < P.num_tiles) stage_issue(P, blockIdx.x, s_dense0, &s_bar[0], lane);
 
-    // 5. Encode this row into the planes; stage its exceptions.
-    if (mine) {
-        const uint32_t B4 = base * 0x01010101u;
-        const RowWords<RD> rw(rowb);
-        uint32_t pos = pre;
-        const uint32_t el0 = (uint32_t)tid * C;   // tile-local element index of the row start
-        uint32_t *pw = reinterpret_cast<uint32_t *>(s_planes);
-        uint32_t *px = reinterpret_cast<uint32_t *>(s_planes + P.smem_planes / 2);
-        uint32_t excm = 0, acc_o = 0, acc_x = 0;
-        // Escape flags of 8 words at a time (bit 4j + i = byte i of word j, so
-        // bit order is element order), then their bytes in order.
-        auto flush_exc = [&](uint32_t k0) {
-            while (excm) {
-                const uint32_t i = (uint32_t)(__ffs(excm) - 1);
-                excm &= excm - 1;
-                s_exc[pos++] = rowb[4 * k0 + i];
-            }
-        };
-        // codes of word k from its bytes x (`valid` = mask of the bytes that
-        // belong to the row: 0xFFFFFFFF except in a tail word)
-        auto encode = [&](uint32_t k, uint32_t x, uint32_t valid) {
-            uint32_t below;
-            const uint32_t d = sub_bytes(x, B4, below);
+    const uint32_t nw = C / 4;                       // whole words of a row
+    const uint32_t tailn = C & 3u;                   // kRdShift only
+    unsigned long long off = 0;                      // exceptions of the tiles before `lo`
+    uint64_t lo = 0;
+    bool bad = false, over = false;
+    for (uint32_t k = 0;; ++k) {
+        const uint64_t tile = blockIdx.x + (uint64_t)k * G;
+        if (tile >= P.num_tiles) break;
+        const int buf = two ? (int)(k & 1u) : 0;
+        const int bar = (int)(k & 1u);
+        uint8_t *s_dense = s_dense0 + (uint32_t)buf * P.smem_dense;
+        if (two && warp == 0 && tile + G < P.num_tiles)
+            stage_issue(P, tile + G, s_dense0 + (uint32_t)(buf ^ 1) * P.smem_dense, &s_bar[bar ^ 1], lane);
+
+        // exceptions of tiles [lo, tile), added to the running offset
+        unsigned long long part = 0;
+        for (uint64_t j = lo + tid; j < tile; j += kRowTile) part += P.tile_total[j];
+        part = warp_sum64(part);
+        if (lane == 0) s_part[k & 1u][warp] = part;
+
+        const uint64_t r0 = tile * (uint64_t)kRowTile;
+        const int nr = (int)tile_rows(P, tile);
+        const bool mine = tid < nr;
+        uint32_t count = 0, base = 0;
+        if (mine) {
+            count = P.exc_index[r0 + tid];
+            base = P.base[r0 + tid];
+        }
+        uint32_t wtot;
+        const uint32_t wex = warp_excl_scan(count, lane, wtot);
+        if (lane == 0) s_wsum[k & 1u][warp] = wtot;
+        stage_wait(P, tile, s_dense, &s_bar[bar], (k >> 1) & 1u, tid);
+        __syncthreads();
+        uint32_t boff = 0, btot = 0;
+#pragma unroll
+        for (int w = 0; w < kRowTile / 32; ++w) {
+            if (w < warp) boff += s_wsum[k & 1u][w];
+            btot += s_wsum[k & 1u][w];
+            off += s_part[k & 1u][w];
+        }
+        lo = tile;
+        const uint32_t pre = boff + wex;
+        if (mine) P.exc_index[r0 + tid] = (uint32_t)(off + pre);
+        if (tile == P.num_tiles - 1 && tid == 0) {
+            const unsigned long long all = off + btot;
+            P.exc_index[P.rows] = (uint32_t)all;
+            if (all > 0xFFFFFFFFull) flag(P.err, CSF_DEV_ERR_CAPACITY);
+        }
+        // the tile's exceptions are staged in shared memory unless they
+        // overflow the stage; then they go straight to the stream
+        const bool staged = btot <= P.exc_stage;
+
+        if (mine) {
+            const uint8_t *rowb = s_dense + (uint32_t)tid * stride;
+            const uint32_t B4 = base * 0x01010101u;
+            const RowWords<RD> rw(rowb);
+            uint32_t pos = pre;                           // the row's next exception, tile position
+            const uint32_t el0 = (uint32_t)tid * C;       // tile-local element index of the row start
+            uint32_t *pw = reinterpret_cast<uint32_t *>(s_planes);
+            uint32_t *px = reinterpret_cast<uint32_t *>(s_planes + P.smem_planes / 2);
+            // the exception bytes of the 8 words from word k0 on: bit 4j + i of
+            // `em` = byte i of word j (bit order = element order)
+            auto emit = [&](uint32_t em, uint32_t k0) {
+                const uint8_t *src = rowb + 4 * k0;
+                if (staged) {
+                    while (em) {
+                        const uint32_t i = (uint32_t)(__ffs(em) - 1);
+                        em &= em - 1;
+                        s_exc[pos++] = src[i];
+                    }
+                } else {
+                    while (em) {
+                        const uint32_t i = (uint32_t)(__ffs(em) - 1);
+                        em &= em - 1;
+                        const unsigned long long g = off + pos++;
+                        if (g < P.exc_capacity) P.exc_bytes[g] = src[i];
+                        else over = true;
+                    }
+                }
+            };
             constexpr uint32_t kW1 = KIND == CSF_NVFP4 ? 0x0F0F0F0Fu : 0x02020202u;   // (w + 1) per byte
-            const uint32_t o = ((((d | kH) - kW1) | d | below) & kH) & valid;     // outside [b, b + w]
-            const uint32_t m = byte_mask(o);
-            const uint32_t esc4 = (o * 0x00204081u) >> 28;                        // bit i = byte i outside
-            excm |= esc4 << (4 * (k & 7u));
-            const uint32_t el = el0 + 4 * k;
-            if (KIND == CSF_NVFP4) {
-                const uint32_t c = ((d & ~m) | (0x0F0F0F0Fu & m)) & valid;
-                const uint32_t t = c | (c >> 4);
-                const uint32_t code = __byte_perm(t, 0, 0x4420);                  // 4 nibbles, element order
+            // codes of word k (bytes x; `valid` masks the bytes of a tail word)
+            // and its escape nibble (bit i = byte i outside [b, b + w])
+            auto code = [&](uint32_t x, uint32_t valid, uint32_t &ob4) -> uint32_t {
+                uint32_t below;
+                const uint32_t d = sub_bytes(x, B4, below);
+                const uint32_t o = ((((d | kH) - kW1) | d | below) & kH) & valid;
+                const uint32_t m = byte_mask(o);
+                if (KIND == CSF_NVFP4) {
+                    const uint32_t c = ((d & ~m) | (0x0F0F0F0Fu & m)) & valid;
+                    const uint32_t t = c | (c >> 4);
+                    ob4 = __byte_perm(t, 0, 0x4420);                                // 4 nibbles
+                } else {
+                    ob4 = (((d & ~m) & 0x01010101u & valid) * 0x10204080u) >> 28;  // 4 offset bits
+                }
+                return (o * 0x00204081u) >> 28;
+            };
+            auto store_nv = [&](uint32_t k, uint32_t cd) {
+                const uint32_t el = el0 + 4 * k;
                 if (RD != kRdShift) {
-                    reinterpret_cast<uint16_t *>(s_planes)[el >> 2] = (uint16_t)code;
+                    reinterpret_cast<uint16_t *>(s_planes)[el >> 2] = (uint16_t)cd;
                 } else {
                     const uint32_t sh = 4 * (el & 7u);
-                    atomicOr(pw + (el >> 3), code << sh);
-                    if (sh > 16 && (code >> (32 - sh)) != 0) atomicOr(pw + (el >> 3) + 1, code >> (32 - sh));
+                    atomicOr(pw + (el >> 3), cd << sh);
+                    if (sh > 16 && (cd >> (32 - sh)) != 0) atomicOr(pw + (el >> 3) + 1, cd >> (32 - sh));
                 }
-            } else {
-                const uint32_t ob4 = (((d & ~m) & 0x01010101u & valid) * 0x10204080u) >> 28;
-                if (RD != kRdShift && (C & 31u) == 0) {
-                    acc_o |= ob4 << (4 * (k & 7u));
-                    acc_x |= esc4 << (4 * (k & 7u));
-                    if ((k & 7u) == 7u) {
-                        pw[(el - 28) >> 5] = acc_o;
-                        px[(el - 28) >> 5] = acc_x;
-                        acc_o = acc_x = 0;
-                    }
-                } else {
-                    const uint32_t sh = el & 31u;
-                    if (ob4) atomicOr(pw + (el >> 5), ob4 << sh);
-                    if (esc4) atomicOr(px + (el >> 5), esc4 << sh);
-                    if (sh > 28) {
-                        if (ob4 >> (32 - sh)) atomicOr(pw + (el >> 5) + 1, ob4 >> (32 - sh));
-                        if (esc4 >> (32 - sh)) atomicOr(px + (el >> 5) + 1, esc4 >> (32 - sh));
+            };
+            auto store_mx = [&](uint32_t el, uint32_t o, uint32_t e, uint32_t bits) {   // `bits` bits at element el
+                const uint32_t sh = el & 31u;
+                if (o) atomicOr(pw + (el >> 5), o << sh);
+                if (e) atomicOr(px + (el >> 5), e << sh);
+                if (sh + bits > 32) {
+                    if (o >> (32 - sh)) atomicOr(pw + (el >> 5) + 1, o >> (32 - sh));
+                    if (e >> (32 - sh)) atomicOr(px + (el >> 5) + 1, e >> (32 - sh));
+                }
+            };
+            for (uint32_t g = 0; g < nw / 8; ++g) {
+                uint32_t x[8];
+                rw.group(g, x);
+                uint32_t em = 0, ow = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t cd;
+                    const uint32_t e4 = code(x[j], 0xFFFFFFFFu, cd);
+                    em |= e4 << (4 * j);
+                    if (KIND == CSF_NVFP4) store_nv(8 * g + j, cd);
+                    else ow |= cd << (4 * j);
+                }
+                if (KIND == CSF_MXFP4) {
+                    const uint32_t el = el0 + 32 * g;
+                    if (RD != kRdShift && (el & 31u) == 0) {
+                        pw[el >> 5] = ow;
+                        px[el >> 5] = em;
+                    } else {
+                        store_mx(el, ow, em, 32);
                     }
                 }
+                if (em) emit(em, 8 * g);
             }
-            if ((k & 7u) == 7u) flush_exc(k - 7);
-        };
-        if (RD == kRdVec) {
-            for (uint32_t q = 0; q < C / 16; ++q) {
-                const uint4 v = rw.quad(q);
-                encode(4 * q, v.x, 0xFFFFFFFFu);
-                encode(4 * q + 1, v.y, 0xFFFFFFFFu);
-                encode(4 * q + 2, v.z, 0xFFFFFFFFu);
-                encode(4 * q + 3, v.w, 0xFFFFFFFFu);
+            // remaining whole words and the tail word, in one last group
+            uint32_t em = 0;
+            const uint32_t k0 = nw & ~7u;
+            for (uint32_t q = k0; q < nw + (tailn ? 1u : 0u); ++q) {
+                const uint32_t valid = q < nw ? 0xFFFFFFFFu : 0xFFFFFFFFu >> (32 - 8 * tailn);
+                uint32_t cd;
+                const uint32_t e4 = code(rw.word(q), valid, cd);
+                em |= e4 << (4 * (q - k0));
+                if (KIND == CSF_NVFP4) store_nv(q, cd);
+                else store_mx(el0 + 4 * q, cd, e4, 4);
+            }
+            emit(em, k0);
+            if (pos != pre + count) bad = true;           // the two kernels must agree on the count
+        }
+        __syncthreads();   // planes and exceptions staged; the tile's rows are read
+        if (!two && bulk && warp == 0 && tile + G < P.num_tiles)
+            stage_issue(P, tile + G, s_dense0, &s_bar[bar ^ 1], lane);
+        // planes of the tile, cleared again for the next one
+        if (KIND == CSF_NVFP4) {
+            const uint32_t nbytes = (((tile_rows(P, tile) * C) + 1) / 2 + 15) & ~15u;
+            uint4 *dst = reinterpret_cast<uint4 *>(P.offsets + r0 * C / 2);
+            for (uint32_t i = tid; i < nbytes / 16; i += kRowTile) {
+                dst[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
+                reinterpret_cast<uint4 *>(s_planes)[i] = make_uint4(0, 0, 0, 0);
             }
         } else {
-            for (uint32_t k = 0; k < nw; ++k) encode(k, rw.word(k), 0xFFFFFFFFu);
-            if (tailn) encode(nw, rw.word(nw), 0xFFFFFFFFu >> (32 - 8 * tailn));
+            const uint32_t nbytes = (((tile_rows(P, tile) * C) + 7) / 8 + 15) & ~15u;
+            const uint32_t pbytes = P.smem_planes / 2;
+            uint4 *dso = reinterpret_cast<uint4 *>(P.offsets + r0 * C / 8);
+            uint4 *dse = reinterpret_cast<uint4 *>(P.escapes + r0 * C / 8);
+            for (uint32_t i = tid; i < nbytes / 16; i += kRowTile) {
+                dso[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
+                dse[i] = reinterpret_cast<const uint4 *>(s_planes + pbytes)[i];
+                reinterpret_cast<uint4 *>(s_planes)[i] = make_uint4(0, 0, 0, 0);
+                reinterpret_cast<uint4 *>(s_planes + pbytes)[i] = make_uint4(0, 0, 0, 0);
+            }
         }
-        const uint32_t kend = nw + (tailn ? 1 : 0);   // words encoded
-        if (kend & 7u) flush_exc(kend & ~7u);
-    }
-    __syncthreads();
-    const unsigned long long excl = s_excl;
-    const uint32_t total = s_total;
-
-    // 6. Outputs.
-    for (int k = tid; k < nr; k += kRowTile) {
-        P.exc_index[r0 + k] = (uint32_t)(excl + s_pre[k]);
-        P.base[r0 + k] = s_base[k];
-    }
-    if (tile == P.num_tiles - 1 && tid == 0) {
-        const unsigned long long all = excl + total;
-        P.exc_index[P.rows] = (uint32_t)all;
-        if (all > 0xFFFFFFFFull) flag(P.err, CSF_DEV_ERR_CAPACITY);
-    }
-    if (KIND == CSF_NVFP4) {
-        const uint32_t nbytes = ((ne + 1) / 2 + 15) & ~15u;
-        uint4 *dst = reinterpret_cast<uint4 *>(P.offsets + e0 / 2);
-        for (uint32_t i = tid; i < nbytes / 16; i += kRowTile) dst[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
-    } else {
-        const uint32_t nbytes = ((ne + 7) / 8 + 15) & ~15u;
-        const uint32_t pbytes = P.smem_planes / 2;
-        uint4 *dso = reinterpret_cast<uint4 *>(P.offsets + e0 / 8);
-        uint4 *dse = reinterpret_cast<uint4 *>(P.escapes + e0 / 8);
-        for (uint32_t i = tid; i < nbytes / 16; i += kRowTile) {
-            dso[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
-            dse[i] = reinterpret_cast<const uint4 *>(s_planes + pbytes)[i];
+        if (staged) {
+            for (uint32_t i = tid; i < btot; i += kRowTile) {
+                const unsigned long long g = off + i;
+                if (g < P.exc_capacity) P.exc_bytes[g] = s_exc[i];
+                else over = true;
+            }
         }
     }
-    bool over = false;
-    for (uint32_t i = tid; i < total; i += kRowTile) {
-        const unsigned long long pos = excl + i;
-        if (pos < P.exc_capacity) P.exc_bytes[pos] = s_exc[i];
-        else over = true;
-    }
-    if (over) flag(P.err, CSF_DEV_ERR_CAPACITY);
+    if (__any_sync(kFull, over) && lane == 0) flag(P.err, CSF_DEV_ERR_CAPACITY);
+    if (__any_sync(kFull, bad) && lane == 0) flag(P.err, CSF_DEV_ERR_CORRUPT);
 }
 
 }  // namespace
@@ -879,35 +1018,59 @@ static uint32_t planes_bytes(int32_t kind, uint64_t te) {
     return kind == CSF_NVFP4 ? round16((te + 1) / 2) : 2 * round16((te + 7) / 8);
 }
 
-// Row-wise kernel: bins (reused for the tile's exception bytes), the staged
-// tile (+16 bytes that a shifted word read may touch), planes, bases, row
-// prefixes.
-static uint32_t rows_hist_bytes(int32_t C) {
-    const uint32_t bins = 4u * kHistWords * kRowTile;
-    const uint32_t exc = round16((uint64_t)kRowTile * C);
-    return bins > exc ? bins : exc;
+// Whether the row kernels stage tiles with bulk copies: the dense pointer
+// must be 16-byte aligned, and the rows either packed (one copy per tile) or
+// of a multiple of 16 bytes (one copy per padded row).  Otherwise every
+// thread loads part of the tile.
+static int rows_stage(int32_t C, const void *dense) {
+    if ((reinterpret_cast<uintptr_t>(dense) & 15u) != 0) return kStagePlain;
+    if (rows_stride(C) == C) return kStageTile;
+    if (C % 16 == 0) return kStageRows;
+    return kStagePlain;
 }
 
+static uint32_t rows_dense_bytes(int32_t C) { return round16((uint64_t)kRowTile * rows_stride(C) + 16); }
+static uint32_t rows_hist_bytes() { return 4u * kHistWords * kRowTile; }
+// Shared-memory stage of the encode kernel's exception bytes: a tile with
+// more exceptions writes them straight to the stream instead.
+static uint32_t rows_exc_stage(int32_t C) {
+    const uint32_t all = round16((uint64_t)kRowTile * C);
+    return all < 4096u ? all : 4096u;
+}
+// Two staging buffers (the next tile loading while one is worked on) unless
+// they would cost the base kernel residency: up to 48 KB with the bins.
+static int rows_nbuf(int32_t C, bool bulk) {
+    return bulk && rows_hist_bytes() + 2u * rows_dense_bytes(C) <= 48u * 1024u ? 2 : 1;
+}
+
+// Dynamic shared memory of a launch.  Row path: the base kernel holds the
+// bins and the staging buffers, the encode kernel the buffers, the planes
+// and the exception stage; `staged` = bulk staging.  The larger of the two
+// is reported.  Wide rows: the single-pass kernel.
 size_t prepare_smem_bytes(int32_t kind, int32_t C, int32_t tr, bool staged) {
-    (void)staged;
     const uint64_t te = (uint64_t)tr * C;
-    if (rows_path(C))
-        return rows_hist_bytes(C) + round16((uint64_t)kRowTile * rows_stride(C) + 16) + planes_bytes(kind, te) +
-               kRowTile + 4u * kRowTile;
+    if (rows_path(C)) {
+        const uint32_t nb = (uint32_t)rows_nbuf(C, staged) * rows_dense_bytes(C);
+        const size_t base = rows_hist_bytes() + nb, enc = nb + planes_bytes(kind, te) + rows_exc_stage(C);
+        return base > enc ? base : enc;
+    }
     return (size_t)round16(te) + planes_bytes(kind, te) + kWarps * 256 * 4 + (size_t)tr * 4 + round16(tr);
 }
 
-// The row-wise kernel always stages its tile in shared memory.
+// true: the row kernels stage tiles with bulk copies.
 bool prepare_stages_rows(int32_t kind, int32_t C, const void *dense) {
     (void)kind;
-    (void)C;
-    (void)dense;
-    return true;
+    return rows_path(C) && rows_stage(C, dense) != kStagePlain;
 }
+
+// The row path sums tile totals (4 bytes a tile, written before they are
+// read); the single-pass wide-row kernel needs its ticket and look-back
+// words zeroed.
+bool prepare_needs_cleared_scratch(int32_t C) { return !rows_path(C); }
 
 void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity,
                       void *scratch, uint64_t rows, uint64_t n, bool staged) {
-    (void)staged;
+    (void)staged;   // implied by the geometry and the dense pointer (prepare_stages_rows)
     const csf_geometry &g = out.g;
     const int32_t tr = prepare_tile_rows(g.kind, g.cols);
     std::memset(&p, 0, sizeof p);
@@ -920,6 +1083,7 @@ void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out,
     p.err = out.error_word;
     p.ticket = static_cast<unsigned int *>(scratch);
     p.status = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(scratch) + 16);
+    p.tile_total = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(scratch) + 16);
     p.exc_capacity = exc_capacity;
     p.rows = rows;
     p.n = n;
@@ -934,14 +1098,11 @@ void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out,
     p.smem_planes = planes_bytes(g.kind, te);
     if (rows_path(g.cols)) {
         p.stride = rows_stride(g.cols);
-        p.smem_hist = rows_hist_bytes(g.cols);
-        p.smem_dense = round16((uint64_t)kRowTile * p.stride + 16);
-        // Bulk copies need 16-byte aligned sources: the whole tile when rows
-        // are packed, one copy per row when rows are padded (C % 16 == 0).
-        if (!p.dense_aligned) p.stage = kStagePlain;
-        else if (p.stride == g.cols && (te % 16) == 0) p.stage = kStageTile;
-        else if (g.cols % 16 == 0) p.stage = kStageRows;
-        else p.stage = kStagePlain;
+        p.smem_hist = rows_hist_bytes();
+        p.smem_dense = rows_dense_bytes(g.cols);
+        p.stage = rows_stage(g.cols, dense);
+        p.nbuf = rows_nbuf(g.cols, p.stage != kStagePlain);
+        p.exc_stage = rows_exc_stage(g.cols);
     } else {
         p.stride = g.cols;
         p.smem_dense = round16(te);
@@ -949,20 +1110,40 @@ void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out,
     }
 }
 
-template <int KIND>
-static cudaError_t launch_rows(const PrepParams &p, size_t smem, cudaStream_t s) {
-    const int rd = row_read(p.C);
-    const auto kernel = rd == kRdVec    ? prepare_rows_kernel<KIND, kRdVec>
-                        : rd == kRdWord ? prepare_rows_kernel<KIND, kRdWord>
-                                        : prepare_rows_kernel<KIND, kRdShift>;
+// Persistent grid of one of the row kernels: as many blocks as stay resident.
+template <typename K>
+static cudaError_t launch_persistent(K kernel, const PrepParams &p, size_t smem, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kernel<<<(unsigned)p.num_tiles, kRowTile, smem, s>>>(p);
+    int dev = 0, sms = 0, occ = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kRowTile, smem)) != cudaSuccess)
+        return e;
+    uint64_t grid = (uint64_t)sms * (uint64_t)(occ > 0 ? occ : 1);
+    if (grid > p.num_tiles) grid = p.num_tiles;
+    kernel<<<(unsigned)grid, kRowTile, smem, s>>>(p);
     return cudaGetLastError();
 }
 
+template <int KIND, int RD>
+static cudaError_t launch_rows_rd(const PrepParams &p, cudaStream_t s) {
+    const uint32_t nb = (uint32_t)p.nbuf * p.smem_dense;
+    cudaError_t e = launch_persistent(prepare_base_kernel<KIND, RD>, p, p.smem_hist + nb, s);
+    if (e != cudaSuccess) return e;
+    return launch_persistent(prepare_encode_kernel<KIND, RD>, p, nb + p.smem_planes + p.exc_stage, s);
+}
+
+template <int KIND>
+static cudaError_t launch_rows(const PrepParams &p, cudaStream_t s) {
+    const int rd = row_read(p.C);
+    if (rd == kRdVec) return launch_rows_rd<KIND, kRdVec>(p, s);
+    if (rd == kRdWord) return launch_rows_rd<KIND, kRdWord>(p, s);
+    return launch_rows_rd<KIND, kRdShift>(p, s);
+}
+
 cudaError_t launch_prepare(const PrepParams &p, size_t smem, cudaStream_t s) {
-    if (rows_path(p.C)) return p.kind == CSF_NVFP4 ? launch_rows<CSF_NVFP4>(p, smem, s) : launch_rows<CSF_MXFP4>(p, smem, s);
+    if (rows_path(p.C)) return p.kind == CSF_NVFP4 ? launch_rows<CSF_NVFP4>(p, s) : launch_rows<CSF_MXFP4>(p, s);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
