@@ -88,8 +88,10 @@ struct PrepParams {
     int32_t stage;               // row-wise kernel: how the tile is staged (plain loads, one bulk copy, a copy per row)
     uint32_t spin_limit;         // polls before a bounded wait gives up (CSF_DEV_ERR_TIMEOUT)
     uint32_t smem_hist;          // row-wise kernel: bytes of the bins / exception staging region
-    int32_t nbuf;                // row kernels: tile staging buffers (2: the next tile loads during this one)
+    int32_t nbuf;                // base kernel: tile staging buffers (2: the next tile loads during this one)
+    int32_t nbuf_enc;            // encode kernel: the same
     uint32_t exc_stage;          // encode kernel: bytes of the shared-memory exception stage
+    uint32_t pad3_;
 };
 
 // Rows per unit so that a unit's first element starts a whole chunk.

@@ -379,16 +379,21 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const __grid_constant
 // (it divides into 32 and 128-element pieces), so each tile's planes start on
 // a 16-byte boundary.
 constexpr int kRowTile = 128;
-// Relative histogram of a row: 32 bins for the values [a, a + 32) around the
-// row's anchor a, and one bin for every byte outside them.
-constexpr int kBins = 32;
-constexpr int kHistWords = kBins + 1;
+// Relative histogram of a row: bins for the values [a, a + bins) around the
+// row's anchor a, and one bin for every byte outside them.  NVFP4 windows
+// span 15 values: 32 bins hold them with room on both sides; MXFP4 windows
+// span 2: 8 bins do.
+template <int KIND> struct Bins {
+    static constexpr int n = KIND == CSF_NVFP4 ? 32 : 8;
+    static constexpr int words = n + 1;
+    static constexpr int lead = KIND == CSF_NVFP4 ? 16 : 3;   // anchor = median - lead
+};
 constexpr uint32_t kH = 0x80808080u;   // bit 7 of each byte
 
 // How a thread reads its row's 4-byte words from the staged tile.
 enum RowRead { kRdWord = 0, kRdVec = 1, kRdShift = 2 };
 // How a tile is staged in shared memory.
-enum Stage { kStagePlain = 0, kStageTile = 1, kStageRows = 2 };
+enum Stage { kStagePlain = 0, kStageTile = 1 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -419,20 +424,26 @@ __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Polls of a staging buffer's barrier before the wait gives up, and how long
+// each poll may suspend the thread (ns) while the copies are in flight, so
+// that waiting threads sleep instead of spinning.
+constexpr uint32_t kMbarPolls = 1u << 16;
+constexpr uint32_t kMbarSuspendNs = 20000;
+
 __device__ __forceinline__ bool mbar_done(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kMbarSuspendNs)
         : "memory");
     return ok != 0;
 }
 
 // Bounded wait for the phase `parity` of a staging buffer's barrier; false
-// when the poll limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
-    for (uint32_t i = 0; i < limit; ++i)
+// when the polls ran out (about a second).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kMbarPolls; ++i)
         if (mbar_done(bar, parity)) return true;
     return false;
 }
@@ -494,26 +505,29 @@ struct RowWords {
 
 // The row's relative histogram: four bytes of a word into the bins of this
 // thread's column (word-sized counters, bank = thread, no conflicts).
+template <int NB>
 __device__ __forceinline__ void hist_word(uint32_t *hcol, uint32_t x, uint32_t A4) {
+    constexpr uint32_t kNB4 = (uint32_t)NB * 0x01010101u;
     uint32_t below;
     const uint32_t d = sub_bytes(x, A4, below);
-    // d >= 32 in a byte: outside [a, a + 32) (bytes below a wrap to >= 32, a <= 224)
-    const uint32_t out = (((d | kH) - 0x20202020u) | d) & kH;
+    // d >= NB in a byte: outside [a, a + NB) (bytes below a wrap past NB, a <= 256 - NB)
+    const uint32_t out = (((d | kH) - kNB4) | d) & kH;
     const uint32_t m = byte_mask(out);                            // 0xFF in each outside byte
-    const uint32_t bins = (d & ~m) | (0x20202020u & m);           // bin 32 = outside
+    const uint32_t bins = (d & ~m) | (kNB4 & m);                  // bin NB = outside
     atomicAdd(hcol + (bins & 0xFFu) * kRowTile, 1u);
     atomicAdd(hcol + __byte_perm(bins, 0, 0x4441) * kRowTile, 1u);
     atomicAdd(hcol + __byte_perm(bins, 0, 0x4442) * kRowTile, 1u);
     atomicAdd(hcol + (bins >> 24) * kRowTile, 1u);
 }
 
+template <int NB>
 __device__ __forceinline__ void hist_byte(uint32_t *hcol, uint32_t v, uint32_t a) {
-    const uint32_t d = v - a;   // below a: wraps far above 32
-    atomicAdd(hcol + min(d, (uint32_t)kBins) * kRowTile, 1u);
+    const uint32_t d = v - a;   // below a: wraps far above NB
+    atomicAdd(hcol + min(d, (uint32_t)NB) * kRowTile, 1u);
 }
 
-// Base rule on the relative histogram h[0..32] (h[32] = bytes outside
-// [a, a + 32)): the best window among those lying inside the bins, and
+// Base rule on the relative histogram h[0..n] (h[n] = bytes outside
+// [a, a + n)): the best window among those lying inside the bins, and
 // whether that is provably the best window of the whole row.  Returns the
 // packed key (count << 8) | (255 - base), 0 when the proof fails.
 //   Windows [v, v + w] with v < a hold at most out + (bytes in [a, a + w))
@@ -524,10 +538,11 @@ __device__ __forceinline__ void hist_byte(uint32_t *hcol, uint32_t v, uint32_t a
 template <int KIND>
 __device__ __forceinline__ uint32_t window_key(const uint32_t *hcol, uint32_t a) {
     constexpr int w = KIND == CSF_NVFP4 ? 14 : 1;
+    constexpr int kBins = Bins<KIND>::n;
     constexpr int jmax = kBins - 1 - w;               // last window that lies inside the bins
-    uint32_t h[kHistWords];
+    uint32_t h[Bins<KIND>::words];
 #pragma unroll
-    for (int i = 0; i < kHistWords; ++i) h[i] = hcol[i * kRowTile];
+    for (int i = 0; i < Bins<KIND>::words; ++i) h[i] = hcol[i * kRowTile];
     const uint32_t out = h[kBins];
     const bool top = a + kBins == 256;                // the bins reach 255: every window is exact
     uint32_t best = 0, S = 0, low = 0, hi = 0;
@@ -559,15 +574,17 @@ __device__ __forceinline__ uint32_t window_key(const uint32_t *hcol, uint32_t a)
 
 // Exact base rule over all 256 values for one row, whole warp (the fallback
 // when the relative histogram cannot prove its answer), in the warp's own
-// columns of the bins.  Returns the packed key (count << 8) | (255 - base).
+// columns of the bins; the row is read from global memory, so the staged
+// tile may already be refilled.  Returns the packed key
+// (count << 8) | (255 - base).
 template <int KIND>
-__device__ uint32_t exact_key(const uint8_t *row, uint32_t C, uint32_t *hist, int warp, int lane) {
+__device__ uint32_t exact_key(const uint8_t *__restrict__ row, uint32_t C, uint32_t *hist, int warp, int lane) {
     constexpr uint32_t w = KIND == CSF_NVFP4 ? 14u : 1u;
     auto at = [&](uint32_t v) -> uint32_t * { return hist + (v >> 5) * kRowTile + 32u * warp + (v & 31u); };
 #pragma unroll
     for (int i = 0; i < 8; ++i) *at((uint32_t)lane + 32u * i) = 0;
     __syncwarp();
-    for (uint32_t c = lane; c < C; c += 32) atomicAdd(at(row[c]), 1u);
+    for (uint32_t c = lane; c < C; c += 32) atomicAdd(at(__ldg(row + c)), 1u);
     __syncwarp();
     uint32_t hv[8], pre[8], run = 0;
 #pragma unroll
@@ -597,8 +614,8 @@ __device__ uint32_t exact_key(const uint8_t *row, uint32_t C, uint32_t *hist, in
 }
 
 // Tile staging shared by the two row kernels: rows of tile t land in a buffer
-// at row * stride.  Bulk copies (one per tile, or one per padded row) are
-// issued by warp 0; with plain staging every thread loads.
+// at row * stride.  The bulk copy of a tile is issued by lane 0 of warp 0;
+// with plain staging every thread loads.
 __device__ __forceinline__ uint32_t tile_rows(const PrepParams &P, uint64_t t) {
     const uint64_t r0 = t * (uint64_t)kRowTile;
     return (uint32_t)(min(r0 + (uint64_t)kRowTile, P.rows) - r0);
@@ -606,22 +623,11 @@ __device__ __forceinline__ uint32_t tile_rows(const PrepParams &P, uint64_t t) {
 
 __device__ __forceinline__ void stage_issue(const PrepParams &P, uint64_t t, uint8_t *dst, uint64_t *bar, int lane) {
     const uint32_t C = (uint32_t)P.C;
-    const uint32_t nr = tile_rows(P, t);
-    const uint8_t *src = P.dense + t * (uint64_t)kRowTile * C;
-    if (P.stage == kStageTile) {
-        const uint32_t nb = (nr * C) & ~15u;   // the last tile's tail (< 16 bytes) is loaded plainly
-        if (lane == 0) {
-            fence_proxy_async();
-            mbar_expect(bar, nb);
-            if (nb) bulk_load(dst, src, nb, bar);
-        }
-    } else {
-        if (lane == 0) {
-            fence_proxy_async();
-            mbar_expect(bar, nr * C);
-        }
-        __syncwarp();
-        for (uint32_t r = lane; r < nr; r += 32) bulk_load(dst + r * (uint32_t)P.stride, src + (uint64_t)r * C, C, bar);
+    const uint32_t nb = (tile_rows(P, t) * C) & ~15u;   // the last tile's tail (< 16 bytes) is loaded plainly
+    if (lane == 0) {
+        fence_proxy_async();
+        mbar_expect(bar, nb);
+        if (nb) bulk_load(dst, P.dense + t * (uint64_t)kRowTile * C, nb, bar);
     }
 }
 
@@ -631,25 +637,17 @@ __device__ __forceinline__ void stage_issue(const PrepParams &P, uint64_t t, uin
 __device__ __forceinline__ void stage_wait(const PrepParams &P, uint64_t t, uint8_t *dst, uint64_t *bar,
                                            uint32_t parity, int tid) {
     const uint32_t C = (uint32_t)P.C;
-    const uint32_t stride = (uint32_t)P.stride;
     const uint32_t ne = tile_rows(P, t) * C;
     const uint8_t *src = P.dense + t * (uint64_t)kRowTile * C;
     if (P.stage == kStagePlain) {
-        if (stride == C) {
-            uint32_t done = 0;
-            if (P.dense_aligned) {
-                const uint32_t n16 = ne / 16;
-                for (uint32_t i = tid; i < n16; i += kRowTile)
-                    reinterpret_cast<uint4 *>(dst)[i] = __ldg(reinterpret_cast<const uint4 *>(src) + i);
-                done = n16 * 16;
-            }
-            for (uint32_t i = done + tid; i < ne; i += kRowTile) dst[i] = __ldg(src + i);
-        } else {
-            for (uint32_t i = tid; i < ne; i += kRowTile) {
-                const uint32_t row = (uint32_t)(((uint64_t)i * P.magic) >> 40);
-                dst[row * stride + (i - row * C)] = __ldg(src + i);
-            }
+        uint32_t done = 0;
+        if (P.dense_aligned) {
+            const uint32_t n16 = ne / 16;
+            for (uint32_t i = tid; i < n16; i += kRowTile)
+                reinterpret_cast<uint4 *>(dst)[i] = __ldg(reinterpret_cast<const uint4 *>(src) + i);
+            done = n16 * 16;
         }
+        for (uint32_t i = done + tid; i < ne; i += kRowTile) dst[i] = __ldg(src + i);
         __syncthreads();
         return;
     }
@@ -657,9 +655,9 @@ __device__ __forceinline__ void stage_wait(const PrepParams &P, uint64_t t, uint
         for (uint32_t i = (ne & ~15u) + tid; i < ne; i += kRowTile) dst[i] = __ldg(src + i);
         __syncthreads();
     }
-    if (!mbar_wait(bar, parity, P.spin_limit)) {
+    if (!mbar_wait(bar, parity)) {
         flag(P.err, CSF_DEV_ERR_TIMEOUT);
-        mbar_wait(bar, parity, P.spin_limit);   // let copies in flight land before going on
+        mbar_wait(bar, parity);   // let copies in flight land before going on
     }
 }
 
@@ -684,7 +682,7 @@ __global__ void __launch_bounds__(kRowTile) prepare_base_kernel(const __grid_con
     const bool two = bulk && P.nbuf == 2;
     const uint64_t G = gridDim.x;
 
-    uint32_t *s_hist = reinterpret_cast<uint32_t *>(smem);          // kHistWords x kRowTile words
+    uint32_t *s_hist = reinterpret_cast<uint32_t *>(smem);          // bins x kRowTile words (8 x 128 at least)
     uint8_t *s_dense0 = smem + P.smem_hist;                          // nbuf staging buffers
 
     if (tid == 0 && bulk) {
@@ -695,60 +693,63 @@ __global__ void __launch_bounds__(kRowTile) prepare_base_kernel(const __grid_con
     if (bulk && warp == 0 && blockIdx.x < P.num_tiles) stage_issue(P, blockIdx.x, s_dense0, &s_bar[0], lane);
 
     const uint32_t nw = C / 4;                       // whole words of a row
-    for (uint32_t k = 0;; ++k) {
-        const uint64_t tile = blockIdx.x + (uint64_t)k * G;
-        if (tile >= P.num_tiles) break;
+    const uint32_t ntiles = (uint32_t)P.num_tiles;
+    for (uint32_t k = 0, tile = blockIdx.x; tile < ntiles; ++k, tile += (uint32_t)G) {
         // buffer and barrier of this tile: with two buffers they alternate;
         // with one, the barrier alternates so that its phases stay in step
         const int buf = two ? (int)(k & 1u) : 0;
         const int bar = (int)(k & 1u);
         uint8_t *s_dense = s_dense0 + (uint32_t)buf * P.smem_dense;
-        if (two && warp == 0 && tile + G < P.num_tiles)
+        if (two && warp == 0 && tile + G < ntiles)
             stage_issue(P, tile + G, s_dense0 + (uint32_t)(buf ^ 1) * P.smem_dense, &s_bar[bar ^ 1], lane);
         stage_wait(P, tile, s_dense, &s_bar[bar], (k >> 1) & 1u, tid);
 
-        const uint64_t r0 = tile * (uint64_t)kRowTile;
+        const uint32_t r0 = tile * (uint32_t)kRowTile;
         const int nr = (int)tile_rows(P, tile);
         const bool mine = tid < nr;
         const uint8_t *rowb = s_dense + (uint32_t)tid * stride;
-        uint32_t key = 0;
+        uint32_t *hcol = s_hist + tid;
+        uint32_t a = 0;
         if (mine) {
-            uint32_t *hcol = s_hist + tid;
+            constexpr int NB = Bins<KIND>::n;
 #pragma unroll
-            for (int i = 0; i < kHistWords; ++i) hcol[i * kRowTile] = 0;
+            for (int i = 0; i < Bins<KIND>::words; ++i) hcol[i * kRowTile] = 0;
             const uint32_t med = median5(rowb[0], rowb[C / 4], rowb[C / 2], rowb[(3 * C) / 4], rowb[C - 1]);
-            const uint32_t a = min(max((int)med - 16, 0), 256 - kBins);
+            a = min(max((int)med - Bins<KIND>::lead, 0), 256 - NB);
             const uint32_t A4 = a * 0x01010101u;
             const RowWords<RD> rw(rowb);
             for (uint32_t g = 0; g < nw / 8; ++g) {
                 uint32_t x[8];
                 rw.group(g, x);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) hist_word(hcol, x[j], A4);
+                for (int j = 0; j < 8; ++j) hist_word<NB>(hcol, x[j], A4);
             }
-            for (uint32_t q = nw & ~7u; q < nw; ++q) hist_word(hcol, rw.word(q), A4);
-            for (uint32_t c = 4 * nw; c < C; ++c) hist_byte(hcol, rowb[c], a);
-            key = window_key<KIND>(hcol, a);
+            for (uint32_t q = nw & ~7u; q < nw; ++q) hist_word<NB>(hcol, rw.word(q), A4);
+            for (uint32_t c = 4 * nw; c < C; ++c) hist_byte<NB>(hcol, rowb[c], a);
         }
+        if (!two) {
+            // every row is histogrammed: with one buffer, refill it now
+            __syncthreads();
+            if (bulk && warp == 0 && tile + G < ntiles) stage_issue(P, tile + G, s_dense0, &s_bar[bar ^ 1], lane);
+        }
+        uint32_t key = mine ? window_key<KIND>(hcol, a) : 0u;
         // rows whose window the bound cannot prove: exact over all 256 values
         uint32_t redo = __ballot_sync(kFull, mine && key == 0);
         while (redo) {
             const int src_lane = __ffs(redo) - 1;
             redo &= redo - 1;
-            const uint32_t k2 = exact_key<KIND>(s_dense + (uint32_t)(32 * warp + src_lane) * stride, C, s_hist,
+            const uint32_t k2 = exact_key<KIND>(P.dense + (uint64_t)(r0 + 32 * warp + src_lane) * C, C, s_hist,
                                                 warp, lane);
             if (lane == src_lane) key = k2;
         }
         const uint32_t count = mine ? C - (key >> 8) : 0u;
         const uint32_t wsum = __reduce_add_sync(kFull, count);
         if (lane == 0) s_wsum[k & 1u][warp] = wsum;
-        __syncthreads();   // the tile's rows are read: its buffer may be refilled
-        if (!two && bulk && warp == 0 && tile + G < P.num_tiles)
-            stage_issue(P, tile + G, s_dense0, &s_bar[bar ^ 1], lane);
         if (mine) {
             P.base[r0 + tid] = (uint8_t)(255u - (key & 0xFFu));
             P.exc_index[r0 + tid] = count;
         }
+        __syncthreads();   // the tile's rows are read: its buffer may be refilled
         if (tid == 0) {
             uint32_t t = 0;
 #pragma unroll
@@ -769,7 +770,7 @@ template <int KIND, int RD>
 __global__ void __launch_bounds__(kRowTile) prepare_encode_kernel(const __grid_constant__ PrepParams P) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint32_t s_wsum[2][kRowTile / 32];
-    __shared__ unsigned long long s_part[2][kRowTile / 32];
+    __shared__ uint32_t s_part[2][kRowTile / 32];
     __shared__ __align__(8) uint64_t s_bar[2];
 
     const int tid = threadIdx.x;
@@ -778,11 +779,11 @@ __global__ void __launch_bounds__(kRowTile) prepare_encode_kernel(const __grid_c
     const uint32_t C = (uint32_t)P.C;
     const uint32_t stride = (uint32_t)P.stride;
     const bool bulk = P.stage != kStagePlain;
-    const bool two = bulk && P.nbuf == 2;
+    const bool two = bulk && P.nbuf_enc == 2;
     const uint64_t G = gridDim.x;
 
     uint8_t *s_dense0 = smem;                                        // nbuf staging buffers
-    uint8_t *s_planes = smem + (uint32_t)P.nbuf * P.smem_dense;
+    uint8_t *s_planes = smem + (uint32_t)P.nbuf_enc * P.smem_dense;
     uint8_t *s_exc = s_planes + P.smem_planes;                       // the tile's exception bytes, in order
 
     if (tid == 0 && bulk) {
@@ -796,32 +797,37 @@ __global__ void __launch_bounds__(kRowTile) prepare_encode_kernel(const __grid_c
 
     const uint32_t nw = C / 4;                       // whole words of a row
     const uint32_t tailn = C & 3u;                   // kRdShift only
-    unsigned long long off = 0;                      // exceptions of the tiles before `lo`
-    uint64_t lo = 0;
+    const uint32_t ntiles = (uint32_t)P.num_tiles;
+    unsigned long long off = 0;                      // exceptions of the tiles before this one
     bool bad = false, over = false;
-    for (uint32_t k = 0;; ++k) {
-        const uint64_t tile = blockIdx.x + (uint64_t)k * G;
-        if (tile >= P.num_tiles) break;
+    // The next tile's row counts and bases, and this thread's share of the
+    // totals of the tiles between it and the previous one, are loaded one
+    // tile ahead (tile totals of one window of G tiles fit 32 bits).
+    uint32_t nx_count = 0, nx_base = 0, nx_part = 0;
+    auto prefetch = [&](uint32_t t, uint32_t from) {
+        nx_count = nx_base = nx_part = 0;
+        if (t >= ntiles) return;
+        const uint32_t r = t * (uint32_t)kRowTile + tid;
+        if (tid < (int)tile_rows(P, t)) {
+            nx_count = P.exc_index[r];
+            nx_base = P.base[r];
+        }
+        for (uint32_t j = from + tid; j < t; j += kRowTile) nx_part += P.tile_total[j];
+    };
+    prefetch(blockIdx.x, 0);
+    for (uint32_t k = 0, tile = blockIdx.x; tile < ntiles; ++k, tile += (uint32_t)G) {
         const int buf = two ? (int)(k & 1u) : 0;
         const int bar = (int)(k & 1u);
         uint8_t *s_dense = s_dense0 + (uint32_t)buf * P.smem_dense;
-        if (two && warp == 0 && tile + G < P.num_tiles)
+        if (two && warp == 0 && tile + G < ntiles)
             stage_issue(P, tile + G, s_dense0 + (uint32_t)(buf ^ 1) * P.smem_dense, &s_bar[bar ^ 1], lane);
 
-        // exceptions of tiles [lo, tile), added to the running offset
-        unsigned long long part = 0;
-        for (uint64_t j = lo + tid; j < tile; j += kRowTile) part += P.tile_total[j];
-        part = warp_sum64(part);
+        const uint32_t count = nx_count, base = nx_base;
+        const uint32_t part = __reduce_add_sync(kFull, nx_part);
         if (lane == 0) s_part[k & 1u][warp] = part;
-
-        const uint64_t r0 = tile * (uint64_t)kRowTile;
+        const uint32_t r0 = tile * (uint32_t)kRowTile;
         const int nr = (int)tile_rows(P, tile);
         const bool mine = tid < nr;
-        uint32_t count = 0, base = 0;
-        if (mine) {
-            count = P.exc_index[r0 + tid];
-            base = P.base[r0 + tid];
-        }
         uint32_t wtot;
         const uint32_t wex = warp_excl_scan(count, lane, wtot);
         if (lane == 0) s_wsum[k & 1u][warp] = wtot;
@@ -834,10 +840,10 @@ __global__ void __launch_bounds__(kRowTile) prepare_encode_kernel(const __grid_c
             btot += s_wsum[k & 1u][w];
             off += s_part[k & 1u][w];
         }
-        lo = tile;
+        prefetch(tile + (uint32_t)G, tile);
         const uint32_t pre = boff + wex;
         if (mine) P.exc_index[r0 + tid] = (uint32_t)(off + pre);
-        if (tile == P.num_tiles - 1 && tid == 0) {
+        if (tile == ntiles - 1 && tid == 0) {
             const unsigned long long all = off + btot;
             P.exc_index[P.rows] = (uint32_t)all;
             if (all > 0xFFFFFFFFull) flag(P.err, CSF_DEV_ERR_CAPACITY);
@@ -948,21 +954,22 @@ __global__ void __launch_bounds__(kRowTile) prepare_encode_kernel(const __grid_c
             if (pos != pre + count) bad = true;           // the two kernels must agree on the count
         }
         __syncthreads();   // planes and exceptions staged; the tile's rows are read
-        if (!two && bulk && warp == 0 && tile + G < P.num_tiles)
+        if (!two && bulk && warp == 0 && tile + G < ntiles)
             stage_issue(P, tile + G, s_dense0, &s_bar[bar ^ 1], lane);
         // planes of the tile, cleared again for the next one
+        const uint64_t e0 = (uint64_t)r0 * C;
         if (KIND == CSF_NVFP4) {
-            const uint32_t nbytes = (((tile_rows(P, tile) * C) + 1) / 2 + 15) & ~15u;
-            uint4 *dst = reinterpret_cast<uint4 *>(P.offsets + r0 * C / 2);
+            const uint32_t nbytes = (((uint32_t)nr * C + 1) / 2 + 15) & ~15u;
+            uint4 *dst = reinterpret_cast<uint4 *>(P.offsets + e0 / 2);
             for (uint32_t i = tid; i < nbytes / 16; i += kRowTile) {
                 dst[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
                 reinterpret_cast<uint4 *>(s_planes)[i] = make_uint4(0, 0, 0, 0);
             }
         } else {
-            const uint32_t nbytes = (((tile_rows(P, tile) * C) + 7) / 8 + 15) & ~15u;
+            const uint32_t nbytes = (((uint32_t)nr * C + 7) / 8 + 15) & ~15u;
             const uint32_t pbytes = P.smem_planes / 2;
-            uint4 *dso = reinterpret_cast<uint4 *>(P.offsets + r0 * C / 8);
-            uint4 *dse = reinterpret_cast<uint4 *>(P.escapes + r0 * C / 8);
+            uint4 *dso = reinterpret_cast<uint4 *>(P.offsets + e0 / 8);
+            uint4 *dse = reinterpret_cast<uint4 *>(P.escapes + e0 / 8);
             for (uint32_t i = tid; i < nbytes / 16; i += kRowTile) {
                 dso[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
                 dse[i] = reinterpret_cast<const uint4 *>(s_planes + pbytes)[i];
@@ -992,16 +999,12 @@ static int row_read(int32_t C) {
     return kRdShift;
 }
 
-// Smem row stride of the staged tile: rows read as 16-byte vectors get an odd
-// number of 16-byte slots (8 lanes of a quarter warp hit distinct banks),
-// rows read as words an odd number of words; byte-aligned rows stay packed.
-static int32_t rows_stride(int32_t C) {
-    switch (row_read(C)) {
-    case kRdVec: return ((C / 16) % 2 == 1) ? C : C + 16;
-    case kRdWord: return ((C / 4) % 2 == 1) ? C : C + 4;
-    default: return C;
-    }
-}
+// Smem row stride of the staged tile: the rows stay packed, as in global
+// memory, so that one bulk copy stages a whole tile.  (Padding rows to an
+// odd number of 16-byte slots made quarter-warp vector reads conflict-free,
+// but a copy per row cost more: MXFP4's 160-byte rows took 128 bulk copies
+// per tile.)
+static int32_t rows_stride(int32_t C) { return C; }
 
 int32_t prepare_tile_rows(int32_t kind, int32_t C) {
     if (rows_path(C)) return kRowTile;
@@ -1018,19 +1021,18 @@ static uint32_t planes_bytes(int32_t kind, uint64_t te) {
     return kind == CSF_NVFP4 ? round16((te + 1) / 2) : 2 * round16((te + 7) / 8);
 }
 
-// Whether the row kernels stage tiles with bulk copies: the dense pointer
-// must be 16-byte aligned, and the rows either packed (one copy per tile) or
-// of a multiple of 16 bytes (one copy per padded row).  Otherwise every
-// thread loads part of the tile.
+// Whether the row kernels stage tiles with bulk copies (one per tile): the
+// dense pointer must be 16-byte aligned.  Otherwise every thread loads part
+// of the tile.
 static int rows_stage(int32_t C, const void *dense) {
-    if ((reinterpret_cast<uintptr_t>(dense) & 15u) != 0) return kStagePlain;
-    if (rows_stride(C) == C) return kStageTile;
-    if (C % 16 == 0) return kStageRows;
-    return kStagePlain;
+    (void)C;
+    return (reinterpret_cast<uintptr_t>(dense) & 15u) != 0 ? kStagePlain : kStageTile;
 }
 
 static uint32_t rows_dense_bytes(int32_t C) { return round16((uint64_t)kRowTile * rows_stride(C) + 16); }
-static uint32_t rows_hist_bytes() { return 4u * kHistWords * kRowTile; }
+// Bins of the base kernel: 33 words a row for NVFP4, 9 for MXFP4, at least
+// the 8 x 32 words a warp's exact fallback uses.
+static uint32_t rows_hist_bytes(int32_t kind) { return 4u * (kind == CSF_NVFP4 ? 33u : 9u) * kRowTile; }
 // Shared-memory stage of the encode kernel's exception bytes: a tile with
 // more exceptions writes them straight to the stream instead.
 static uint32_t rows_exc_stage(int32_t C) {
@@ -1039,8 +1041,12 @@ static uint32_t rows_exc_stage(int32_t C) {
 }
 // Two staging buffers (the next tile loading while one is worked on) unless
 // they would cost the base kernel residency: up to 48 KB with the bins.
-static int rows_nbuf(int32_t C, bool bulk) {
-    return bulk && rows_hist_bytes() + 2u * rows_dense_bytes(C) <= 48u * 1024u ? 2 : 1;
+static int rows_nbuf(int32_t kind, int32_t C, bool bulk) {
+    return bulk && rows_hist_bytes(kind) + 2u * rows_dense_bytes(C) <= 52u * 1024u ? 2 : 1;
+}
+static int rows_nbuf_enc(int32_t kind, int32_t C, bool bulk) {
+    const uint32_t rest = planes_bytes(kind, (uint64_t)kRowTile * C) + rows_exc_stage(C);
+    return bulk && 2u * rows_dense_bytes(C) + rest <= 52u * 1024u ? 2 : 1;
 }
 
 // Dynamic shared memory of a launch.  Row path: the base kernel holds the
@@ -1050,8 +1056,9 @@ static int rows_nbuf(int32_t C, bool bulk) {
 size_t prepare_smem_bytes(int32_t kind, int32_t C, int32_t tr, bool staged) {
     const uint64_t te = (uint64_t)tr * C;
     if (rows_path(C)) {
-        const uint32_t nb = (uint32_t)rows_nbuf(C, staged) * rows_dense_bytes(C);
-        const size_t base = rows_hist_bytes() + nb, enc = nb + planes_bytes(kind, te) + rows_exc_stage(C);
+        const size_t base = rows_hist_bytes(kind) + (uint32_t)rows_nbuf(kind, C, staged) * rows_dense_bytes(C);
+        const size_t enc = (uint32_t)rows_nbuf_enc(kind, C, staged) * rows_dense_bytes(C) + planes_bytes(kind, te) +
+                           rows_exc_stage(C);
         return base > enc ? base : enc;
     }
     return (size_t)round16(te) + planes_bytes(kind, te) + kWarps * 256 * 4 + (size_t)tr * 4 + round16(tr);
@@ -1098,10 +1105,11 @@ void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out,
     p.smem_planes = planes_bytes(g.kind, te);
     if (rows_path(g.cols)) {
         p.stride = rows_stride(g.cols);
-        p.smem_hist = rows_hist_bytes();
+        p.smem_hist = rows_hist_bytes(g.kind);
         p.smem_dense = rows_dense_bytes(g.cols);
         p.stage = rows_stage(g.cols, dense);
-        p.nbuf = rows_nbuf(g.cols, p.stage != kStagePlain);
+        p.nbuf = rows_nbuf(g.kind, g.cols, p.stage != kStagePlain);
+        p.nbuf_enc = rows_nbuf_enc(g.kind, g.cols, p.stage != kStagePlain);
         p.exc_stage = rows_exc_stage(g.cols);
     } else {
         p.stride = g.cols;
@@ -1128,10 +1136,10 @@ static cudaError_t launch_persistent(K kernel, const PrepParams &p, size_t smem,
 
 template <int KIND, int RD>
 static cudaError_t launch_rows_rd(const PrepParams &p, cudaStream_t s) {
-    const uint32_t nb = (uint32_t)p.nbuf * p.smem_dense;
-    cudaError_t e = launch_persistent(prepare_base_kernel<KIND, RD>, p, p.smem_hist + nb, s);
+    cudaError_t e = launch_persistent(prepare_base_kernel<KIND, RD>, p, p.smem_hist + (uint32_t)p.nbuf * p.smem_dense, s);
     if (e != cudaSuccess) return e;
-    return launch_persistent(prepare_encode_kernel<KIND, RD>, p, nb + p.smem_planes + p.exc_stage, s);
+    return launch_persistent(prepare_encode_kernel<KIND, RD>, p,
+                             (uint32_t)p.nbuf_enc * p.smem_dense + p.smem_planes + p.exc_stage, s);
 }
 
 template <int KIND>
