@@ -1046,7 +1046,7 @@ static int rows_nbuf(int32_t kind, int32_t C, bool bulk) {
 }
 static int rows_nbuf_enc(int32_t kind, int32_t C, bool bulk) {
     const uint32_t rest = planes_bytes(kind, (uint64_t)kRowTile * C) + rows_exc_stage(C);
-    return bulk && 2u * rows_dense_bytes(C) + rest <= 52u * 1024u ? 2 : 1;
+    return bulk && 2u * rows_dense_bytes(C) + rest <= 40u * 1024u ? 2 : 1;
 }
 
 // Dynamic shared memory of a launch.  Row path: the base kernel holds the
