@@ -408,7 +408,13 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm, max_steps):
     pk = timed_steps(torch, lambda i: csf.tiled_pack(bc[i % 4]), n(20), 3)
     rec("gate_tiled_packed", durs, packed + bw[0].numel(),
         {"packed_MB": round(packed / 1e6, 3), "pack_us": round(1e3 * pk[0] / pk[1], 1)})
-    del bc, bw, tps
+    # the same tiles rebuilt per stage in shared memory only (the device
+    # decoder of include/csf_tile.cuh), one 4-byte checksum per tile written
+    sums = [torch.empty(tps[0].tile_index.numel() - 1, dtype=torch.int32, device="cuda") for _ in range(4)]
+    durs = timed_steps(torch, lambda i: csf.tiled_checksums(tps[i % 4], sums[i % 4]), n(400), 20)
+    rec("gate_tiled_stage_read", durs, packed + 4 * sums[0].numel(),
+        {"written_MB": round(4 * sums[0].numel() / 1e6, 3), "decoded_to": "shared memory"})
+    del bc, bw, tps, sums
 
     # the down stack alone (C = 50: lane chunks span up to three rows), then
     # paired with the gate

@@ -72,7 +72,7 @@
 extern "C" {
 #endif
 
-#define CSF_ABI_VERSION 4
+#define CSF_ABI_VERSION 5
 
 typedef enum {
     CSF_OK = 0,
@@ -373,6 +373,27 @@ csf_status csf_tiled_pack(const csf_stack *src, csf_tiled *dst, uint64_t exc_cap
  */
 csf_status csf_tiled_decode(const csf_tiled *t, uint8_t *ws, size_t ws_bytes,
                             const void *expert_start, int expert_start_is_int64, void *stream);
+
+/*
+ * Stage-read check of a tile-packed stack ([B478] commit message on packed
+ * experts whose scales each GEMM pipeline stage rebuilds in shared memory):
+ * every tile of the selected experts is rebuilt in shared memory by the
+ * device decoder of csf_tile.cuh (csf_tile_decode_warp), as a stage would
+ * before consuming it, and only a 32-bit checksum per tile is written -- no
+ * decoded scales reach global memory.  Checksum of a tile = sum over its 128
+ * little-endian 32-bit words w_i, in the CSF_LAYOUT_BLOCKED order of the
+ * tile's 512 bytes, of w_i * (2i + 1), modulo 2^32.
+ *
+ *   sums, sums_count  device array of at least E * T uint32, T = tiles per
+ *                     expert (ceil(R/128) * ceil(C/4)); sums[e*T + t].
+ *   expert_start      as csf_decode: entries of inactive experts are not
+ *                     written.
+ * A tile whose index disagrees with its codes sets CSF_DEV_ERR_CORRUPT.
+ * Errors: CSF_ERR_ARG, CSF_ERR_SIZE (sums_count < E*T), CSF_ERR_UNSUPPORTED
+ * (routing with E > 8192), CSF_ERR_CUDA.
+ */
+csf_status csf_tiled_checksum(const csf_tiled *t, uint32_t *sums, size_t sums_count, const void *expert_start,
+                              int expert_start_is_int64, void *stream);
 
 /*
  * Failure-detection self-test of the prepare's bounded waits, synchronous.

@@ -33,7 +33,7 @@ def nvcc() -> str:
 def _inputs():
     files = [os.path.join(CSRC, s) for s in SOURCES]
     files += [os.path.join(CSRC, "csf_internal.cuh"), os.path.join(CSRC, "csf_device.cuh"),
-              os.path.join(INCLUDE, "csf.h")]
+              os.path.join(INCLUDE, "csf.h"), os.path.join(INCLUDE, "csf_tile.cuh")]
     return files
 
 

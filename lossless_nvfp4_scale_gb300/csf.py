@@ -16,6 +16,7 @@ Typical use::
     sf = csf.decode(stack, layout=csf.LAYOUT_BLOCKED)     # GEMM scale-operand layout
     tp = csf.tiled_pack(stack)                            # stage-readable tile-packed form
     sf = csf.tiled_decode(tp)                             # same bytes as the line above
+    sums = csf.tiled_checksums(tp)                        # each tile rebuilt in shared memory only
     ev = csf.expand_scales([(gate, gate_ws), (down, down_ws)], side_stream, after=last_read)
     torch.cuda.current_stream().wait_event(ev)            # before the call that reads them
 """
@@ -106,6 +107,8 @@ def _load():
     lib.csf_tiled_pack.restype = ctypes.c_int
     lib.csf_tiled_decode.argtypes = [ctypes.POINTER(CTiled), _c_vp, ctypes.c_size_t, _c_vp, ctypes.c_int, _c_vp]
     lib.csf_tiled_decode.restype = ctypes.c_int
+    lib.csf_tiled_checksum.argtypes = [ctypes.POINTER(CTiled), _c_vp, ctypes.c_size_t, _c_vp, ctypes.c_int, _c_vp]
+    lib.csf_tiled_checksum.restype = ctypes.c_int
     lib.csf_selftest_lookback_timeout.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.csf_selftest_lookback_timeout.restype = ctypes.c_int
     return lib
@@ -449,6 +452,27 @@ def tiled_decode(t: Tiled, ws: torch.Tensor | None = None, expert_start: torch.T
     _check(lib.csf_tiled_decode(ctypes.byref(ct), ws.data_ptr(), ws.numel(), ptr, is64, _stream(stream)),
            "csf_tiled_decode")
     return ws
+
+
+def tiled_checksums(t: Tiled, sums: torch.Tensor | None = None, expert_start: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """Rebuild every tile of a tile-packed stack in shared memory with the
+    device decoder of include/csf_tile.cuh (as a GEMM pipeline stage would)
+    and return one 32-bit checksum per tile (csf_tiled_checksum): sum of
+    w_i * (2i + 1) mod 2^32 over the tile's 128 little-endian words, as int32
+    storage of uint32 values [E * T]."""
+    tiles = sizes(t.kind, t.E, t.R, t.C)["tiled_index"] // 4 - 1
+    if sums is None:
+        sums = torch.zeros(tiles, dtype=torch.int32, device=t.codes.device)
+    if sums.dtype != torch.int32 or not sums.is_cuda or not sums.is_contiguous():
+        raise CsfError("tiled_checksums: sums must be a contiguous int32 CUDA tensor")
+    if expert_start is not None and expert_start.numel() != t.E + 1:
+        raise CsfError("expert_start must have E+1 entries")
+    ptr, is64 = _es(expert_start)
+    ct = t.cstruct()
+    _check(lib.csf_tiled_checksum(ctypes.byref(ct), sums.data_ptr(), sums.numel(), ptr, is64, _stream(stream)),
+           "csf_tiled_checksum")
+    return sums
 
 
 def selftest_lookback_timeout() -> int:

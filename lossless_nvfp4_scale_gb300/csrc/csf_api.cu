@@ -538,6 +538,58 @@ csf_status csf_tiled_decode(const csf_tiled *t, uint8_t *ws, size_t ws_bytes, co
     return CSF_OK;
 }
 
+csf_status csf_tiled_checksum(const csf_tiled *t, uint32_t *sums, size_t sums_count, const void *expert_start,
+                              int expert_start_is_int64, void *stream) {
+    if (!t || !sums) return CSF_ERR_ARG;
+    uint64_t n = 0, rows = 0;
+    csf_status st = geometry(&t->g, &n, &rows);
+    if (st != CSF_OK) return st;
+    const csf_geometry &g = t->g;
+    if (!t->codes || !t->bases || !t->tile_index || !aligned16(t->codes) || !aligned16(t->bases)) return CSF_ERR_ARG;
+    if (t->num_exc > 0 && !t->exc_bytes) return CSF_ERR_ARG;
+    if (t->num_exc > 0xFFFFFFFFull) return CSF_ERR_ARG;
+    const uint64_t tiles = (uint64_t)g.num_experts * (((uint64_t)g.rows + kTileRows - 1) / kTileRows) *
+                           (((uint64_t)g.cols + 3) / 4);
+    if (sums_count < tiles) return CSF_ERR_SIZE;
+    if (expert_start && g.num_experts > kMaxRoutedExperts) return CSF_ERR_UNSUPPORTED;
+    DecStack S;
+    std::memset(&S, 0, sizeof S);
+    S.err = t->error_word;
+    S.rows = rows;
+    S.n = n;
+    S.R = g.rows;
+    S.C = g.cols;
+    S.kind = g.kind;
+    TiledIn I;
+    std::memset(&I, 0, sizeof I);
+    I.codes = t->codes;
+    I.bases = t->bases;
+    I.tile_index = t->tile_index;
+    I.exc_bytes = t->exc_bytes;
+    I.num_exc = t->num_exc;
+    I.expert_start = expert_start;
+    I.es64 = expert_start_is_int64 ? 1 : 0;
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != CSF_OK) return st;
+    const size_t smem = expert_start ? 4ull * (uint64_t)g.num_experts : 0;
+    int occ = 0;
+    if (tiled_checksum_occupancy(g.kind, smem, &occ) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    if (occ < 1) occ = 1;
+    uint64_t grid = (uint64_t)di.sms * (uint64_t)occ;
+    const uint64_t need = (tiles + 3) / 4;
+    if (need < grid) grid = need;
+    if (grid < 1) grid = 1;
+    if (launch_tiled_checksum(S, I, sums, (int)grid, smem, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return CSF_ERR_CUDA;
+    }
+    return CSF_OK;
+}
+
 csf_status csf_selftest_lookback_timeout(uint32_t *error_word) {
     if (!error_word) return CSF_ERR_ARG;
     *error_word = 0;

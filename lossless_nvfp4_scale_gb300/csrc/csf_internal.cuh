@@ -152,6 +152,9 @@ struct TiledIn {
 cudaError_t launch_tiled_pack(const DecStack &S, const TiledOut &O, int grid, cudaStream_t s);
 cudaError_t tiled_decode_occupancy(int kind, size_t smem, int *blocks_per_sm);
 cudaError_t launch_tiled_decode(const DecStack &S, const TiledIn &I, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_tiled_checksum(const DecStack &S, const TiledIn &I, uint32_t *sums, int grid, size_t smem,
+                                  cudaStream_t s);
+cudaError_t tiled_checksum_occupancy(int kind, size_t smem, int *blocks_per_sm);
 
 // Geometry checks shared by every entry point: sets N = E*R*C and rows = E*R.
 csf_status check_geometry(const csf_geometry *g, uint64_t *n, uint64_t *rows);

@@ -26,11 +26,11 @@
 // in the block-scaled layout, which sits at byte 512*(global tile) + 16*b.
 #include "csf_device.cuh"
 #include "csf_internal.cuh"
+#include "csf_tile.cuh"
 
 namespace csfk {
 namespace {
 
-using dev::add_base;
 using dev::flag;
 using dev::kFull;
 using dev::lanemask_lt;
@@ -181,145 +181,110 @@ __global__ void __launch_bounds__(kTlThreads) tiled_pack_kernel(const __grid_con
 }
 
 // ---------------------------------------------------------------- decode
+//
+// The per-tile decode is the public device API of include/csf_tile.cuh
+// (csf_tile_load, csf_tile_expand, csf_tile_patch, csf_tile_mask_edge), so
+// this kernel and any consumer kernel that rebuilds tiles in shared memory
+// run the same code.
 
-// The raw inputs of one tile for lane b: its 8 code bytes (NVFP4) or 2 + 2
-// plane bytes (MXFP4), its 4 row bases, and the tile's index entries.
-struct TileRaw {
-    uint64_t code;
-    uint32_t bw;
-    uint32_t x0, x1;     // tile_index[tile], tile_index[tile + 1] (lane 0 only)
-};
-
-// `tile` is the global tile, `rbg` the global row block (expert * nrb + rb).
-template <int KIND>
-__device__ __forceinline__ TileRaw tile_load(const TiledIn &I, uint64_t tile, uint64_t rbg, int lane) {
-    TileRaw r;
-    r.bw = __ldg(reinterpret_cast<const uint32_t *>(I.bases) + rbg * 32 + lane);
-    if (KIND == CSF_NVFP4) {
-        r.code = __ldg(reinterpret_cast<const unsigned long long *>(I.codes + tile * 256) + lane);
-    } else {
-        const uint16_t *c16 = reinterpret_cast<const uint16_t *>(I.codes + tile * 128);
-        r.code = (uint64_t)__ldg(c16 + lane) | ((uint64_t)__ldg(c16 + 32 + lane) << 32);
-    }
-    r.x0 = r.x1 = 0;
-    if (lane == 0) {
-        r.x0 = __ldg(I.tile_index + tile);
-        r.x1 = __ldg(I.tile_index + tile + 1);
-    }
-    return r;
+__device__ __forceinline__ csf_tile_src tile_src(const DecStack &S, const TiledIn &I) {
+    csf_tile_src s;
+    s.codes = I.codes;
+    s.bases = I.bases;
+    s.tile_index = I.tile_index;
+    s.exc_bytes = I.exc_bytes;
+    s.num_exc = (uint32_t)I.num_exc;
+    s.kind = S.kind;
+    s.R = S.R;
+    s.C = S.C;
+    return s;
 }
 
-// One tile from its raw inputs, whole warp: lane b writes line b (16 bytes)
-// at dst + 16*b.  `line` is the lane's own 16-byte shared-memory slot, where
-// it patches its exceptions byte by byte; `edge` says that the tile holds
-// padding (rows past R or columns past C), which is written as 0.  Returns
-// true when the tile's index disagrees with its codes.
-template <int KIND>
-__device__ __forceinline__ bool tile_finish(const TiledIn &I, const Geo &g, uint32_t rb, uint32_t cb, bool edge,
-                                            const TileRaw &r, uint8_t *dst, uint4 *line, int lane) {
-    const uint32_t bw = r.bw;
-    uint32_t w0, w1, w2, w3, cnt;
-    uint64_t f;                                                 // escape flags: bit 4j (NVFP4) / bit j (MXFP4)
-    if (KIND == CSF_NVFP4) {
-        const uint32_t x0 = (uint32_t)r.code, x1 = (uint32_t)(r.code >> 32);
-        const uint32_t l0 = x0 & 0x0F0F0F0Fu, h0 = (x0 >> 4) & 0x0F0F0F0Fu;
-        const uint32_t l1 = x1 & 0x0F0F0F0Fu, h1 = (x1 >> 4) & 0x0F0F0F0Fu;
-        w0 = __byte_perm(l0, h0, 0x5140);
-        w1 = __byte_perm(l0, h0, 0x7362);
-        w2 = __byte_perm(l1, h1, 0x5140);
-        w3 = __byte_perm(l1, h1, 0x7362);
-        const uint32_t f0 = x0 & (x0 >> 1) & (x0 >> 2) & (x0 >> 3) & 0x11111111u;
-        const uint32_t f1 = x1 & (x1 >> 1) & (x1 >> 2) & (x1 >> 3) & 0x11111111u;
-        cnt = __popc(f0) + __popc(f1);
-        f = (uint64_t)f0 | ((uint64_t)f1 << 32);
-    } else {
-        const uint32_t o16 = (uint32_t)r.code & 0xFFFFu, x16 = (uint32_t)(r.code >> 32) & 0xFFFFu;
-        w0 = ((o16 & 0xFu) * 0x00204081u) & 0x01010101u;          // bit i -> byte i
-        w1 = (((o16 >> 4) & 0xFu) * 0x00204081u) & 0x01010101u;
-        w2 = (((o16 >> 8) & 0xFu) * 0x00204081u) & 0x01010101u;
-        w3 = ((o16 >> 12) * 0x00204081u) & 0x01010101u;
-        f = x16;
-        cnt = __popc(x16);
-    }
-    // row bases, byte a of bw for word a, added byte by byte modulo 256
-    w0 = add_base(__byte_perm(bw, 0, 0x0000), w0);
-    w1 = add_base(__byte_perm(bw, 0, 0x1111), w1);
-    w2 = add_base(__byte_perm(bw, 0, 0x2222), w2);
-    w3 = add_base(__byte_perm(bw, 0, 0x3333), w3);
-    uint32_t tot;
-    const uint32_t pre = warp_excl_scan(cnt, lane, tot);
-    const uint32_t X = __shfl_sync(kFull, r.x0, 0);
-    bool bad = false;
-    if (cnt) {
-        // Lane-private patch: no other lane reads or writes this slot.
-        *line = make_uint4(w0, w1, w2, w3);
-        uint8_t *lb = reinterpret_cast<uint8_t *>(line);
-        uint32_t k = X + pre;
-        do {
-            const uint32_t j = KIND == CSF_NVFP4 ? (uint32_t)(__ffsll((long long)f) - 1) >> 2
-                                                 : (uint32_t)(__ffsll((long long)f) - 1);
-            f &= f - 1;
-            uint8_t v = 0;
-            if (k < (uint32_t)I.num_exc) v = __ldg(I.exc_bytes + k);
-            else bad = true;
-            ++k;
-            lb[j] = v;
-        } while (f);
+// One tile from its raw inputs, whole warp.  `line` is the lane's own
+// 16-byte shared-memory slot, where lanes with exceptions patch them byte by
+// byte; `edge` says that the tile holds padding (rows past R or columns past
+// C), which is written as 0.  STAGE = false: lane b writes line b (16 bytes)
+// at dst + 16*b.  STAGE = true: the warp's 32 slots hold the rebuilt tile (512
+// bytes, block-scaled order) in shared memory, as a pipeline stage would
+// consume it, and lane 0 writes the tile's checksum to *sum (the sum of its
+// 128 little-endian words w_i times 2i + 1, mod 2^32).  Returns true when the
+// tile's index disagrees with its codes.
+template <int KIND, bool STAGE>
+__device__ __forceinline__ bool tile_finish(const csf_tile_src &src, uint32_t rb, uint32_t cb, bool edge,
+                                            const csf_tile_raw &r, uint8_t *dst, uint32_t *sum, uint4 *line,
+                                            int lane) {
+    const csf_tile_line L = csf_tile_expand<KIND>(r);
+    uint32_t w0 = L.w0, w1 = L.w1, w2 = L.w2, w3 = L.w3;
+    if (STAGE || L.cnt) *line = make_uint4(w0, w1, w2, w3);
+    const bool bad = csf_tile_patch<KIND>(src, r, L, reinterpret_cast<uint8_t *>(line), lane);
+    if (L.cnt) {
         const uint4 q = *line;
         w0 = q.x; w1 = q.y; w2 = q.z; w3 = q.w;
     }
-    if (edge) {
-        const uint32_t rl = rb * kTileRows + (uint32_t)lane;
-        const uint32_t cv = min(4u, g.C - 4u * cb);
-        const uint32_t cm = cv >= 4 ? 0xFFFFFFFFu : (1u << (8 * cv)) - 1;
-        w0 = rl < g.R ? w0 & cm : 0u;
-        w1 = rl + 32 < g.R ? w1 & cm : 0u;
-        w2 = rl + 64 < g.R ? w2 & cm : 0u;
-        w3 = rl + 96 < g.R ? w3 & cm : 0u;
+    if (edge) csf_tile_mask_edge(src, rb, cb, lane, w0, w1, w2, w3);
+    if (STAGE) {
+        if (edge) *line = make_uint4(w0, w1, w2, w3);
+        __syncwarp();   // the whole tile is in shared memory
+        const uint32_t k = 8u * (uint32_t)lane + 1u;   // 2 * (4 lane) + 1
+        const uint32_t part = w0 * k + w1 * (k + 2u) + w2 * (k + 4u) + w3 * (k + 6u);
+        const uint32_t tsum = __reduce_add_sync(kFull, part);
+        if (lane == 0) *sum = tsum;
+        __syncwarp();   // the slots may be reused for the next tile
+    } else {
+        *reinterpret_cast<uint4 *>(dst + 16u * (uint32_t)lane) = make_uint4(w0, w1, w2, w3);
     }
-    *reinterpret_cast<uint4 *>(dst + 16u * (uint32_t)lane) = make_uint4(w0, w1, w2, w3);
-    if (lane == 0 && X + tot != r.x1) bad = true;
     return bad;
 }
 
-template <int KIND>
+// The experts to decode, compacted into `act` in shared memory with ballots
+// (whole block; routing read on the device).  Returns how many; without
+// routing every expert, and `act` is not used.
+__device__ uint32_t active_experts(const TiledIn &I, uint32_t E, uint32_t *act, uint32_t *s_cnt) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    if (I.expert_start == nullptr) return E;
+    uint32_t n_act = 0;
+    for (uint32_t e0 = 0; e0 < E; e0 += kTlThreads) {
+        const uint32_t e = e0 + threadIdx.x;
+        bool a = false;
+        if (e < E) {
+            if (I.es64) {
+                const long long *st = static_cast<const long long *>(I.expert_start);
+                a = __ldg(st + e + 1) > __ldg(st + e);
+            } else {
+                const int *st = static_cast<const int *>(I.expert_start);
+                a = __ldg(st + e + 1) > __ldg(st + e);
+            }
+        }
+        const uint32_t bal = __ballot_sync(kFull, a);
+        if (lane == 0) s_cnt[warp] = __popc(bal);
+        __syncthreads();
+        uint32_t bn = n_act, tn = 0;
+#pragma unroll
+        for (int w = 0; w < kTlWarps; ++w) {
+            if (w < warp) bn += s_cnt[w];
+            tn += s_cnt[w];
+        }
+        if (a) act[bn + __popc(bal & lanemask_lt())] = e;
+        n_act += tn;
+        __syncthreads();
+    }
+    return n_act;
+}
+
+// Decode (STAGE = false: into the block-scaled workspace S.ws) or stage-read
+// (STAGE = true: each tile rebuilt in shared memory, one checksum per tile
+// written to sums[e * T + t]) the tiles of the selected experts.
+template <int KIND, bool STAGE>
 __global__ void __launch_bounds__(kTlThreads) tiled_decode_kernel(const __grid_constant__ DecStack S,
-                                                                   const __grid_constant__ TiledIn I) {
+                                                                   const __grid_constant__ TiledIn I,
+                                                                   uint32_t *sums) {
     extern __shared__ __align__(16) uint32_t act[];
     __shared__ uint32_t s_cnt[kTlWarps];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const Geo g = geo_of(S);
-    const uint32_t E = (uint32_t)(S.rows / g.R);
-    uint32_t n_act = E;
-    if (I.expert_start != nullptr) {
-        n_act = 0;
-        for (uint32_t e0 = 0; e0 < E; e0 += kTlThreads) {
-            const uint32_t e = e0 + threadIdx.x;
-            bool a = false;
-            if (e < E) {
-                if (I.es64) {
-                    const long long *st = static_cast<const long long *>(I.expert_start);
-                    a = __ldg(st + e + 1) > __ldg(st + e);
-                } else {
-                    const int *st = static_cast<const int *>(I.expert_start);
-                    a = __ldg(st + e + 1) > __ldg(st + e);
-                }
-            }
-            const uint32_t bal = __ballot_sync(kFull, a);
-            if (lane == 0) s_cnt[warp] = __popc(bal);
-            __syncthreads();
-            uint32_t bn = n_act, tn = 0;
-#pragma unroll
-            for (int w = 0; w < kTlWarps; ++w) {
-                if (w < warp) bn += s_cnt[w];
-                tn += s_cnt[w];
-            }
-            if (a) act[bn + __popc(bal & lanemask_lt())] = e;
-            n_act += tn;
-            __syncthreads();
-        }
-    }
+    const uint32_t n_act = active_experts(I, (uint32_t)(S.rows / g.R), act, s_cnt);
     const uint64_t total = (uint64_t)n_act * g.T;
     const uint64_t nw = (uint64_t)gridDim.x * kTlWarps;
     const uint64_t w = (uint64_t)blockIdx.x * kTlWarps + warp;
@@ -329,6 +294,7 @@ __global__ void __launch_bounds__(kTlThreads) tiled_decode_kernel(const __grid_c
     __shared__ uint4 s_line[kTlWarps][32];
     uint4 *line = &s_line[warp][lane];
     const uint32_t full_rb = g.R / kTileRows, full_cb = g.C / 4;  // row / column blocks without padding
+    const csf_tile_src src = tile_src(S, I);
     bool bad = false;
     const uint64_t it0 = total * w / nw;
     uint32_t n = (uint32_t)(total * (w + 1) / nw - it0);
@@ -337,8 +303,8 @@ __global__ void __launch_bounds__(kTlThreads) tiled_decode_kernel(const __grid_c
     uint32_t rb = t / g.ncb, cb = t - rb * g.ncb;
     uint64_t e = I.expert_start != nullptr && n ? act[j] : j;
     uint64_t tile = e * g.T + t, rbg = e * g.nrb + rb;
-    TileRaw cur;
-    if (n) cur = tile_load<KIND>(I, tile, rbg, lane);
+    csf_tile_raw cur;
+    if (n) cur = csf_tile_load<KIND>(src, tile, rbg, lane);
     for (; n; --n) {
         uint32_t jn = j, tn = t + 1, rbn = rb, cbn = cb + 1;
         uint64_t tilen = tile + 1, rbgn = rbg;
@@ -351,10 +317,11 @@ __global__ void __launch_bounds__(kTlThreads) tiled_decode_kernel(const __grid_c
                 rbgn = en * g.nrb;
             }
         }
-        TileRaw nxt;
-        if (n > 1) nxt = tile_load<KIND>(I, tilen, rbgn, lane);
+        csf_tile_raw nxt;
+        if (n > 1) nxt = csf_tile_load<KIND>(src, tilen, rbgn, lane);
         const bool edge = rb >= full_rb || cb >= full_cb;
-        bad |= tile_finish<KIND>(I, g, rb, cb, edge, cur, S.ws + tile * 512, line, lane);
+        bad |= tile_finish<KIND, STAGE>(src, rb, cb, edge, cur, STAGE ? nullptr : S.ws + tile * 512,
+                                        STAGE ? sums + tile : nullptr, line, lane);
         cur = nxt;
         j = jn; t = tn; rb = rbn; cb = cbn; tile = tilen; rbg = rbgn;
     }
@@ -362,6 +329,23 @@ __global__ void __launch_bounds__(kTlThreads) tiled_decode_kernel(const __grid_c
 }
 
 }  // namespace
+
+cudaError_t launch_tiled_checksum(const DecStack &S, const TiledIn &I, uint32_t *sums, int grid, size_t smem,
+                                  cudaStream_t s) {
+    if (S.kind == CSF_NVFP4)
+        tiled_decode_kernel<CSF_NVFP4, true><<<grid, kTlThreads, smem, s>>>(S, I, sums);
+    else
+        tiled_decode_kernel<CSF_MXFP4, true><<<grid, kTlThreads, smem, s>>>(S, I, sums);
+    return cudaGetLastError();
+}
+
+cudaError_t tiled_checksum_occupancy(int kind, size_t smem, int *blocks_per_sm) {
+    if (kind == CSF_NVFP4)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tiled_decode_kernel<CSF_NVFP4, true>,
+                                                             kTlThreads, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tiled_decode_kernel<CSF_MXFP4, true>,
+                                                         kTlThreads, smem);
+}
 
 cudaError_t launch_tiled_pack(const DecStack &S, const TiledOut &O, int grid, cudaStream_t s) {
     if (S.kind == CSF_NVFP4)
@@ -373,17 +357,17 @@ cudaError_t launch_tiled_pack(const DecStack &S, const TiledOut &O, int grid, cu
 
 cudaError_t tiled_decode_occupancy(int kind, size_t smem, int *blocks_per_sm) {
     if (kind == CSF_NVFP4)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tiled_decode_kernel<CSF_NVFP4>,
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tiled_decode_kernel<CSF_NVFP4, false>,
                                                              kTlThreads, smem);
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tiled_decode_kernel<CSF_MXFP4>, kTlThreads,
-                                                         smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tiled_decode_kernel<CSF_MXFP4, false>,
+                                                         kTlThreads, smem);
 }
 
 cudaError_t launch_tiled_decode(const DecStack &S, const TiledIn &I, int grid, size_t smem, cudaStream_t s) {
     if (S.kind == CSF_NVFP4)
-        tiled_decode_kernel<CSF_NVFP4><<<grid, kTlThreads, smem, s>>>(S, I);
+        tiled_decode_kernel<CSF_NVFP4, false><<<grid, kTlThreads, smem, s>>>(S, I, nullptr);
     else
-        tiled_decode_kernel<CSF_MXFP4><<<grid, kTlThreads, smem, s>>>(S, I);
+        tiled_decode_kernel<CSF_MXFP4, false><<<grid, kTlThreads, smem, s>>>(S, I, nullptr);
     return cudaGetLastError();
 }
 

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(csf):
 
 
 def test_abi_version_and_status_strings(csf):
-    assert csf.lib.csf_abi_version() == 4
+    assert csf.lib.csf_abi_version() == 5
     for code, text in [(0, "ok"), (1, "invalid argument"), (2, "buffer too small"),
                        (3, "unsupported geometry"), (4, "CUDA error")]:
         assert csf.lib.csf_status_string(code).decode() == text
