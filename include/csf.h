@@ -184,8 +184,9 @@ csf_status csf_prepare(const uint8_t *dense, csf_stack *out, uint64_t exc_capaci
  * process whose caching allocator owns all device memory, code that runs
  * where an allocation would implicitly synchronise the device or disturb a
  * stream capture, code with a fixed memory budget.  This entry point
- * allocates nothing: its scratch (a ticket counter and one look-back word per
- * tile of rows) is a CSF_STATIC_SCRATCH_BYTES device array inside the library.
+ * allocates nothing: its scratch (the per-tile exception totals of rows up
+ * to 255 bytes; a ticket counter and one look-back word per tile of wider
+ * rows) is a CSF_STATIC_SCRATCH_BYTES device array inside the library.
  * The caller still passes `dense` and every output buffer, as for csf_prepare,
  * and the results are the same bytes.
  *
@@ -194,8 +195,9 @@ csf_status csf_prepare(const uint8_t *dense, csf_stack *out, uint64_t exc_capaci
  * context; make that first call before any stream capture.  A device reset
  * (cudaDeviceReset) destroys the context and the array with it: the next call
  * runs in a new context and looks the address up again, as a first call.
- * Every call shares the one array and clears the part it uses on `stream`
- * first: calls that overlap on the GPU race, so order them.
+ * Every call shares the one array (rows wider than 255 bytes clear the part
+ * they use on `stream` first): calls that overlap on the GPU race, so order
+ * them.
  * Errors: as csf_prepare, plus CSF_ERR_SIZE when the geometry needs more than
  * CSF_STATIC_SCRATCH_BYTES of scratch (16 + 8 bytes per tile of rows; tiles
  * are 128 rows when C <= 255, so about 4 million rows).

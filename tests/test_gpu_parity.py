@@ -530,11 +530,12 @@ def test_mxfp4_word_wise_and_general_segments_in_one_launch(csf, C):
     assert st.errors() == 0
 
 
-# Row widths that reach every way the prepare kernel reads rows and stages
-# tiles: 16-byte vectors with one bulk copy per tile (C/16 odd) or one per row
-# (C/16 even, padded rows), words with a tile copy (C/4 odd) or plain loads
-# (C/4 even, padded rows), and byte-shifted words for C % 4 != 0; wider rows
-# than 255 bytes take the warp-per-row kernel.
+# Row widths that reach every way the two row kernels read a staged row:
+# 16-byte vectors (C % 16 == 0), aligned words (C % 4 == 0) and byte-shifted
+# words (C % 4 != 0); narrow rows run double-buffered and wide ones (C of 200
+# and more) single-buffered; ragged last tiles and tiles whose byte count is
+# not a multiple of 16 (tail loaded plainly).  Rows wider than 255 bytes take
+# the single-pass kernel with the decoupled look-back.
 PREP_WIDTHS = [(0, 3, 150, 48), (0, 3, 150, 128), (0, 2, 130, 200), (0, 2, 70, 252), (0, 3, 131, 100),
                (0, 2, 140, 8), (0, 2, 133, 72), (0, 3, 129, 7), (0, 2, 150, 50), (0, 2, 135, 255),
                (0, 2, 60, 256), (1, 3, 150, 160), (1, 2, 100, 200), (1, 2, 140, 96), (1, 2, 131, 100),
