@@ -379,14 +379,15 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const __grid_constant
 // (it divides into 32 and 128-element pieces), so each tile's planes start on
 // a 16-byte boundary.
 constexpr int kRowTile = 128;
-// Relative histogram of a row: bins for the values [a, a + bins) around the
-// row's anchor a, and one bin for every byte outside them.  NVFP4 windows
-// span 15 values: 32 bins hold them with room on both sides; MXFP4 windows
-// span 2: 8 bins do.
+// NVFP4 base search: a relative histogram of the row, with bins for the
+// values [a, a + 32) around the row's anchor a = median - 16 and one bin for
+// every byte outside them (windows span 15 values: 32 bins hold them with
+// room on both sides).  MXFP4 windows span 2 values: the row's counts of
+// the three values a, a + 1, a + 2 around a = median - 1 decide it (no bins).
 template <int KIND> struct Bins {
     static constexpr int n = KIND == CSF_NVFP4 ? 32 : 8;
     static constexpr int words = n + 1;
-    static constexpr int lead = KIND == CSF_NVFP4 ? 16 : 3;   // anchor = median - lead
+    static constexpr int lead = KIND == CSF_NVFP4 ? 16 : 1;   // anchor = median - lead
 };
 constexpr uint32_t kH = 0x80808080u;   // bit 7 of each byte
 
@@ -526,6 +527,37 @@ __device__ __forceinline__ void hist_byte(uint32_t *hcol, uint32_t v, uint32_t a
     atomicAdd(hcol + min(d, (uint32_t)NB) * kRowTile, 1u);
 }
 
+// MXFP4: counts of the row's bytes in [a, a + 1), [a, a + 2) and [a, a + 3)
+// from one word (A4 = a in every byte).  Bytes below a wrap to at least
+// 256 - a >= 3 (a <= 253), so they are never counted.
+__device__ __forceinline__ void count3_word(uint32_t x, uint32_t A4, uint32_t &n1, uint32_t &n2, uint32_t &n3) {
+    uint32_t below;
+    const uint32_t d = sub_bytes(x, A4, below);
+    const uint32_t dh = d | kH;
+    // d < k in a byte: bit 7 clear both in d and in (d | 0x80) - k
+    n1 += __popc(~(dh - 0x01010101u) & ~d & kH);
+    n2 += __popc(~(dh - 0x02020202u) & ~d & kH);
+    n3 += __popc(~(dh - 0x03030303u) & ~d & kH);
+}
+
+// MXFP4 base rule from the counts c0, c1, c2 of the values a, a + 1, a + 2
+// (a <= 253): the better of the windows [a, a + 1] and [a + 1, a + 2] (each
+// only if its first value is present), when a bound proves it the best of
+// the row.  Windows [v, v + 1] with v < a hold at most one of the counted
+// values, a: at most C - c1 - c2 bytes, which must be fewer than the best
+// (ties go to the smaller value); windows with v > a + 1 hold at most a + 2:
+// at most C - c0 - c1, which may equal it.  Returns the packed key
+// (count << 8) | (255 - base), 0 when the proof fails.
+__device__ __forceinline__ uint32_t count3_key(uint32_t C, uint32_t a, uint32_t c0, uint32_t c1, uint32_t c2) {
+    uint32_t best = 0;
+    if (c0) best = ((c0 + c1) << 8) | (255u - a);
+    if (c1) best = max(best, ((c1 + c2) << 8) | (254u - a));
+    const uint32_t M = best >> 8;
+    const bool ok_low = a == 0 || C - c1 - c2 < M;
+    const bool ok_high = C - c0 - c1 <= M;
+    return ok_low && ok_high ? best : 0u;
+}
+
 // Base rule on the relative histogram h[0..n] (h[n] = bytes outside
 // [a, a + n)): the best window among those lying inside the bins, and
 // whether that is provably the best window of the whole row.  Returns the
@@ -661,10 +693,12 @@ __device__ __forceinline__ void stage_wait(const PrepParams &P, uint64_t t, uint
     }
 }
 
-// Base kernel: one thread per row.  Each row is histogrammed into 32 bins
-// around the median of five of its bytes; the best window inside them is its
-// base when the bound of window_key proves it, else the row's warp finds the
-// base exactly over all 256 values (exact_key).  Writes base[row], the row's
+// Base kernel: one thread per row.  NVFP4 rows are histogrammed into 32 bins
+// around the median of five of their bytes and the best window inside them
+// is the base when the bound of window_key proves it; MXFP4 rows count the
+// three values around that median and count3_key proves one of their two
+// windows.  Without a proof, the row's warp finds the base exactly over all
+// 256 values (exact_key).  Writes base[row], the row's
 // exception count into exc_index[row] (until the encode kernel replaces it)
 // and the tile's total into the scratch.
 template <int KIND, int RD>
@@ -709,30 +743,52 @@ __global__ void __launch_bounds__(kRowTile) prepare_base_kernel(const __grid_con
         const bool mine = tid < nr;
         const uint8_t *rowb = s_dense + (uint32_t)tid * stride;
         uint32_t *hcol = s_hist + tid;
-        uint32_t a = 0;
+        uint32_t a = 0, n1 = 0, n2 = 0, n3 = 0;
         if (mine) {
             constexpr int NB = Bins<KIND>::n;
-#pragma unroll
-            for (int i = 0; i < Bins<KIND>::words; ++i) hcol[i * kRowTile] = 0;
             const uint32_t med = median5(rowb[0], rowb[C / 4], rowb[C / 2], rowb[(3 * C) / 4], rowb[C - 1]);
-            a = min(max((int)med - Bins<KIND>::lead, 0), 256 - NB);
-            const uint32_t A4 = a * 0x01010101u;
             const RowWords<RD> rw(rowb);
-            for (uint32_t g = 0; g < nw / 8; ++g) {
-                uint32_t x[8];
-                rw.group(g, x);
+            if constexpr (KIND == CSF_NVFP4) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) hist_word<NB>(hcol, x[j], A4);
+                for (int i = 0; i < Bins<KIND>::words; ++i) hcol[i * kRowTile] = 0;
+                a = min(max((int)med - Bins<KIND>::lead, 0), 256 - NB);
+                const uint32_t A4 = a * 0x01010101u;
+                for (uint32_t g = 0; g < nw / 8; ++g) {
+                    uint32_t x[8];
+                    rw.group(g, x);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) hist_word<NB>(hcol, x[j], A4);
+                }
+                for (uint32_t q = nw & ~7u; q < nw; ++q) hist_word<NB>(hcol, rw.word(q), A4);
+                for (uint32_t c = 4 * nw; c < C; ++c) hist_byte<NB>(hcol, rowb[c], a);
+            } else {
+                a = min(max((int)med - Bins<KIND>::lead, 0), 253);
+                const uint32_t A4 = a * 0x01010101u;
+                for (uint32_t g = 0; g < nw / 8; ++g) {
+                    uint32_t x[8];
+                    rw.group(g, x);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) count3_word(x[j], A4, n1, n2, n3);
+                }
+                for (uint32_t q = nw & ~7u; q < nw; ++q) count3_word(rw.word(q), A4, n1, n2, n3);
+                for (uint32_t c = 4 * nw; c < C; ++c) {
+                    const uint32_t d = (uint32_t)rowb[c] - a;   // below a: wraps far above 3
+                    n1 += d < 1u;
+                    n2 += d < 2u;
+                    n3 += d < 3u;
+                }
             }
-            for (uint32_t q = nw & ~7u; q < nw; ++q) hist_word<NB>(hcol, rw.word(q), A4);
-            for (uint32_t c = 4 * nw; c < C; ++c) hist_byte<NB>(hcol, rowb[c], a);
         }
         if (!two) {
-            // every row is histogrammed: with one buffer, refill it now
+            // every row is read: with one buffer, refill it now
             __syncthreads();
             if (bulk && warp == 0 && tile + G < ntiles) stage_issue(P, tile + G, s_dense0, &s_bar[bar ^ 1], lane);
         }
-        uint32_t key = mine ? window_key<KIND>(hcol, a) : 0u;
+        uint32_t key = 0;
+        if (mine) {
+            if constexpr (KIND == CSF_NVFP4) key = window_key<KIND>(hcol, a);
+            else key = count3_key(C, a, n1, n2 - n1, n3 - n2);
+        }
         // rows whose window the bound cannot prove: exact over all 256 values
         uint32_t redo = __ballot_sync(kFull, mine && key == 0);
         while (redo) {
@@ -1030,19 +1086,21 @@ static int rows_stage(int32_t C, const void *dense) {
 }
 
 static uint32_t rows_dense_bytes(int32_t C) { return round16((uint64_t)kRowTile * rows_stride(C) + 16); }
-// Bins of the base kernel: 33 words a row for NVFP4, 9 for MXFP4, at least
-// the 8 x 32 words a warp's exact fallback uses.
-static uint32_t rows_hist_bytes(int32_t kind) { return 4u * (kind == CSF_NVFP4 ? 33u : 9u) * kRowTile; }
+// Bins of the base kernel: 33 words a row for NVFP4; MXFP4 keeps none, but
+// every kind needs the 8 x 32 words a warp's exact fallback uses.
+static uint32_t rows_hist_bytes(int32_t kind) { return 4u * (kind == CSF_NVFP4 ? 33u : 8u) * kRowTile; }
 // Shared-memory stage of the encode kernel's exception bytes: a tile with
 // more exceptions writes them straight to the stream instead.
 static uint32_t rows_exc_stage(int32_t C) {
     const uint32_t all = round16((uint64_t)kRowTile * C);
     return all < 4096u ? all : 4096u;
 }
-// Two staging buffers (the next tile loading while one is worked on) unless
-// they would cost the base kernel residency: up to 48 KB with the bins.
+// Two staging buffers (the next tile loading while one is worked on) only
+// while the base kernel keeps 8 blocks per SM (24 KB with the bins); else one
+// buffer, refilled as soon as its rows have been read: more resident blocks
+// hide the copies better (gate 53.7 -> 52.2 us, MXFP4 122.5 -> 117.7 us).
 static int rows_nbuf(int32_t kind, int32_t C, bool bulk) {
-    return bulk && rows_hist_bytes(kind) + 2u * rows_dense_bytes(C) <= 52u * 1024u ? 2 : 1;
+    return bulk && rows_hist_bytes(kind) + 2u * rows_dense_bytes(C) <= 24u * 1024u ? 2 : 1;
 }
 static int rows_nbuf_enc(int32_t kind, int32_t C, bool bulk) {
     const uint32_t rest = planes_bytes(kind, (uint64_t)kRowTile * C) + rows_exc_stage(C);

@@ -560,11 +560,12 @@ def test_prepare_rows_every_staging_path(csf, kind, E, R, C, offset):
 
 
 def _adversarial_rows(kind, C, seed):
-    """Rows built against the prepare's fast base search: it histograms each
-    row in 32 bins around the median of the bytes at columns 0, C/4, C/2,
-    3C/4 and C-1, and proves the best window there against the bytes it
-    cannot see.  These rows defeat the anchor or the proof, or sit on the
-    edges of the byte range, so both the fast and the exact paths run."""
+    """Rows built against the prepare's fast base search: around the median m
+    of the bytes at columns 0, C/4, C/2, 3C/4 and C-1 it histograms each
+    NVFP4 row in 32 bins, and counts the values m-1, m, m+1 of each MXFP4
+    row; it then proves the best window there against the bytes it cannot
+    see.  These rows defeat the anchor or the proof, or sit on the edges of
+    the byte range, so both the fast and the exact paths run."""
     rng = np.random.default_rng(seed)
     w = 14 if kind == 0 else 1
     rows = []
@@ -589,6 +590,24 @@ def _adversarial_rows(kind, C, seed):
         rows.append(np.clip(r, 0, 255))
         rows.append(np.full(C, int(rng.integers(0, 256))))                    # constant
         rows.append((np.arange(C) * 7 + int(rng.integers(0, 256))) % 256)      # every value once or so
+        if kind == 1:
+            # MXFP4: the counted values m-1, m, m+1 against the windows beside them
+            probes_at = np.zeros(C, bool)
+            probes_at[probes] = True
+            m = int(rng.integers(3, 250))
+            r = np.where(rng.random(C) < 0.5, m - 2, m - 1)                  # best window just below m - 1
+            r[probes_at] = m
+            rows.append(r)
+            r = np.where(rng.random(C) < 0.5, m + 2, m + 3)                  # best window just above m + 1
+            r[probes_at] = m
+            rows.append(r)
+            r = rng.choice([m - 1, m, m + 1], C)                              # [m-1, m] and [m, m+1] tie or nearly
+            rows.append(r)
+            r = np.where(rng.random(C) < 0.4, m, m + 1)
+            r[rng.random(C) < 0.3] = m + 2                                    # a third value beside the window
+            rows.append(r)
+            rows.append(rng.choice([253, 254, 255], C))                       # median at the top: m - 1 clamped
+            rows.append(rng.choice([0, 1, 2], C))                             # median 0: no window below
     return np.array(rows, dtype=np.uint8)
 
 
