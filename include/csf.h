@@ -106,7 +106,7 @@ typedef struct {
     uint64_t offsets;         /* packed offsets rounded up to 16 */
     uint64_t escapes;         /* MXFP4 escape plane rounded up to 16; 0 for NVFP4 */
     uint64_t exc_index;       /* 4*(rows+1) */
-    uint64_t prepare_scratch; /* scratch for csf_prepare */
+    uint64_t prepare_scratch; /* scratch for csf_prepare's fastest path */
     uint64_t blocked;         /* a workspace in CSF_LAYOUT_BLOCKED: E * (R up to 128) * (C up to 4) */
     uint64_t tiled_codes;     /* csf_tiled codes: 256 (NVFP4) or 128 (MXFP4) bytes a tile */
     uint64_t tiled_bases;     /* csf_tiled bases: 128 bytes per expert and 128-row block */
@@ -157,18 +157,30 @@ csf_status csf_sizes(const csf_geometry *g, csf_sizes_t *out);
  *                  dropped and CSF_DEV_ERR_CAPACITY is set; exc_index is
  *                  complete either way, so the caller can re-run with a
  *                  buffer of exc_index[rows] bytes.  E*R*C always suffices.
- *   scratch        device, csf_sizes().prepare_scratch bytes, 8-byte
- *                  aligned; needs no initialisation.  Calls that share a
- *                  scratch buffer must not overlap on the GPU.
- * Rows of up to 255 bytes take two kernels: the first picks each row's base
- * and counts its exceptions (per-tile totals go to the scratch), the second
- * places each tile in the exception stream from the totals before it and
- * encodes; no block waits on another.  Wider rows take one kernel whose
- * blocks pass exception-count prefixes to later blocks through the scratch
- * (a decoupled look-back, cleared by this call on `stream`); every wait is
- * bounded and sets CSF_DEV_ERR_TIMEOUT rather than hang.
+ *   scratch        device, 8-byte aligned, scratch_bytes long; needs no
+ *                  initialisation.  Calls that share a scratch buffer must
+ *                  not overlap on the GPU.  csf_sizes().prepare_scratch is
+ *                  the size that takes the fastest path; the least accepted
+ *                  size is 16 bytes plus 8 per tile of rows (128-row tiles
+ *                  for rows of up to 255 bytes).
+ * Rows of up to 255 bytes (tiles of 128 rows, one thread per row):
+ *   - with at least csf_sizes().prepare_scratch bytes of scratch, and up to
+ *     8192 tiles (1 M rows), one pass per tile picks each row's base,
+ *     writes the planes, each row's place inside its tile in exc_index and
+ *     the tile's exception bytes to its slot in the scratch (128 * C bytes
+ *     a tile: the scratch is about the size of the dense stack); a second
+ *     kernel adds each tile's offset in the stream (the sum of the earlier
+ *     tiles' totals) to the exc_index entries and copies the slots into the
+ *     stream;
+ *   - with less, two kernels: the first picks the bases and counts the
+ *     exceptions (per-tile totals in the scratch), the second places each
+ *     tile in the stream from the totals before it and encodes.
+ * No block waits on another.  Wider rows take one kernel whose blocks pass
+ * exception-count prefixes to later blocks through the scratch (a decoupled
+ * look-back, cleared by this call on `stream`); every wait is bounded and
+ * sets CSF_DEV_ERR_TIMEOUT rather than hang.
  * Errors: CSF_ERR_ARG (NULL, misaligned planes, dense not in device memory),
- * CSF_ERR_SIZE (scratch too small), CSF_ERR_CUDA.
+ * CSF_ERR_SIZE (scratch smaller than the least accepted size), CSF_ERR_CUDA.
  */
 csf_status csf_prepare(const uint8_t *dense, csf_stack *out, uint64_t exc_capacity,
                        void *scratch, size_t scratch_bytes, void *stream);

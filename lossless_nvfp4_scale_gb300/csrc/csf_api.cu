@@ -36,6 +36,8 @@ csf_status prepare_check(const uint8_t *dense, const csf_stack *out, uint64_t ex
     const int32_t tr = prepare_tile_rows(g.kind, g.cols);
     if ((uint64_t)tr * g.cols >= (1ull << 24)) return CSF_ERR_UNSUPPORTED;
     plan->scratch_bytes = 16 + 8 * ((plan->rows + tr - 1) / tr);
+    plan->fused_bytes = prepare_fused_scratch_bytes(g.kind, g.cols, plan->rows);
+    plan->fused = false;
     plan->staged = true;
     plan->smem = 0;
     return CSF_OK;
@@ -63,7 +65,7 @@ csf_status prepare_enqueue(const uint8_t *dense, const csf_stack &out, uint64_t 
         return CSF_ERR_CUDA;
     }
     PrepParams p;
-    make_prep_params(p, dense, out, exc_capacity, scratch, plan.rows, plan.n, plan.staged);
+    make_prep_params(p, dense, out, exc_capacity, scratch, plan.rows, plan.n, plan.staged, plan.fused);
     if (launch_prepare(p, plan.smem, s) != cudaSuccess) {
         cudaGetLastError();
         return CSF_ERR_CUDA;
@@ -118,9 +120,13 @@ uint64_t round16(uint64_t v) { return (v + 15) & ~15ull; }
 
 csf_status geometry(const csf_geometry *g, uint64_t *n, uint64_t *rows) { return check_geometry(g, n, rows); }
 
-// Look-back scratch of a prepare: a ticket counter (16 bytes) and one 8-byte
-// status word per tile of rows.
+// Scratch of a prepare.  Rows of up to 255 bytes, up to 1 M of them: the
+// fused path's per-tile totals and exception slots (about the dense size).
+// Otherwise 16 bytes and one 8-byte word per tile of rows (per-tile totals
+// of the two-kernel path, or a ticket counter and look-back words).
 uint64_t prepare_scratch_bytes(const csf_geometry *g, uint64_t rows) {
+    const uint64_t fused = prepare_fused_scratch_bytes(g->kind, g->cols, rows);
+    if (fused) return fused;
     const int32_t tr = prepare_tile_rows(g->kind, g->cols);
     const uint64_t tiles = (rows + tr - 1) / tr;
     return 16 + 8 * tiles;
@@ -394,6 +400,7 @@ csf_status csf_prepare(const uint8_t *dense, csf_stack *out, uint64_t exc_capaci
     if (st != CSF_OK) return st;
     if ((reinterpret_cast<uintptr_t>(scratch) & 7u) != 0) return CSF_ERR_ARG;
     if (scratch_bytes < plan.scratch_bytes) return CSF_ERR_SIZE;
+    plan.fused = plan.fused_bytes != 0 && scratch_bytes >= plan.fused_bytes;
     st = prepare_configure(dense, out->g, &plan);
     if (st != CSF_OK) return st;
     return prepare_enqueue(dense, *out, exc_capacity, scratch, plan, static_cast<cudaStream_t>(stream));
@@ -627,7 +634,7 @@ csf_status csf_selftest_lookback_timeout(uint32_t *error_word) {
     st.exc_index = reinterpret_cast<uint32_t *>(mem + off_index);
     st.exc_bytes = mem + off_exc;
     st.error_word = reinterpret_cast<uint32_t *>(mem + off_err);
-    make_prep_params(p, mem + off_dense, st, n, mem + off_scratch, rows, n, false);
+    make_prep_params(p, mem + off_dense, st, n, mem + off_scratch, rows, n, false, false);
     p.spin_limit = 4096;
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess ||
         cudaMemsetAsync(mem, 0, off_scratch + need, s) != cudaSuccess ||

@@ -91,7 +91,10 @@ struct PrepParams {
     int32_t nbuf;                // base kernel: tile staging buffers (2: the next tile loads during this one)
     int32_t nbuf_enc;            // encode kernel: the same
     uint32_t exc_stage;          // encode kernel: bytes of the shared-memory exception stage
-    uint32_t pad3_;
+    uint32_t slot_bytes;         // fused path: bytes of a tile's exception slot in the scratch
+    uint8_t *slot;               // fused path: the slots (scratch), one per tile
+    int32_t fused;               // row path in one pass per tile plus a placing kernel
+    int32_t pad4_;
 };
 
 // Rows per unit so that a unit's first element starts a whole chunk.
@@ -167,7 +170,9 @@ csf_status check_geometry(const csf_geometry *g, uint64_t *n, uint64_t *rows);
 struct PrepPlan {
     uint64_t n;
     uint64_t rows;
-    uint64_t scratch_bytes;   // ticket counter + one look-back word per tile
+    uint64_t scratch_bytes;   // the least scratch: per-tile totals or look-back words
+    uint64_t fused_bytes;     // scratch of the fused row path (0: not available)
+    bool fused;               // the caller's scratch takes the fused row path
     bool staged;
     size_t smem;
 };
@@ -178,7 +183,10 @@ csf_status prepare_enqueue(const uint8_t *dense, const csf_stack &out, uint64_t 
 
 cudaError_t launch_prepare(const PrepParams &p, size_t smem, cudaStream_t s);
 void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity,
-                      void *scratch, uint64_t rows, uint64_t n, bool staged);
+                      void *scratch, uint64_t rows, uint64_t n, bool staged, bool fused);
+// Scratch bytes of the fused row path (rows of up to 255 bytes; 0 for wider
+// rows, which have no fused path).
+uint64_t prepare_fused_scratch_bytes(int32_t kind, int32_t C, uint64_t rows);
 size_t prepare_smem_bytes(int32_t kind, int32_t C, int32_t tr, bool staged);
 bool prepare_stages_rows(int32_t kind, int32_t C, const void *dense);
 bool prepare_needs_cleared_scratch(int32_t C);

@@ -16,9 +16,11 @@
 // exception stream): the smallest byte value present in the row whose window
 // [v, v+w] (w = 14 NVFP4, 1 MXFP4) holds the most of the row's bytes.
 //
-// Rows of up to 255 bytes (every workload of the pages) take two kernels, a
-// base kernel and an encode kernel, with no wait between blocks (see the
-// row-wise section below).  Wider rows take one single-pass kernel
+// Rows of up to 255 bytes (every workload of the pages) take one pass per
+// 128-row tile that writes each tile's exception bytes to a slot of the
+// scratch, then a kernel that places the slots in the stream; with a smaller
+// scratch, a base kernel and an encode kernel (see the row-wise section
+// below).  No block waits on another.  Wider rows take one single-pass kernel
 // (prepare_kernel): per tile of rows, one warp per row picks the base from a
 // 256-bin histogram, all threads pack the planes, and a block scan of the
 // exception counts is chained to the earlier tiles by a decoupled look-back
@@ -359,11 +361,19 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const __grid_constant
 
 // ---------------------------------------------------------------- row-wise
 //
-// Rows of C <= 255 bytes are prepared by two kernels with no wait between
-// blocks.  The exception stream needs every tile's position, which depends on
-// the exception counts of all earlier tiles; a single pass would make each
-// tile wait for the slowest of the hundreds of tiles in flight before it (a
+// Rows of C <= 255 bytes are prepared without any wait between blocks.  The
+// exception stream needs every tile's position, which depends on the
+// exception counts of all earlier tiles; a single pass would make each tile
+// wait for the slowest of the hundreds of tiles in flight before it (a
 // decoupled look-back measured 20 us of the gate stack's 78 us this way).
+// Fused path (the scratch holds a slot of 128 * C bytes per tile):
+//   fused kernel   per tile: each row's base, the planes, each row's place
+//                  inside the tile (exc_index[]), the tile's exception bytes
+//                  in its slot and its total.
+//   place kernel   per tile: its offset in the stream (the sum of the
+//                  earlier totals) added to its rows' exc_index entries, and
+//                  its slot copied into the stream.
+// Two-kernel path (a scratch of 8 bytes per tile):
 //   base kernel    per row: base byte and exception count (into base[] and,
 //                  for now, exc_index[]); per tile: its exception total.
 //   encode kernel  per tile: its offset in the exception stream (the sum of
@@ -371,9 +381,9 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const __grid_constant
 //                  (offset + block scan of the counts), the offset / escape
 //                  planes, and the exception bytes written straight to their
 //                  final positions.
-// Both are persistent: block b takes tiles b, b + G, b + 2G, ... (G = grid),
-// staging each tile in shared memory with bulk copies while it works on the
-// one before.
+// The fused, base and encode kernels are persistent: block b takes tiles b,
+// b + G, b + 2G, ... (G = grid), staging each tile in shared memory with bulk
+// copies while it works on the one before.
 
 // Rows (and threads) per block; a multiple of every chunk-alignment row count
 // (it divides into 32 and 128-element pieces), so each tile's planes start on
@@ -386,7 +396,6 @@ constexpr int kRowTile = 128;
 // the three values a, a + 1, a + 2 around a = median - 1 decide it (no bins).
 template <int KIND> struct Bins {
     static constexpr int n = KIND == CSF_NVFP4 ? 32 : 8;
-    static constexpr int words = n + 1;
     static constexpr int lead = KIND == CSF_NVFP4 ? 16 : 1;   // anchor = median - lead
 };
 constexpr uint32_t kH = 0x80808080u;   // bit 7 of each byte
@@ -572,9 +581,9 @@ __device__ __forceinline__ uint32_t window_key(const uint32_t *hcol, uint32_t a)
     constexpr int w = KIND == CSF_NVFP4 ? 14 : 1;
     constexpr int kBins = Bins<KIND>::n;
     constexpr int jmax = kBins - 1 - w;               // last window that lies inside the bins
-    uint32_t h[Bins<KIND>::words];
+    uint32_t h[Bins<KIND>::n + 1];
 #pragma unroll
-    for (int i = 0; i < Bins<KIND>::words; ++i) h[i] = hcol[i * kRowTile];
+    for (int i = 0; i <= Bins<KIND>::n; ++i) h[i] = hcol[i * kRowTile];
     const uint32_t out = h[kBins];
     const bool top = a + kBins == 256;                // the bins reach 255: every window is exact
     uint32_t best = 0, S = 0, low = 0, hi = 0;
@@ -693,14 +702,227 @@ __device__ __forceinline__ void stage_wait(const PrepParams &P, uint64_t t, uint
     }
 }
 
-// Base kernel: one thread per row.  NVFP4 rows are histogrammed into 32 bins
-// around the median of five of their bytes and the best window inside them
-// is the base when the bound of window_key proves it; MXFP4 rows count the
-// three values around that median and count3_key proves one of their two
-// windows.  Without a proof, the row's warp finds the base exactly over all
-// 256 values (exact_key).  Writes base[row], the row's
-// exception count into exc_index[row] (until the encode kernel replaces it)
-// and the tile's total into the scratch.
+// First pass over a staged row for its base: NVFP4 rows are histogrammed
+// into 32 bins around the median of five of their bytes (bins in the
+// thread's column `hcol`); MXFP4 rows count the three values around that
+// median (n1, n2, n3: bytes in [a, a+1), [a, a+2), [a, a+3)).  Returns the
+// anchor a.
+template <int KIND, int RD>
+__device__ __forceinline__ uint32_t row_scan(const uint8_t *rowb, uint32_t C, uint32_t *hcol, uint32_t &n1,
+                                             uint32_t &n2, uint32_t &n3) {
+    constexpr int NB = Bins<KIND>::n;
+    const uint32_t nw = C / 4;   // whole words of the row
+    const uint32_t med = median5(rowb[0], rowb[C / 4], rowb[C / 2], rowb[(3 * C) / 4], rowb[C - 1]);
+    const RowWords<RD> rw(rowb);
+    uint32_t a;
+    if constexpr (KIND == CSF_NVFP4) {
+#pragma unroll
+        for (int i = 0; i <= Bins<KIND>::n; ++i) hcol[i * kRowTile] = 0;
+        a = min(max((int)med - Bins<KIND>::lead, 0), 256 - NB);
+        const uint32_t A4 = a * 0x01010101u;
+        for (uint32_t g = 0; g < nw / 8; ++g) {
+            uint32_t x[8];
+            rw.group(g, x);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) hist_word<NB>(hcol, x[j], A4);
+        }
+        for (uint32_t q = nw & ~7u; q < nw; ++q) hist_word<NB>(hcol, rw.word(q), A4);
+        for (uint32_t c = 4 * nw; c < C; ++c) hist_byte<NB>(hcol, rowb[c], a);
+    } else {
+        a = min(max((int)med - Bins<KIND>::lead, 0), 253);
+        const uint32_t A4 = a * 0x01010101u;
+        for (uint32_t g = 0; g < nw / 8; ++g) {
+            uint32_t x[8];
+            rw.group(g, x);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) count3_word(x[j], A4, n1, n2, n3);
+        }
+        for (uint32_t q = nw & ~7u; q < nw; ++q) count3_word(rw.word(q), A4, n1, n2, n3);
+        for (uint32_t c = 4 * nw; c < C; ++c) {
+            const uint32_t d = (uint32_t)rowb[c] - a;   // below a: wraps far above 3
+            n1 += d < 1u;
+            n2 += d < 2u;
+            n3 += d < 3u;
+        }
+    }
+    return a;
+}
+
+// The row's base key (count << 8) | (255 - base) from its first pass when a
+// bound proves it (window_key, count3_key), else 0.
+template <int KIND>
+__device__ __forceinline__ uint32_t row_fast_key(const uint32_t *hcol, uint32_t C, uint32_t a, uint32_t n1,
+                                                 uint32_t n2, uint32_t n3) {
+    if constexpr (KIND == CSF_NVFP4) return window_key<KIND>(hcol, a);
+    else return count3_key(C, a, n1, n2 - n1, n3 - n2);
+}
+
+// Rows of the warp whose key is 0 (no proof): their warp applies the exact
+// rule over all 256 values, one row at a time, reading the row from global
+// memory (row0 = the row of lane 0).  Whole warp; uses the warp's columns of
+// the bins.
+template <int KIND>
+__device__ __forceinline__ uint32_t settle_keys(const PrepParams &P, uint32_t key, bool mine, uint64_t row0,
+                                                uint32_t *s_hist, int warp, int lane) {
+    const uint32_t C = (uint32_t)P.C;
+    uint32_t redo = __ballot_sync(kFull, mine && key == 0);
+    while (redo) {
+        const int src_lane = __ffs(redo) - 1;
+        redo &= redo - 1;
+        const uint32_t k2 = exact_key<KIND>(P.dense + (row0 + (uint64_t)src_lane) * C, C, s_hist, warp, lane);
+        if (lane == src_lane) key = k2;
+    }
+    return key;
+}
+
+// Encodes one staged row against its base: its codes go into the tile's
+// planes in shared memory (s_planes: NVFP4 nibbles, or MXFP4 offset bits
+// then escape bits in the second half; the row starts at tile element el0)
+// and its exception bytes to positions pos, pos + 1, ... of `stage` (shared
+// memory) when `staged`, else of `gdst` (global memory, `gcap` bytes
+// available: later bytes are dropped and `over` set).  Word by word:
+// byte-wise subtract, range test, nibble or bit gather; escape positions are
+// taken 8 words at a time and walked in element order.  Returns the position
+// after the row's last exception.
+template <int KIND, int RD>
+__device__ __forceinline__ uint32_t encode_row(const uint8_t *rowb, uint32_t C, uint32_t base, uint32_t el0,
+                                               uint8_t *s_planes, uint32_t planes_bytes, uint8_t *stage, bool staged,
+                                               uint8_t *gdst, uint64_t gcap, uint32_t pos, bool &over) {
+    const uint32_t nw = C / 4;                       // whole words of the row
+    const uint32_t tailn = C & 3u;                   // kRdShift only
+    const uint32_t B4 = base * 0x01010101u;
+    const RowWords<RD> rw(rowb);
+    uint32_t *pw = reinterpret_cast<uint32_t *>(s_planes);
+    uint32_t *px = reinterpret_cast<uint32_t *>(s_planes + planes_bytes / 2);
+    // the exception bytes of the 8 words from word k0 on: bit 4j + i of
+    // `em` = byte i of word j (bit order = element order)
+    auto emit = [&](uint32_t em, uint32_t k0) {
+        const uint8_t *src = rowb + 4 * k0;
+        if (staged) {
+            while (em) {
+                const uint32_t i = (uint32_t)(__ffs(em) - 1);
+                em &= em - 1;
+                stage[pos++] = src[i];
+            }
+        } else {
+            while (em) {
+                const uint32_t i = (uint32_t)(__ffs(em) - 1);
+                em &= em - 1;
+                if (pos < gcap) gdst[pos] = src[i];
+                else over = true;
+                ++pos;
+            }
+        }
+    };
+    constexpr uint32_t kW1 = KIND == CSF_NVFP4 ? 0x0F0F0F0Fu : 0x02020202u;   // (w + 1) per byte
+    // codes of word k (bytes x; `valid` masks the bytes of a tail word)
+    // and its escape nibble (bit i = byte i outside [b, b + w])
+    auto code = [&](uint32_t x, uint32_t valid, uint32_t &ob4) -> uint32_t {
+        uint32_t below;
+        const uint32_t d = sub_bytes(x, B4, below);
+        const uint32_t o = ((((d | kH) - kW1) | d | below) & kH) & valid;
+        const uint32_t m = byte_mask(o);
+        if (KIND == CSF_NVFP4) {
+            const uint32_t c = ((d & ~m) | (0x0F0F0F0Fu & m)) & valid;
+            const uint32_t t = c | (c >> 4);
+            ob4 = __byte_perm(t, 0, 0x4420);                                // 4 nibbles
+        } else {
+            ob4 = (((d & ~m) & 0x01010101u & valid) * 0x10204080u) >> 28;  // 4 offset bits
+        }
+        return (o * 0x00204081u) >> 28;
+    };
+    auto store_nv = [&](uint32_t k, uint32_t cd) {
+        const uint32_t el = el0 + 4 * k;
+        if (RD != kRdShift) {
+            reinterpret_cast<uint16_t *>(s_planes)[el >> 2] = (uint16_t)cd;
+        } else {
+            const uint32_t sh = 4 * (el & 7u);
+            atomicOr(pw + (el >> 3), cd << sh);
+            if (sh > 16 && (cd >> (32 - sh)) != 0) atomicOr(pw + (el >> 3) + 1, cd >> (32 - sh));
+        }
+    };
+    auto store_mx = [&](uint32_t el, uint32_t o, uint32_t e, uint32_t bits) {   // `bits` bits at element el
+        const uint32_t sh = el & 31u;
+        if (o) atomicOr(pw + (el >> 5), o << sh);
+        if (e) atomicOr(px + (el >> 5), e << sh);
+        if (sh + bits > 32) {
+            if (o >> (32 - sh)) atomicOr(pw + (el >> 5) + 1, o >> (32 - sh));
+            if (e >> (32 - sh)) atomicOr(px + (el >> 5) + 1, e >> (32 - sh));
+        }
+    };
+    for (uint32_t g = 0; g < nw / 8; ++g) {
+        uint32_t x[8];
+        rw.group(g, x);
+        uint32_t em = 0, ow = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t cd;
+            const uint32_t e4 = code(x[j], 0xFFFFFFFFu, cd);
+            em |= e4 << (4 * j);
+            if (KIND == CSF_NVFP4) store_nv(8 * g + j, cd);
+            else ow |= cd << (4 * j);
+        }
+        if (KIND == CSF_MXFP4) {
+            const uint32_t el = el0 + 32 * g;
+            if (RD != kRdShift && (el & 31u) == 0) {
+                pw[el >> 5] = ow;
+                px[el >> 5] = em;
+            } else {
+                store_mx(el, ow, em, 32);
+            }
+        }
+        if (em) emit(em, 8 * g);
+    }
+    // remaining whole words and the tail word, in one last group
+    uint32_t em = 0;
+    const uint32_t k0 = nw & ~7u;
+    for (uint32_t q = k0; q < nw + (tailn ? 1u : 0u); ++q) {
+        const uint32_t valid = q < nw ? 0xFFFFFFFFu : 0xFFFFFFFFu >> (32 - 8 * tailn);
+        uint32_t cd;
+        const uint32_t e4 = code(rw.word(q), valid, cd);
+        em |= e4 << (4 * (q - k0));
+        if (KIND == CSF_NVFP4) store_nv(q, cd);
+        else store_mx(el0 + 4 * q, cd, e4, 4);
+    }
+    emit(em, k0);
+    return pos;
+}
+
+// Writes the tile's planes from shared memory to the stack (16-byte pieces;
+// the tile starts at element e0 on a 16-byte boundary of each plane) and,
+// when `clear`, zeroes them for the next tile.  Whole block.
+template <int KIND>
+__device__ __forceinline__ void write_planes(const PrepParams &P, uint8_t *s_planes, uint64_t e0, uint32_t nr,
+                                             bool clear, int tid) {
+    const uint32_t C = (uint32_t)P.C;
+    if (KIND == CSF_NVFP4) {
+        const uint32_t nbytes = ((nr * C + 1) / 2 + 15) & ~15u;
+        uint4 *dst = reinterpret_cast<uint4 *>(P.offsets + e0 / 2);
+        for (uint32_t i = tid; i < nbytes / 16; i += kRowTile) {
+            dst[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
+            if (clear) reinterpret_cast<uint4 *>(s_planes)[i] = make_uint4(0, 0, 0, 0);
+        }
+    } else {
+        const uint32_t nbytes = ((nr * C + 7) / 8 + 15) & ~15u;
+        const uint32_t pbytes = P.smem_planes / 2;
+        uint4 *dso = reinterpret_cast<uint4 *>(P.offsets + e0 / 8);
+        uint4 *dse = reinterpret_cast<uint4 *>(P.escapes + e0 / 8);
+        for (uint32_t i = tid; i < nbytes / 16; i += kRowTile) {
+            dso[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
+            dse[i] = reinterpret_cast<const uint4 *>(s_planes + pbytes)[i];
+            if (clear) {
+                reinterpret_cast<uint4 *>(s_planes)[i] = make_uint4(0, 0, 0, 0);
+                reinterpret_cast<uint4 *>(s_planes + pbytes)[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
+}
+
+// Base kernel (two-kernel path): one thread per row.  Each row's base comes
+// from row_scan and row_fast_key, or from the exact rule when no bound
+// proves it.  Writes base[row], the row's exception count into
+// exc_index[row] (until the encode kernel replaces it) and the tile's total
+// into the scratch.
 template <int KIND, int RD>
 __global__ void __launch_bounds__(kRowTile) prepare_base_kernel(const __grid_constant__ PrepParams P) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -726,7 +948,6 @@ __global__ void __launch_bounds__(kRowTile) prepare_base_kernel(const __grid_con
     __syncthreads();
     if (bulk && warp == 0 && blockIdx.x < P.num_tiles) stage_issue(P, blockIdx.x, s_dense0, &s_bar[0], lane);
 
-    const uint32_t nw = C / 4;                       // whole words of a row
     const uint32_t ntiles = (uint32_t)P.num_tiles;
     for (uint32_t k = 0, tile = blockIdx.x; tile < ntiles; ++k, tile += (uint32_t)G) {
         // buffer and barrier of this tile: with two buffers they alternate;
@@ -744,60 +965,14 @@ __global__ void __launch_bounds__(kRowTile) prepare_base_kernel(const __grid_con
         const uint8_t *rowb = s_dense + (uint32_t)tid * stride;
         uint32_t *hcol = s_hist + tid;
         uint32_t a = 0, n1 = 0, n2 = 0, n3 = 0;
-        if (mine) {
-            constexpr int NB = Bins<KIND>::n;
-            const uint32_t med = median5(rowb[0], rowb[C / 4], rowb[C / 2], rowb[(3 * C) / 4], rowb[C - 1]);
-            const RowWords<RD> rw(rowb);
-            if constexpr (KIND == CSF_NVFP4) {
-#pragma unroll
-                for (int i = 0; i < Bins<KIND>::words; ++i) hcol[i * kRowTile] = 0;
-                a = min(max((int)med - Bins<KIND>::lead, 0), 256 - NB);
-                const uint32_t A4 = a * 0x01010101u;
-                for (uint32_t g = 0; g < nw / 8; ++g) {
-                    uint32_t x[8];
-                    rw.group(g, x);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) hist_word<NB>(hcol, x[j], A4);
-                }
-                for (uint32_t q = nw & ~7u; q < nw; ++q) hist_word<NB>(hcol, rw.word(q), A4);
-                for (uint32_t c = 4 * nw; c < C; ++c) hist_byte<NB>(hcol, rowb[c], a);
-            } else {
-                a = min(max((int)med - Bins<KIND>::lead, 0), 253);
-                const uint32_t A4 = a * 0x01010101u;
-                for (uint32_t g = 0; g < nw / 8; ++g) {
-                    uint32_t x[8];
-                    rw.group(g, x);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) count3_word(x[j], A4, n1, n2, n3);
-                }
-                for (uint32_t q = nw & ~7u; q < nw; ++q) count3_word(rw.word(q), A4, n1, n2, n3);
-                for (uint32_t c = 4 * nw; c < C; ++c) {
-                    const uint32_t d = (uint32_t)rowb[c] - a;   // below a: wraps far above 3
-                    n1 += d < 1u;
-                    n2 += d < 2u;
-                    n3 += d < 3u;
-                }
-            }
-        }
+        if (mine) a = row_scan<KIND, RD>(rowb, C, hcol, n1, n2, n3);
         if (!two) {
             // every row is read: with one buffer, refill it now
             __syncthreads();
             if (bulk && warp == 0 && tile + G < ntiles) stage_issue(P, tile + G, s_dense0, &s_bar[bar ^ 1], lane);
         }
-        uint32_t key = 0;
-        if (mine) {
-            if constexpr (KIND == CSF_NVFP4) key = window_key<KIND>(hcol, a);
-            else key = count3_key(C, a, n1, n2 - n1, n3 - n2);
-        }
-        // rows whose window the bound cannot prove: exact over all 256 values
-        uint32_t redo = __ballot_sync(kFull, mine && key == 0);
-        while (redo) {
-            const int src_lane = __ffs(redo) - 1;
-            redo &= redo - 1;
-            const uint32_t k2 = exact_key<KIND>(P.dense + (uint64_t)(r0 + 32 * warp + src_lane) * C, C, s_hist,
-                                                warp, lane);
-            if (lane == src_lane) key = k2;
-        }
+        uint32_t key = mine ? row_fast_key<KIND>(hcol, C, a, n1, n2, n3) : 0u;
+        key = settle_keys<KIND>(P, key, mine, r0 + 32u * (uint32_t)warp, s_hist, warp, lane);
         const uint32_t count = mine ? C - (key >> 8) : 0u;
         const uint32_t wsum = __reduce_add_sync(kFull, count);
         if (lane == 0) s_wsum[k & 1u][warp] = wsum;
@@ -815,13 +990,12 @@ __global__ void __launch_bounds__(kRowTile) prepare_base_kernel(const __grid_con
     }
 }
 
-// Encode kernel: one thread per row.  The tile's offset in the exception
-// stream is the sum of the earlier tiles' totals (each block keeps a running
-// sum over its tiles); exc_index entries follow from a block scan of the
-// counts; each thread encodes its row word by word (byte-wise subtract, range
-// test, nibble or bit gather) into the tile's planes in shared memory and
-// writes its exception bytes to their positions in the stream (escape
-// positions taken 8 words at a time and walked in element order).
+// Encode kernel (two-kernel path): one thread per row.  The tile's offset in
+// the exception stream is the sum of the earlier tiles' totals (each block
+// keeps a running sum over its tiles); exc_index entries follow from a block
+// scan of the counts; each thread encodes its row (encode_row) into the
+// tile's planes and writes its exception bytes to their positions in the
+// stream, through a shared-memory stage when the tile's exceptions fit it.
 template <int KIND, int RD>
 __global__ void __launch_bounds__(kRowTile) prepare_encode_kernel(const __grid_constant__ PrepParams P) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -851,8 +1025,6 @@ __global__ void __launch_bounds__(kRowTile) prepare_encode_kernel(const __grid_c
     __syncthreads();
     if (bulk && warp == 0 && blockIdx.x < P.num_tiles) stage_issue(P, blockIdx.x, s_dense0, &s_bar[0], lane);
 
-    const uint32_t nw = C / 4;                       // whole words of a row
-    const uint32_t tailn = C & 3u;                   // kRdShift only
     const uint32_t ntiles = (uint32_t)P.num_tiles;
     unsigned long long off = 0;                      // exceptions of the tiles before this one
     bool bad = false, over = false;
@@ -907,132 +1079,18 @@ __global__ void __launch_bounds__(kRowTile) prepare_encode_kernel(const __grid_c
         // the tile's exceptions are staged in shared memory unless they
         // overflow the stage; then they go straight to the stream
         const bool staged = btot <= P.exc_stage;
-
         if (mine) {
-            const uint8_t *rowb = s_dense + (uint32_t)tid * stride;
-            const uint32_t B4 = base * 0x01010101u;
-            const RowWords<RD> rw(rowb);
-            uint32_t pos = pre;                           // the row's next exception, tile position
-            const uint32_t el0 = (uint32_t)tid * C;       // tile-local element index of the row start
-            uint32_t *pw = reinterpret_cast<uint32_t *>(s_planes);
-            uint32_t *px = reinterpret_cast<uint32_t *>(s_planes + P.smem_planes / 2);
-            // the exception bytes of the 8 words from word k0 on: bit 4j + i of
-            // `em` = byte i of word j (bit order = element order)
-            auto emit = [&](uint32_t em, uint32_t k0) {
-                const uint8_t *src = rowb + 4 * k0;
-                if (staged) {
-                    while (em) {
-                        const uint32_t i = (uint32_t)(__ffs(em) - 1);
-                        em &= em - 1;
-                        s_exc[pos++] = src[i];
-                    }
-                } else {
-                    while (em) {
-                        const uint32_t i = (uint32_t)(__ffs(em) - 1);
-                        em &= em - 1;
-                        const unsigned long long g = off + pos++;
-                        if (g < P.exc_capacity) P.exc_bytes[g] = src[i];
-                        else over = true;
-                    }
-                }
-            };
-            constexpr uint32_t kW1 = KIND == CSF_NVFP4 ? 0x0F0F0F0Fu : 0x02020202u;   // (w + 1) per byte
-            // codes of word k (bytes x; `valid` masks the bytes of a tail word)
-            // and its escape nibble (bit i = byte i outside [b, b + w])
-            auto code = [&](uint32_t x, uint32_t valid, uint32_t &ob4) -> uint32_t {
-                uint32_t below;
-                const uint32_t d = sub_bytes(x, B4, below);
-                const uint32_t o = ((((d | kH) - kW1) | d | below) & kH) & valid;
-                const uint32_t m = byte_mask(o);
-                if (KIND == CSF_NVFP4) {
-                    const uint32_t c = ((d & ~m) | (0x0F0F0F0Fu & m)) & valid;
-                    const uint32_t t = c | (c >> 4);
-                    ob4 = __byte_perm(t, 0, 0x4420);                                // 4 nibbles
-                } else {
-                    ob4 = (((d & ~m) & 0x01010101u & valid) * 0x10204080u) >> 28;  // 4 offset bits
-                }
-                return (o * 0x00204081u) >> 28;
-            };
-            auto store_nv = [&](uint32_t k, uint32_t cd) {
-                const uint32_t el = el0 + 4 * k;
-                if (RD != kRdShift) {
-                    reinterpret_cast<uint16_t *>(s_planes)[el >> 2] = (uint16_t)cd;
-                } else {
-                    const uint32_t sh = 4 * (el & 7u);
-                    atomicOr(pw + (el >> 3), cd << sh);
-                    if (sh > 16 && (cd >> (32 - sh)) != 0) atomicOr(pw + (el >> 3) + 1, cd >> (32 - sh));
-                }
-            };
-            auto store_mx = [&](uint32_t el, uint32_t o, uint32_t e, uint32_t bits) {   // `bits` bits at element el
-                const uint32_t sh = el & 31u;
-                if (o) atomicOr(pw + (el >> 5), o << sh);
-                if (e) atomicOr(px + (el >> 5), e << sh);
-                if (sh + bits > 32) {
-                    if (o >> (32 - sh)) atomicOr(pw + (el >> 5) + 1, o >> (32 - sh));
-                    if (e >> (32 - sh)) atomicOr(px + (el >> 5) + 1, e >> (32 - sh));
-                }
-            };
-            for (uint32_t g = 0; g < nw / 8; ++g) {
-                uint32_t x[8];
-                rw.group(g, x);
-                uint32_t em = 0, ow = 0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t cd;
-                    const uint32_t e4 = code(x[j], 0xFFFFFFFFu, cd);
-                    em |= e4 << (4 * j);
-                    if (KIND == CSF_NVFP4) store_nv(8 * g + j, cd);
-                    else ow |= cd << (4 * j);
-                }
-                if (KIND == CSF_MXFP4) {
-                    const uint32_t el = el0 + 32 * g;
-                    if (RD != kRdShift && (el & 31u) == 0) {
-                        pw[el >> 5] = ow;
-                        px[el >> 5] = em;
-                    } else {
-                        store_mx(el, ow, em, 32);
-                    }
-                }
-                if (em) emit(em, 8 * g);
-            }
-            // remaining whole words and the tail word, in one last group
-            uint32_t em = 0;
-            const uint32_t k0 = nw & ~7u;
-            for (uint32_t q = k0; q < nw + (tailn ? 1u : 0u); ++q) {
-                const uint32_t valid = q < nw ? 0xFFFFFFFFu : 0xFFFFFFFFu >> (32 - 8 * tailn);
-                uint32_t cd;
-                const uint32_t e4 = code(rw.word(q), valid, cd);
-                em |= e4 << (4 * (q - k0));
-                if (KIND == CSF_NVFP4) store_nv(q, cd);
-                else store_mx(el0 + 4 * q, cd, e4, 4);
-            }
-            emit(em, k0);
-            if (pos != pre + count) bad = true;           // the two kernels must agree on the count
+            const uint64_t gcap = off < P.exc_capacity ? P.exc_capacity - off : 0;
+            const uint32_t end = encode_row<KIND, RD>(s_dense + (uint32_t)tid * stride, C, base, (uint32_t)tid * C,
+                                                      s_planes, P.smem_planes, s_exc, staged, P.exc_bytes + off, gcap,
+                                                      pre, over);
+            if (end != pre + count) bad = true;           // the two kernels must agree on the count
         }
         __syncthreads();   // planes and exceptions staged; the tile's rows are read
         if (!two && bulk && warp == 0 && tile + G < ntiles)
             stage_issue(P, tile + G, s_dense0, &s_bar[bar ^ 1], lane);
         // planes of the tile, cleared again for the next one
-        const uint64_t e0 = (uint64_t)r0 * C;
-        if (KIND == CSF_NVFP4) {
-            const uint32_t nbytes = (((uint32_t)nr * C + 1) / 2 + 15) & ~15u;
-            uint4 *dst = reinterpret_cast<uint4 *>(P.offsets + e0 / 2);
-            for (uint32_t i = tid; i < nbytes / 16; i += kRowTile) {
-                dst[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
-                reinterpret_cast<uint4 *>(s_planes)[i] = make_uint4(0, 0, 0, 0);
-            }
-        } else {
-            const uint32_t nbytes = (((uint32_t)nr * C + 7) / 8 + 15) & ~15u;
-            const uint32_t pbytes = P.smem_planes / 2;
-            uint4 *dso = reinterpret_cast<uint4 *>(P.offsets + e0 / 8);
-            uint4 *dse = reinterpret_cast<uint4 *>(P.escapes + e0 / 8);
-            for (uint32_t i = tid; i < nbytes / 16; i += kRowTile) {
-                dso[i] = reinterpret_cast<const uint4 *>(s_planes)[i];
-                dse[i] = reinterpret_cast<const uint4 *>(s_planes + pbytes)[i];
-                reinterpret_cast<uint4 *>(s_planes)[i] = make_uint4(0, 0, 0, 0);
-                reinterpret_cast<uint4 *>(s_planes + pbytes)[i] = make_uint4(0, 0, 0, 0);
-            }
-        }
+        write_planes<KIND>(P, s_planes, (uint64_t)r0 * C, (uint32_t)nr, true, tid);
         if (staged) {
             for (uint32_t i = tid; i < btot; i += kRowTile) {
                 const unsigned long long g = off + i;
@@ -1043,6 +1101,239 @@ __global__ void __launch_bounds__(kRowTile) prepare_encode_kernel(const __grid_c
     }
     if (__any_sync(kFull, over) && lane == 0) flag(P.err, CSF_DEV_ERR_CAPACITY);
     if (__any_sync(kFull, bad) && lane == 0) flag(P.err, CSF_DEV_ERR_CORRUPT);
+}
+
+// Fused kernel (one pass per tile; the scratch holds a slot of 128 * C bytes
+// per tile): one thread per row.  Base search as in the base kernel, then a
+// block scan of the counts gives each row's exceptions' place inside the
+// tile, and each thread encodes its row from the same staged copy: planes to
+// the stack, exception bytes to the tile's slot (through a shared-memory
+// stage when they fit it), exc_index[row] = the row's place inside the tile,
+// the tile's total to the scratch.  The bins, and after them the planes and
+// the exception stage, share one region of shared memory.
+template <int KIND, int RD>
+__global__ void __launch_bounds__(kRowTile) prepare_fused_kernel(const __grid_constant__ PrepParams P) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ uint32_t s_wsum[kRowTile / 32];
+    __shared__ __align__(8) uint64_t s_bar[2];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const uint32_t C = (uint32_t)P.C;
+    const uint32_t stride = (uint32_t)P.stride;
+    const bool bulk = P.stage != kStagePlain;
+    const bool two = bulk && P.nbuf == 2;
+    const uint64_t G = gridDim.x;
+
+    uint32_t *s_hist = reinterpret_cast<uint32_t *>(smem);          // the bins, during the base search
+    uint8_t *s_planes = smem;                                        // then the tile's planes
+    uint8_t *s_exc = smem + P.smem_planes;                           // and its exception bytes, in order
+    uint8_t *s_dense0 = smem + P.smem_hist;                          // nbuf staging buffers
+
+    if (tid == 0 && bulk) {
+        mbar_init(&s_bar[0]);
+        mbar_init(&s_bar[1]);
+    }
+    __syncthreads();
+    if (bulk && warp == 0 && blockIdx.x < P.num_tiles) stage_issue(P, blockIdx.x, s_dense0, &s_bar[0], lane);
+    // The placing kernel may be scheduled now: it waits for this grid to
+    // complete before it reads anything (the grid is persistent, so all its
+    // blocks are already resident).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    const uint32_t ntiles = (uint32_t)P.num_tiles;
+    bool bad = false, over = false;
+    for (uint32_t k = 0, tile = blockIdx.x; tile < ntiles; ++k, tile += (uint32_t)G) {
+        const int buf = two ? (int)(k & 1u) : 0;
+        const int bar = (int)(k & 1u);
+        uint8_t *s_dense = s_dense0 + (uint32_t)buf * P.smem_dense;
+        if (two && warp == 0 && tile + G < ntiles)
+            stage_issue(P, tile + G, s_dense0 + (uint32_t)(buf ^ 1) * P.smem_dense, &s_bar[bar ^ 1], lane);
+        stage_wait(P, tile, s_dense, &s_bar[bar], (k >> 1) & 1u, tid);
+
+        const uint32_t r0 = tile * (uint32_t)kRowTile;
+        const int nr = (int)tile_rows(P, tile);
+        const bool mine = tid < nr;
+        const uint8_t *rowb = s_dense + (uint32_t)tid * stride;
+        uint32_t *hcol = s_hist + tid;
+        uint32_t a = 0, n1 = 0, n2 = 0, n3 = 0;
+        if (mine) a = row_scan<KIND, RD>(rowb, C, hcol, n1, n2, n3);
+        uint32_t key = mine ? row_fast_key<KIND>(hcol, C, a, n1, n2, n3) : 0u;
+        key = settle_keys<KIND>(P, key, mine, r0 + 32u * (uint32_t)warp, s_hist, warp, lane);
+        const uint32_t count = mine ? C - (key >> 8) : 0u;
+        const uint32_t base = 255u - (key & 0xFFu);
+        uint32_t wtot;
+        const uint32_t wex = warp_excl_scan(count, lane, wtot);
+        if (lane == 0) s_wsum[warp] = wtot;
+        __syncthreads();   // the bins are read: their space takes the planes
+        for (uint32_t i = tid; i < P.smem_planes / 16; i += kRowTile)
+            reinterpret_cast<uint4 *>(s_planes)[i] = make_uint4(0, 0, 0, 0);
+        uint32_t boff = 0, btot = 0;
+#pragma unroll
+        for (int w = 0; w < kRowTile / 32; ++w) {
+            if (w < warp) boff += s_wsum[w];
+            btot += s_wsum[w];
+        }
+        const uint32_t pre = boff + wex;
+        const bool staged = btot <= P.exc_stage;
+        uint8_t *slot = P.slot + (uint64_t)tile * P.slot_bytes;
+        __syncthreads();   // planes cleared
+        if (mine) {
+            const uint32_t end = encode_row<KIND, RD>(rowb, C, base, (uint32_t)tid * C, s_planes, P.smem_planes, s_exc,
+                                                      staged, slot, P.slot_bytes, pre, over);
+            if (end != pre + count) bad = true;
+            P.base[r0 + tid] = (uint8_t)base;
+            P.exc_index[r0 + tid] = pre;
+        }
+        __syncthreads();   // planes and exceptions staged; the tile's rows are read
+        if (!two && bulk && warp == 0 && tile + G < ntiles)
+            stage_issue(P, tile + G, s_dense0, &s_bar[bar ^ 1], lane);
+        write_planes<KIND>(P, s_planes, (uint64_t)r0 * C, (uint32_t)nr, false, tid);
+        if (staged) {
+            // whole 16-byte pieces (the slot is 16-byte aligned and private
+            // to the tile; bytes past the total are never read)
+            for (uint32_t i = tid; i < (btot + 15) / 16; i += kRowTile)
+                reinterpret_cast<uint4 *>(slot)[i] = reinterpret_cast<const uint4 *>(s_exc)[i];
+        }
+        if (tid == 0) P.tile_total[tile] = btot;
+        __syncthreads();   // the shared region is read before the next tile's bins
+    }
+    if (__any_sync(kFull, over) && lane == 0) flag(P.err, CSF_DEV_ERR_CORRUPT);   // a slot holds a whole tile
+    if (__any_sync(kFull, bad) && lane == 0) flag(P.err, CSF_DEV_ERR_CORRUPT);
+}
+
+// Copies a tile's n exception bytes from its slot (16-byte aligned) to
+// stream position o (whole warp).  Whole 4-byte words of the stream take
+// one funnel-shifted word store each, the partial words at both ends byte
+// stores.  The slot is read 8 words a lane per round, loaded together; the
+// slot word before each comes from the next lower lane (lane 0: lane 31 of
+// the step before).  `first` holds the first round's words, loaded by the
+// caller.
+__device__ __forceinline__ void place_words(uint32_t *d32, const uint32_t *__restrict__ s32, uint32_t a,
+                                            uint32_t n, const uint32_t (&first)[8], int lane) {
+    const uint32_t nwords = (a + n + 3) / 4;   // stream word j holds slot bytes 4j - a .. 4j - a + 3
+    uint32_t carry = 0;
+    for (uint32_t jb = 0; jb < nwords; jb += 8 * 32) {
+        uint32_t hi[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t j = jb + 32u * (uint32_t)k + (uint32_t)lane;
+            hi[k] = jb == 0 ? first[k] : (4 * j < n ? __ldg(s32 + j) : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t j = jb + 32u * (uint32_t)k + (uint32_t)lane;
+            uint32_t lo = __shfl_up_sync(kFull, hi[k], 1);
+            const uint32_t top = __shfl_sync(kFull, hi[k], 31);
+            if (lane == 0) lo = carry;
+            carry = top;
+            if (j >= nwords) continue;
+            const uint32_t v = a == 0 ? hi[k] : __funnelshift_r(lo, hi[k], 8u * (4u - a));
+            const uint32_t b0 = 4 * j;                     // stream bytes o - a + b0 .. + 3
+            if (b0 >= a && b0 + 4 <= a + n) {
+                d32[j] = v;
+            } else {
+                uint8_t *d8 = reinterpret_cast<uint8_t *>(d32 + j);
+#pragma unroll
+                for (uint32_t q = 0; q < 4; ++q)
+                    if (b0 + q >= a && b0 + q < a + n) d8[q] = (uint8_t)(v >> (8 * q));
+            }
+        }
+    }
+}
+
+// Second kernel of the fused path: each warp places one tile, tile
+// 4 * block + warp.  Everything that does not depend on the tile's offset
+// is loaded first, in one round trip: the tile's total and its rows'
+// exc_index entries (each row's place inside the tile), the first 256 words
+// of its slot, and the block's share of the totals of all earlier tiles.
+// Then the offset (the block's sum plus a scan of its four totals) is added
+// to the entries and the slot is copied to its place in the stream.  With
+// the stream pointer not 4-byte aligned, or a slot that would pass the
+// capacity, the bytes are copied one by one (bytes past the capacity are
+// dropped and CSF_DEV_ERR_CAPACITY set).
+__global__ void __launch_bounds__(kRowTile) prepare_place_kernel(const __grid_constant__ PrepParams P) {
+    __shared__ unsigned long long s_red[kRowTile / 32];
+    __shared__ uint32_t s_tot[kRowTile / 32];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const uint64_t ntiles = P.num_tiles;
+    const uint64_t t0 = (uint64_t)blockIdx.x * (kRowTile / 32);
+    const uint64_t tile = t0 + (uint64_t)warp;
+    const bool have = tile < ntiles;
+    // Launched as a programmatic dependent of the fused kernel: wait until
+    // that grid has completed and its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // loads that need no offset
+    const uint32_t n = have ? __ldg(P.tile_total + tile) : 0u;
+    const uint64_t r_lo = tile * kRowTile, r_hi = have ? min(r_lo + (uint64_t)kRowTile, P.rows) : r_lo;
+    uint32_t e[kRowTile / 32];
+#pragma unroll
+    for (int i = 0; i < kRowTile / 32; ++i) {
+        const uint64_t r = r_lo + (uint64_t)(lane + 32 * i);
+        e[i] = r < r_hi ? P.exc_index[r] : 0u;
+    }
+    const uint8_t *slot = P.slot + tile * (uint64_t)P.slot_bytes;
+    const uint32_t *s32 = reinterpret_cast<const uint32_t *>(slot);
+    uint32_t first[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t j = 32u * (uint32_t)k + (uint32_t)lane;
+        first[k] = have && 4 * j < P.slot_bytes ? __ldg(s32 + j) : 0u;
+    }
+    // totals of the tiles before the block: eight loads in flight a thread
+    unsigned long long run = 0;
+    uint64_t j = tid;
+    for (; j + 7 * kRowTile < t0; j += 8 * kRowTile) {
+        uint32_t v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __ldg(P.tile_total + j + i * kRowTile);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) run += v[i];
+    }
+    for (; j < t0; j += kRowTile) run += __ldg(P.tile_total + j);
+    run = warp_sum64(run);
+    if (lane == 0) {
+        s_red[warp] = run;
+        s_tot[warp] = n;
+    }
+    __syncthreads();
+    unsigned long long o = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kRowTile / 32; ++w) {
+        o += s_red[w];
+        all += s_tot[w];
+    }
+    all += o;
+#pragma unroll
+    for (int w = 0; w < kRowTile / 32; ++w) o += w < warp ? s_tot[w] : 0u;
+
+    if (have) {
+#pragma unroll
+        for (int i = 0; i < kRowTile / 32; ++i) {
+            const uint64_t r = r_lo + (uint64_t)(lane + 32 * i);
+            if (r < r_hi) P.exc_index[r] = (uint32_t)(o + e[i]);
+        }
+        uint8_t *dst = P.exc_bytes;
+        if ((reinterpret_cast<uintptr_t>(dst) & 3u) == 0 && o + n <= P.exc_capacity) {
+            place_words(reinterpret_cast<uint32_t *>(dst) + (o >> 2), s32, (uint32_t)(o & 3u), n, first, lane);
+        } else {
+            bool over = false;
+            for (uint32_t i = lane; i < n; i += 32) {
+                if (o + i < P.exc_capacity) dst[o + i] = __ldg(slot + i);
+                else over = true;
+            }
+            if (__any_sync(kFull, over) && lane == 0) flag(P.err, CSF_DEV_ERR_CAPACITY);
+        }
+    }
+    if (t0 + kRowTile / 32 >= ntiles && tid == 0) {
+        P.exc_index[P.rows] = (uint32_t)all;
+        if (all > 0xFFFFFFFFull) flag(P.err, CSF_DEV_ERR_CAPACITY);
+    }
 }
 
 }  // namespace
@@ -1106,6 +1397,34 @@ static int rows_nbuf_enc(int32_t kind, int32_t C, bool bulk) {
     const uint32_t rest = planes_bytes(kind, (uint64_t)kRowTile * C) + rows_exc_stage(C);
     return bulk && 2u * rows_dense_bytes(C) + rest <= 40u * 1024u ? 2 : 1;
 }
+// Fused kernel: one region for the bins and, after them, the planes and the
+// exception stage; staging buffers as the base kernel's.
+static uint32_t fused_region_bytes(int32_t kind, int32_t C) {
+    const uint32_t enc = planes_bytes(kind, (uint64_t)kRowTile * C) + rows_exc_stage(C);
+    const uint32_t h = rows_hist_bytes(kind);
+    return h > enc ? h : enc;
+}
+static int fused_nbuf(int32_t kind, int32_t C, bool bulk) {
+    return bulk && fused_region_bytes(kind, C) + 2u * rows_dense_bytes(C) <= 24u * 1024u ? 2 : 1;
+}
+// A tile's exception slot in the scratch: room for every byte of the tile.
+static uint32_t slot_bytes(int32_t C) { return round16((uint64_t)kRowTile * C); }
+// Fused scratch: 16 bytes, a 4-byte total per tile, then the slots (256-byte
+// aligned).
+static uint64_t slots_offset(uint64_t tiles) { return (16 + 4 * tiles + 255) & ~255ull; }
+
+// Tiles up to which the fused path runs: each block of its placing kernel
+// sums the totals of all tiles before it, which costs tiles^2 / 8 loads in
+// all (8.4 M at this limit of 1 M rows); larger stacks take the two-kernel
+// path, whose running sums cost a few loads per tile.
+constexpr uint64_t kFusedMaxTiles = 8192;
+
+uint64_t prepare_fused_scratch_bytes(int32_t kind, int32_t C, uint64_t rows) {
+    (void)kind;
+    const uint64_t tiles = (rows + kRowTile - 1) / kRowTile;
+    if (!rows_path(C) || tiles > kFusedMaxTiles) return 0;
+    return slots_offset(tiles) + tiles * slot_bytes(C);
+}
 
 // Dynamic shared memory of a launch.  Row path: the base kernel holds the
 // bins and the staging buffers, the encode kernel the buffers, the planes
@@ -1134,7 +1453,7 @@ bool prepare_stages_rows(int32_t kind, int32_t C, const void *dense) {
 bool prepare_needs_cleared_scratch(int32_t C) { return !rows_path(C); }
 
 void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out, uint64_t exc_capacity,
-                      void *scratch, uint64_t rows, uint64_t n, bool staged) {
+                      void *scratch, uint64_t rows, uint64_t n, bool staged, bool fused) {
     (void)staged;   // implied by the geometry and the dense pointer (prepare_stages_rows)
     const csf_geometry &g = out.g;
     const int32_t tr = prepare_tile_rows(g.kind, g.cols);
@@ -1169,6 +1488,13 @@ void make_prep_params(PrepParams &p, const uint8_t *dense, const csf_stack &out,
         p.nbuf = rows_nbuf(g.kind, g.cols, p.stage != kStagePlain);
         p.nbuf_enc = rows_nbuf_enc(g.kind, g.cols, p.stage != kStagePlain);
         p.exc_stage = rows_exc_stage(g.cols);
+        if (fused) {
+            p.fused = 1;
+            p.smem_hist = fused_region_bytes(g.kind, g.cols);
+            p.nbuf = fused_nbuf(g.kind, g.cols, p.stage != kStagePlain);
+            p.slot_bytes = slot_bytes(g.cols);
+            p.slot = static_cast<uint8_t *>(scratch) + slots_offset(p.num_tiles);
+        }
     } else {
         p.stride = g.cols;
         p.smem_dense = round16(te);
@@ -1200,9 +1526,37 @@ static cudaError_t launch_rows_rd(const PrepParams &p, cudaStream_t s) {
                              (uint32_t)p.nbuf_enc * p.smem_dense + p.smem_planes + p.exc_stage, s);
 }
 
+// Fused path: the one-pass kernel, then the placing kernel: a block per 4
+// tiles (one per warp).
+template <int KIND, int RD>
+static cudaError_t launch_fused_rd(const PrepParams &p, cudaStream_t s) {
+    cudaError_t e = launch_persistent(prepare_fused_kernel<KIND, RD>, p, p.smem_hist + (uint32_t)p.nbuf * p.smem_dense, s);
+    if (e != cudaSuccess) return e;
+    // programmatic dependent launch: the placing grid is scheduled while the
+    // fused grid runs and starts as soon as it completes
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((p.num_tiles + 3) / 4));
+    cfg.blockDim = dim3(kRowTile);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, prepare_place_kernel, p) == cudaSuccess) return cudaSuccess;
+    cudaGetLastError();
+    prepare_place_kernel<<<cfg.gridDim, kRowTile, 0, s>>>(p);   // without the programmatic edge
+    return cudaGetLastError();
+}
+
 template <int KIND>
 static cudaError_t launch_rows(const PrepParams &p, cudaStream_t s) {
     const int rd = row_read(p.C);
+    if (p.fused) {
+        if (rd == kRdVec) return launch_fused_rd<KIND, kRdVec>(p, s);
+        if (rd == kRdWord) return launch_fused_rd<KIND, kRdWord>(p, s);
+        return launch_fused_rd<KIND, kRdShift>(p, s);
+    }
     if (rd == kRdVec) return launch_rows_rd<KIND, kRdVec>(p, s);
     if (rd == kRdWord) return launch_rows_rd<KIND, kRdWord>(p, s);
     return launch_rows_rd<KIND, kRdShift>(p, s);

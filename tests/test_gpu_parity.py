@@ -542,21 +542,61 @@ PREP_WIDTHS = [(0, 3, 150, 48), (0, 3, 150, 128), (0, 2, 130, 200), (0, 2, 70, 2
                (1, 3, 129, 33), (1, 2, 140, 8), (1, 2, 50, 300)]
 
 
+def _least_scratch_bytes(csf, kind, E, R, C):
+    # The smallest scratch csf_prepare accepts for rows of up to 255 bytes:
+    # 16 bytes and 8 per 128-row tile.  It takes the two-kernel path instead
+    # of the fused one.  Wider rows have one path, whose scratch csf_sizes()
+    # reports.
+    if C > 255:
+        return csf.sizes(kind, E, R, C)["prepare_scratch"]
+    return 16 + 8 * -(-(E * R) // 128)
+
+
+def _prepare_with_scratch(csf, d, kind, nbytes):
+    E, R, C = (int(x) for x in d.shape)
+    st = csf.empty_stack(kind, E, R, C, exc_capacity=E * R * C)
+    scratch = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda")   # no initialisation needed
+    csf.prepare_async(d, st, scratch)
+    st.num_exc = int(st.exc_index[E * R].item()) & 0xFFFFFFFF
+    return st
+
+
 @pytest.mark.parametrize("kind,E,R,C", PREP_WIDTHS)
 @pytest.mark.parametrize("offset", [0, 1])
-def test_prepare_rows_every_staging_path(csf, kind, E, R, C, offset):
+@pytest.mark.parametrize("path", ["fused", "two_kernels"])
+def test_prepare_rows_every_staging_path(csf, kind, E, R, C, offset, path):
     # A dense pointer one byte off alignment takes plain loads; aligned ones
-    # take the bulk copies where the row layout allows.  All give the
-    # oracle's streams, with a ragged last tile of rows.
+    # take the bulk copies where the row layout allows.  The scratch size
+    # csf_sizes() reports takes the fused path (one pass per tile, then the
+    # placing kernel); the least accepted size takes the base and encode
+    # kernels.  All give the oracle's streams, with a ragged last tile of rows.
     dense = _small_dense(kind, E, R, C, seed=C + 17 * E)
     enc = oracle.encode(kind, dense)
     buf = torch.zeros(dense.size + offset, dtype=torch.uint8, device="cuda")
     d = buf[offset:].view(E, R, C)
     d.copy_(_dense_cuda(dense))
-    st = csf.prepare(d, kind)
+    if path == "fused":
+        st = csf.prepare(d, kind)
+    else:
+        st = _prepare_with_scratch(csf, d, kind, _least_scratch_bytes(csf, kind, E, R, C))
     torch.cuda.synchronize()
     assert st.errors() == 0
     assert_stack_matches(st, enc)
+
+
+@pytest.mark.parametrize("kind,C", [(0, 100), (1, 160), (0, 50)])
+def test_prepare_both_paths_full_size(csf, kind, C):
+    # Full-size stacks (the gate, MXFP4 and down shapes) through both paths,
+    # in a scratch filled with garbage, agree with the oracle.
+    dense = {(0, 100): synth.gate_stack, (1, 160): synth.mxfp4_stack, (0, 50): synth.down_stack}[(kind, C)](seed=3)
+    enc = oracle.encode(kind, dense)
+    E, R, _ = dense.shape
+    d = _dense_cuda(dense)
+    for nbytes in (csf.sizes(kind, E, R, C)["prepare_scratch"], _least_scratch_bytes(csf, kind, E, R, C)):
+        st = _prepare_with_scratch(csf, d, kind, nbytes)
+        torch.cuda.synchronize()
+        assert st.errors() == 0
+        assert_stack_matches(st, enc)
 
 
 def _adversarial_rows(kind, C, seed):
