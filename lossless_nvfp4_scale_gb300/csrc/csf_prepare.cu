@@ -467,8 +467,15 @@ __device__ __forceinline__ uint32_t median5(uint32_t p0, uint32_t p1, uint32_t p
     return max(min(p4, e), min(max(p4, e), f));
 }
 
-// 0xFF in each byte whose bit 7 is set in `f` (f has no other bits set).
-__device__ __forceinline__ uint32_t byte_mask(uint32_t f) { return (f >> 7) * 0xFFu; }
+// 0xFF in each byte whose bit 7 is set in `f`, 0x00 in the others (the other
+// bits of f are ignored): a byte permute whose selector nibbles 8..B pick
+// bytes 0..3 and replicate their sign bit.  (PTX prmt; CUDA's __byte_perm
+// keeps only the low 3 bits of each selector nibble, so it cannot do this.)
+__device__ __forceinline__ uint32_t byte_mask(uint32_t f) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(f), "r"(0xBA98u));
+    return r;
+}
 
 // Byte-wise x - b (mod 256 in each byte, no borrow across bytes) and, in bit
 // 7 of each byte of `below`, whether that byte of x is below b.
@@ -484,9 +491,11 @@ struct RowWords {
     const uint32_t *w;   // kRdShift: the aligned word at or below the row start
     uint32_t sh;         // kRdShift: 8 * (row start % 4)
     __device__ __forceinline__ explicit RowWords(const uint8_t *r) {
-        const uintptr_t a = reinterpret_cast<uintptr_t>(r);
-        w = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
-        sh = 8u * (uint32_t)(a & 3u);
+        // rounded down by pointer arithmetic (not through an integer), so the
+        // loads stay shared-memory loads
+        const uint32_t m = (uint32_t)reinterpret_cast<uintptr_t>(r) & 3u;
+        w = reinterpret_cast<const uint32_t *>(r - m);
+        sh = 8u * m;
     }
     // word k (bytes 4k .. 4k+3 of the row); kRdShift reads one word past them
     __device__ __forceinline__ uint32_t word(uint32_t k) const {
@@ -520,8 +529,8 @@ __device__ __forceinline__ void hist_word(uint32_t *hcol, uint32_t x, uint32_t A
     constexpr uint32_t kNB4 = (uint32_t)NB * 0x01010101u;
     uint32_t below;
     const uint32_t d = sub_bytes(x, A4, below);
-    // d >= NB in a byte: outside [a, a + NB) (bytes below a wrap past NB, a <= 256 - NB)
-    const uint32_t out = (((d | kH) - kNB4) | d) & kH;
+    // d >= NB in a byte (bit 7): outside [a, a + NB) (bytes below a wrap past NB, a <= 256 - NB)
+    const uint32_t out = ((d | kH) - kNB4) | d;
     const uint32_t m = byte_mask(out);                            // 0xFF in each outside byte
     const uint32_t bins = (d & ~m) | (kNB4 & m);                  // bin NB = outside
     atomicAdd(hcol + (bins & 0xFFu) * kRowTile, 1u);
@@ -798,7 +807,20 @@ __device__ __forceinline__ uint32_t encode_row(const uint8_t *rowb, uint32_t C, 
     // `em` = byte i of word j (bit order = element order)
     auto emit = [&](uint32_t em, uint32_t k0) {
         const uint8_t *src = rowb + 4 * k0;
-        if (staged) {
+        if (staged && KIND == CSF_MXFP4) {
+            // dense exceptions: two a trip, their loads issued together
+            while (em) {
+                const uint32_t i0 = (uint32_t)(__ffs(em) - 1);
+                em &= em - 1;
+                const bool two_more = em != 0;
+                const uint32_t i1 = two_more ? (uint32_t)(__ffs(em) - 1) : i0;
+                em &= em - 1;
+                const uint8_t v0 = src[i0], v1 = src[i1];
+                stage[pos] = v0;
+                if (two_more) stage[pos + 1] = v1;
+                pos += two_more ? 2u : 1u;
+            }
+        } else if (staged) {
             while (em) {
                 const uint32_t i = (uint32_t)(__ffs(em) - 1);
                 em &= em - 1;
