@@ -697,3 +697,36 @@ def test_pair_of_different_kinds(csf, Cm, routed, layout, half):
     assert np.array_equal(_np(gws).ravel(), gw.ravel())
     assert np.array_equal(_np(mws).ravel(), mw.ravel())
     assert g_up.errors() == 0 and m_up.errors() == 0
+
+
+@pytest.mark.parametrize("kind,C", [(0, 100), (1, 160)])
+def test_prepare_fused_into_unaligned_exception_buffer(csf, kind, C):
+    # The placing kernel copies whole words into a 4-byte aligned exception
+    # buffer; any other alignment takes its byte-by-byte copy.
+    E, R = 4, 1000
+    dense = _small_dense(kind, E, R, C, seed=91 + kind)
+    enc = oracle.encode(kind, dense)
+    for off in (1, 2, 3):
+        st = csf.empty_stack(kind, E, R, C, exc_capacity=E * R * C)
+        buf = torch.full((E * R * C + 16,), 0xEE, dtype=torch.uint8, device="cuda")
+        st.exc_bytes = buf[off:off + E * R * C]
+        csf.prepare_async(_dense_cuda(dense), st, csf.prepare_scratch(kind, E, R, C))
+        torch.cuda.synchronize()
+        st.num_exc = int(st.exc_index[E * R].item()) & 0xFFFFFFFF
+        assert st.errors() == 0
+        assert_stack_matches(st, enc)
+        assert (_np(buf[:off]) == 0xEE).all() and (_np(buf[off + st.num_exc:]) == 0xEE).all()
+
+
+@pytest.mark.parametrize("tiles", [8192, 8193])
+def test_prepare_at_the_fused_tile_limit(csf, tiles):
+    # Up to 8192 tiles of 128 rows the reported scratch takes the fused path;
+    # one more tile and csf_sizes() reports the two-kernel scratch.
+    E, R, C = 1, tiles * 128 - 5, 8
+    dense = synth.random_rows(tiles, E * R, C, spread=20, replace_p=0.05).reshape(E, R, C)
+    enc = oracle.encode(0, dense)
+    need = csf.sizes(0, E, R, C)["prepare_scratch"]
+    assert (need > 16 + 8 * tiles) == (tiles <= 8192)
+    st = csf.prepare(_dense_cuda(dense), 0)
+    assert st.errors() == 0
+    assert_stack_matches(st, enc)
