@@ -791,9 +791,11 @@ __device__ __forceinline__ uint32_t settle_keys(const PrepParams &P, uint32_t ke
 // memory) when `staged`, else of `gdst` (global memory, `gcap` bytes
 // available: later bytes are dropped and `over` set).  Word by word:
 // byte-wise subtract, range test, nibble or bit gather; escape positions are
-// taken 8 words at a time and walked in element order.  Returns the position
-// after the row's last exception.
-template <int KIND, int RD>
+// taken 8 words at a time and walked in element order.  LOW: the base is at
+// most 241 (NVFP4) or 254 (MXFP4), so a byte below it wraps to at least
+// w + 1 in the byte-wise subtract and needs no test of its own.  Returns the
+// position after the row's last exception.
+template <int KIND, int RD, bool LOW>
 __device__ __forceinline__ uint32_t encode_row(const uint8_t *rowb, uint32_t C, uint32_t base, uint32_t el0,
                                                uint8_t *s_planes, uint32_t planes_bytes, uint8_t *stage, bool staged,
                                                uint8_t *gdst, uint64_t gcap, uint32_t pos, bool &over) {
@@ -842,7 +844,8 @@ __device__ __forceinline__ uint32_t encode_row(const uint8_t *rowb, uint32_t C, 
     auto code = [&](uint32_t x, uint32_t valid, uint32_t &ob4) -> uint32_t {
         uint32_t below;
         const uint32_t d = sub_bytes(x, B4, below);
-        const uint32_t o = ((((d | kH) - kW1) | d | below) & kH) & valid;
+        const uint32_t wrapped = LOW ? 0u : below;
+        const uint32_t o = ((((d | kH) - kW1) | d | wrapped) & kH) & valid;
         const uint32_t m = byte_mask(o);
         if (KIND == CSF_NVFP4) {
             const uint32_t c = ((d & ~m) | (0x0F0F0F0Fu & m)) & valid;
@@ -909,6 +912,11 @@ __device__ __forceinline__ uint32_t encode_row(const uint8_t *rowb, uint32_t C, 
     emit(em, k0);
     return pos;
 }
+
+// Highest base for which no byte below it can wrap into its window in the
+// byte-wise subtract (base + w + 1 <= 256).
+template <int KIND>
+__device__ __forceinline__ constexpr uint32_t low_base() { return KIND == CSF_NVFP4 ? 241u : 254u; }
 
 // Writes the tile's planes from shared memory to the stack (16-byte pieces;
 // the tile starts at element e0 on a 16-byte boundary of each plane) and,
@@ -1101,11 +1109,15 @@ __global__ void __launch_bounds__(kRowTile) prepare_encode_kernel(const __grid_c
         // the tile's exceptions are staged in shared memory unless they
         // overflow the stage; then they go straight to the stream
         const bool staged = btot <= P.exc_stage;
+        const bool low = __all_sync(kFull, !mine || base <= low_base<KIND>());
         if (mine) {
             const uint64_t gcap = off < P.exc_capacity ? P.exc_capacity - off : 0;
-            const uint32_t end = encode_row<KIND, RD>(s_dense + (uint32_t)tid * stride, C, base, (uint32_t)tid * C,
-                                                      s_planes, P.smem_planes, s_exc, staged, P.exc_bytes + off, gcap,
-                                                      pre, over);
+            const uint8_t *rowb = s_dense + (uint32_t)tid * stride;
+            const uint32_t end =
+                low ? encode_row<KIND, RD, true>(rowb, C, base, (uint32_t)tid * C, s_planes, P.smem_planes, s_exc,
+                                                 staged, P.exc_bytes + off, gcap, pre, over)
+                    : encode_row<KIND, RD, false>(rowb, C, base, (uint32_t)tid * C, s_planes, P.smem_planes, s_exc,
+                                                  staged, P.exc_bytes + off, gcap, pre, over);
             if (end != pre + count) bad = true;           // the two kernels must agree on the count
         }
         __syncthreads();   // planes and exceptions staged; the tile's rows are read
@@ -1134,7 +1146,7 @@ __global__ void __launch_bounds__(kRowTile) prepare_encode_kernel(const __grid_c
 // the tile's total to the scratch.  The bins, and after them the planes and
 // the exception stage, share one region of shared memory.
 template <int KIND, int RD>
-__global__ void __launch_bounds__(kRowTile) prepare_fused_kernel(const __grid_constant__ PrepParams P) {
+__global__ void __launch_bounds__(kRowTile, 7) prepare_fused_kernel(const __grid_constant__ PrepParams P) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint32_t s_wsum[kRowTile / 32];
     __shared__ __align__(8) uint64_t s_bar[2];
@@ -1201,9 +1213,13 @@ __global__ void __launch_bounds__(kRowTile) prepare_fused_kernel(const __grid_co
         const bool staged = btot <= P.exc_stage;
         uint8_t *slot = P.slot + (uint64_t)tile * P.slot_bytes;
         __syncthreads();   // planes cleared
+        const bool low = __all_sync(kFull, !mine || base <= low_base<KIND>());
         if (mine) {
-            const uint32_t end = encode_row<KIND, RD>(rowb, C, base, (uint32_t)tid * C, s_planes, P.smem_planes, s_exc,
-                                                      staged, slot, P.slot_bytes, pre, over);
+            const uint32_t end =
+                low ? encode_row<KIND, RD, true>(rowb, C, base, (uint32_t)tid * C, s_planes, P.smem_planes, s_exc,
+                                                 staged, slot, P.slot_bytes, pre, over)
+                    : encode_row<KIND, RD, false>(rowb, C, base, (uint32_t)tid * C, s_planes, P.smem_planes, s_exc,
+                                                  staged, slot, P.slot_bytes, pre, over);
             if (end != pre + count) bad = true;
             P.base[r0 + tid] = (uint8_t)base;
             P.exc_index[r0 + tid] = pre;
