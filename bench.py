@@ -502,13 +502,26 @@ def measure_rows(torch, csf, synth, gate, gate_dense, hbm, max_steps):
     sb = mx.stream_bytes()
     rec("prepare_mxfp4", durs, mx.dense_bytes + sb["offsets"] + sb["escapes"] + sb["base"] + sb["exc_index"]
         + sb["exc_bytes"], {"exception_rate": round(mx.num_exc / mx.dense_bytes, 4)})
-    del pst, scr
     mx2 = clone_stack(torch, mx)
     mws = [torch.empty_like(mx_dense), torch.empty_like(mx_dense)]
     mcs = [mx, mx2]
     durs = timed_steps(torch, lambda i: csf.decode(mcs[i % 2], mws[i % 2]), n(100), 5)
     assert torch.equal(mws[0], mx_dense)
     rec("decode_mxfp4", durs, stack_traffic(mx))
+    # the MXFP4 workload as one step: prepare the stack, then decode what was
+    # just prepared (the bytes of both)
+    pst.num_exc = mx.num_exc
+    mws[0].zero_()
+
+    def prep_dec(i):
+        csf.prepare_async(mx_dense, pst, scr)
+        csf.decode(pst, mws[0])
+
+    durs = timed_steps(torch, prep_dec, n(50), 5)
+    assert torch.equal(mws[0], mx_dense) and pst.errors() == 0
+    rec("mxfp4_prepare_then_decode", durs, 2 * (mx.dense_bytes + sb["offsets"] + sb["escapes"] + sb["base"]
+                                              + sb["exc_index"] + sb["exc_bytes"]))
+    del pst, scr
     return rows
 
 
