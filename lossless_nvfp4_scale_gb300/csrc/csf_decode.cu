@@ -422,23 +422,24 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                 for (int s = 0; s < 4; ++s)
                     *reinterpret_cast<uint4 *>(my + ((16 * s) ^ gs)) =
                         make_uint4(out[4 * s], out[4 * s + 1], out[4 * s + 2], out[4 * s + 3]);
-                if (cnt) {
-                    if (xl <= nexc && cnt <= nexc - xl) {
-                        // The lane's exceptions are consecutive in the stream.
-                        const uint8_t *ep = S.exc_bytes + xl;
-                        uint32_t f = f0;
-                        while (f) {
-                            my[(uint32_t)(__ffs(f) - 1) ^ gs] = __ldg(ep++);
-                            f &= f - 1;
-                        }
-                        f = f1;
-                        while (f) {
-                            my[(uint32_t)(__ffs(f) + 31) ^ gs] = __ldg(ep++);
-                            f &= f - 1;
-                        }
-                    } else {
-                        bad = true;   // index points past the stream: leave the bytes, report
-                    }
+                // The lane's exceptions are consecutive in the stream.  An index
+                // that points past it leaves the bytes and is reported.  (No
+                // branch around the loops: they do nothing on empty masks, and
+                // fewer divergent regions cost fewer instructions.)
+                if (cnt && !(xl <= nexc && cnt <= nexc - xl)) {
+                    bad = true;
+                    f0 = f1 = 0;
+                }
+                const uint8_t *ep = S.exc_bytes + xl;
+                uint32_t f = f0;
+                while (f) {
+                    my[(uint32_t)(__ffs(f) - 1) ^ gs] = __ldg(ep++);
+                    f &= f - 1;
+                }
+                f = f1;
+                while (f) {
+                    my[(uint32_t)(__ffs(f) + 31) ^ gs] = __ldg(ep++);
+                    f &= f - 1;
                 }
 #pragma unroll
                 for (int s = 0; s < 4; ++s) {
