@@ -233,10 +233,12 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
     uint32_t q = ((uint32_t)lane * kLaneNv) % C;
     uint32_t w[8], bA = 0, bB = 0, bD = 0;
 
+    // chunks below nch8 are whole 32-byte pieces that one 256-bit load reads
+    const uint32_t nch8 = v8ok ? min(nch, avail / 32) : 0u;
     auto load = [&](uint32_t c, uint32_t r) {
         if (c < nch) {
             const uint8_t *p = offs + (size_t)c * 32;
-            if (v8ok && c * 32 + 32 <= avail) {
+            if (c < nch8) {
                 ld_v8(p, w);
             } else {
                 const uint4 a = __ldg(reinterpret_cast<const uint4 *>(p));
