@@ -89,13 +89,23 @@ __device__ __forceinline__ uint32_t add_base(uint32_t bw, uint32_t off) {
     return ((bw & 0x7F7F7F7Fu) + off) ^ (bw & 0x80808080u);
 }
 
+/* One step of a warp inclusive scan: the shuffle's predicate (the source lane
+ * exists) guards the add, so no lane-index compare is needed. */
+template <int D>
+__device__ __forceinline__ void scan_step(uint32_t &x) {
+    asm("{\n .reg .b32 y;\n .reg .pred p;\n shfl.sync.up.b32 y|p, %0, %1, 0, -1;\n @p add.u32 %0, %0, y;\n}"
+        : "+r"(x)
+        : "n"(D));
+}
+
 __device__ __forceinline__ uint32_t excl_scan(uint32_t v, int lane, uint32_t &total) {
+    (void)lane;
     uint32_t x = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, d);
-        if (lane >= d) x += y;
-    }
+    scan_step<1>(x);
+    scan_step<2>(x);
+    scan_step<4>(x);
+    scan_step<8>(x);
+    scan_step<16>(x);
     total = __shfl_sync(0xFFFFFFFFu, x, 31);
     return x - v;
 }

@@ -66,13 +66,23 @@ using dev::lanemask_lt;
 
 constexpr int kStageBytes = 4096;   // per warp: 32 lanes x 128 bytes
 
+// Exclusive warp prefix sum of v (and the warp total).  Each step's shuffle
+// also yields whether the source lane exists (PTX shfl.sync.up's predicate),
+// which guards the add: no lane-index compare per step.
+template <int D>
+__device__ __forceinline__ void scan_step(uint32_t &x) {
+    asm("{\n .reg .b32 y;\n .reg .pred p;\n shfl.sync.up.b32 y|p, %0, %1, 0, -1;\n @p add.u32 %0, %0, y;\n}"
+        : "+r"(x)
+        : "n"(D));
+}
 __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, int lane, uint32_t &total) {
+    (void)lane;
     uint32_t x = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t y = __shfl_up_sync(kFull, x, d);
-        if (lane >= d) x += y;
-    }
+    scan_step<1>(x);
+    scan_step<2>(x);
+    scan_step<4>(x);
+    scan_step<8>(x);
+    scan_step<16>(x);
     total = __shfl_sync(kFull, x, 31);
     return x - v;
 }
