@@ -284,14 +284,10 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
         constexpr bool WORDS = decltype(words_tag)::value;
         for (uint32_t cb = 0; cb < nch; cb += 32) {
             const uint32_t cc = cb + lane;
-            uint32_t cw[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) cw[i] = w[i];
-            const uint32_t cA = bA, cB = bB, cD = bD, cq = q, crr = rr;
-            q += S.step_q;
-            rr += S.step_r;
-            if (q >= C) { q -= C; ++rr; }
-            if (cb + 32 < nch) load(cc + 32, rr);                // prefetch the next piece
+            // this step's piece and bases, read in place: the next piece is
+            // loaded into the same registers once the expansion has used them
+            const uint32_t(&cw)[8] = w;
+            const uint32_t &cA = bA, &cB = bB, &cD = bD, &cq = q, &crr = rr;
 
             const uint32_t p = cc * kLaneNv;
             const int nv = cc < nch ? (int)min(nel - p, (uint32_t)kLaneNv) : 0;
@@ -389,6 +385,10 @@ __device__ void segment_nvfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                     out[2 * i + 1] = add_base(bw[2 * i + 1], __byte_perm(lo4, hi4, 0x7362));
                 }
             }
+            q += S.step_q;
+            rr += S.step_r;
+            if (q >= C) { q -= C; ++rr; }
+            if (cb + 32 < nch) load(cc + 32, rr);                // the next piece, while this one is patched
             // Element-ordered escape masks: bit j of f_h <-> element 32h + j.
             uint32_t f0 = __byte_perm(__byte_perm(fl[0], fl[1], 0x0040), __byte_perm(fl[2], fl[3], 0x0040), 0x5410);
             uint32_t f1 = __byte_perm(__byte_perm(fl[4], fl[5], 0x0040), __byte_perm(fl[6], fl[7], 0x0040), 0x5410);
@@ -554,10 +554,6 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
         const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
         uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
         const uint32_t cA = bA, cB = bB, cq = q, crr = rr;
-        q += S.step_q;
-        rr += S.step_r;
-        if (q >= C) { q -= C; ++rr; }
-        if (cb + 32 < nch) load(cc + 32, rr);
 
         const uint32_t p = cc * kLaneMx;
         const int nv = cc < nch ? (int)min(nel - p, (uint32_t)kLaneMx) : 0;
@@ -638,6 +634,13 @@ __device__ void segment_mxfp4(const DecStack &S, uint64_t row_a, uint64_t row_b,
                 qg += 32;
                 while (qg >= C) { qg -= C; ++rg; }
             }
+        }
+        // the next piece, into the registers the expansion has just read
+        q += S.step_q;
+        rr += S.step_r;
+        if (q >= C) { q -= C; ++rr; }
+        if (cb + 32 < nch) load(cc + 32, rr);
+        if (nv > 0) {
             if (cnt) {
                 if (xl <= nexc && cnt <= nexc - xl) {
                     const uint8_t *ep = S.exc_bytes + xl;
