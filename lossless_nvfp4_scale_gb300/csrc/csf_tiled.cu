@@ -211,9 +211,8 @@ __device__ __forceinline__ csf_tile_src tile_src(const DecStack &S, const TiledI
 // tile's index disagrees with its codes.
 template <int KIND, bool STAGE>
 __device__ __forceinline__ bool tile_finish(const csf_tile_src &src, uint32_t rb, uint32_t cb, bool edge,
-                                            const csf_tile_raw &r, uint8_t *dst, uint32_t *sum, uint4 *line,
-                                            int lane) {
-    const csf_tile_line L = csf_tile_expand<KIND>(r);
+                                            const csf_tile_line &L, const csf_tile_raw &r, uint8_t *dst,
+                                            uint32_t *sum, uint4 *line, int lane) {
     uint32_t w0 = L.w0, w1 = L.w1, w2 = L.w2, w3 = L.w3;
     if (STAGE || L.cnt) *line = make_uint4(w0, w1, w2, w3);
     const bool bad = csf_tile_patch<KIND>(src, r, L, reinterpret_cast<uint8_t *>(line), lane);
@@ -317,12 +316,18 @@ __global__ void __launch_bounds__(kTlThreads) tiled_decode_kernel(const __grid_c
                 rbgn = en * g.nrb;
             }
         }
-        csf_tile_raw nxt;
-        if (n > 1) nxt = csf_tile_load<KIND>(src, tilen, rbgn, lane);
+        // expand this tile, then load the next one into the registers the
+        // expansion has read (the patch needs only the index entries)
+        const csf_tile_line L = csf_tile_expand<KIND>(cur);
+        csf_tile_raw idx;
+        idx.code = 0;
+        idx.bw = 0;
+        idx.x0 = cur.x0;
+        idx.x1 = cur.x1;
+        if (n > 1) cur = csf_tile_load<KIND>(src, tilen, rbgn, lane);
         const bool edge = rb >= full_rb || cb >= full_cb;
-        bad |= tile_finish<KIND, STAGE>(src, rb, cb, edge, cur, STAGE ? nullptr : S.ws + tile * 512,
+        bad |= tile_finish<KIND, STAGE>(src, rb, cb, edge, L, idx, STAGE ? nullptr : S.ws + tile * 512,
                                         STAGE ? sums + tile : nullptr, line, lane);
-        cur = nxt;
         j = jn; t = tn; rb = rbn; cb = cbn; tile = tilen; rbg = rbgn;
     }
     if (__any_sync(kFull, bad) && lane == 0) flag(S.err, CSF_DEV_ERR_CORRUPT);
